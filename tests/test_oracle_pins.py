@@ -1,0 +1,272 @@
+"""Pins for the CPU oracle: each check comes from outside the oracle's own code.
+
+Brute force on tiny inputs (per-token loops, exact rationals), closed forms
+worked by hand, invariants of the mathematics, and special cases that reduce
+to library routines.  A plausible mistake in the oracle (a dropped 1/sqrt(d),
+a softmax over the wrong axis, heads averaged instead of summed, a wrong RoPE
+pairing or sign, an off-by-one view position, a wrong tie-break) fails at
+least one of them.
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import synth
+from oracle import kvm_oracle as O
+
+RNG = np.random.default_rng(12345)
+
+
+def rand_bf16(shape, scale=1.0):
+    return O.f64_to_bf16(RNG.normal(0.0, scale, size=shape))
+
+
+# ----------------------------------------------------------------------------- bf16
+def test_bf16_exact_values_and_ties():
+    assert O.f64_to_bf16([1.0, -2.0, 0.0, 0.5, 3.0]).tolist() == [0x3F80, 0xC000, 0x0000, 0x3F00, 0x4040]
+    # 1 + 2^-8 sits halfway between 1 and 1 + 2^-7: ties go to the even pattern 0x3F80.
+    assert int(O.f64_to_bf16(1 + 2.0 ** -8)) == 0x3F80
+    # 1 + 3*2^-8 is halfway between 0x3F81 and 0x3F82: even is 0x3F82.
+    assert int(O.f64_to_bf16(1 + 3 * 2.0 ** -8)) == 0x3F82
+    # Just above the tie: must round up.  Going through fp32 first would lose the 2^-40 and tie down.
+    assert int(O.f64_to_bf16(1 + 2.0 ** -8 + 2.0 ** -40)) == 0x3F81
+    assert int(O.f64_to_bf16(-(1 + 2.0 ** -8 + 2.0 ** -40))) == 0xBF81
+
+
+def test_bf16_matches_torch_from_fp32():
+    x = RNG.normal(0, 3, size=20000).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(O.f64_to_bf16(x.astype(np.float64)), ref)
+
+
+def test_bf16_roundtrip_all_finite_patterns():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):
+        vals = O.bf16_to_f64(bits)
+    fin = np.isfinite(vals)
+    back = O.f64_to_bf16(vals[fin])
+    # -0.0 and +0.0 both survive with their sign
+    assert np.array_equal(back, bits[fin])
+
+
+# ----------------------------------------------------------------------------- Mean-K
+def test_mean_k_equals_exact_rational_mean():
+    keys = rand_bf16((3 * 32 + 7, 8))          # two full blocks ... and a partial tail block
+    idx = O.mean_k_index(keys)
+    vals = O.bf16_to_f64(keys)
+    assert idx.shape == (4, 8)
+    for b in range(4):
+        rows = range(b * 32, min(len(vals), b * 32 + 32))
+        for i in range(8):
+            exact = sum(Fraction(float(vals[t, i])) for t in rows) / len(rows)
+            assert abs(Fraction(float(idx[b, i])) - exact) <= abs(exact) * Fraction(1, 2 ** 52)
+
+
+def test_index_append_matches_full_build_and_is_position_free():
+    keys = rand_bf16((300, 16))
+    full = O.mean_k_index(keys)
+    idx = O.mean_k_index(keys[:45])
+    for a, b in [(45, 70), (70, 64), (134, 1), (135, 165)]:
+        idx = O.index_append(idx, keys[:a + b], a, b)
+    assert np.array_equal(idx, full)
+    # Zero-length append changes nothing.
+    assert np.array_equal(O.index_append(full, keys, 300, 0), full)
+
+
+# ----------------------------------------------------------------------------- scores
+def test_block_score_is_mean_of_per_token_scores():
+    """s_b = <q, mean_t k_t>/sqrt(d) must equal mean_t <q, k_t>/sqrt(d) (linearity), by per-token loops."""
+    h_q, h_kv, d, n_tok = 6, 2, 16, 96
+    keys = [rand_bf16((n_tok, d)) for _ in range(h_kv)]
+    q = rand_bf16((h_q, d))
+    idx = np.stack([O.mean_k_index(k) for k in keys])
+    s = O.block_scores(q, idx)
+    qf = O.bf16_to_f64(q)
+    for h in range(h_q):
+        kv = O.bf16_to_f64(keys[h // 3])
+        for b in range(n_tok // 32):
+            per_tok = [sum(qf[h, i] * kv[t, i] for i in range(d)) / math.sqrt(d) for t in range(b * 32, b * 32 + 32)]
+            assert s[h, b] == pytest.approx(sum(per_tok) / 32, rel=1e-12, abs=1e-14)
+
+
+def test_softmax_single_head_group_is_library_softmax():
+    s = RNG.normal(0, 4, size=(3, 50))
+    gs = O.gqa_softmax_sum(s, 3)
+    assert np.allclose(gs, scipy.special.softmax(s, axis=1), rtol=1e-14, atol=0)
+
+
+def test_group_sum_closed_forms():
+    ln3 = math.log(3.0)
+    # Two heads in one group: p1 = (1/4, 3/4), p2 = (3/4, 1/4): the sum is (1, 1).
+    assert np.allclose(O.gqa_softmax_sum(np.array([[0.0, ln3], [ln3, 0.0]]), 1), [[1.0, 1.0]], atol=1e-15)
+    # p1 = (1/4, 3/4), p2 = (1/2, 1/2): the sum is (3/4, 5/4); an average would give half of that.
+    assert np.allclose(O.gqa_softmax_sum(np.array([[0.0, ln3], [7.0, 7.0]]), 1), [[0.75, 1.25]], atol=1e-15)
+    # Two groups keep apart: rows 0-1 -> group 0, rows 2-3 -> group 1.
+    s = np.array([[0.0, ln3], [ln3, 0.0], [0.0, 0.0], [0.0, ln3]])
+    assert np.allclose(O.gqa_softmax_sum(s, 2), [[1.0, 1.0], [0.75, 1.25]], atol=1e-15)
+
+
+def test_group_scores_sum_to_group_size():
+    s = RNG.normal(0, 2, size=(40, 777))
+    gs = O.gqa_softmax_sum(s, 8)
+    assert np.allclose(gs.sum(axis=1), 5.0, rtol=1e-13)
+
+
+def test_withdrawn_averaging_is_distinguishable():
+    """Head A likes block 0, head B block 1, both like block 3 moderately.
+
+    Per-head softmax then sum ranks blocks 0 and 1 first; averaging the query
+    heads first ranks block 3 first.  Closed form worked by hand.
+    """
+    r2 = math.sqrt(2.0)
+    q = O.f64_to_bf16([[1.0, 0.0], [0.0, 1.0]])                        # h_q = 2, h_kv = 1, d = 2
+    idx = np.array([[[5 * r2, 0.0], [0.0, 5 * r2], [0.0, 0.0], [2.6 * r2, 2.6 * r2]]])
+    s = O.block_scores(q, idx)
+    assert np.allclose(s, [[5, 0, 0, 2.6], [0, 5, 0, 2.6]], atol=1e-12)
+    za = math.exp(5) + 2 + math.exp(2.6)
+    expect = np.array([(math.exp(5) + 1) / za, (1 + math.exp(5)) / za, 2 / za, 2 * math.exp(2.6) / za])
+    gs = O.gqa_softmax_sum(s, 1)
+    assert np.allclose(gs[0], expect, rtol=1e-13)
+    wd = O.withdrawn_group_scores(q, idx)
+    assert int(np.argmax(gs[0])) in (0, 1) and int(np.argmax(wd[0])) == 3
+
+
+def test_step_scores_single_token_and_mass():
+    idx = RNG.normal(0, 0.3, size=(2, 40, 8))
+    qs = rand_bf16((3, 4, 8))
+    one = O.step_group_scores(qs[:1], idx)
+    assert np.array_equal(one, O.gqa_softmax_sum(O.block_scores(qs[0], idx), 2))
+    assert np.allclose(O.step_group_scores(qs, idx).sum(axis=1), 3 * 2, rtol=1e-13)
+
+
+# ----------------------------------------------------------------------------- selection
+def brute_select(gs, n_blk, n_sink, n_recent, top_k):
+    if n_blk <= n_sink + n_recent + top_k:
+        return list(range(n_blk))
+    keep = set(range(n_sink)) | set(range(n_blk - n_recent, n_blk))
+    cands = sorted(range(n_sink, n_blk - n_recent), key=lambda b: (-gs[b], b))
+    return sorted(keep | set(cands[:top_k]))
+
+
+@pytest.mark.parametrize("n_blk,n_sink,n_recent,top_k", [
+    (50, 1, 2, 7), (50, 4, 8, 20), (50, 0, 0, 5), (12, 4, 4, 4), (11, 4, 4, 4), (3, 4, 8, 2), (0, 1, 2, 3),
+    (40, 0, 5, 10), (40, 6, 0, 10)])
+def test_select_matches_brute_force_with_ties(n_blk, n_sink, n_recent, top_k):
+    gs = np.round(RNG.uniform(0, 1, size=n_blk), 1)          # many exact ties
+    ids = O.select_blocks(gs, n_blk, n_sink, n_recent, top_k)
+    assert ids.tolist() == brute_select(gs, n_blk, n_sink, n_recent, top_k)
+    assert len(ids) == min(n_blk, n_sink + n_recent + top_k)
+    assert np.all(np.diff(ids) > 0)
+
+
+def test_select_tie_goes_to_lower_id():
+    gs = np.zeros(20)
+    gs[[7, 9, 11, 13]] = 1.0
+    assert O.select_blocks(gs, 20, 1, 1, 2).tolist() == [0, 7, 9, 19]
+
+
+# ----------------------------------------------------------------------------- RoPE
+def test_rope_matches_complex_rotation():
+    """RoFormer's complex form: z_i = x_i + i x_{i+d/2} is multiplied by exp(i p theta^(-2i/d))."""
+    d, theta = 16, 1e4
+    x = RNG.normal(size=(5, d))
+    pos = np.array([0.0, 1.0, 7.0, 1000.0, 65535.0])
+    got = O.rope(x, pos, theta)
+    for r in range(5):
+        for i in range(d // 2):
+            z = complex(x[r, i], x[r, i + d // 2]) * np.exp(1j * pos[r] * theta ** (-2.0 * i / d))
+            assert got[r, i] == pytest.approx(z.real, abs=1e-9)
+            assert got[r, i + d // 2] == pytest.approx(z.imag, abs=1e-9)
+
+
+def test_rope_invariants():
+    d, theta = 128, 1e6
+    x = RNG.normal(size=(7, d))
+    assert np.array_equal(O.rope(x, 0, theta), x)                      # identity at p = 0
+    for p0, p in [(0, 5), (31, 32), (4096, 65535), (1048000, 1048575)]:
+        # RoPE(x, p) = R(p - p0) applied to RoPE(x, p0)
+        assert np.allclose(O.rope(O.rope(x, p0, theta), p - p0, theta), O.rope(x, p, theta), atol=1e-9)
+    assert np.allclose(np.linalg.norm(O.rope(x, 12345, theta), axis=1), np.linalg.norm(x, axis=1), rtol=1e-14)
+    q, k = RNG.normal(size=d), RNG.normal(size=d)
+    a = O.rope(q, 100, theta) @ O.rope(k, 40, theta)
+    b = O.rope(q, 1060, theta) @ O.rope(k, 1000, theta)
+    assert a == pytest.approx(b, rel=1e-9)                              # depends on m - n only
+
+
+# ----------------------------------------------------------------------------- view + attention
+def test_materialize_positions_and_copies():
+    d, n_tok, theta = 8, 5 * 32 + 9, 1e4
+    keys, vals = rand_bf16((n_tok, d)), rand_bf16((n_tok, d))
+    ids = np.array([0, 2, 5])                                          # block 5 is the 9-token tail
+    kv, vv = O.materialize(keys, vals, ids, n_tok, theta)
+    rows = list(range(0, 32)) + list(range(64, 96)) + list(range(160, 169))
+    assert kv.shape == (73, d) and np.array_equal(vv, vals[rows])
+    for j, t in enumerate(rows):
+        expect = O.f64_to_bf16(O.rope(O.bf16_to_f64(keys[t]), j, theta))
+        assert np.array_equal(kv[j], expect)
+
+
+def brute_full_attention(q_bits, keys_bits, vals_bits, theta):
+    """Standard decode over a conventional post-RoPE bf16 KV cache, token by token."""
+    qf, kf, vf = O.bf16_to_f64(q_bits), O.bf16_to_f64(keys_bits), O.bf16_to_f64(vals_bits)
+    n, d = kf.shape
+    out = []
+    for h in range(qf.shape[0]):
+        qr = O.rope(qf[h], n, theta)
+        logits = []
+        for t in range(n):
+            kt = O.bf16_to_f64(O.f64_to_bf16(O.rope(kf[t], t, theta)))
+            logits.append(sum(qr[i] * kt[i] for i in range(d)) / math.sqrt(d))
+        m = max(logits)
+        w = [math.exp(v - m) for v in logits]
+        z = sum(w)
+        out.append([sum(w[t] * vf[t, i] for t in range(n)) / z for i in range(d)])
+    return np.array(out)
+
+
+def test_all_blocks_kept_equals_full_attention():
+    d, n_tok, theta = 16, 3 * 32 + 5, 1e4
+    keys, vals, q = rand_bf16((n_tok, d)), rand_bf16((n_tok, d)), rand_bf16((2, d))
+    ids = O.select_blocks(np.zeros(4), 4, 1, 1, 8)                     # budget covers every block
+    kv, vv = O.materialize(keys, vals, ids, n_tok, theta)
+    got = O.decode_attention(q, kv, vv, theta)
+    assert np.allclose(got, brute_full_attention(q, keys, vals, theta), rtol=1e-12, atol=1e-13)
+
+
+def test_attention_special_cases():
+    d, theta = 8, 1e4
+    q, v = rand_bf16((3, d)), rand_bf16((1, d))
+    k = rand_bf16((1, d))
+    assert np.allclose(O.decode_attention(q, k, v, theta), O.bf16_to_f64(v).repeat(3, 0), atol=0)   # L = 1
+    vals = rand_bf16((40, d))
+    zeros = np.zeros((40, d), dtype=np.uint16)                          # all keys zero: uniform weights
+    assert np.allclose(O.decode_attention(q, zeros, vals, theta), O.bf16_to_f64(vals).mean(0), rtol=1e-13)
+    assert np.array_equal(O.decode_attention(q, zeros[:0], vals[:0], theta), np.zeros((3, d)))
+
+
+# ----------------------------------------------------------------------------- planted recovery
+def _recovered(w, layer=0):
+    li = synth.layer_inputs(w, layer)
+    res = O.kvmem_layer(li.k_pool, li.v_pool, li.block_table[0], li.q[0, 0], w.n_tok, w.n_sink,
+                        w.n_recent, w.top_k, w.rope_theta, heads=[])
+    hits = []
+    for g in range(w.h_kv):
+        ids = O.select_blocks(res["gs"][g], w.n_blk, w.n_sink, w.n_recent, w.top_k)
+        hits.append(len(set(ids.tolist()) & set(li.planted[0, g].tolist())))
+    return hits
+
+
+def test_planted_blocks_recovered_on_tiny_seed0():
+    assert _recovered(synth.WORKLOADS["tiny_8k_g4_d64"]) [0] >= 3
+
+
+def test_clean_variant_recovers_every_planted_block():
+    w = synth.WORKLOADS["tiny_8k_g4_d64"].with_(eps_scale=0.1, q_noise_var=0.0)
+    assert _recovered(w) == [4]
+    # GQA geometry, 4 planted topics per KV head: signal <mu_b, sum mu> ~ 32 against cross-talk std ~ 5.7.
+    w2 = synth.WORKLOADS["gqa40x8_256k"].with_(n_tok=32768, top_k=64, n_planted=4, eps_scale=0.1, q_noise_var=0.0)
+    assert _recovered(w2) == [4] * 8
