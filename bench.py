@@ -1,0 +1,439 @@
+"""Benchmark of the KVMem decode hot path on B300: one JSON line on stdout.
+
+Default workload (ws1m_16layer): 40 query heads / 8 KV heads, d = 128, a
+1,048,576-token history per layer with 16 layers resident in HBM (64 GiB of
+bf16 K/V pages + 2 GiB fp32 Mean-K index), a 65,536-token view per layer
+(4 sink + 32 recent + 2012 top-k blocks), one decode query per layer.  One
+step = for each of the 16 layers, in order:
+    kvm_index_append (the step's 512 new tokens) -> kvm_score_select
+    -> kvm_materialize_attn (gather + re-RoPE view, decode attention).
+Metric: step latency per layer (us) and the HBM GB/s of the bytes each layer
+must touch (index read + appended keys + kept K/V read + view write).
+
+    python bench.py [--steps K] [--warmup W] [--gpus N] [--impl kvm|reference]
+                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+
+--impl reference times the CPU oracle on a bounded sample of the same workload
+(one KV head of one layer per step) on the host's cores.
+Under torchrun (N > 1) every rank runs its own independent replica (separate
+sessions: the path shards with no exchange); rank 0 prints the line with the
+maximum time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "select+materialize+attend step µs and HBM GB/s at 1M-token history, per layer"
+BLOCK = 32
+
+
+def must_touch_bytes(w: synth.Workload) -> int:
+    """Algorithmic bytes one layer of a step must move (all sessions)."""
+    per_sess = 0
+    idx_read = w.h_kv * w.n_blk * w.d * 4
+    app_blocks = -(-w.append_tok // BLOCK) if w.append_tok else 0
+    app = w.append_tok * w.h_kv * w.d * 2 + app_blocks * w.h_kv * w.d * 4
+    view = w.h_kv * w.view_tokens * w.d * 2          # one of K or V
+    per_sess = idx_read + app + 2 * view + 2 * view  # kept K/V read + K/V view written
+    return per_sess * w.n_sessions
+
+
+def view_call_bytes(w: synth.Workload) -> int:
+    """Algorithmic bytes of one kvm_materialize_attn call (kept K/V read + view written)."""
+    return 4 * w.h_kv * w.view_tokens * w.d * 2 * w.n_sessions
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle timing
+def oracle_sample(w: synth.Workload, reps: int, warmup: int):
+    """Times the oracle on one KV head of layer 0 (the step's work for that head), per step.
+
+    Returns (seconds per sampled (layer, KV head) step, BLAS threads, description).
+    """
+    from oracle import kvm_oracle as O
+    try:
+        from threadpoolctl import threadpool_info
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except Exception:
+        threads = 1
+    g = 0
+    bt = synth.block_table(w)
+    k, v = synth.kv_pool(w, 0, bt, sessions=[0], heads=(g, g + 1))
+    q = synth.queries(w, 0)[0, 0]
+    keys = O.paged_tokens(k, bt[0], g, w.n_tok)
+    vals = O.paged_tokens(v, bt[0], g, w.n_tok)
+    n_hist = w.n_tok - w.append_tok
+    hist_index = O.mean_k_index(keys[:n_hist]) if n_hist > 0 else np.zeros((0, w.d))
+    G = w.group
+    qg = q[G * g:G * (g + 1)]
+    times = []
+    for i in range(warmup + reps):
+        t0 = time.perf_counter()
+        idx = O.index_append(hist_index, keys, n_hist, w.append_tok) if w.append_tok else O.mean_k_index(keys)
+        gs = O.gqa_softmax_sum(O.block_scores(qg, idx[None]), 1)[0]
+        ids = O.select_blocks(gs, w.n_blk, w.n_sink, w.n_recent, w.top_k)
+        kv, vv = O.materialize(keys, vals, ids, w.n_tok, w.rope_theta)
+        O.decode_attention(qg, kv, vv, w.rope_theta)
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    desc = (f"oracle on KV head 0 of layer 0 of {w.name} (append {w.append_tok} tokens, score {w.n_blk} blocks for "
+            f"{G} query heads, select, materialise {len(ids)} blocks, attend); per-layer value = 8 heads x that time")
+    return statistics.median(times), threads, desc
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per_head_s, threads, desc = oracle_sample(w, args.steps, args.warmup)
+    us_layer = per_head_s * w.h_kv * w.n_sessions * 1e6
+    gbs = must_touch_bytes(w) / (us_layer * 1e-6) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(us_layer, 1), "unit": "us/layer",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_layer * w.n_layers / 1e3, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "sample": "1 KV head of 1 layer per step"},
+            "hbm_gbps_equivalent": round(gbs, 3),
+            "cpu_baseline": {"value": round(us_layer, 1), "unit": "us/layer", "cores": threads, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(us_layer, 1), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU bench
+def run_kvm(args, w):
+    import torch
+    import torch.distributed as dist
+
+    import sparse_attention_decode_04_b300 as K
+    from synth import device as synth_dev
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    S, L = w.n_sessions, w.n_layers
+    ctx = K.Context.for_workload(w)
+    n_pages = w.n_pages
+    n_hist = w.n_tok - w.append_tok
+    bt = torch.from_numpy(synth.block_table(w)).to(dev)
+    kp, vp, index, qs, outs = [], [], [], [], []
+    for layer in range(L):
+        k = torch.empty((n_pages, w.h_kv, BLOCK, w.d), dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        synth_dev.fill_kv_pool(w, layer, bt, k.view(torch.int16), v.view(torch.int16))
+        kp.append(k)
+        vp.append(v)
+        q = synth.queries(w, layer)
+        qs.append(torch.from_numpy(q[:, 0].view(np.int16)).to(dev).view(torch.bfloat16).contiguous())
+        idx = torch.zeros((S, w.h_kv, w.n_blk, w.d), dtype=torch.float32, device=dev)
+        K.kvm_index_append(ctx, k, n_pages, bt, [0] * S, [n_hist] * S, idx)  # the history before this step
+        index.append(idx)
+        outs.append(torch.empty((S, w.h_q, w.d), dtype=torch.float32, device=dev))
+    kept = torch.empty((S, w.h_kv, ctx.budget), dtype=torch.int32, device=dev)
+    k_view = torch.empty((S, w.h_kv, BLOCK * ctx.budget, w.d), dtype=torch.bfloat16, device=dev)
+    v_view = torch.empty_like(k_view)
+    view_len = torch.empty((S, w.h_kv), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    n_tok = [w.n_tok] * S
+    launches_per_layer = (1 if w.append_tok else 0) + 2 + 2
+
+    def layer_calls(layer, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        if w.append_tok:
+            K.kvm_index_append(ctx, kp[layer], n_pages, bt, [n_hist] * S, [w.append_tok] * S, index[layer])
+        if ev is not None:
+            ev[1].record(stream)
+        K.kvm_score_select(ctx, qs[layer], 1, index[layer], n_tok, kept)
+        if ev is not None:
+            ev[2].record(stream)
+        K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept, qs[layer], k_view, v_view,
+                               view_len, outs[layer])
+        if ev is not None:
+            ev[3].record(stream)
+
+    def step():
+        for layer in range(L):
+            layer_calls(layer)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+
+    # CUDA graph of one whole step (all layers)
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()  # warm the side stream
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=side):
+            step()
+        torch.cuda.synchronize()
+        for _ in range(max(1, args.warmup)):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    gpu_index = local
+    if os.environ.get("CUDA_VISIBLE_DEVICES"):
+        try:
+            gpu_index = int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])
+        except ValueError:
+            gpu_index = local
+    sampler = ClockSampler(gpu_index)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        time.sleep(0.3)
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for _ in range(args.steps):
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        step_ms = t0.elapsed_time(t1) / args.steps
+        # per-call durations: the same steps launched call by call with events on the launching stream
+        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(L)]
+               for _ in range(args.steps)]
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for s_ in range(args.steps):
+            for layer in range(L):
+                layer_calls(layer, evs[s_][layer])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1) / args.steps
+    st = K.kvm_device_status(ctx)
+    if st != 0:
+        raise RuntimeError(f"device status 0x{st:x} after the timed region")
+    stage = {"index_append": [], "score_select": [], "materialize_attn": []}
+    for s_ in range(args.steps):
+        for layer in range(L):
+            e = evs[s_][layer]
+            stage["index_append"].append(e[0].elapsed_time(e[1]) * 1e3)
+            stage["score_select"].append(e[1].elapsed_time(e[2]) * 1e3)
+            stage["materialize_attn"].append(e[2].elapsed_time(e[3]) * 1e3)
+    stage_us = {k: round(statistics.mean(v), 2) for k, v in stage.items()}
+
+    if world > 1:
+        t = torch.tensor([step_ms, eager_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        step_ms, eager_ms = float(t[0]), float(t[1])
+
+    us_layer = step_ms * 1e3 / L
+    bytes_layer = must_touch_bytes(w)
+    gbs = bytes_layer / (us_layer * 1e-6) / 1e9 * world
+    peak, peak_kind = load_peaks()
+    vb = view_call_bytes(w)
+    view_us = stage_us["materialize_attn"]
+    achieved = vb / (view_us * 1e-6) / 1e9
+
+    # end-to-end through the public API with host buffers: H2D of the step's queries and new K/V pages,
+    # D2H of every layer's attention output
+    e2e = None
+    if not args.no_e2e:
+        app_blocks = -(-w.append_tok // BLOCK) if w.append_tok else 0
+        first_new_page = [int(x) for x in synth.block_table(w)[:, w.n_blk - app_blocks]] if app_blocks else []
+        q_host = torch.empty((L, S, w.h_q, w.d), dtype=torch.bfloat16).pin_memory()
+        for layer in range(L):
+            q_host[layer].copy_(qs[layer].cpu())
+        new_k = [kp[layer][first_new_page[0]:first_new_page[0] + app_blocks].cpu().pin_memory() for layer in range(L)] \
+            if app_blocks and S == 1 else None
+        new_v = [vp[layer][first_new_page[0]:first_new_page[0] + app_blocks].cpu().pin_memory() for layer in range(L)] \
+            if app_blocks and S == 1 else None
+        out_host = torch.empty((L, S, w.h_q, w.d), dtype=torch.float32).pin_memory()
+        q_dev = torch.empty((L, S, w.h_q, w.d), dtype=torch.bfloat16, device=dev)
+        h2d = q_host.numel() * 2 + (sum(t.numel() * 2 for t in new_k) * 2 if new_k else 0)
+        d2h = out_host.numel() * 4
+
+        def e2e_step():
+            q_dev.copy_(q_host, non_blocking=True)
+            for layer in range(L):
+                if new_k:
+                    p0 = first_new_page[0]
+                    kp[layer][p0:p0 + app_blocks].copy_(new_k[layer], non_blocking=True)
+                    vp[layer][p0:p0 + app_blocks].copy_(new_v[layer], non_blocking=True)
+                if w.append_tok:
+                    K.kvm_index_append(ctx, kp[layer], n_pages, bt, [n_hist] * S, [w.append_tok] * S, index[layer])
+                K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept)
+                K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept, q_dev[layer], k_view,
+                                       v_view, view_len, outs[layer])
+            for layer in range(L):
+                out_host[layer].copy_(outs[layer], non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        wall0 = time.perf_counter()
+        a0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        a1.record(stream)
+        torch.cuda.synchronize()
+        wall = (time.perf_counter() - wall0) / args.steps
+        e2e_ms = max(a0.elapsed_time(a1) / args.steps, wall * 1e3)
+        e2e = {"value": round(e2e_ms * 1e3 / L, 2), "unit": "us/layer", "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        per_head_s, threads, desc = oracle_sample(w, 1, 0)
+        cpu = {"value": round(per_head_s * w.h_kv * w.n_sessions * 1e6, 1), "unit": "us/layer", "cores": threads,
+               "kind": "oracle", "sample": desc}
+
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            tr = json.load(f).get(w.name)
+        if tr and tr.get("source_hash") == K_source_hash():
+            traffic = tr.get("bytes_per_launch")
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(us_layer, 2), "unit": "us/layer", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d, "history_tokens": w.n_tok,
+                       "layers": L, "sessions_per_gpu": S, "view_tokens": w.view_tokens, "append_tokens": w.append_tok,
+                       "kv_dtype": "bf16", "cuda_graph": graph is not None,
+                       "l2": "inputs larger than L2 (index 128 MiB + K/V pool 4 GiB per layer), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "hbm_gbps": round(gbs, 1), "must_touch_bytes_per_layer": bytes_layer,
+            "hbm_frac_of_measured": round(bytes_layer / (us_layer * 1e-6) / 1e9 / peak, 4),
+            "stages_us_per_layer": stage_us, "ms_per_step_eager": round(eager_ms, 4),
+            "roofline": {"bound": "hbm", "kernel": "kvm_materialize_attn (view kernel + combine)",
+                         "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": traffic,
+                         "algorithmic_bytes_per_launch": vb},
+            "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches_per_layer * L * args.steps * 2,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def K_source_hash() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_decode_04_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kvm", choices=["kvm", "reference"])
+    ap.add_argument("--workload", default="ws1m_16layer", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    w = synth.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_kvm(args, w)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+/*
+ * kvm.h — C ABI of the KVMem decode hot path on one B300 (sm_103a).
+ *
+ * KVMem keeps a long agent history as paged KV and, for each decode step,
+ * selects the history blocks relevant to the current query and materialises
+ * them into a bounded execution view (KVMEM reproduction README, "Background
+ * and main changes"; Evolve review of KVMem, "Summary").  Per layer and KV
+ * head the path is:
+ *   1. kvm_index_append   Mean-K index: the mean of each 32-token block's
+ *                         pre-RoPE keys, accumulated in fp32.
+ *   2. kvm_score_select   s_b = <q, kbar_b>/sqrt(d) per query head; softmax over
+ *                         blocks per head; probabilities summed over each GQA
+ *                         group; sink + recent blocks forced, top-k of the rest.
+ *   3. kvm_materialize    kept blocks gathered in original order into a
+ *                         contiguous bf16 view; keys re-rotated (RoPE) at view
+ *                         positions 0..L-1, values copied bit for bit.
+ *   4. kvm_decode_attn    single-token attention over the view.
+ *   kvm_materialize_attn  3 + 4 in one pass (the view is written once and never
+ *                         re-read from HBM).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - bf16 tensors are passed as uint16_t bit patterns.  fp32 is float.
+ * - Unless a parameter says "host", every pointer is DEVICE memory owned by the
+ *   caller (for example a PyTorch tensor); the library never frees it.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *   stream).  Every call only enqueues work on it and returns; nothing
+ *   synchronises the host except kvm_create, kvm_destroy and kvm_device_status.
+ * - Block size is fixed: 32 tokens per block, one block per physical page.
+ * - One context serves one device (the device current at kvm_create) and one
+ *   head geometry.  Calls on one context must not run concurrently on
+ *   different streams: they share the context's scratch buffers.
+ * - Layouts (all row-major, innermost last):
+ *     pool (K or V) of one layer   [n_pages][h_kv][32][d]            bf16 (a page = 32 tokens, all KV heads)
+ *     block_table                  [n_sessions][max_blocks]          int32: block -> page
+ *     index of one layer           [n_sessions][h_kv][max_blocks][d] fp32
+ *     q (one decode token)         [n_sessions][h_q][d]              bf16, post-q-norm, pre-RoPE
+ *     q (step of n_q tokens)       [n_sessions][n_q][h_q][d]         bf16
+ *     kept_ids                     [n_sessions][h_kv][budget]        int32 ascending, -1 padded
+ *     k_view, v_view               [n_sessions][h_kv][32*budget][d]  bf16
+ *     view_len                     [n_sessions][h_kv]                int32 tokens in the view
+ *     out                          [n_sessions][h_q][d]              fp32
+ *   where budget = n_sink + n_recent + top_k blocks and query head h belongs
+ *   to KV head h / (h_q / h_kv).
+ * - History length n_tok is given per session on the host; n_blk =
+ *   ceil(n_tok / 32).  A partial last block is averaged over the tokens
+ *   present, and only those tokens enter the view.
+ * - Errors: each call validates its arguments on the host and returns a
+ *   kvm_status without launching anything when they are wrong;
+ *   kvm_last_error() then describes the problem (thread-local).  Data errors
+ *   only the device can see (a page id outside the pool, a kept id outside
+ *   the history) skip the access and set a bit in the context's device status
+ *   word, read with kvm_device_status().  No kernel traps.
+ */
+#ifndef KVM_H_
+#define KVM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVM_OK = 0,
+  KVM_ERR_INVALID_ARG = 1, /* null pointer, negative size, unsupported value          */
+  KVM_ERR_SHAPE = 2,       /* size beyond the context's capacity or unsupported d      */
+  KVM_ERR_BUDGET = 3,      /* budget fields inconsistent (negative, top_k < 0, ...)    */
+  KVM_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed              */
+  KVM_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (status word bit)     */
+  KVM_ERR_DEVICE = 6       /* the device status word reports a data error              */
+} kvm_status;
+
+/* Bits of the device status word. */
+#define KVM_DEV_BAD_PAGE 0x1u    /* block_table entry outside [0, n_pages)          */
+#define KVM_DEV_BAD_BLOCK 0x2u   /* kept id outside [0, n_blk) or not ascending     */
+#define KVM_DEV_TIMEOUT 0x4u     /* a pipeline wait exceeded its iteration limit    */
+
+typedef struct kvm_ctx kvm_ctx; /* opaque */
+
+typedef struct {
+  int32_t h_q;          /* query heads                                                 */
+  int32_t h_kv;         /* KV heads; h_q % h_kv == 0, group h_q / h_kv in [1, 8]        */
+  int32_t d;            /* head dimension: 64 or 128                                   */
+  int32_t n_sink;       /* leading blocks always kept                                  */
+  int32_t n_recent;     /* trailing blocks always kept                                 */
+  int32_t top_k;        /* further blocks kept by group score                         */
+  float rope_theta;     /* RoPE base (rotate-half pairing, full head dimension)        */
+  int64_t max_blocks;   /* block capacity per session (block-table row, index rows)    */
+  int32_t max_sessions; /* sessions per call, 1..64                                    */
+  int32_t max_queries;  /* query tokens per session in one kvm_score_select, >= 1      */
+} kvm_params;
+
+/* Human-readable name of a status code (static storage). */
+const char* kvm_status_string(kvm_status s);
+
+/* Message describing the last error returned on this thread (static, thread-local). */
+const char* kvm_last_error(void);
+
+/*
+ * Creates a context on the current CUDA device: validates `p`, allocates the
+ * scratch buffers (score, softmax and attention partials; RoPE tables, filled
+ * in fp64 by a kernel) and the device status word.  Synchronises the device.
+ * *out receives the context; free it with kvm_destroy.
+ */
+kvm_status kvm_create(const kvm_params* p, kvm_ctx** out);
+
+/* Frees everything kvm_create allocated (synchronises the device first). NULL is accepted. */
+kvm_status kvm_destroy(kvm_ctx* ctx);
+
+/* Device bytes the context allocated (scratch + tables); 0 for NULL. */
+size_t kvm_scratch_bytes(const kvm_ctx* ctx);
+
+/*
+ * Index append (step 1).  KVMEM reproduction README, "Core equation" (index
+ * vector kbar_b); Evolve review, "Summary" (position-independent Mean-K index
+ * over 32-token blocks).
+ *
+ * For each session s, tokens [tok_begin[s], tok_begin[s] + n_tok[s]) have
+ * already been written into the pool (pre-RoPE, post-k-norm keys).  Every
+ * block those tokens touch is recomputed from the pool:
+ *   index[s][g][b][:] = fp32 mean of the keys of block b present so far.
+ * Rows of other blocks are not touched.
+ *   k_pool       [n_pages][h_kv][32][d] bf16 (this layer)
+ *   block_table  [n_sessions][max_blocks] int32
+ *   tok_begin    host int64[n_sessions]
+ *   n_tok        host int64[n_sessions] (0 = nothing to do for that session)
+ *   index        [n_sessions][h_kv][max_blocks][d] fp32, updated in place
+ */
+kvm_status kvm_index_append(kvm_ctx* ctx, const uint16_t* k_pool, int64_t n_pages,
+                            const int32_t* block_table, int32_t n_sessions,
+                            const int64_t* tok_begin, const int64_t* n_tok, float* index,
+                            void* stream);
+
+/*
+ * Score and select (step 2).  KVMEM reproduction README, "Core equation"
+ * (s_b = <q, kbar_b>/sqrt d, selection within the block budget) and
+ * "2026-09-08 validation correction" (normalised query; softmax per query
+ * head, not over heads averaged first).
+ *
+ * For each session and KV head g:
+ *   s[h][b]  = <q_h, index[g][b]>/sqrt(d) for the group's query heads h
+ *   Gs[g][b] = sum_{h in g} softmax_b(s[h][:])[b]          (one query)
+ *   Gs[g][b] = sum_t sum_{h in g} softmax_b(s_t[h][:])[b]   (n_q > 1 query tokens)
+ * The softmax runs over all n_blk blocks.  Kept = blocks [0, n_sink) and the
+ * last n_recent blocks, plus the top_k remaining blocks by Gs (equal scores:
+ * the lower id first); if n_blk <= budget every block is kept.
+ *   q            [n_sessions][n_q][h_q][d] bf16, post-q-norm, pre-RoPE
+ *   n_q          query tokens per session, 1..max_queries
+ *   index        [n_sessions][h_kv][max_blocks][d] fp32
+ *   n_tok        host int64[n_sessions] history length (n_blk = ceil(n_tok/32) <= max_blocks)
+ *   kept_ids     [n_sessions][h_kv][budget] int32 out: ascending ids, -1 after n_keep
+ *   group_scores [n_sessions][h_kv][max_blocks] fp32 out, or NULL
+ *   head_scores  [n_sessions][h_q][max_blocks] fp32 out (raw s, n_q == 1 only), or NULL
+ */
+kvm_status kvm_score_select(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const float* index,
+                            const int64_t* n_tok, int32_t n_sessions, int32_t* kept_ids,
+                            float* group_scores, float* head_scores, void* stream);
+
+/*
+ * Materialise (step 3).  KVMEM reproduction README, "Core equation"
+ * (selected KV concatenated; address space and execution window kept apart);
+ * Evolve review, "Summary" / "Scope & Claims" (blocks restored with
+ * position-consistent re-RoPE into a bounded view).
+ *
+ * View slot j of (s, g) holds the j-th token of the kept blocks, in block
+ * order.  v_view[s][g][j] is a bit copy of the value; k_view[s][g][j] is the
+ * key rotated at position j (rotate-half pairing: dimension i with i + d/2,
+ * angle j * theta^(-2i/d)) and rounded to bf16, nearest even.  Slots past
+ * view_len are not written.
+ *   k_pool, v_pool [n_pages][h_kv][32][d] bf16 (this layer)
+ *   block_table    [n_sessions][max_blocks] int32
+ *   n_tok          host int64[n_sessions]
+ *   kept_ids       [n_sessions][h_kv][budget] int32 (as written by kvm_score_select)
+ *   k_view, v_view [n_sessions][h_kv][32*budget][d] bf16 out
+ *   view_len       [n_sessions][h_kv] int32 out
+ */
+kvm_status kvm_materialize(kvm_ctx* ctx, const uint16_t* k_pool, const uint16_t* v_pool,
+                           int64_t n_pages, const int32_t* block_table, const int64_t* n_tok,
+                           int32_t n_sessions, const int32_t* kept_ids, uint16_t* k_view,
+                           uint16_t* v_view, int32_t* view_len, void* stream);
+
+/*
+ * Decode attention over a view (step 4).  KVMEM reproduction README, "Local
+ * reproduction" (the view replaces full attention) and "2026-09-08
+ * validation correction" (RoPE applied to the query).
+ *   out[s][h] = sum_j softmax_j(<RoPE(q_h, L), k_view[g][j]>/sqrt(d)) v_view[g][j]
+ * with L = view_len[s][g] (the query sits at the slot after the view).  An
+ * empty view gives zeros.
+ *   q         [n_sessions][h_q][d] bf16, post-q-norm, pre-RoPE
+ *   k_view, v_view, view_len as written by kvm_materialize
+ *   out       [n_sessions][h_q][d] fp32
+ */
+kvm_status kvm_decode_attn(kvm_ctx* ctx, const uint16_t* q, const uint16_t* k_view,
+                           const uint16_t* v_view, const int32_t* view_len, int32_t n_sessions,
+                           float* out, void* stream);
+
+/*
+ * Steps 3 and 4 fused: the same outputs as kvm_materialize followed by
+ * kvm_decode_attn, reading each kept page once.
+ */
+kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint16_t* v_pool,
+                                int64_t n_pages, const int32_t* block_table, const int64_t* n_tok,
+                                int32_t n_sessions, const int32_t* kept_ids, const uint16_t* q,
+                                uint16_t* k_view, uint16_t* v_view, int32_t* view_len, float* out,
+                                void* stream);
+
+/*
+ * Reads (and optionally clears) the device status word after synchronising
+ * `stream`.  *out receives the KVM_DEV_* bits.  Returns KVM_OK when the word
+ * is zero, KVM_ERR_DEVICE or KVM_ERR_TIMEOUT otherwise.
+ */
+kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KVM_H_ */

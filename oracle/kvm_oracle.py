@@ -17,7 +17,7 @@ CPU tests in tests/test_oracle_pins.py against brute force, closed forms,
 invariants or library routines; none is "parity unpinned".
 
 Layouts (bf16 is carried as its uint16 bit pattern):
-  pool      uint16 [h_kv][n_pages][32][d]   pre-RoPE keys / values, one 32-token page per block
+  pool      uint16 [n_pages][h_kv][32][d]   pre-RoPE keys / values; a page holds one block of every KV head
   page_of   int32  [n_blk]                  logical block -> physical page (the block table row)
   index     f64    [h_kv][n_blk][d]         Mean-K vectors
   q         uint16 [h_q][d]                 post-q-norm, pre-RoPE query (one decode token)
@@ -58,7 +58,7 @@ def paged_tokens(pool, page_of, head: int, n_tok: int) -> np.ndarray:
     b of the history lives in physical page page_of[b].
     """
     n_blk = -(-n_tok // BLOCK)
-    pages = np.asarray(pool)[head, np.asarray(page_of)[:n_blk]]      # [n_blk][32][d]
+    pages = np.asarray(pool)[np.asarray(page_of)[:n_blk], head]      # [n_blk][32][d]
     return pages.reshape(n_blk * BLOCK, pages.shape[-1])[:n_tok]
 
 
@@ -269,7 +269,7 @@ def kvmem_layer(k_pool, v_pool, page_of, q_bits, n_tok: int, n_sink: int, n_rece
     index [h_kv][n_blk][d], gs [h_kv][n_blk], ids {g: [n_keep]},
     k_view/v_view {g: [L][d] bits} and out [h_q][d] (rows of the heads done).
     """
-    h_kv = np.asarray(k_pool).shape[0]
+    h_kv = np.asarray(k_pool).shape[1]
     q_bits = np.asarray(q_bits)
     multi = q_bits.ndim == 3
     h_q = q_bits.shape[-2]

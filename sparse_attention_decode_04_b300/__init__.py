@@ -1,0 +1,175 @@
+"""Python binding of libkvm.so, the KVMem decode hot path for B300 (sm_103a).
+
+Argument marshalling only: every computation runs in the CUDA kernels behind
+the C ABI declared in include/kvm.h.  Tensors are PyTorch CUDA tensors (torch
+is used for device memory and streams); bf16 tensors may be passed as
+torch.bfloat16 or as 16-bit integer bit patterns.  Host-side per-session
+arrays (history lengths, append ranges) are Python sequences.
+
+There is no fallback: if libkvm.so is missing the import of any entry point
+raises, and a failing call raises KvmError with the library's message.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libkvm.so")
+BLOCK = 32
+
+KVM_OK = 0
+STATUS_NAMES = {0: "KVM_OK", 1: "KVM_ERR_INVALID_ARG", 2: "KVM_ERR_SHAPE", 3: "KVM_ERR_BUDGET", 4: "KVM_ERR_CUDA",
+                5: "KVM_ERR_TIMEOUT", 6: "KVM_ERR_DEVICE"}
+DEV_BAD_PAGE, DEV_BAD_BLOCK, DEV_TIMEOUT = 0x1, 0x2, 0x4
+
+
+class KvmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32), ("d", ctypes.c_int32),
+                ("n_sink", ctypes.c_int32), ("n_recent", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("rope_theta", ctypes.c_float), ("max_blocks", ctypes.c_int64), ("max_sessions", ctypes.c_int32),
+                ("max_queries", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libkvm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing; build it with: python -m sparse_attention_decode_04_b300.build")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.kvm_status_string.argtypes = [ctypes.c_int]
+        L.kvm_status_string.restype = ctypes.c_char_p
+        L.kvm_last_error.argtypes = []
+        L.kvm_last_error.restype = ctypes.c_char_p
+        L.kvm_create.argtypes = [ctypes.POINTER(Params), ctypes.POINTER(P)]
+        L.kvm_destroy.argtypes = [P]
+        L.kvm_scratch_bytes.argtypes = [P]
+        L.kvm_scratch_bytes.restype = ctypes.c_size_t
+        L.kvm_index_append.argtypes = [P, P, i64, P, i32, P, P, P, P]
+        L.kvm_score_select.argtypes = [P, P, i32, P, P, i32, P, P, P, P]
+        L.kvm_materialize.argtypes = [P, P, P, i64, P, P, i32, P, P, P, P, P]
+        L.kvm_decode_attn.argtypes = [P, P, P, P, P, i32, P, P]
+        L.kvm_materialize_attn.argtypes = [P, P, P, i64, P, P, i32, P, P, P, P, P, P, P]
+        L.kvm_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
+        for name in ("kvm_create", "kvm_destroy", "kvm_index_append", "kvm_score_select", "kvm_materialize",
+                     "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int):
+    if status != KVM_OK:
+        raise KvmError(status, lib().kvm_last_error().decode(errors="replace"))
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libkvm must be contiguous")
+    return t.data_ptr()
+
+
+def _i64(vals):
+    vals = [int(v) for v in vals]
+    return (ctypes.c_int64 * max(1, len(vals)))(*vals)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, int):
+        return ctypes.c_void_p(stream)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Context:
+    """A libkvm context: head geometry, budget, capacities and the device scratch."""
+
+    def __init__(self, h_q: int, h_kv: int, d: int, n_sink: int, n_recent: int, top_k: int, rope_theta: float,
+                 max_blocks: int, max_sessions: int = 1, max_queries: int = 1):
+        self.params = Params(h_q, h_kv, d, n_sink, n_recent, top_k, rope_theta, max_blocks, max_sessions,
+                             max_queries)
+        h = ctypes.c_void_p()
+        _check(lib().kvm_create(ctypes.byref(self.params), ctypes.byref(h)))
+        self.handle = h
+        self.h_q, self.h_kv, self.d = h_q, h_kv, d
+        self.n_sink, self.n_recent, self.top_k = n_sink, n_recent, top_k
+        self.budget = n_sink + n_recent + top_k
+        self.max_blocks, self.max_sessions, self.max_queries = max_blocks, max_sessions, max_queries
+
+    @classmethod
+    def for_workload(cls, w, max_blocks=None, max_sessions=None):
+        return cls(w.h_q, w.h_kv, w.d, w.n_sink, w.n_recent, w.top_k, w.rope_theta,
+                   max_blocks or w.n_blk, max_sessions or w.n_sessions, w.n_q)
+
+    @property
+    def scratch_bytes(self) -> int:
+        return int(lib().kvm_scratch_bytes(self.handle))
+
+    def close(self):
+        if getattr(self, "handle", None):
+            _check(lib().kvm_destroy(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def kvm_index_append(ctx: Context, k_pool, n_pages: int, block_table, tok_begin, n_tok, index, stream=None):
+    n = len(n_tok)
+    _check(lib().kvm_index_append(ctx.handle, _ptr(k_pool), int(n_pages), _ptr(block_table), n, _i64(tok_begin),
+                                  _i64(n_tok), _ptr(index), _stream(stream)))
+
+
+def kvm_score_select(ctx: Context, q, n_q: int, index, n_tok, kept_ids, group_scores=None, head_scores=None,
+                     stream=None):
+    n = len(n_tok)
+    _check(lib().kvm_score_select(ctx.handle, _ptr(q), int(n_q), _ptr(index), _i64(n_tok), n, _ptr(kept_ids),
+                                  _ptr(group_scores), _ptr(head_scores), _stream(stream)))
+
+
+def kvm_materialize(ctx: Context, k_pool, v_pool, n_pages: int, block_table, n_tok, kept_ids, k_view, v_view,
+                    view_len, stream=None):
+    n = len(n_tok)
+    _check(lib().kvm_materialize(ctx.handle, _ptr(k_pool), _ptr(v_pool), int(n_pages), _ptr(block_table),
+                                 _i64(n_tok), n, _ptr(kept_ids), _ptr(k_view), _ptr(v_view), _ptr(view_len),
+                                 _stream(stream)))
+
+
+def kvm_decode_attn(ctx: Context, q, k_view, v_view, view_len, n_sessions: int, out, stream=None):
+    _check(lib().kvm_decode_attn(ctx.handle, _ptr(q), _ptr(k_view), _ptr(v_view), _ptr(view_len), int(n_sessions),
+                                 _ptr(out), _stream(stream)))
+
+
+def kvm_materialize_attn(ctx: Context, k_pool, v_pool, n_pages: int, block_table, n_tok, kept_ids, q, k_view,
+                         v_view, view_len, out, stream=None):
+    n = len(n_tok)
+    _check(lib().kvm_materialize_attn(ctx.handle, _ptr(k_pool), _ptr(v_pool), int(n_pages), _ptr(block_table),
+                                      _i64(n_tok), n, _ptr(kept_ids), _ptr(q), _ptr(k_view), _ptr(v_view),
+                                      _ptr(view_len), _ptr(out), _stream(stream)))
+
+
+def kvm_device_status(ctx: Context, clear: bool = True, stream=None) -> int:
+    """Device status word (KVM_DEV_* bits) after synchronising the stream; never raises on a non-zero word."""
+    out = ctypes.c_uint32(0)
+    st = lib().kvm_device_status(ctx.handle, ctypes.byref(out), int(bool(clear)), _stream(stream))
+    if st not in (0, 5, 6):
+        _check(st)
+    return int(out.value)

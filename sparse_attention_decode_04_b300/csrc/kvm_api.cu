@@ -1,0 +1,313 @@
+// C ABI of the KVMem decode hot path: context, validation, launches.
+// Every entry point checks its arguments on the host before anything is
+// enqueued; the kernels only ever see sizes the checks accepted.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "kvm.h"
+#include "kvm_internal.h"
+
+using kvm::Ctx;
+using kvm::SessionArgs;
+
+struct kvm_ctx {
+  Ctx c;
+};
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+kvm_status fail(kvm_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+kvm_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Largest block capacity the cluster select keeps in shared memory (8 CTAs,
+// 40960 fp32 keys each).
+constexpr int64_t kMaxBlocksLimit = 8 * 40960;
+
+kvm_status check_ctx(const kvm_ctx* ctx) {
+  if (!ctx) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != ctx->c.device)
+    return fail(KVM_ERR_INVALID_ARG, "current device %d is not the context's device %d", dev, ctx->c.device);
+  return KVM_OK;
+}
+
+kvm_status check_sessions(const Ctx& c, int32_t n_sessions) {
+  if (n_sessions < 0 || n_sessions > c.p.max_sessions)
+    return fail(KVM_ERR_SHAPE, "n_sessions=%d outside [0, %d]", n_sessions, c.p.max_sessions);
+  return KVM_OK;
+}
+
+// Fills n_tok / n_blk / n_keep / seg_base from host history lengths.
+kvm_status history_args(const Ctx& c, const int64_t* n_tok, int32_t n_sessions, SessionArgs* a) {
+  memset(a, 0, sizeof(*a));
+  if (n_sessions > 0 && !n_tok) return fail(KVM_ERR_INVALID_ARG, "n_tok is NULL");
+  int64_t base = 0;
+  for (int s = 0; s < n_sessions; ++s) {
+    if (n_tok[s] < 0) return fail(KVM_ERR_INVALID_ARG, "n_tok[%d]=%lld is negative", s, (long long)n_tok[s]);
+    const int64_t nb = (n_tok[s] + kvm::kBlock - 1) / kvm::kBlock;
+    if (nb > c.p.max_blocks)
+      return fail(KVM_ERR_SHAPE, "session %d: %lld blocks exceed max_blocks=%lld", s, (long long)nb,
+                  (long long)c.p.max_blocks);
+    a->n_tok[s] = n_tok[s];
+    a->n_blk[s] = (int32_t)nb;
+    a->n_keep[s] = (int32_t)(nb < c.budget ? nb : c.budget);
+    a->seg_base[s] = base;
+    base += (int64_t)c.p.h_kv * a->n_keep[s];
+  }
+  a->seg_base[n_sessions] = base;
+  return KVM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* kvm_status_string(kvm_status s) {
+  switch (s) {
+    case KVM_OK: return "KVM_OK";
+    case KVM_ERR_INVALID_ARG: return "KVM_ERR_INVALID_ARG";
+    case KVM_ERR_SHAPE: return "KVM_ERR_SHAPE";
+    case KVM_ERR_BUDGET: return "KVM_ERR_BUDGET";
+    case KVM_ERR_CUDA: return "KVM_ERR_CUDA";
+    case KVM_ERR_TIMEOUT: return "KVM_ERR_TIMEOUT";
+    case KVM_ERR_DEVICE: return "KVM_ERR_DEVICE";
+  }
+  return "KVM_ERR_UNKNOWN";
+}
+
+const char* kvm_last_error(void) { return g_err; }
+
+kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
+  if (!p || !out) return fail(KVM_ERR_INVALID_ARG, "params or out is NULL");
+  *out = nullptr;
+  if (p->d != 64 && p->d != 128) return fail(KVM_ERR_SHAPE, "d=%d: only 64 and 128 are built", p->d);
+  if (p->h_q <= 0 || p->h_kv <= 0 || p->h_q % p->h_kv != 0)
+    return fail(KVM_ERR_SHAPE, "h_q=%d must be a positive multiple of h_kv=%d", p->h_q, p->h_kv);
+  if (p->h_q / p->h_kv > kvm::kMaxGroup)
+    return fail(KVM_ERR_SHAPE, "GQA group %d exceeds %d", p->h_q / p->h_kv, kvm::kMaxGroup);
+  if (p->n_sink < 0 || p->n_recent < 0 || p->top_k < 0)
+    return fail(KVM_ERR_BUDGET, "n_sink, n_recent and top_k must be >= 0");
+  const int64_t budget = (int64_t)p->n_sink + p->n_recent + p->top_k;
+  if (budget < 1 || budget > (1 << 20)) return fail(KVM_ERR_BUDGET, "budget %lld outside [1, 2^20]", (long long)budget);
+  if (!(p->rope_theta > 1.0f)) return fail(KVM_ERR_INVALID_ARG, "rope_theta must be > 1");
+  if (p->max_blocks < 1 || p->max_blocks > kMaxBlocksLimit)
+    return fail(KVM_ERR_SHAPE, "max_blocks=%lld outside [1, %lld]", (long long)p->max_blocks,
+                (long long)kMaxBlocksLimit);
+  if (p->max_sessions < 1 || p->max_sessions > kvm::kMaxSessionsHost)
+    return fail(KVM_ERR_SHAPE, "max_sessions=%d outside [1, %d]", p->max_sessions, kvm::kMaxSessionsHost);
+  if (p->max_queries < 1) return fail(KVM_ERR_SHAPE, "max_queries must be >= 1");
+
+  kvm_ctx* ctx = new (std::nothrow) kvm_ctx();
+  if (!ctx) return fail(KVM_ERR_CUDA, "host allocation failed");
+  Ctx& c = ctx->c;
+  c.p = *p;
+  c.group = p->h_q / p->h_kv;
+  c.budget = (int)budget;
+  cudaError_t e = cudaGetDevice(&c.device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, c.device);
+  if (e != cudaSuccess) {
+    delete ctx;
+    return cuda_fail(e, "device query");
+  }
+  c.view_ctas = c.num_sms;
+  c.max_tiles = (p->max_blocks + 31) / 32;
+  const size_t S = (size_t)p->max_sessions;
+  const size_t sz_e = S * p->h_kv * (size_t)p->max_blocks * c.group * sizeof(float);
+  const size_t sz_part = S * p->h_q * (size_t)c.max_tiles * sizeof(float2);
+  const size_t sz_rec = ((size_t)c.view_ctas + S * p->h_kv) * c.group * (2 + p->d) * sizeof(float);
+  const size_t sz_base = (size_t)(budget + 1) * (p->d / 2) * sizeof(float2);
+  const size_t sz_off = (size_t)32 * (p->d / 2) * sizeof(float2);
+  void* ptrs[6] = {};
+  const size_t sizes[6] = {sz_e, sz_part, sz_rec, sz_base, sz_off, 256};
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], sizes[i]);
+  if (e != cudaSuccess) {
+    for (void* q : ptrs)
+      if (q) cudaFree(q);
+    delete ctx;
+    return cuda_fail(e, "cudaMalloc of context scratch");
+  }
+  c.e_buf = (float*)ptrs[0];
+  c.part = (float2*)ptrs[1];
+  c.rec = (float*)ptrs[2];
+  c.rope_base = (float*)ptrs[3];
+  c.rope_off = (float*)ptrs[4];
+  c.status = (uint32_t*)ptrs[5];
+  for (size_t s : sizes) c.bytes += s;
+  e = cudaMemset(c.status, 0, 256);
+  if (e == cudaSuccess) e = kvm::launch_rope_tables(c, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    kvm_destroy(ctx);
+    return cuda_fail(e, "context initialisation");
+  }
+  *out = ctx;
+  return KVM_OK;
+}
+
+kvm_status kvm_destroy(kvm_ctx* ctx) {
+  if (!ctx) return KVM_OK;
+  Ctx& c = ctx->c;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != c.device) cudaSetDevice(c.device);
+  cudaError_t e = cudaDeviceSynchronize();
+  void* ptrs[6] = {c.e_buf, c.part, c.rec, c.rope_base, c.rope_off, c.status};
+  for (void* q : ptrs)
+    if (q) cudaFree(q);
+  if (prev >= 0 && prev != c.device) cudaSetDevice(prev);
+  delete ctx;
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_destroy");
+}
+
+size_t kvm_scratch_bytes(const kvm_ctx* ctx) { return ctx ? ctx->c.bytes : 0; }
+
+kvm_status kvm_index_append(kvm_ctx* ctx, const uint16_t* k_pool, int64_t n_pages, const int32_t* block_table,
+                            int32_t n_sessions, const int64_t* tok_begin, const int64_t* n_tok, float* index,
+                            void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_sessions == 0) return KVM_OK;
+  if (!k_pool || !block_table || !tok_begin || !n_tok || !index)
+    return fail(KVM_ERR_INVALID_ARG, "kvm_index_append: NULL pointer argument");
+  if (n_pages < 1) return fail(KVM_ERR_INVALID_ARG, "n_pages=%lld must be >= 1", (long long)n_pages);
+  if (!aligned(k_pool, 16) || !aligned(index, 16))
+    return fail(KVM_ERR_INVALID_ARG, "k_pool and index must be 16-byte aligned");
+  SessionArgs a;
+  memset(&a, 0, sizeof(a));
+  int max_count = 0;
+  for (int i = 0; i < n_sessions; ++i) {
+    if (tok_begin[i] < 0 || n_tok[i] < 0)
+      return fail(KVM_ERR_INVALID_ARG, "session %d: negative tok_begin or n_tok", i);
+    const int64_t end = tok_begin[i] + n_tok[i];
+    if ((end + kvm::kBlock - 1) / kvm::kBlock > c.p.max_blocks)
+      return fail(KVM_ERR_SHAPE, "session %d: token %lld beyond max_blocks", i, (long long)end);
+    const int64_t b0 = tok_begin[i] / kvm::kBlock;
+    const int64_t b1 = n_tok[i] ? (end + kvm::kBlock - 1) / kvm::kBlock : b0;
+    a.n_tok[i] = end;  // tokens present after the append
+    a.aux[i] = b0;     // first block touched
+    a.count[i] = (int32_t)(b1 - b0);
+    if (a.count[i] > max_count) max_count = a.count[i];
+  }
+  cudaError_t e = kvm::launch_index_append(c, k_pool, n_pages, block_table, n_sessions, a, max_count, index,
+                                           (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_index_append launch");
+}
+
+kvm_status kvm_score_select(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const float* index, const int64_t* n_tok,
+                            int32_t n_sessions, int32_t* kept_ids, float* group_scores, float* head_scores,
+                            void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_sessions == 0) return KVM_OK;
+  if (!q || !index || !kept_ids) return fail(KVM_ERR_INVALID_ARG, "kvm_score_select: NULL pointer argument");
+  if (n_q < 1 || n_q > c.p.max_queries)
+    return fail(KVM_ERR_SHAPE, "n_q=%d outside [1, max_queries=%d]", n_q, c.p.max_queries);
+  if (n_q > 1 && head_scores) return fail(KVM_ERR_INVALID_ARG, "head_scores is only written for n_q == 1");
+  if (n_q > 1) return fail(KVM_ERR_SHAPE, "step-level scoring of n_q > 1 query tokens is not built in this library yet");
+  if (!aligned(q, 16) || !aligned(index, 16) || !aligned(kept_ids, 4) || !aligned(group_scores, 4) ||
+      !aligned(head_scores, 4))
+    return fail(KVM_ERR_INVALID_ARG, "q and index must be 16-byte aligned, outputs 4-byte aligned");
+  SessionArgs a;
+  if ((s = history_args(c, n_tok, n_sessions, &a)) != KVM_OK) return s;
+  cudaError_t e = kvm::launch_score_select(c, q, n_q, index, n_sessions, a, kept_ids, group_scores, head_scores,
+                                           (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_score_select launch");
+}
+
+static kvm_status view_call(kvm_ctx* ctx, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,
+                            const int32_t* block_table, const int64_t* n_tok, int32_t n_sessions,
+                            const int32_t* kept_ids, const uint16_t* q, uint16_t* k_view, uint16_t* v_view,
+                            int32_t* view_len, float* out, void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_sessions == 0) return KVM_OK;
+  if (!k_src || !v_src || !view_len) return fail(KVM_ERR_INVALID_ARG, "NULL K/V source or view_len");
+  if (mode != 1 && (!block_table || !kept_ids || !k_view || !v_view))
+    return fail(KVM_ERR_INVALID_ARG, "NULL block_table, kept_ids or view output");
+  if (mode != 0 && (!q || !out)) return fail(KVM_ERR_INVALID_ARG, "NULL q or out");
+  if (mode != 1 && n_pages < 1) return fail(KVM_ERR_INVALID_ARG, "n_pages=%lld must be >= 1", (long long)n_pages);
+  if (!aligned(k_src, 16) || !aligned(v_src, 16) || !aligned(k_view, 16) || !aligned(v_view, 16) ||
+      !aligned(q, 16) || !aligned(out, 4) || !aligned(view_len, 4) || !aligned(kept_ids, 4))
+    return fail(KVM_ERR_INVALID_ARG, "K/V/q buffers must be 16-byte aligned");
+  SessionArgs a;
+  if (mode == 1) {
+    // the view lengths live on the device: walk every slot of each view, skip the empty ones
+    memset(&a, 0, sizeof(a));
+    int64_t base = 0;
+    for (int i = 0; i < n_sessions; ++i) {
+      a.n_keep[i] = c.budget;
+      a.n_blk[i] = c.budget;
+      a.n_tok[i] = (int64_t)c.budget * kvm::kBlock;
+      a.seg_base[i] = base;
+      base += (int64_t)c.p.h_kv * c.budget;
+    }
+    a.seg_base[n_sessions] = base;
+  } else if ((s = history_args(c, n_tok, n_sessions, &a)) != KVM_OK) {
+    return s;
+  }
+  cudaError_t e = kvm::launch_view(c, mode, k_src, v_src, n_pages, block_table, n_sessions, a, kept_ids, q, k_view,
+                                   v_view, view_len, out, (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "view kernel launch");
+}
+
+kvm_status kvm_materialize(kvm_ctx* ctx, const uint16_t* k_pool, const uint16_t* v_pool, int64_t n_pages,
+                           const int32_t* block_table, const int64_t* n_tok, int32_t n_sessions,
+                           const int32_t* kept_ids, uint16_t* k_view, uint16_t* v_view, int32_t* view_len,
+                           void* stream) {
+  return view_call(ctx, 0, k_pool, v_pool, n_pages, block_table, n_tok, n_sessions, kept_ids, nullptr, k_view,
+                   v_view, view_len, nullptr, stream);
+}
+
+kvm_status kvm_decode_attn(kvm_ctx* ctx, const uint16_t* q, const uint16_t* k_view, const uint16_t* v_view,
+                           const int32_t* view_len, int32_t n_sessions, float* out, void* stream) {
+  return view_call(ctx, 1, k_view, v_view, 0, nullptr, nullptr, n_sessions, nullptr, q, nullptr, nullptr,
+                   const_cast<int32_t*>(view_len), out, stream);
+}
+
+kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint16_t* v_pool, int64_t n_pages,
+                                const int32_t* block_table, const int64_t* n_tok, int32_t n_sessions,
+                                const int32_t* kept_ids, const uint16_t* q, uint16_t* k_view, uint16_t* v_view,
+                                int32_t* view_len, float* out, void* stream) {
+  return view_call(ctx, 2, k_pool, v_pool, n_pages, block_table, n_tok, n_sessions, kept_ids, q, k_view, v_view,
+                   view_len, out, stream);
+}
+
+kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  if (!out) return fail(KVM_ERR_INVALID_ARG, "out is NULL");
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e == cudaSuccess) e = cudaMemcpy(out, ctx->c.status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(ctx->c.status, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) return cuda_fail(e, "kvm_device_status");
+  if (*out == 0) return KVM_OK;
+  if (*out & KVM_DEV_TIMEOUT) return fail(KVM_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", *out);
+  return fail(KVM_ERR_DEVICE, "device status 0x%x (bad page / block id)", *out);
+}
+
+}  // extern "C"

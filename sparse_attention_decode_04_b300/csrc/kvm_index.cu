@@ -1,0 +1,84 @@
+// Step 1 — Mean-K index append.
+//
+// KVMEM reproduction README, "Core equation" (index vector kbar_b per block);
+// Evolve review of KVMem, "Summary" (a position-independent Mean-K index over
+// 32-token blocks).  kbar_b is the mean of the block's pre-RoPE keys,
+// accumulated in fp32.
+//
+// One warp per (session, KV head, block touched by the append).  Lane l owns
+// d/32 consecutive dimensions; the warp walks the block's rows in token order,
+// so every load instruction reads one contiguous 2*d-byte key row.  A partial
+// last block is averaged over the tokens present.  Rows are independent, so
+// re-running an append over the same tokens rewrites the same values.
+#include "kvm_device.cuh"
+#include "kvm_internal.h"
+
+namespace kvm {
+namespace {
+
+constexpr int kWarps = 4;
+
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_t* __restrict__ k_pool,
+                                                                   int64_t n_pages,
+                                                                   const int32_t* __restrict__ bt,
+                                                                   int64_t max_blocks, int h_kv, SessionArgs a,
+                                                                   float* __restrict__ index,
+                                                                   uint32_t* __restrict__ status) {
+  constexpr int PER = D / 32;  // dims per lane
+  const int s = blockIdx.z, g = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t bi = (int64_t)blockIdx.x * kWarps + warp;
+  if (bi >= a.count[s]) return;
+  const int64_t b = a.aux[s] + bi;                         // block id
+  const int64_t present = a.n_tok[s] - b * kBlock;          // tokens of this block present so far
+  const int nv = present >= kBlock ? kBlock : (int)present;
+  const int32_t page = bt[(int64_t)s * max_blocks + b];
+  if (page < 0 || page >= n_pages) {
+    if (lane == 0) atomicOr(status, KVM_DEV_BAD_PAGE);
+    return;
+  }
+  const uint16_t* src = k_pool + ((int64_t)page * h_kv + g) * (int64_t)(kBlock * D) + lane * PER;
+  float acc[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) acc[i] = 0.f;
+#pragma unroll 8
+  for (int t = 0; t < nv; ++t) {
+    if constexpr (PER == 4) {
+      const uint2 w = __ldg(reinterpret_cast<const uint2*>(src + t * D));
+      acc[0] += bf16lo(w.x);
+      acc[1] += bf16hi(w.x);
+      acc[2] += bf16lo(w.y);
+      acc[3] += bf16hi(w.y);
+    } else {
+      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src + t * D));
+      acc[0] += bf16lo(w);
+      acc[1] += bf16hi(w);
+    }
+  }
+  float* dst = index + (((int64_t)s * h_kv + g) * max_blocks + b) * D + lane * PER;
+  const float n = (float)nv;  // 32 for full blocks: the division is then exact
+  if constexpr (PER == 4) {
+    *reinterpret_cast<float4*>(dst) = make_float4(acc[0] / n, acc[1] / n, acc[2] / n, acc[3] / n);
+  } else {
+    *reinterpret_cast<float2*>(dst) = make_float2(acc[0] / n, acc[1] / n);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_index_append(const Ctx& c, const uint16_t* k_pool, int64_t n_pages, const int32_t* bt,
+                                int n_sessions, const SessionArgs& a, int max_count, float* index,
+                                cudaStream_t st) {
+  if (max_count <= 0) return cudaSuccess;
+  dim3 grid((max_count + kWarps - 1) / kWarps, c.p.h_kv, n_sessions);
+  if (c.p.d == 128)
+    index_append_kernel<128><<<grid, kWarps * 32, 0, st>>>(k_pool, n_pages, bt, c.p.max_blocks, c.p.h_kv, a,
+                                                            index, c.status);
+  else
+    index_append_kernel<64><<<grid, kWarps * 32, 0, st>>>(k_pool, n_pages, bt, c.p.max_blocks, c.p.h_kv, a,
+                                                           index, c.status);
+  return cudaGetLastError();
+}
+
+}  // namespace kvm

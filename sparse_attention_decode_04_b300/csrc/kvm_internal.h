@@ -1,0 +1,75 @@
+// Internal interface between the C-ABI layer (kvm_api.cu) and the kernel
+// files: the context object and the per-step launch functions.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvm.h"
+
+namespace kvm {
+
+constexpr int kBlock = 32;            // tokens per block / page
+constexpr int kMaxGroup = 8;          // query heads per KV head
+constexpr int kMaxSessionsHost = 64;  // sessions per call (kernel-parameter arrays)
+
+// Per-session values passed by value to the kernels (they size the grids, so
+// they live on the host; passing them as kernel parameters keeps every call
+// capturable in a CUDA graph).
+struct SessionArgs {
+  int64_t n_tok[kMaxSessionsHost];   // history tokens
+  int64_t aux[kMaxSessionsHost];     // call-specific (first block of an append, ...)
+  int32_t n_blk[kMaxSessionsHost];   // ceil(n_tok / 32)
+  int32_t n_keep[kMaxSessionsHost];  // kept blocks per KV head
+  int32_t count[kMaxSessionsHost];   // call-specific (blocks touched by an append, ...)
+  int64_t seg_base[kMaxSessionsHost + 1];  // flat offset of session s's first kept block over all heads
+};
+
+struct Ctx {
+  kvm_params p;
+  int device = 0;
+  int num_sms = 0;
+  int group = 1;        // h_q / h_kv
+  int budget = 0;       // n_sink + n_recent + top_k
+  int view_ctas = 0;    // persistent CTAs of the view kernels
+  size_t bytes = 0;     // device bytes allocated
+  // scratch (device)
+  float* e_buf = nullptr;      // [S][h_kv][max_blocks][group] exp(s - tile max), log2 domain
+  float2* part = nullptr;      // [S][h_q][max_tiles] (tile max, tile sum) in log2 domain
+  float* rec = nullptr;        // [view_ctas + S*h_kv][group][2 + d] attention partials
+  float* rope_base = nullptr;  // [budget + 1][d/2][2] cos/sin of 32*slot*theta_i
+  float* rope_off = nullptr;   // [32][d/2][2] cos/sin of r*theta_i
+  uint32_t* status = nullptr;  // device status word
+  int64_t max_tiles = 0;
+};
+
+// kvm_index.cu
+cudaError_t launch_index_append(const Ctx& c, const uint16_t* k_pool, int64_t n_pages, const int32_t* bt,
+                                int n_sessions, const SessionArgs& a, int max_count, float* index,
+                                cudaStream_t st);
+
+// kvm_score.cu
+cudaError_t launch_score_select(const Ctx& c, const uint16_t* q, int n_q, const float* index, int n_sessions,
+                                const SessionArgs& a, int32_t* kept, float* group_scores, float* head_scores,
+                                cudaStream_t st);
+
+// kvm_view.cu — mode: 0 materialise, 1 attend over a view, 2 fused
+cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,
+                        const int32_t* bt, int n_sessions, const SessionArgs& a, const int32_t* kept,
+                        const uint16_t* q, uint16_t* k_view, uint16_t* v_view, int32_t* view_len, float* out,
+                        cudaStream_t st);
+
+cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st);
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device), so
+// that steady-state calls (and calls under CUDA-graph capture) make no
+// attribute calls.  `cache` is a per-kernel array indexed by device.
+template <typename F>
+cudaError_t ensure_smem(F* kernel, int device, size_t bytes, int* cache) {
+  if (device >= 0 && device < 64 && cache[device] >= (int)bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && device >= 0 && device < 64) cache[device] = (int)bytes;
+  return e;
+}
+
+}  // namespace kvm

@@ -54,7 +54,7 @@ def _load():
             lib.synth_bf16_rne.restype = ctypes.c_uint16
             lib.synth_topics.argtypes = [u32, i32, i32, i32, i32, P, i64, P]
             lib.synth_topics.restype = None
-            lib.synth_kv_pages.argtypes = [u32, i32, i32, i32, i32, i64, i64, f64, P, i64, P, P, i32]
+            lib.synth_kv_pages.argtypes = [u32, i32, i32, i32, i32, i64, i64, f64, P, i64, P, P, i32, i32, i32]
             lib.synth_kv_pages.restype = i32
             lib.synth_planted.argtypes = [u32, i32, i32, i32, i64, i64, i32, P]
             lib.synth_planted.restype = i32
@@ -202,24 +202,25 @@ def planted(w: Workload, layer: int) -> np.ndarray:
 
 
 def kv_pool(w: Workload, layer: int, bt: np.ndarray | None = None, sessions=None,
-            out_k: np.ndarray | None = None, out_v: np.ndarray | None = None, t_range=None):
-    """bf16 bits (uint16) K and V pools [h_kv][n_pages][32][d] for one layer.
+            out_k: np.ndarray | None = None, out_v: np.ndarray | None = None, t_range=None, heads=None):
+    """bf16 bits (uint16) K and V pools [n_pages][h_kv][32][d] for one layer.
 
-    t_range=(t0, t1) fills only those tokens of each session (the rest of the
-    arrays are left as given).
+    t_range=(t0, t1) fills only those tokens of each session and heads=(lo, hi)
+    only those KV heads (the rest of the arrays are left as given).
     """
     lib = _load()
     if bt is None:
         bt = block_table(w)
-    shape = (w.h_kv, w.n_pages, BLOCK, w.d)
+    shape = (w.n_pages, w.h_kv, BLOCK, w.d)
     k = out_k if out_k is not None else np.zeros(shape, dtype=np.uint16)
     v = out_v if out_v is not None else np.zeros(shape, dtype=np.uint16)
     assert k.shape == shape and v.shape == shape
     t0, t1 = t_range if t_range is not None else (0, w.n_tok)
     for s in (range(w.n_sessions) if sessions is None else sessions):
         row = np.ascontiguousarray(bt[s])
+        h_lo, h_hi = heads if heads is not None else (0, w.h_kv)
         rc = lib.synth_kv_pages(w.session_seed(s), s, layer, w.h_kv, w.d, t0, t1, w.eps_scale,
-                                _ptr(row), w.n_pages, _ptr(k), _ptr(v), threads())
+                                _ptr(row), w.n_pages, _ptr(k), _ptr(v), threads(), h_lo, h_hi)
         if rc != 0:
             raise ValueError(f"synth_kv_pages failed ({rc})")
     return k, v
@@ -252,8 +253,8 @@ def topics(w: Workload, session: int, layer: int, head: int, blocks) -> np.ndarr
 
 @dataclasses.dataclass
 class LayerInputs:
-    k_pool: np.ndarray       # uint16 [h_kv][n_pages][32][d]
-    v_pool: np.ndarray       # uint16 [h_kv][n_pages][32][d]
+    k_pool: np.ndarray       # uint16 [n_pages][h_kv][32][d]
+    v_pool: np.ndarray       # uint16 [n_pages][h_kv][32][d]
     block_table: np.ndarray  # int32 [n_sessions][n_blk]
     q: np.ndarray            # uint16 [n_sessions][n_q][h_q][d]
     planted: np.ndarray      # int64 [n_sessions][h_kv][n_planted]

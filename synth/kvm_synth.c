@@ -114,14 +114,15 @@ void synth_topics(uint32_t seed, int session, int layer, int head, int d, const 
 }
 
 /*
- * Keys and values of tokens [t0, t1) of one session and layer, all KV heads,
- * written straight into a paged pool laid out [h_kv][n_pages][32][d] (bf16 bits).
+ * Keys and values of tokens [t0, t1) of one session and layer, KV heads
+ * [h_lo, h_hi), written straight into a paged pool laid out
+ * [n_pages][h_kv][32][d] (bf16 bits).
  * page_of_block[b] is the physical page of logical block b.
  */
 int synth_kv_pages(uint32_t seed, int session, int layer, int h_kv, int d, int64_t t0, int64_t t1,
                    double eps_scale, const int32_t* page_of_block, int64_t n_pages, uint16_t* k_pool,
-                   uint16_t* v_pool, int n_threads) {
-  if (d % 4 != 0 || d > 1024 || t0 < 0 || t1 < t0) return 1;
+                   uint16_t* v_pool, int n_threads, int h_lo, int h_hi) {
+  if (d % 4 != 0 || d > 1024 || t0 < 0 || t1 < t0 || h_lo < 0 || h_hi > h_kv || h_lo > h_hi) return 1;
   const int64_t b0 = t0 / 32, b1 = (t1 + 31) / 32;
   const int64_t nb = b1 - b0;
   int bad = 0;
@@ -129,7 +130,7 @@ int synth_kv_pages(uint32_t seed, int session, int layer, int h_kv, int d, int64
   if (n_threads > 0) omp_set_num_threads(n_threads);
 #pragma omp parallel for schedule(dynamic, 4) collapse(2) reduction(| : bad)
 #endif
-  for (int h = 0; h < h_kv; ++h) {
+  for (int h = h_lo; h < h_hi; ++h) {
     for (int64_t bi = 0; bi < nb; ++bi) {
       double mu[1024], x[1024];
       const int64_t b = b0 + bi;
@@ -139,8 +140,8 @@ int synth_kv_pages(uint32_t seed, int session, int layer, int h_kv, int d, int64
       const int64_t ta = (b * 32 > t0) ? b * 32 : t0;
       const int64_t tb = (b * 32 + 32 < t1) ? b * 32 + 32 : t1;
       for (int64_t t = ta; t < tb; ++t) {
-        uint16_t* krow = k_pool + (((int64_t)h * n_pages + page) * 32 + (t - b * 32)) * d;
-        uint16_t* vrow = v_pool + (((int64_t)h * n_pages + page) * 32 + (t - b * 32)) * d;
+        uint16_t* krow = k_pool + (((int64_t)page * h_kv + h) * 32 + (t - b * 32)) * d;
+        uint16_t* vrow = v_pool + (((int64_t)page * h_kv + h) * 32 + (t - b * 32)) * d;
         normal_row(seed, TAG_KEY_NOISE, (uint32_t)t, lh_of(layer, h), (uint32_t)session, d, x);
         for (int k = 0; k < d; ++k) x[k] = 0.5 * mu[k] + eps_scale * x[k];
         rms_normalise(x, d);

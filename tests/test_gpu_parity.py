@@ -1,0 +1,214 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on seeded inputs.
+
+Tolerances are listed and derived in tests/harness.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+import sparse_attention_decode_04_b300 as K
+from oracle import kvm_oracle as O
+
+from harness import (LayerOnDevice, check_group_scores, check_head_scores, check_ids, check_index, check_out,
+                     check_view, host_u16, kept_tensor, oracle_keys, oracle_layer)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_full_path(w, li, fused=True, heads=None):
+    ctx = K.Context.for_workload(w)
+    dev = LayerOnDevice(w, li, ctx)
+    dev.index_build()
+    dev.score_select()
+    if fused:
+        dev.fused()
+    else:
+        dev.materialize()
+        dev.attend()
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    return ctx, dev
+
+
+def compare_layer(w, li, dev, session=0, heads=None):
+    ora = oracle_layer(w, li, session, heads=heads)
+    idx = dev.index[session].cpu().numpy()
+    gs = dev.gs[session].cpu().numpy()
+    hs = dev.hs[session].cpu().numpy()
+    kept = dev.kept[session].cpu().numpy()
+    kv, vv = host_u16(dev.k_view[session]), host_u16(dev.v_view[session])
+    vlen = dev.view_len[session].cpu().numpy()
+    out = dev.out[session].cpu().numpy()
+    G = w.group
+    identical = 0
+    for g in (range(w.h_kv) if heads is None else heads):
+        check_index(idx[g, :w.n_blk], oracle_keys(w, li, session, g), ora["index"][g])
+        check_head_scores(hs[G * g:G * (g + 1), :w.n_blk], li.q[session, 0, G * g:G * (g + 1)],
+                          ora["index"][g:g + 1], O.block_scores(li.q[session, 0, G * g:G * (g + 1)], ora["index"][g:g + 1]))
+        check_group_scores(gs[g, :w.n_blk], ora["gs"][g])
+        same = check_ids(kept[g], ora["ids"][g], ora["gs"][g], w)
+        if same:
+            identical += 1
+            L = ora["k_view"][g].shape[0]
+            assert vlen[g] == L
+            check_view(kv[g], vv[g], ora["k_view"][g], ora["v_view"][g])
+            check_out(out[G * g:G * (g + 1)], ora["out"][G * g:G * (g + 1)])
+    return identical
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_tiny_full_path(fused):
+    w = synth.WORKLOADS["tiny_8k_g4_d64"]
+    li = synth.layer_inputs(w, 0)
+    ctx, dev = run_full_path(w, li, fused=fused)
+    assert compare_layer(w, li, dev) == 1
+    ctx.close()
+
+
+def test_gqa40x8_256k_full_path():
+    w = synth.WORKLOADS["gqa40x8_256k"]
+    li = synth.layer_inputs(w, 0)
+    ctx, dev = run_full_path(w, li, fused=True)
+    assert compare_layer(w, li, dev) >= 7      # a near-tie swap may change one head's list
+    ctx.close()
+
+
+def _view_case(w, ids_for_head, fused):
+    li = synth.layer_inputs(w, 0)
+    ctx = K.Context.for_workload(w)
+    dev = LayerOnDevice(w, li, ctx)
+    ids = {(s, g): ids_for_head(g) for s in range(w.n_sessions) for g in range(w.h_kv)}
+    kept = kept_tensor(ids, (w.n_sessions, w.h_kv, ctx.budget))
+    if fused:
+        dev.fused(kept)
+    else:
+        dev.materialize(kept)
+        dev.attend()
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    G = w.group
+    for s in range(w.n_sessions):
+        for g in range(w.h_kv):
+            keys = O.paged_tokens(li.k_pool, li.block_table[s], g, w.n_tok)
+            vals = O.paged_tokens(li.v_pool, li.block_table[s], g, w.n_tok)
+            kv, vv = O.materialize(keys, vals, ids[(s, g)], w.n_tok, w.rope_theta)
+            assert int(dev.view_len[s, g]) == kv.shape[0]
+            check_view(host_u16(dev.k_view[s, g]), host_u16(dev.v_view[s, g]), kv, vv)
+            ref = O.decode_attention(li.q[s, 0, G * g:G * (g + 1)], kv, vv, w.rope_theta)
+            check_out(dev.out[s, G * g:G * (g + 1)].cpu().numpy(), ref)
+    ctx.close()
+
+
+@pytest.mark.parametrize("fused", [True, False])
+@pytest.mark.parametrize("d,h_q,h_kv", [(64, 4, 1), (128, 40, 8), (128, 8, 8), (64, 16, 2)])
+def test_view_and_attention_on_given_ids_ragged_tail(fused, d, h_q, h_kv):
+    # 3000 tokens: 93 full blocks + a 24-token tail; the tail block is kept
+    w = synth.Workload("ragged", h_q=h_q, h_kv=h_kv, d=d, n_tok=3000, n_sink=2, n_recent=3, top_k=20,
+                       rope_theta=1e4 if d == 64 else 1e6, n_planted=4, seed=11)
+    rng = np.random.default_rng(5)
+
+    def ids(g):
+        mid = np.sort(rng.choice(np.arange(2, w.n_blk - 3), size=20, replace=False))
+        return np.concatenate([[0, 1], mid, np.arange(w.n_blk - 3, w.n_blk)])
+    _view_case(w, ids, fused)
+
+
+def test_all_kept_short_history_and_empty_sessions():
+    # 3 sessions in one call: 700 tokens (22 blocks <= budget), 0 tokens, 5000 tokens
+    base = synth.Workload("mixed", h_q=8, h_kv=2, d=128, n_tok=5000, n_sessions=1, n_sink=1, n_recent=2, top_k=30,
+                          rope_theta=1e6, n_planted=4, seed=21)
+    lens = [700, 0, 5000]
+    ctx = K.Context(base.h_q, base.h_kv, base.d, base.n_sink, base.n_recent, base.top_k, base.rope_theta,
+                    max_blocks=base.n_blk, max_sessions=3)
+    # one pool holding the three sessions' pages
+    bt = np.full((3, base.n_blk), -1, dtype=np.int32)
+    # sessions are generated with at least 512 tokens; the call uses only the first n of each
+    per = [synth.layer_inputs(base.with_(n_tok=max(n, 512), seed=21 + s), 0) for s, n in enumerate(lens)]
+    n_pages = sum(p.k_pool.shape[0] for p in per)
+    kp = np.concatenate([p.k_pool for p in per], axis=0)
+    vp = np.concatenate([p.v_pool for p in per], axis=0)
+    off = 0
+    for s, p in enumerate(per):
+        bt[s, :p.block_table.shape[1]] = p.block_table[0] + off
+        off += p.k_pool.shape[0]
+    from harness import dev_u16
+    q = dev_u16(np.stack([p.q[0, 0] for p in per]))
+    index = torch.zeros((3, base.h_kv, base.n_blk, base.d), dtype=torch.float32, device="cuda")
+    kept = torch.full((3, base.h_kv, ctx.budget), -7, dtype=torch.int32, device="cuda")
+    gs = torch.zeros((3, base.h_kv, base.n_blk), dtype=torch.float32, device="cuda")
+    kv = torch.zeros((3, base.h_kv, 32 * ctx.budget, base.d), dtype=torch.bfloat16, device="cuda")
+    vv = torch.zeros_like(kv)
+    vlen = torch.full((3, base.h_kv), -7, dtype=torch.int32, device="cuda")
+    out = torch.full((3, base.h_q, base.d), float("nan"), device="cuda")
+    kpd, vpd, btd = dev_u16(kp), dev_u16(vp), torch.from_numpy(bt).cuda()
+    K.kvm_index_append(ctx, kpd, n_pages, btd, [0, 0, 0], lens, index)
+    K.kvm_score_select(ctx, q, 1, index, lens, kept, gs)
+    K.kvm_materialize_attn(ctx, kpd, vpd, n_pages, btd, lens, kept, q, kv, vv, vlen, out)
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    G = base.group
+    for s, n in enumerate(lens):
+        if n == 0:
+            assert (kept[s].cpu().numpy() == -1).all() and (vlen[s].cpu().numpy() == 0).all()
+            assert torch.all(out[s] == 0)
+            continue
+        n_blk = -(-n // 32)
+        keys = [O.paged_tokens(kp, bt[s], h, n) for h in range(base.h_kv)]
+        idx = np.stack([O.mean_k_index(k) for k in keys])
+        gs_o = O.gqa_softmax_sum(O.block_scores(per[s].q[0, 0], idx), base.h_kv)
+        for g in range(base.h_kv):
+            ids = kept[s, g].cpu().numpy()
+            ora_ids = O.select_blocks(gs_o[g], n_blk, base.n_sink, base.n_recent, base.top_k)
+            if n_blk <= ctx.budget:
+                assert ora_ids.tolist() == list(range(n_blk))
+            check_index(index[s, g, :n_blk].cpu().numpy(), keys[g], idx[g])
+            check_group_scores(gs[s, g, :n_blk].cpu().numpy(), gs_o[g])
+            if not check_ids(ids, ora_ids, gs_o[g], base.with_(n_tok=n)):
+                continue
+            vals = O.paged_tokens(vp, bt[s], g, n)
+            k_o, v_o = O.materialize(keys[g], vals, ora_ids, n, base.rope_theta)
+            assert int(vlen[s, g]) == k_o.shape[0]
+            check_view(host_u16(kv[s, g]), host_u16(vv[s, g]), k_o, v_o)
+            ref = O.decode_attention(per[s].q[0, 0, G * g:G * (g + 1)], k_o, v_o, base.rope_theta)
+            check_out(out[s, G * g:G * (g + 1)].cpu().numpy(), ref)
+    ctx.close()
+
+
+def test_index_append_in_ragged_pieces_equals_full_build():
+    w = synth.WORKLOADS["gqa40x8_256k"].with_(n_tok=20000)
+    li = synth.layer_inputs(w, 0)
+    ctx = K.Context.for_workload(w)
+    dev = LayerOnDevice(w, li, ctx)
+    dev.index_build()
+    full = dev.index.clone()
+    dev.index.zero_()
+    done = 0
+    for piece in [45, 19, 3000, 1, 64, 6871, 10000]:
+        K.kvm_index_append(ctx, dev.k_pool, dev.n_pages, dev.bt, [done], [piece], dev.index)
+        done += piece
+    assert done == w.n_tok
+    torch.cuda.synchronize()
+    assert torch.equal(dev.index, full)
+    for g in range(w.h_kv):
+        keys = oracle_keys(w, li, 0, g)
+        check_index(full[0, g, :w.n_blk].cpu().numpy(), keys, O.mean_k_index(keys))
+    ctx.close()
+
+
+def test_bad_page_is_reported_not_faulted():
+    w = synth.WORKLOADS["tiny_8k_g4_d64"]
+    li = synth.layer_inputs(w, 0)
+    ctx = K.Context.for_workload(w)
+    dev = LayerOnDevice(w, li, ctx)
+    dev.index_build()
+    dev.score_select()
+    torch.cuda.synchronize()
+    victim = int(dev.kept[0, 0, 5])
+    dev.bt[0, victim] = w.n_pages + 1000          # outside the pool: the kernel must skip it
+    dev.fused()
+    st = K.kvm_device_status(ctx, clear=True)
+    assert st & K.DEV_BAD_PAGE
+    assert K.kvm_device_status(ctx) == 0          # cleared
+    assert torch.isfinite(dev.out).all()
+    ctx.close()

@@ -25,7 +25,7 @@ def test_recipe_statistics_and_determinism():
     q = O.bf16_to_f64(a.q)
     assert np.allclose(np.mean(q ** 2, axis=-1), 1.0, atol=1e-2)
     # within a block, keys share the topic: same-block key pairs correlate, cross-block ones do not
-    kk = k[0, :, :, :].reshape(-1, 32, w.d)
+    kk = k[:, 0].reshape(-1, 32, w.d)
     same = np.mean(np.sum(kk[:, 0] * kk[:, 1], axis=-1)) / w.d
     cross = np.mean(np.sum(kk[:-1, 0] * kk[1:, 0], axis=-1)) / w.d
     assert 0.15 < same < 0.25 and abs(cross) < 0.03          # 0.25 / 1.25 = 0.2 expected
