@@ -123,11 +123,8 @@ def oracle_sample(w: synth.Workload, reps: int, warmup: int):
     Returns (seconds per sampled (layer, KV head) step, BLAS threads, description).
     """
     from oracle import kvm_oracle as O
-    try:
-        from threadpoolctl import threadpool_info
-        threads = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
-    except Exception:
-        threads = 1
+    from threadpoolctl import threadpool_limits
+    threads = 1  # numpy elementwise work is single-threaded; BLAS is pinned to one thread to match
     g = 0
     bt = synth.block_table(w)
     k, v = synth.kv_pool(w, 0, bt, sessions=[0], heads=(g, g + 1))
@@ -139,6 +136,7 @@ def oracle_sample(w: synth.Workload, reps: int, warmup: int):
     G = w.group
     qg = q[G * g:G * (g + 1)]
     times = []
+    limiter = threadpool_limits(limits=threads)
     for i in range(warmup + reps):
         t0 = time.perf_counter()
         idx = O.index_append(hist_index, keys, n_hist, w.append_tok) if w.append_tok else O.mean_k_index(keys)
@@ -148,6 +146,7 @@ def oracle_sample(w: synth.Workload, reps: int, warmup: int):
         O.decode_attention(qg, kv, vv, w.rope_theta)
         if i >= warmup:
             times.append(time.perf_counter() - t0)
+    limiter.unregister()
     desc = (f"oracle on KV head 0 of layer 0 of {w.name} (append {w.append_tok} tokens, score {w.n_blk} blocks for "
             f"{G} query heads, select, materialise {len(ids)} blocks, attend); per-layer value = 8 heads x that time")
     return statistics.median(times), threads, desc
@@ -206,7 +205,7 @@ def run_kvm(args, w):
         K.kvm_index_append(ctx, k, n_pages, bt, [0] * S, [n_hist] * S, idx)  # the history before this step
         index.append(idx)
         outs.append(torch.empty((S, w.h_q, w.d), dtype=torch.float32, device=dev))
-    kept = torch.empty((S, w.h_kv, ctx.budget), dtype=torch.int32, device=dev)
+    kept = [torch.empty((S, w.h_kv, ctx.budget), dtype=torch.int32, device=dev) for _ in range(L)]
     k_view = torch.empty((S, w.h_kv, BLOCK * ctx.budget, w.d), dtype=torch.bfloat16, device=dev)
     v_view = torch.empty_like(k_view)
     view_len = torch.empty((S, w.h_kv), dtype=torch.int32, device=dev)
@@ -215,45 +214,65 @@ def run_kvm(args, w):
     n_tok = [w.n_tok] * S
     launches_per_layer = (1 if w.append_tok else 0) + 2 + 2
 
-    def layer_calls(layer, ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def call_append(layer):
         if w.append_tok:
             K.kvm_index_append(ctx, kp[layer], n_pages, bt, [n_hist] * S, [w.append_tok] * S, index[layer])
-        if ev is not None:
-            ev[1].record(stream)
-        K.kvm_score_select(ctx, qs[layer], 1, index[layer], n_tok, kept)
-        if ev is not None:
-            ev[2].record(stream)
-        K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept, qs[layer], k_view, v_view,
-                               view_len, outs[layer])
-        if ev is not None:
-            ev[3].record(stream)
+
+    def call_select(layer):
+        K.kvm_score_select(ctx, qs[layer], 1, index[layer], n_tok, kept[layer])
+
+    def call_view(layer):
+        K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer], qs[layer], k_view,
+                               v_view, view_len, outs[layer])
 
     def step():
         for layer in range(L):
-            layer_calls(layer)
+            call_append(layer)
+            call_select(layer)
+            call_view(layer)
+
+    stage_fns = {"index_append": call_append, "score_select": call_select, "materialize_attn": call_view}
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert K.kvm_device_status(ctx) == 0
 
-    # CUDA graph of one whole step (all layers)
-    graph = None
-    if not args.no_graph:
-        graph = torch.cuda.CUDAGraph()
-        side = torch.cuda.Stream()
-        side.wait_stream(stream)
+    if args.profile_step:
+        # one eager step between cudaProfilerStart/Stop, for `ncu --profile-from-start off`
+        torch.cuda.profiler.start()
+        step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        if rank == 0:
+            print(json.dumps({"profile_step": w.name, "launches": launches_per_layer * L}), flush=True)
+        return
+
+    # CUDA graphs: one whole step (all layers), and each stage alone over all layers (per-call durations)
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(side):
-            step()  # warm the side stream
+            fn()  # warm the side stream
         torch.cuda.synchronize()
-        with torch.cuda.graph(graph, stream=side):
-            step()
+        with torch.cuda.graph(g, stream=side):
+            fn()
         torch.cuda.synchronize()
-        for _ in range(max(1, args.warmup)):
+        return g
+
+    graph = capture(step) if not args.no_graph else None
+    stage_graphs = {}
+    if not args.no_graph:
+        for name, fn in stage_fns.items():
+            stage_graphs[name] = capture(lambda fn=fn: [fn(layer) for layer in range(L)])
+    for _ in range(max(1, args.warmup)):
+        if graph is not None:
             graph.replay()
-        torch.cuda.synchronize()
+        else:
+            step()
+    torch.cuda.synchronize()
 
     gpu_index = local
     if os.environ.get("CUDA_VISIBLE_DEVICES"):
@@ -265,42 +284,26 @@ def run_kvm(args, w):
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    with sampler:
-        time.sleep(0.3)
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for _ in range(args.steps):
-            if graph is not None:
-                graph.replay()
-            else:
-                step()
-        t1.record(stream)
-        torch.cuda.synchronize()
-        step_ms = t0.elapsed_time(t1) / args.steps
-        # per-call durations: the same steps launched call by call with events on the launching stream
-        evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(L)]
-               for _ in range(args.steps)]
+
+    def timed(fn, reps):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for s_ in range(args.steps):
-            for layer in range(L):
-                layer_calls(layer, evs[s_][layer])
+        for _ in range(reps):
+            fn()
         e1.record(stream)
         torch.cuda.synchronize()
-    eager_ms = e0.elapsed_time(e1) / args.steps
+        return e0.elapsed_time(e1) / reps
+
+    with sampler:
+        time.sleep(0.3)
+        step_ms = timed(graph.replay if graph is not None else step, args.steps)
+        stage_ms = {name: timed(g.replay, args.steps) for name, g in stage_graphs.items()}
     st = K.kvm_device_status(ctx)
     if st != 0:
         raise RuntimeError(f"device status 0x{st:x} after the timed region")
-    stage = {"index_append": [], "score_select": [], "materialize_attn": []}
-    for s_ in range(args.steps):
-        for layer in range(L):
-            e = evs[s_][layer]
-            stage["index_append"].append(e[0].elapsed_time(e[1]) * 1e3)
-            stage["score_select"].append(e[1].elapsed_time(e[2]) * 1e3)
-            stage["materialize_attn"].append(e[2].elapsed_time(e[3]) * 1e3)
-    stage_us = {k: round(statistics.mean(v), 2) for k, v in stage.items()}
+    stage_us = {name: round(ms * 1e3 / L, 2) for name, ms in stage_ms.items()}
+    eager_ms = timed(step, max(1, min(args.steps, 3)))
 
     if world > 1:
         t = torch.tensor([step_ms, eager_ms], device=dev)
@@ -312,7 +315,7 @@ def run_kvm(args, w):
     gbs = bytes_layer / (us_layer * 1e-6) / 1e9 * world
     peak, peak_kind = load_peaks()
     vb = view_call_bytes(w)
-    view_us = stage_us["materialize_attn"]
+    view_us = stage_us.get("materialize_attn") or us_layer
     achieved = vb / (view_us * 1e-6) / 1e9
 
     # end-to-end through the public API with host buffers: H2D of the step's queries and new K/V pages,
@@ -342,8 +345,8 @@ def run_kvm(args, w):
                     vp[layer][p0:p0 + app_blocks].copy_(new_v[layer], non_blocking=True)
                 if w.append_tok:
                     K.kvm_index_append(ctx, kp[layer], n_pages, bt, [n_hist] * S, [w.append_tok] * S, index[layer])
-                K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept)
-                K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept, q_dev[layer], k_view,
+                K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept[layer])
+                K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer], q_dev[layer], k_view,
                                        v_view, view_len, outs[layer])
             for layer in range(L):
                 out_host[layer].copy_(outs[layer], non_blocking=True)
@@ -390,13 +393,13 @@ def run_kvm(args, w):
                        "parallelism": f"replicas x{world}"},
             "hbm_gbps": round(gbs, 1), "must_touch_bytes_per_layer": bytes_layer,
             "hbm_frac_of_measured": round(bytes_layer / (us_layer * 1e-6) / 1e9 / peak, 4),
-            "stages_us_per_layer": stage_us, "ms_per_step_eager": round(eager_ms, 4),
+            "stages_us_per_layer": stage_us, "ms_per_step_eager_untimed": round(eager_ms, 4),
             "roofline": {"bound": "hbm", "kernel": "kvm_materialize_attn (view kernel + combine)",
                          "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes_per_launch": vb},
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_layer * L * args.steps * 2,
+            "gpu_launches": launches_per_layer * L * args.steps * (2 if stage_graphs else 1),
             "clocks": sampler.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -425,6 +428,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="after warm-up, run one step between cudaProfilerStart/Stop and exit (for ncu)")
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

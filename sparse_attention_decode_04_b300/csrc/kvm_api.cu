@@ -6,7 +6,10 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <map>
+#include <mutex>
 #include <new>
+#include <utility>
 
 #include "kvm.h"
 #include "kvm_internal.h"
@@ -79,6 +82,17 @@ kvm_status history_args(const Ctx& c, const int64_t* n_tok, int32_t n_sessions, 
 
 }  // namespace
 
+cudaError_t kvm::ensure_smem_impl(const void* kernel, int device, size_t bytes) {
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> limit;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& cur = limit[{kernel, device}];
+  if (cur >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) cur = bytes;
+  return e;
+}
+
 extern "C" {
 
 const char* kvm_status_string(kvm_status s) {
@@ -136,9 +150,10 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   const size_t sz_rec = ((size_t)c.view_ctas + S * p->h_kv) * c.group * (2 + p->d) * sizeof(float);
   const size_t sz_base = (size_t)(budget + 1) * (p->d / 2) * sizeof(float2);
   const size_t sz_off = (size_t)32 * (p->d / 2) * sizeof(float2);
-  void* ptrs[6] = {};
-  const size_t sizes[6] = {sz_e, sz_part, sz_rec, sz_base, sz_off, 256};
-  for (int i = 0; i < 6 && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], sizes[i]);
+  constexpr int kBufs = 8;
+  void* ptrs[kBufs] = {};
+  const size_t sizes[kBufs] = {sz_e, sz_part, sz_rec, sz_base, sz_off, 256, 2 * sz_base, 2 * sz_off};
+  for (int i = 0; i < kBufs && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], sizes[i]);
   if (e != cudaSuccess) {
     for (void* q : ptrs)
       if (q) cudaFree(q);
@@ -151,6 +166,8 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   c.rope_base = (float*)ptrs[3];
   c.rope_off = (float*)ptrs[4];
   c.status = (uint32_t*)ptrs[5];
+  c.rope_base64 = (double*)ptrs[6];
+  c.rope_off64 = (double*)ptrs[7];
   for (size_t s : sizes) c.bytes += s;
   e = cudaMemset(c.status, 0, 256);
   if (e == cudaSuccess) e = kvm::launch_rope_tables(c, 0);
@@ -170,7 +187,7 @@ kvm_status kvm_destroy(kvm_ctx* ctx) {
   cudaGetDevice(&prev);
   if (prev != c.device) cudaSetDevice(c.device);
   cudaError_t e = cudaDeviceSynchronize();
-  void* ptrs[6] = {c.e_buf, c.part, c.rec, c.rope_base, c.rope_off, c.status};
+  void* ptrs[8] = {c.e_buf, c.part, c.rec, c.rope_base, c.rope_off, c.status, c.rope_base64, c.rope_off64};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   if (prev >= 0 && prev != c.device) cudaSetDevice(prev);

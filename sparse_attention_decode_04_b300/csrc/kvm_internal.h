@@ -39,6 +39,8 @@ struct Ctx {
   float* rec = nullptr;        // [view_ctas + S*h_kv][group][2 + d] attention partials
   float* rope_base = nullptr;  // [budget + 1][d/2][2] cos/sin of 32*slot*theta_i
   float* rope_off = nullptr;   // [32][d/2][2] cos/sin of r*theta_i
+  double* rope_base64 = nullptr;  // the same tables in fp64 (cancellation fallback)
+  double* rope_off64 = nullptr;
   uint32_t* status = nullptr;  // device status word
   int64_t max_tiles = 0;
 };
@@ -61,15 +63,14 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
 
 cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st);
 
-// Raises a kernel's dynamic shared-memory limit once per (kernel, device), so
-// that steady-state calls (and calls under CUDA-graph capture) make no
-// attribute calls.  `cache` is a per-kernel array indexed by device.
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on `device`.
+// The limit only ever grows, and each (kernel, device) pair is configured once
+// per size, so steady-state calls (and calls under CUDA-graph capture) make no
+// attribute calls.  Defined in kvm_api.cu.
+cudaError_t ensure_smem_impl(const void* kernel, int device, size_t bytes);
 template <typename F>
-cudaError_t ensure_smem(F* kernel, int device, size_t bytes, int* cache) {
-  if (device >= 0 && device < 64 && cache[device] >= (int)bytes) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e == cudaSuccess && device >= 0 && device < 64) cache[device] = (int)bytes;
-  return e;
+cudaError_t ensure_smem(F* kernel, int device, size_t bytes) {
+  return ensure_smem_impl(reinterpret_cast<const void*>(kernel), device, bytes);
 }
 
 }  // namespace kvm

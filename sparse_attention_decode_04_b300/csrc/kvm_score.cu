@@ -401,8 +401,7 @@ cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_
   const int tiles = (max_blk + rpt - 1) / rpt;
   const size_t smem_a = (size_t)kStages * kStageRows * D * 4 + (size_t)rpt * G * 4;
   auto ka = score_tile_kernel<D, G>;
-  static int cache_a[64] = {};
-  cudaError_t e = ensure_smem(ka, c.device, smem_a, cache_a);
+  cudaError_t e = ensure_smem(ka, c.device, smem_a);
   if (e != cudaSuccess) return e;
   ka<<<dim3(tiles, c.p.h_kv, n_sessions), kScoreThreads, smem_a, st>>>(
       q, index, c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.e_buf, c.part, c.max_tiles, head_scores, c.status);
@@ -414,8 +413,7 @@ cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_
   const int tiles_cap = slice_cap / rpt + 2;
   const size_t smem_b = (size_t)slice_cap * 4 + (size_t)tiles_cap * G * 4;
   auto kb = select_kernel<G>;
-  static int cache_b[64] = {};
-  if ((e = ensure_smem(kb, c.device, smem_b, cache_b)) != cudaSuccess) return e;
+  if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C, c.p.h_kv, n_sessions);
   cfg.blockDim = dim3(kSelectThreads);

@@ -55,6 +55,8 @@ struct ViewParams {
   float* rec;
   const float2* rope_base;  // [budget + 1][d/2]
   const float2* rope_off;   // [32][d/2]
+  const double2* rope_base64;  // fp64 copies, read only on the cancellation fallback
+  const double2* rope_off64;
   float* out;
   uint32_t* status;
   int64_t total;  // kept blocks over all (session, KV head)
@@ -364,7 +366,7 @@ __global__ void __launch_bounds__(Geo<D>::NT, 1) view_kernel(const ViewParams vp
           uint32_t o1[4], o2[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            float yv1[2], yv2[2];
+            uint32_t h1[2], h2[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int v = 2 * u + e;
@@ -372,11 +374,25 @@ __global__ void __launch_bounds__(Geo<D>::NT, 1) view_kernel(const ViewParams vp
               rope_cs(bb[v], off[v], cs_, sn_);
               const float x1 = e ? bf16hi(ka[u]) : bf16lo(ka[u]);
               const float x2 = e ? bf16hi(kb[u]) : bf16lo(kb[u]);
-              yv1[e] = fmaf(x1, cs_, -x2 * sn_);
-              yv2[e] = fmaf(x2, cs_, x1 * sn_);
+              const float f1 = fmaf(x1, cs_, -x2 * sn_);
+              const float f2 = fmaf(x2, cs_, x1 * sn_);
+              // fp32 tables put |error| <= 3e-7 (|x1| + |x2|) on f; that stays below one bf16 ulp of the
+              // result unless the rotation cancels (|f| < ~8e-5 (|x1| + |x2|)).  Those pairs are redone
+              // from the fp64 tables so the stored key is always within one ulp of the exact rotation.
+              const float tau = 0x1p-12f * (fabsf(x1) + fabsf(x2));
+              if (fabsf(f1) < tau || fabsf(f2) < tau) {
+                const double2 b64 = vp.rope_base64[(int64_t)cur.i * (D / 2) + 8 * cp + v];
+                const double2 o64 = vp.rope_off64[r * (D / 2) + 8 * cp + v];
+                const double c64 = b64.x * o64.x - b64.y * o64.y, s64 = b64.y * o64.x + b64.x * o64.y;
+                h1[e] = __bfloat16_as_ushort(__double2bfloat16((double)x1 * c64 - (double)x2 * s64));
+                h2[e] = __bfloat16_as_ushort(__double2bfloat16((double)x2 * c64 + (double)x1 * s64));
+              } else {
+                h1[e] = __bfloat16_as_ushort(__float2bfloat16_rn(f1));
+                h2[e] = __bfloat16_as_ushort(__float2bfloat16_rn(f2));
+              }
             }
-            o1[u] = pack_bf16x2(yv1[0], yv1[1]);
-            o2[u] = pack_bf16x2(yv2[0], yv2[1]);
+            o1[u] = h1[0] | (h1[1] << 16);
+            o2[u] = h2[0] | (h2[1] << 16);
             y1[2 * u] = bf16lo(o1[u]);
             y1[2 * u + 1] = bf16hi(o1[u]);
             y2[2 * u] = bf16lo(o2[u]);
@@ -485,12 +501,16 @@ __global__ void combine_kernel(const ViewParams vp, const SessionArgs a, int att
   if (!attend) return;
   const int64_t start = a.seg_base[s] + (int64_t)g * nk, end = start + nk - 1;
   const int c0 = cta_of(start, vp.total, vp.P), c1 = cta_of(end, vp.total, vp.P);
+  // CTAs between c0 and c1 with an empty share wrote no record: skip them
+  auto empty = [&](int c) { return cta_begin(c, vp.total, vp.P) >= cta_begin(c + 1, vp.total, vp.P); };
   float M = -INFINITY;
-  for (int c = c0; c <= c1; ++c) M = fmaxf(M, vp.rec[((int64_t)(c + q) * G + hh) * (2 + D)]);
+  for (int c = c0; c <= c1; ++c)
+    if (!empty(c)) M = fmaxf(M, vp.rec[((int64_t)(c + q) * G + hh) * (2 + D)]);
   for (int dim = threadIdx.x; dim < D; dim += blockDim.x) {
     float av = 0.f, lv = 0.f;
     if (M != -INFINITY) {
       for (int c = c0; c <= c1; ++c) {
+        if (empty(c)) continue;
         const float* rc = vp.rec + ((int64_t)(c + q) * G + hh) * (2 + D);
         const float sc = exp2f(rc[0] - M);
         av = fmaf(rc[2 + dim], sc, av);
@@ -510,8 +530,7 @@ cudaError_t launch_dg(const Ctx& c, int mode, const ViewParams& vp, const Sessio
   if (vp.total > 0) {
     void (*kern)(const ViewParams, const SessionArgs) =
         mode == 0 ? view_kernel<D, G, 0> : (mode == 1 ? view_kernel<D, G, 1> : view_kernel<D, G, 2>);
-    static int cache[3][64] = {};
-    if ((e = ensure_smem(kern, c.device, smem, cache[mode])) != cudaSuccess) return e;
+    if ((e = ensure_smem(kern, c.device, smem)) != cudaSuccess) return e;
     kern<<<vp.P, Q::NT, smem, st>>>(vp, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -534,9 +553,10 @@ cudaError_t launch_d(const Ctx& c, int mode, const ViewParams& vp, const Session
   return cudaErrorInvalidValue;
 }
 
-// fp64 RoPE tables: base[slot][i] = (cos, sin)(32*slot*theta_i), off[r][i] = (cos, sin)(r*theta_i),
-// theta_i = rope_theta^(-2i/d).
-__global__ void rope_table_kernel(float2* base, int n_slots, float2* off, int d, double rope_theta) {
+// RoPE tables computed in fp64: base[slot][i] = (cos, sin)(32*slot*theta_i), off[r][i] = (cos, sin)(r*theta_i),
+// theta_i = rope_theta^(-2i/d); stored as fp32 and as fp64.
+__global__ void rope_table_kernel(float2* base, int n_slots, float2* off, double2* base64, double2* off64, int d,
+                                  double rope_theta) {
   const int half = d / 2;
   const int64_t n = (int64_t)(n_slots + 32) * half;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
@@ -547,9 +567,11 @@ __global__ void rope_table_kernel(float2* base, int n_slots, float2* off, int d,
     if (row < n_slots) {
       sincos(32.0 * (double)row * inv_freq, &sn, &cs);
       base[row * half + i] = make_float2((float)cs, (float)sn);
+      base64[row * half + i] = make_double2(cs, sn);
     } else {
       sincos((double)(row - n_slots) * inv_freq, &sn, &cs);
       off[(row - n_slots) * half + i] = make_float2((float)cs, (float)sn);
+      off64[(row - n_slots) * half + i] = make_double2(cs, sn);
     }
   }
 }
@@ -574,6 +596,8 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
   vp.rec = c.rec;
   vp.rope_base = reinterpret_cast<const float2*>(c.rope_base);
   vp.rope_off = reinterpret_cast<const float2*>(c.rope_off);
+  vp.rope_base64 = reinterpret_cast<const double2*>(c.rope_base64);
+  vp.rope_off64 = reinterpret_cast<const double2*>(c.rope_off64);
   vp.out = out;
   vp.status = c.status;
   vp.total = a.seg_base[n_sessions];
@@ -588,7 +612,9 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
 
 cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st) {
   rope_table_kernel<<<256, 256, 0, st>>>(reinterpret_cast<float2*>(c.rope_base), c.budget + 1,
-                                         reinterpret_cast<float2*>(c.rope_off), c.p.d, (double)c.p.rope_theta);
+                                         reinterpret_cast<float2*>(c.rope_off),
+                                         reinterpret_cast<double2*>(c.rope_base64),
+                                         reinterpret_cast<double2*>(c.rope_off64), c.p.d, (double)c.p.rope_theta);
   return cudaGetLastError();
 }
 
