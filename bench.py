@@ -117,14 +117,10 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
-def oracle_sample(w: synth.Workload, reps: int, warmup: int):
-    """Times the oracle on one KV head of layer 0 (the step's work for that head), per step.
-
-    Returns (seconds per sampled (layer, KV head) step, BLAS threads, description).
-    """
+def _oracle_child(name: str, reps: int, warmup: int):
+    """Child-process body: times the oracle on one KV head of layer 0 and prints JSON."""
     from oracle import kvm_oracle as O
-    from threadpoolctl import threadpool_limits
-    threads = 1  # numpy elementwise work is single-threaded; BLAS is pinned to one thread to match
+    w = synth.WORKLOADS[name]
     g = 0
     bt = synth.block_table(w)
     k, v = synth.kv_pool(w, 0, bt, sessions=[0], heads=(g, g + 1))
@@ -135,21 +131,36 @@ def oracle_sample(w: synth.Workload, reps: int, warmup: int):
     hist_index = O.mean_k_index(keys[:n_hist]) if n_hist > 0 else np.zeros((0, w.d))
     G = w.group
     qg = q[G * g:G * (g + 1)]
-    times = []
-    limiter = threadpool_limits(limits=threads)
+    times, n_keep = [], 0
+    static_idx = None if w.append_tok else O.mean_k_index(keys)  # no append: the index is state, as on the GPU
     for i in range(warmup + reps):
         t0 = time.perf_counter()
-        idx = O.index_append(hist_index, keys, n_hist, w.append_tok) if w.append_tok else O.mean_k_index(keys)
+        idx = O.index_append(hist_index, keys, n_hist, w.append_tok) if w.append_tok else static_idx
         gs = O.gqa_softmax_sum(O.block_scores(qg, idx[None]), 1)[0]
         ids = O.select_blocks(gs, w.n_blk, w.n_sink, w.n_recent, w.top_k)
         kv, vv = O.materialize(keys, vals, ids, w.n_tok, w.rope_theta)
         O.decode_attention(qg, kv, vv, w.rope_theta)
+        n_keep = len(ids)
         if i >= warmup:
             times.append(time.perf_counter() - t0)
-    limiter.unregister()
-    desc = (f"oracle on KV head 0 of layer 0 of {w.name} (append {w.append_tok} tokens, score {w.n_blk} blocks for "
-            f"{G} query heads, select, materialise {len(ids)} blocks, attend); per-layer value = 8 heads x that time")
-    return statistics.median(times), threads, desc
+    print(json.dumps({"seconds": statistics.median(times), "n_keep": n_keep, "reps": len(times)}), flush=True)
+
+
+def oracle_sample(w: synth.Workload, reps: int, warmup: int):
+    """Times the oracle on one KV head of layer 0 (the step's work for that head), in a child
+    process with every BLAS / OpenMP pool pinned to one thread (so `cores` is exact).
+
+    Returns (seconds per sampled (layer, KV head) step, threads used, description).
+    """
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", w.name, str(reps), str(warmup)],
+                       capture_output=True, text=True, env=env, check=True)
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    desc = (f"oracle (numpy fp64, 1 thread) on KV head 0 of layer 0 of {w.name}: append {w.append_tok} tokens, "
+            f"score {w.n_blk} blocks for {w.group} query heads, select, materialise {res['n_keep']} blocks, attend; "
+            f"per-layer value = {w.h_kv * w.n_sessions} (session, KV head) units x that time")
+    return res["seconds"], 1, desc
 
 
 def run_reference(args, w):
@@ -430,6 +441,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-step", action="store_true",
                     help="after warm-up, run one step between cudaProfilerStart/Stop and exit (for ncu)")
+    if len(sys.argv) > 1 and sys.argv[1] == "--oracle-child":
+        _oracle_child(sys.argv[2], int(sys.argv[3]), int(sys.argv[4]))
+        return
     args = ap.parse_args()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)

@@ -81,6 +81,29 @@ def mean_k_index(keys_bits) -> np.ndarray:
     return out
 
 
+def mean_k_index_bf16(keys_bits) -> np.ndarray:
+    """Mean-K vectors as the bf16 operand of step-level (tensor-core) scoring: uint16 [n_blk][d].
+
+    READING: the step-level scoring contraction takes bf16 operands, so the
+    index is rounded to bf16 first.  That rounding is a quantisation decided in
+    floating point, so it is taken in the kernel's precision: the block's keys
+    are summed in fp32 in token order, divided by the token count in fp32, and
+    the fp32 mean is rounded to bf16 (nearest even).
+    """
+    k = bf16_to_f64(keys_bits).astype(np.float32)
+    n_tok, d = k.shape
+    n_blk = -(-n_tok // BLOCK)
+    acc = np.zeros((n_blk, d), dtype=np.float32)
+    cnt = np.zeros(n_blk, dtype=np.float32)
+    for t in range(BLOCK):                       # token order within each block
+        rows = np.arange(t, n_blk * BLOCK, BLOCK)
+        rows = rows[rows < n_tok]
+        acc[rows // BLOCK] = acc[rows // BLOCK] + k[rows]
+        cnt[rows // BLOCK] += 1
+    mean32 = (acc / cnt[:, None]).astype(np.float32)
+    return f64_to_bf16(mean32.astype(np.float64))
+
+
 def index_append(index, keys_bits, tok_begin: int, n_tok: int) -> np.ndarray:
     """Index after tokens [tok_begin, tok_begin + n_tok) were appended.
 
@@ -133,6 +156,11 @@ def gqa_softmax_sum(s, h_kv: int) -> np.ndarray:
     p = np.exp(s - s.max(axis=1, keepdims=True))
     p /= p.sum(axis=1, keepdims=True)
     return p.reshape(h_kv, h_q // h_kv, n_blk).sum(axis=1)
+
+
+def step_group_scores_bf16(q_steps_bits, index_bf16_bits) -> np.ndarray:
+    """Step-level group scores with the bf16 index operand (fp64 arithmetic on the bf16 values)."""
+    return step_group_scores(q_steps_bits, bf16_to_f64(index_bf16_bits))
 
 
 def step_group_scores(q_steps_bits, index) -> np.ndarray:

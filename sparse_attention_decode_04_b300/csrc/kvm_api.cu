@@ -129,6 +129,8 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   if (p->max_sessions < 1 || p->max_sessions > kvm::kMaxSessionsHost)
     return fail(KVM_ERR_SHAPE, "max_sessions=%d outside [1, %d]", p->max_sessions, kvm::kMaxSessionsHost);
   if (p->max_queries < 1) return fail(KVM_ERR_SHAPE, "max_queries must be >= 1");
+  if ((int64_t)p->max_queries * (p->h_q / (p->h_kv > 0 ? p->h_kv : 1)) > 8192)
+    return fail(KVM_ERR_SHAPE, "max_queries * group must be <= 8192");
 
   kvm_ctx* ctx = new (std::nothrow) kvm_ctx();
   if (!ctx) return fail(KVM_ERR_CUDA, "host allocation failed");
@@ -166,9 +168,29 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   c.rope_base = (float*)ptrs[3];
   c.rope_off = (float*)ptrs[4];
   c.status = (uint32_t*)ptrs[5];
-  c.rope_base64 = (double*)ptrs[6];
-  c.rope_off64 = (double*)ptrs[7];
+  c.rope_base_hl = (float4*)ptrs[6];
+  c.rope_off_hl = (float4*)ptrs[7];
   for (size_t s : sizes) c.bytes += s;
+  if (p->max_queries > 1) {
+    c.step_blk_cap_pad = (p->max_blocks + 255) / 256 * 256;
+    c.step_rows_cap_pad = (int)(((int64_t)p->max_queries * c.group + 255) / 256 * 256);
+    const size_t SG = S * p->h_kv;
+    const size_t sz[5] = {SG * c.step_blk_cap_pad * p->d * 2, SG * c.step_rows_cap_pad * p->d * 2,
+                          SG * kvm::kStepMaxRanges * c.step_rows_cap_pad * sizeof(float2),
+                          SG * c.step_rows_cap_pad * sizeof(float2), SG * p->max_blocks * sizeof(float)};
+    void* q5[5] = {};
+    for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaMalloc(&q5[i], sz[i]);
+    c.step_kpk = (uint16_t*)q5[0];
+    c.step_qpk = (uint16_t*)q5[1];
+    c.step_part = (float2*)q5[2];
+    c.step_stats = (float2*)q5[3];
+    c.step_gs = (float*)q5[4];
+    for (size_t b : sz) c.bytes += b;
+    if (e != cudaSuccess) {
+      kvm_destroy(ctx);
+      return cuda_fail(e, "cudaMalloc of step-scoring scratch");
+    }
+  }
   e = cudaMemset(c.status, 0, 256);
   if (e == cudaSuccess) e = kvm::launch_rope_tables(c, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -187,7 +209,8 @@ kvm_status kvm_destroy(kvm_ctx* ctx) {
   cudaGetDevice(&prev);
   if (prev != c.device) cudaSetDevice(c.device);
   cudaError_t e = cudaDeviceSynchronize();
-  void* ptrs[8] = {c.e_buf, c.part, c.rec, c.rope_base, c.rope_off, c.status, c.rope_base64, c.rope_off64};
+  void* ptrs[13] = {c.e_buf,      c.part,       c.rec,      c.rope_base, c.rope_off,   c.status,  c.rope_base_hl,
+                    c.rope_off_hl, c.step_kpk,   c.step_qpk, c.step_part, c.step_stats, c.step_gs};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   if (prev >= 0 && prev != c.device) cudaSetDevice(prev);
@@ -243,7 +266,8 @@ kvm_status kvm_score_select(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const 
   if (n_q < 1 || n_q > c.p.max_queries)
     return fail(KVM_ERR_SHAPE, "n_q=%d outside [1, max_queries=%d]", n_q, c.p.max_queries);
   if (n_q > 1 && head_scores) return fail(KVM_ERR_INVALID_ARG, "head_scores is only written for n_q == 1");
-  if (n_q > 1) return fail(KVM_ERR_SHAPE, "step-level scoring of n_q > 1 query tokens is not built in this library yet");
+  if (n_q > 1 && !ctx->c.step_kpk)
+    return fail(KVM_ERR_SHAPE, "n_q > 1 needs a context created with max_queries > 1");
   if (!aligned(q, 16) || !aligned(index, 16) || !aligned(kept_ids, 4) || !aligned(group_scores, 4) ||
       !aligned(head_scores, 4))
     return fail(KVM_ERR_INVALID_ARG, "q and index must be 16-byte aligned, outputs 4-byte aligned");

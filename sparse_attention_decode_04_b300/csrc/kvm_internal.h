@@ -39,11 +39,21 @@ struct Ctx {
   float* rec = nullptr;        // [view_ctas + S*h_kv][group][2 + d] attention partials
   float* rope_base = nullptr;  // [budget + 1][d/2][2] cos/sin of 32*slot*theta_i
   float* rope_off = nullptr;   // [32][d/2][2] cos/sin of r*theta_i
-  double* rope_base64 = nullptr;  // the same tables in fp64 (cancellation fallback)
-  double* rope_off64 = nullptr;
+  float4* rope_base_hl = nullptr;  // the same tables as fp32 hi/lo pairs (cos_h, cos_l, sin_h, sin_l)
+  float4* rope_off_hl = nullptr;   // read only on the cancellation fallback
   uint32_t* status = nullptr;  // device status word
   int64_t max_tiles = 0;
+  // step-level (multi-query) scoring scratch, allocated when max_queries > 1
+  int64_t step_blk_cap_pad = 0;  // max_blocks rounded up to 256
+  int step_rows_cap_pad = 0;     // max_queries * group rounded up to 256
+  uint16_t* step_kpk = nullptr;  // packed bf16 index [S*h_kv][step_blk_cap_pad][d] (core-matrix order)
+  uint16_t* step_qpk = nullptr;  // packed bf16 query rows [S*h_kv][step_rows_cap_pad][d]
+  float2* step_part = nullptr;   // row (max, sum) per column range [S*h_kv][kStepMaxRanges][rows]
+  float2* step_stats = nullptr;  // row (max, 1/sum) [S*h_kv][rows]
+  float* step_gs = nullptr;      // group scores when the caller does not ask for them [S][h_kv][max_blocks]
 };
+
+constexpr int kStepMaxRanges = 64;
 
 // kvm_index.cu
 cudaError_t launch_index_append(const Ctx& c, const uint16_t* k_pool, int64_t n_pages, const int32_t* bt,
@@ -54,6 +64,13 @@ cudaError_t launch_index_append(const Ctx& c, const uint16_t* k_pool, int64_t n_
 cudaError_t launch_score_select(const Ctx& c, const uint16_t* q, int n_q, const float* index, int n_sessions,
                                 const SessionArgs& a, int32_t* kept, float* group_scores, float* head_scores,
                                 cudaStream_t st);
+
+// kvm_step_score.cu: step-level scores of n_q > 1 query tokens (tcgen05) into gs_out [S][h_kv][max_blocks]
+cudaError_t launch_step_scores(const Ctx& c, const uint16_t* q, int n_q, const float* index, int n_sessions,
+                               const SessionArgs& a, float* gs_out, cudaStream_t st);
+// kvm_score.cu: the cluster top-k on given group scores
+cudaError_t launch_select_given(const Ctx& c, const float* gs, int n_sessions, const SessionArgs& a, int32_t* kept,
+                                float* group_scores_out, cudaStream_t st);
 
 // kvm_view.cu — mode: 0 materialise, 1 attend over a view, 2 fused
 cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,

@@ -209,7 +209,7 @@ template <int G>
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     const float* __restrict__ e_buf, const float2* __restrict__ part, int64_t max_tiles, int64_t max_blocks,
     int h_kv, int h_q, SessionArgs a, int rows_per_tile, int n_sink, int n_recent, int top_k, int budget,
-    int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores) {
+    int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores, const float* __restrict__ gs_in) {
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
   const int C = (int)cluster.num_blocks();
@@ -230,6 +230,18 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
   const int n_tiles = (n_blk + rows_per_tile - 1) / rows_per_tile;
   int32_t* kept_row = kept + ((int64_t)s * h_kv + g) * budget;
 
+  if (gs_in != nullptr) {
+    // group scores given (step-level scoring): keys straight from them
+    const float* src = gs_in + ((int64_t)s * h_kv + g) * max_blocks;
+    float* gs_dst = (group_scores && group_scores != gs_in) ? group_scores + ((int64_t)s * h_kv + g) * max_blocks
+                                                              : nullptr;
+    for (int b = lo + tid; b < hi; b += kSelectThreads) {
+      const float gs = src[b];
+      key[b - lo] = order_key(gs);
+      if (gs_dst) gs_dst[b] = gs;
+    }
+    __syncthreads();
+  } else {
   // 1. softmax normalisers of the group's heads (every CTA computes them the same way)
   if (warp < G) {
     const float2* p = part + ((int64_t)s * h_q + g * G + warp) * max_tiles;
@@ -268,6 +280,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     if (gs_dst) gs_dst[b] = gs;
   }
   __syncthreads();
+  }
 
   if (n_blk <= budget) {  // every block is kept (uniform across the cluster)
     for (int b = lo + tid; b < hi; b += kSelectThreads) kept_row[b] = b;
@@ -381,6 +394,34 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
   cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
+template <int G>
+cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, int rpt, int max_blk, int32_t* kept,
+                          float* group_scores, const float* gs_in, cudaStream_t st) {
+  int C = (max_blk + 4095) / 4096;
+  C = C < 1 ? 1 : (C > 8 ? 8 : C);
+  const int slice_cap = (max_blk + C - 1) / C;
+  const int tiles_cap = slice_cap / rpt + 2;
+  const size_t smem_b = (size_t)slice_cap * 4 + (size_t)tiles_cap * G * 4;
+  auto kb = select_kernel<G>;
+  cudaError_t e;
+  if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C, c.p.h_kv, n_sessions);
+  cfg.blockDim = dim3(kSelectThreads);
+  cfg.dynamicSmemBytes = smem_b;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kb, (const float*)c.e_buf, (const float2*)c.part, c.max_tiles, c.p.max_blocks,
+                            c.p.h_kv, c.p.h_q, a, rpt, c.p.n_sink, c.p.n_recent, c.p.top_k, c.budget, slice_cap,
+                            kept, group_scores, gs_in);
+}
+
 template <int D, int G>
 cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_sessions, const SessionArgs& a,
                      int32_t* kept, float* group_scores, float* head_scores, cudaStream_t st) {
@@ -407,28 +448,7 @@ cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_
       q, index, c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.e_buf, c.part, c.max_tiles, head_scores, c.status);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-  int C = (max_blk + 4095) / 4096;
-  C = C < 1 ? 1 : (C > 8 ? 8 : C);
-  const int slice_cap = (max_blk + C - 1) / C;
-  const int tiles_cap = slice_cap / rpt + 2;
-  const size_t smem_b = (size_t)slice_cap * 4 + (size_t)tiles_cap * G * 4;
-  auto kb = select_kernel<G>;
-  if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, c.p.h_kv, n_sessions);
-  cfg.blockDim = dim3(kSelectThreads);
-  cfg.dynamicSmemBytes = smem_b;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kb, (const float*)c.e_buf, (const float2*)c.part, c.max_tiles, c.p.max_blocks,
-                            c.p.h_kv, c.p.h_q, a, rpt, c.p.n_sink, c.p.n_recent, c.p.top_k, c.budget, slice_cap,
-                            kept, group_scores);
+  return launch_select<G>(c, n_sessions, a, rpt, max_blk, kept, group_scores, nullptr, st);
 }
 
 template <int D>
@@ -449,10 +469,34 @@ cudaError_t launch_d(const Ctx& c, const uint16_t* q, const float* index, int n_
 
 }  // namespace
 
+cudaError_t launch_select_given(const Ctx& c, const float* gs, int n_sessions, const SessionArgs& a, int32_t* kept,
+                                float* group_scores_out, cudaStream_t st) {
+  int max_blk = 0;
+  for (int s = 0; s < n_sessions; ++s) max_blk = max(max_blk, a.n_blk[s]);
+  if (max_blk == 0)
+    return cudaMemsetAsync(kept, 0xFF, sizeof(int32_t) * (size_t)n_sessions * c.p.h_kv * c.budget, st);
+  switch (c.group) {
+    case 1: return launch_select<1>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
+    case 2: return launch_select<2>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
+    case 3: return launch_select<3>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
+    case 4: return launch_select<4>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
+    case 5: return launch_select<5>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
+    case 6: return launch_select<6>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
+    case 7: return launch_select<7>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
+    case 8: return launch_select<8>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_score_select(const Ctx& c, const uint16_t* q, int n_q, const float* index, int n_sessions,
                                 const SessionArgs& a, int32_t* kept, float* group_scores, float* head_scores,
                                 cudaStream_t st) {
-  if (n_q != 1) return cudaErrorNotSupported;
+  if (n_q != 1) {
+    float* gs = group_scores ? group_scores : c.step_gs;
+    cudaError_t e = launch_step_scores(c, q, n_q, index, n_sessions, a, gs, st);
+    if (e != cudaSuccess) return e;
+    return launch_select_given(c, gs, n_sessions, a, kept, group_scores, st);
+  }
   return c.p.d == 128 ? launch_d<128>(c, q, index, n_sessions, a, kept, group_scores, head_scores, st)
                       : launch_d<64>(c, q, index, n_sessions, a, kept, group_scores, head_scores, st);
 }

@@ -55,8 +55,8 @@ struct ViewParams {
   float* rec;
   const float2* rope_base;  // [budget + 1][d/2]
   const float2* rope_off;   // [32][d/2]
-  const double2* rope_base64;  // fp64 copies, read only on the cancellation fallback
-  const double2* rope_off64;
+  const float4* rope_base_hl;  // hi/lo copies, read only on the cancellation fallback
+  const float4* rope_off_hl;
   float* out;
   uint32_t* status;
   int64_t total;  // kept blocks over all (session, KV head)
@@ -112,6 +112,37 @@ __device__ __forceinline__ void advance(Cursor& c, const SessionArgs& a, int n_s
 __device__ __forceinline__ int block_tokens(int64_t id, const SessionArgs& a, int s) {
   const int tail = (int)(a.n_tok[s] & 31);
   return (id == a.n_blk[s] - 1 && tail) ? tail : 32;
+}
+
+// Float-float (unevaluated hi + lo) arithmetic, Dekker / Knuth error-free transformations.
+struct ff {
+  float h, l;
+};
+__device__ __forceinline__ ff two_prod(float a, float b) {
+  const float p = a * b;
+  return ff{p, fmaf(a, b, -p)};
+}
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  const float s = a + b, bb = s - a;
+  return ff{s, (a - (s - bb)) + (b - bb)};
+}
+// x*y - u*v for hi/lo operands, to ~2^-44 of the operand magnitudes.
+__device__ __forceinline__ ff ff_dot2(ff x, ff y, ff u, ff v) {
+  const ff p = two_prod(x.h, y.h), q = two_prod(u.h, v.h);
+  const ff s = two_sum(p.h, -q.h);
+  const float lo = s.l + (p.l - q.l) + (fmaf(x.h, y.l, x.l * y.h) - fmaf(u.h, v.l, u.l * v.h));
+  return two_sum(s.h, lo);
+}
+// Rotation of one (x1, x2) pair by the angle whose cos/sin are composed from the hi/lo base and offset
+// tables; the result hi + lo is within ~2^-44 (|x1| + |x2|) of the exact rotation.
+__device__ __forceinline__ void rotate_exact(float x1, float x2, float4 b, float4 o, float& y1, float& y2) {
+  const ff cb{b.x, b.y}, sb{b.z, b.w}, co{o.x, o.y}, so{o.z, o.w};
+  const ff c = ff_dot2(cb, co, sb, so);                 // cos(A + B)
+  const ff s = ff_dot2(sb, co, ff{-cb.h, -cb.l}, so);   // sin(A + B) = sb co + cb so
+  const ff r1 = ff_dot2(ff{x1, 0.f}, c, ff{x2, 0.f}, s);
+  const ff r2 = ff_dot2(ff{x2, 0.f}, c, ff{-x1, 0.f}, s);
+  y1 = r1.h + r1.l;
+  y2 = r2.h + r2.l;
 }
 
 __device__ __forceinline__ void rope_cs(const float2 b, const float2 o, float& c, float& s) {
@@ -366,7 +397,7 @@ __global__ void __launch_bounds__(Geo<D>::NT, 1) view_kernel(const ViewParams vp
           uint32_t o1[4], o2[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            uint32_t h1[2], h2[2];
+            float f1[2], f2[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int v = 2 * u + e;
@@ -374,25 +405,19 @@ __global__ void __launch_bounds__(Geo<D>::NT, 1) view_kernel(const ViewParams vp
               rope_cs(bb[v], off[v], cs_, sn_);
               const float x1 = e ? bf16hi(ka[u]) : bf16lo(ka[u]);
               const float x2 = e ? bf16hi(kb[u]) : bf16lo(kb[u]);
-              const float f1 = fmaf(x1, cs_, -x2 * sn_);
-              const float f2 = fmaf(x2, cs_, x1 * sn_);
+              f1[e] = fmaf(x1, cs_, -x2 * sn_);
+              f2[e] = fmaf(x2, cs_, x1 * sn_);
               // fp32 tables put |error| <= 3e-7 (|x1| + |x2|) on f; that stays below one bf16 ulp of the
-              // result unless the rotation cancels (|f| < ~8e-5 (|x1| + |x2|)).  Those pairs are redone
-              // from the fp64 tables so the stored key is always within one ulp of the exact rotation.
+              // result unless the rotation cancels (|f| < ~8e-5 (|x1| + |x2|)).  Those pairs are redone in
+              // float-float from hi/lo tables, so the stored key is always within one ulp of the exact rotation.
               const float tau = 0x1p-12f * (fabsf(x1) + fabsf(x2));
-              if (fabsf(f1) < tau || fabsf(f2) < tau) {
-                const double2 b64 = vp.rope_base64[(int64_t)cur.i * (D / 2) + 8 * cp + v];
-                const double2 o64 = vp.rope_off64[r * (D / 2) + 8 * cp + v];
-                const double c64 = b64.x * o64.x - b64.y * o64.y, s64 = b64.y * o64.x + b64.x * o64.y;
-                h1[e] = __bfloat16_as_ushort(__double2bfloat16((double)x1 * c64 - (double)x2 * s64));
-                h2[e] = __bfloat16_as_ushort(__double2bfloat16((double)x2 * c64 + (double)x1 * s64));
-              } else {
-                h1[e] = __bfloat16_as_ushort(__float2bfloat16_rn(f1));
-                h2[e] = __bfloat16_as_ushort(__float2bfloat16_rn(f2));
+              if (fminf(fabsf(f1[e]), fabsf(f2[e])) < tau) {
+                rotate_exact(x1, x2, vp.rope_base_hl[(int64_t)cur.i * (D / 2) + 8 * cp + v],
+                             vp.rope_off_hl[r * (D / 2) + 8 * cp + v], f1[e], f2[e]);
               }
             }
-            o1[u] = h1[0] | (h1[1] << 16);
-            o2[u] = h2[0] | (h2[1] << 16);
+            o1[u] = pack_bf16x2(f1[0], f1[1]);
+            o2[u] = pack_bf16x2(f2[0], f2[1]);
             y1[2 * u] = bf16lo(o1[u]);
             y1[2 * u + 1] = bf16hi(o1[u]);
             y2[2 * u] = bf16lo(o2[u]);
@@ -554,8 +579,12 @@ cudaError_t launch_d(const Ctx& c, int mode, const ViewParams& vp, const Session
 }
 
 // RoPE tables computed in fp64: base[slot][i] = (cos, sin)(32*slot*theta_i), off[r][i] = (cos, sin)(r*theta_i),
-// theta_i = rope_theta^(-2i/d); stored as fp32 and as fp64.
-__global__ void rope_table_kernel(float2* base, int n_slots, float2* off, double2* base64, double2* off64, int d,
+// theta_i = rope_theta^(-2i/d); stored as fp32 and as fp32 hi/lo pairs (value = hi + lo to ~2^-48).
+__device__ __forceinline__ float4 hilo(double c, double s) {
+  const float ch = (float)c, sh = (float)s;
+  return make_float4(ch, (float)(c - (double)ch), sh, (float)(s - (double)sh));
+}
+__global__ void rope_table_kernel(float2* base, int n_slots, float2* off, float4* base_hl, float4* off_hl, int d,
                                   double rope_theta) {
   const int half = d / 2;
   const int64_t n = (int64_t)(n_slots + 32) * half;
@@ -567,11 +596,11 @@ __global__ void rope_table_kernel(float2* base, int n_slots, float2* off, double
     if (row < n_slots) {
       sincos(32.0 * (double)row * inv_freq, &sn, &cs);
       base[row * half + i] = make_float2((float)cs, (float)sn);
-      base64[row * half + i] = make_double2(cs, sn);
+      base_hl[row * half + i] = hilo(cs, sn);
     } else {
       sincos((double)(row - n_slots) * inv_freq, &sn, &cs);
       off[(row - n_slots) * half + i] = make_float2((float)cs, (float)sn);
-      off64[(row - n_slots) * half + i] = make_double2(cs, sn);
+      off_hl[(row - n_slots) * half + i] = hilo(cs, sn);
     }
   }
 }
@@ -596,8 +625,8 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
   vp.rec = c.rec;
   vp.rope_base = reinterpret_cast<const float2*>(c.rope_base);
   vp.rope_off = reinterpret_cast<const float2*>(c.rope_off);
-  vp.rope_base64 = reinterpret_cast<const double2*>(c.rope_base64);
-  vp.rope_off64 = reinterpret_cast<const double2*>(c.rope_off64);
+  vp.rope_base_hl = c.rope_base_hl;
+  vp.rope_off_hl = c.rope_off_hl;
   vp.out = out;
   vp.status = c.status;
   vp.total = a.seg_base[n_sessions];
@@ -613,8 +642,7 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
 cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st) {
   rope_table_kernel<<<256, 256, 0, st>>>(reinterpret_cast<float2*>(c.rope_base), c.budget + 1,
                                          reinterpret_cast<float2*>(c.rope_off),
-                                         reinterpret_cast<double2*>(c.rope_base64),
-                                         reinterpret_cast<double2*>(c.rope_off64), c.p.d, (double)c.p.rope_theta);
+                                         c.rope_base_hl, c.rope_off_hl, c.p.d, (double)c.p.rope_theta);
   return cudaGetLastError();
 }
 

@@ -66,6 +66,26 @@ def test_mean_k_equals_exact_rational_mean():
             assert abs(Fraction(float(idx[b, i])) - exact) <= abs(exact) * Fraction(1, 2 ** 52)
 
 
+def test_bf16_index_operand_is_the_rounded_fp32_mean():
+    """fp32 mean within the fp32 error bound of the exact mean, then RNE to bf16 as torch does it."""
+    keys = rand_bf16((5 * 32 + 11, 24), scale=2.0)
+    got = O.mean_k_index_bf16(keys)
+    exact = O.mean_k_index(keys)
+    vals = np.abs(O.bf16_to_f64(keys))
+    n_blk = exact.shape[0]
+    for b in range(n_blk):
+        rows = vals[b * 32:(b + 1) * 32]
+        bound = len(rows) * 2.0 ** -24 * rows.sum(axis=0) / len(rows) + 2.0 ** -24 * np.abs(exact[b])
+        # the fp32 mean the kernel forms, recomputed token by token with Python floats rounded to fp32
+        acc = np.zeros(24, dtype=np.float32)
+        for t in range(len(rows)):
+            acc = (acc + O.bf16_to_f64(keys[b * 32 + t]).astype(np.float32)).astype(np.float32)
+        mean32 = (acc / np.float32(len(rows))).astype(np.float32)
+        assert np.all(np.abs(mean32.astype(np.float64) - exact[b]) <= bound)
+        ref = torch.from_numpy(mean32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(got[b], ref)
+
+
 def test_index_append_matches_full_build_and_is_position_free():
     keys = rand_bf16((300, 16))
     full = O.mean_k_index(keys)
