@@ -213,6 +213,36 @@ kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint
  */
 kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* stream);
 
+/*
+ * Allocation-free score and select for one decode query.  The paper has no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory, for example a runtime whose memory pool owns every device byte, or
+ * code that must not synchronise the device (cudaMalloc and cudaFree may), and
+ * so cannot create a context with kvm_create.
+ *
+ * It computes exactly what kvm_score_select computes for n_q = 1 (same
+ * kernels, same results), taking the head geometry and budget from `p`
+ * (max_sessions and max_queries are ignored; the index rows and block-table
+ * rows have max_blocks entries).  Arguments and layouts are those of
+ * kvm_score_select; there is no head_scores output.
+ *
+ * Scratch: one fixed array of KVM_NOALLOC_SCRATCH_BYTES in device global memory,
+ * which every GPU that loads this library holds until the process exits.  It
+ * must fit n_sessions * (h_q * ceil(max_blocks/32) * 8 + h_kv * max_blocks *
+ * (h_q/h_kv) * 4) bytes plus 512; larger calls return KVM_ERR_SHAPE and launch
+ * nothing (one session of 40/8 heads fits 32,768 blocks).  The first call on
+ * each device looks up the array's device address with that device current;
+ * make that first call before any stream capture.  Every call reuses the same
+ * array and leaves its contents behind, so calls whose work overlaps on the
+ * GPU (different streams, or other threads) race and must be serialised by
+ * the caller.  No device memory is allocated or freed; errors are reported as
+ * by the other calls (kvm_last_error()).
+ */
+#define KVM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+kvm_status kvm_score_select_noalloc(const kvm_params* p, const uint16_t* q, const float* index,
+                                   const int64_t* n_tok, int32_t n_sessions, int32_t* kept_ids,
+                                   float* group_scores, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -173,3 +173,23 @@ def kvm_device_status(ctx: Context, clear: bool = True, stream=None) -> int:
     if st not in (0, 5, 6):
         _check(st)
     return int(out.value)
+
+
+def kvm_score_select_noalloc(params: Params, q, index, n_tok, kept_ids, group_scores=None, stream=None):
+    """Score and select for one decode query without any device allocation.
+
+    For callers that cannot allocate device memory (and so cannot build a
+    Context): the head geometry and budget come from `params`; the scratch is a
+    fixed array inside libkvm.so (KVM_NOALLOC_SCRATCH_BYTES per GPU) that every
+    call reuses, so calls that overlap on the GPU must be serialised.  The
+    first call on a device should come before any stream capture.
+    """
+    L = lib()
+    f = L.kvm_score_select_noalloc
+    if f.argtypes is None:
+        P = ctypes.c_void_p
+        f.argtypes = [ctypes.POINTER(Params), P, P, P, ctypes.c_int32, P, P, P]
+        f.restype = ctypes.c_int
+    n = len(n_tok)
+    _check(f(ctypes.byref(params), _ptr(q), _ptr(index), _i64(n_tok), n, _ptr(kept_ids), _ptr(group_scores),
+             _stream(stream)))

@@ -82,6 +82,8 @@ kvm_status history_args(const Ctx& c, const int64_t* n_tok, int32_t n_sessions, 
 
 }  // namespace
 
+void kvm::set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 cudaError_t kvm::ensure_smem_impl(const void* kernel, int device, size_t bytes) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, size_t> limit;

@@ -80,6 +80,9 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
 
 cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st);
 
+// Sets the message kvm_last_error() returns on this thread (kvm_api.cu).
+void set_last_error(const char* msg);
+
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on `device`.
 // The limit only ever grows, and each (kernel, device) pair is configured once
 // per size, so steady-state calls (and calls under CUDA-graph capture) make no
