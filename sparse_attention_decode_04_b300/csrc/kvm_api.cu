@@ -151,7 +151,7 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   const size_t S = (size_t)p->max_sessions;
   const size_t sz_e = S * p->h_kv * (size_t)p->max_blocks * c.group * sizeof(float);
   const size_t sz_part = S * p->h_q * (size_t)c.max_tiles * sizeof(float2);
-  const size_t sz_rec = ((size_t)c.view_ctas + S * p->h_kv) * c.group * (2 + p->d) * sizeof(float);
+  const size_t sz_rec = ((size_t)c.view_ctas + S * p->h_kv) * kvm::kViewWarps * c.group * (2 + p->d) * sizeof(float);
   const size_t sz_base = (size_t)(budget + 1) * (p->d / 2) * sizeof(float2);
   const size_t sz_off = (size_t)32 * (p->d / 2) * sizeof(float2);
   constexpr int kBufs = 8;

@@ -8,53 +8,62 @@
 // KVMEM reproduction README, "Local reproduction": the view replaces full
 // attention; "2026-09-08 validation correction": RoPE is applied to the query.
 //
-// Design (one kernel, three modes):
+// One kernel, three modes:
 //   mode 0  materialise: pages -> rotated K view + copied V view
 //   mode 1  attend:      view  -> attention partials
 //   mode 2  fused:       pages -> views + attention partials (each page read once)
-// The work is the flat list of kept blocks over (session, KV head); a
-// persistent grid of P CTAs (one per SM) takes contiguous equal shares of it,
-// so every SM streams the same number of pages.  Warp-specialised CTA:
-//   producer warp  - resolves kept id -> page through the block table (32 blocks
-//                    at a time, one per lane), then lane 0 issues 1-D bulk copies
-//                    (K page + V page) into an NSTAGE-deep shared-memory ring,
-//                    each stage completing on its own mbarrier;
-//   consumer warps - CP = d/16 warps; warp w owns 32/CP tokens of each page and
-//                    each token is split over CP lanes (dims [8c, 8c+8) and
-//                    [d/2+8c, d/2+8c+8): the rotate-half pairs).  They rotate K
-//                    at view position 32*i + r (cos/sin composed from a per-slot
-//                    base table and a per-offset table, both filled in fp64),
-//                    round to bf16 and store; copy V; dot the rounded keys with
-//                    the rotated query (fp32, log2 domain); keep a per-warp
-//                    online softmax; accumulate V (lane owns d/32 dims).
-// At a segment boundary (new session/KV head) or the end of its share, the CTA
-// merges its warps' states and writes one partial record (m, l, acc[d]) per
-// query head at index cta + segment, which is unique.  A combine kernel merges
-// the records of each (session, query head) with the log-sum-exp rule.
-// Every mbarrier wait is bounded; a timeout sets KVM_DEV_TIMEOUT, the CTA
-// drains its copies in flight and returns.
+// Work: the flat list of kept blocks over (session, KV head).  A persistent grid
+// of one CTA per SM takes equal contiguous shares, so every SM streams the same
+// number of pages.  Inside a CTA, eight warps each own one shared-memory stage
+// (a K page and a V page) and take every eighth block of the share; warps never
+// wait on one another.  Per block, a warp:
+//   - receives the K and V pages by TMA tiled loads (64-column boxes) with the
+//     128-byte swizzle, so the ldmatrix reads below are free of bank conflicts;
+//   - rotates K in place at view positions 32*i + r (cos/sin composed in fp32
+//     from a per-slot and a per-offset table, both filled in fp64; pairs whose
+//     rotation cancels are redone in float-float), rounds to bf16, and writes
+//     the rotated K and the untouched V to the view with TMA tiled stores;
+//   - computes the scores with mma.sync (m16n8k16, bf16 -> fp32): A rows 0..7
+//     hold the rotated, scaled query heads rounded to bf16 and rows 8..15 their
+//     bf16 residuals, so one MMA gives both halves and their sum is an
+//     fp32-accurate score;
+//   - keeps an online softmax per head in the log2 domain (the running maximum
+//     is raised only when it grows by more than 8, so rescaling is rare);
+//   - accumulates P.V with mma.sync, P split the same way into bf16 + residual.
+// The next block's K page is fetched as soon as the scores are done, its V page
+// as soon as P.V is done, so the copies overlap the rest of the block's work.
+// Each warp writes one partial record (max, sum, output) per segment (session,
+// KV head) of its CTA's share — a neutral record for a segment it had no block
+// of — at index ((cta + segment) * 8 + warp), which is unique.  The combine
+// kernel merges the records of each (session, query head).
+// Every mbarrier wait is bounded; a timeout sets KVM_DEV_TIMEOUT and the warp
+// drains its copies and stops.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <string.h>
+
+#include <mutex>
+
 #include "kvm_device.cuh"
 #include "kvm_internal.h"
 
 namespace kvm {
 namespace {
 
-constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kWarps = kViewWarps;
 
 struct ViewParams {
-  const uint16_t* k_src;
-  const uint16_t* v_src;
-  int64_t n_pages;
   const int32_t* bt;
   int64_t max_blocks;
+  int64_t n_pages;
   const int32_t* kept;
   const uint16_t* q;
   uint16_t* k_view;
   uint16_t* v_view;
   int32_t* view_len;
   float* rec;
-  const float2* rope_base;  // [budget + 1][d/2]
-  const float2* rope_off;   // [32][d/2]
+  const float2* rope_base;     // [budget + 1][d/2]
+  const float2* rope_off;      // [32][d/2]
   const float4* rope_base_hl;  // hi/lo copies, read only on the cancellation fallback
   const float4* rope_off_hl;
   float* out;
@@ -70,14 +79,14 @@ struct ViewParams {
 
 template <int D>
 struct Geo {
-  static constexpr int CP = D / 16;       // lanes per token (chunk pairs)
-  static constexpr int NCW = CP;          // consumer warps
-  static constexpr int TPW = 32 / CP;     // tokens per consumer warp
-  static constexpr int NCT = NCW * 32;    // consumer threads
-  static constexpr int NT = NCT + 32;     // + producer warp
-  static constexpr int PVD = D / 32;      // dims per lane in P.V
-  static constexpr int NSTAGE = 8;
-  static constexpr uint32_t PAGE = 32u * D * 2u;  // bytes of one K (or V) page
+  static constexpr int BOXES = D / 64;          // 64-column (128-byte) boxes per page row
+  static constexpr uint32_t BOX = 32 * 128;     // bytes of one box (32 rows)
+  static constexpr uint32_t PAGE = 32 * D * 2;  // bytes of one K (or V) page
+  static constexpr int CPR = D / 16;            // rotation items (chunk pairs) per row
+  static constexpr int RPP = 32 / CPR;          // rows per rotation pass
+  static constexpr int PASSES = CPR;            // rotation passes per page
+  static constexpr int KS = D / 16;             // MMA k-steps over the head dimension
+  static constexpr int NO = D / 8;              // output n-tiles
 };
 
 __device__ __forceinline__ int64_t cta_begin(int c, int64_t total, int P) { return (int64_t)c * total / P; }
@@ -86,32 +95,32 @@ __device__ __forceinline__ int cta_of(int64_t f, int64_t total, int P) {
   return (int)(((f + 1) * (int64_t)P - 1) / total);
 }
 
-// Position of flat block f: session, KV head, index within the head's kept list.
 struct Cursor {
   int s, g, i;
 };
-__device__ __forceinline__ Cursor locate(int64_t f, const SessionArgs& a, int n_sessions, int h_kv) {
+__device__ __forceinline__ Cursor locate(int64_t f, const SessionArgs& a, int n_sessions) {
   int s = 0;
   while (s + 1 < n_sessions && a.seg_base[s + 1] <= f) ++s;
   const int64_t local = f - a.seg_base[s];
   const int nk = a.n_keep[s];
   return Cursor{s, (int)(local / nk), (int)(local % nk)};
 }
-__device__ __forceinline__ void advance(Cursor& c, const SessionArgs& a, int n_sessions, int h_kv) {
-  if (c.s >= n_sessions) return;
-  if (++c.i < a.n_keep[c.s]) return;
-  c.i = 0;
-  if (++c.g < h_kv) return;
-  c.g = 0;
-  do {
-    ++c.s;
-  } while (c.s < n_sessions && a.n_keep[c.s] == 0);
-}
 
 // Tokens of kept block `id` present in session s's history.
 __device__ __forceinline__ int block_tokens(int64_t id, const SessionArgs& a, int s) {
   const int tail = (int)(a.n_tok[s] & 31);
   return (id == a.n_blk[s] - 1 && tail) ? tail : 32;
+}
+
+// Byte offset of logical 16-byte chunk k of row r inside a 128-byte-swizzled page.
+__device__ __forceinline__ uint32_t chunk_off(int r, int k) {
+  return (uint32_t)((k >> 3) * (32 * 128) + r * 128 + (((k & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void rope_cs(const float2 b, const float c, const float s, float& co, float& sn) {
+  // cos/sin of (base + offset) from cos/sin of each (angle addition)
+  co = fmaf(b.x, c, -b.y * s);
+  sn = fmaf(b.y, c, b.x * s);
 }
 
 // Float-float (unevaluated hi + lo) arithmetic, Dekker / Knuth error-free transformations.
@@ -133,380 +142,458 @@ __device__ __forceinline__ ff ff_dot2(ff x, ff y, ff u, ff v) {
   const float lo = s.l + (p.l - q.l) + (fmaf(x.h, y.l, x.l * y.h) - fmaf(u.h, v.l, u.l * v.h));
   return two_sum(s.h, lo);
 }
-// Rotation of one (x1, x2) pair by the angle whose cos/sin are composed from the hi/lo base and offset
-// tables; the result hi + lo is within ~2^-44 (|x1| + |x2|) of the exact rotation.
+// Rotation of (x1, x2) by the angle whose cos/sin are composed from hi/lo base and offset tables;
+// the result is within ~2^-44 (|x1| + |x2|) of the exact rotation.
 __device__ __forceinline__ void rotate_exact(float x1, float x2, float4 b, float4 o, float& y1, float& y2) {
   const ff cb{b.x, b.y}, sb{b.z, b.w}, co{o.x, o.y}, so{o.z, o.w};
-  const ff c = ff_dot2(cb, co, sb, so);                 // cos(A + B)
-  const ff s = ff_dot2(sb, co, ff{-cb.h, -cb.l}, so);   // sin(A + B) = sb co + cb so
+  const ff c = ff_dot2(cb, co, sb, so);
+  const ff s = ff_dot2(sb, co, ff{-cb.h, -cb.l}, so);
   const ff r1 = ff_dot2(ff{x1, 0.f}, c, ff{x2, 0.f}, s);
   const ff r2 = ff_dot2(ff{x2, 0.f}, c, ff{-x1, 0.f}, s);
   y1 = r1.h + r1.l;
   y2 = r2.h + r2.l;
 }
 
-__device__ __forceinline__ void rope_cs(const float2 b, const float2 o, float& c, float& s) {
-  // cos/sin of (base + offset) angle from cos/sin of each (angle addition)
-  c = fmaf(b.x, o.x, -b.y * o.y);
-  s = fmaf(b.y, o.x, b.x * o.y);
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 
+// hi = bf16(x), lo = bf16(x - hi) for two values, each pair packed.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16x2(x0, x1);
+  lo = pack_bf16x2(x0 - bf16lo(hi), x1 - bf16hi(hi));
+}
+
+struct BlockMeta {
+  int q;      // segment = s * h_kv + g
+  int s;
+  int i;      // index in the segment's kept list (view slot)
+  int valid;  // tokens present (0: skipped)
+  int ysrc;   // source tile row
+};
+
 template <int D, int G, int MODE>
-__global__ void __launch_bounds__(Geo<D>::NT, 1) view_kernel(const ViewParams vp, const SessionArgs a) {
+__global__ void __launch_bounds__(kWarps * 32, 1)
+    view_kernel(const __grid_constant__ CUtensorMap tm_ksrc, const __grid_constant__ CUtensorMap tm_vsrc,
+                const __grid_constant__ CUtensorMap tm_kdst, const __grid_constant__ CUtensorMap tm_vdst,
+                const ViewParams vp, const SessionArgs a) {
   using Q = Geo<D>;
-  constexpr int CP = Q::CP, NCW = Q::NCW, TPW = Q::TPW, NCT = Q::NCT, PVD = Q::PVD, NS = Q::NSTAGE;
-  constexpr bool kWrite = MODE != 1;  // writes the view
+  constexpr bool kWrite = MODE != 1;
   constexpr bool kAttend = MODE != 0;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  uint16_t* kbuf = reinterpret_cast<uint16_t*>(smem_raw);         // [NS][32][D]
-  uint16_t* vbuf = kbuf + NS * 32 * D;                            // [NS][32][D]
-  float* mscr = reinterpret_cast<float*>(vbuf + NS * 32 * D);     // [NCW][G][2 + D]
-  float* pbuf = mscr + NCW * G * (2 + D);                         // [NCW][TPW][8]
-  __shared__ __align__(8) uint64_t full_bar[NS];
-  __shared__ __align__(8) uint64_t empty_bar[NS];
-  __shared__ int meta[NS];
-  __shared__ volatile int abort_flag;
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // 1024-byte aligned stages: [warp][K page | V page]; then the offset table [32][4][CPR] float4
+  unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
+  float4* off_s = reinterpret_cast<float4*>(smem + kWarps * 2 * Q::PAGE);
+  __shared__ __align__(8) uint64_t full_k[kWarps], full_v[kWarps];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
   const int64_t fa = cta_begin(c, vp.total, vp.P), fb = cta_begin(c + 1, vp.total, vp.P);
   if (fa >= fb) return;
+  const int Lcap = 32 * vp.budget;
 
-  if (tid == 0) {
-    abort_flag = 0;
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], NCW);
+  if (kWrite) {
+    for (int idx = tid; idx < 32 * 4 * Q::CPR; idx += kWarps * 32) {
+      const int r = idx / (4 * Q::CPR), u = (idx / Q::CPR) % 4, cc = idx % Q::CPR;
+      const float2 o0 = vp.rope_off[r * (D / 2) + 8 * cc + 2 * u];
+      const float2 o1 = vp.rope_off[r * (D / 2) + 8 * cc + 2 * u + 1];
+      off_s[idx] = make_float4(o0.x, o0.y, o1.x, o1.y);
     }
+  }
+  if (lane == 0) {
+    mbar_init(&full_k[warp], 1);
+    mbar_init(&full_v[warp], 1);
     mbar_fence_init();
   }
   __syncthreads();
 
-  if (warp == NCW) {
-    // ------------------------------------------------------------ producer warp
-    Cursor cur = locate(fa, a, vp.n_sessions, vp.h_kv);
-    int64_t k = 0;
-    int prev_id = -1;
-    for (int64_t f0 = fa; f0 < fb; f0 += 32) {
-      // lane j resolves flat block f0 + j
-      Cursor cj = cur;
-      if (f0 + lane < fb)
-        for (int j = 0; j < lane; ++j) advance(cj, a, vp.n_sessions, vp.h_kv);
-      int valid = 0;
-      int64_t src_off = 0;
-      int id = -1;
-      if (f0 + lane < fb) {
-        const int q = cj.s * vp.h_kv + cj.g;
-        if (MODE == 1) {
-          const int L = min(vp.view_len[q], 32 * vp.budget);
-          valid = max(0, min(32, L - 32 * cj.i));
-          src_off = ((int64_t)q * vp.budget * 32 + (int64_t)cj.i * 32) * D;
+  unsigned char* kbuf = smem + warp * 2 * Q::PAGE;
+  unsigned char* vbuf = kbuf + Q::PAGE;
+  const uint32_t kaddr = smem_addr(kbuf), vaddr = smem_addr(vbuf);
+  const Cursor firstc = locate(fa, a, vp.n_sessions), lastc = locate(fb - 1, a, vp.n_sessions);
+  const int seg_first = firstc.s * vp.h_kv + firstc.g;
+  const int seg_last = lastc.s * vp.h_kv + lastc.g;
+
+  // ------------------------------------------------------------ per-block metadata, 32 blocks at a time
+  // lane l describes this warp's block number jb + l: flat index fa + warp + 8 * (jb + l)
+  const int64_t nblk_w = (fb - fa - warp + kWarps - 1) / kWarps;  // blocks this warp processes (may be <= 0)
+  auto resolve = [&](int64_t jb) -> BlockMeta {
+    BlockMeta m{-1, 0, 0, 0, 0};
+    const int64_t j = jb + lane;
+    if (j >= nblk_w) return m;
+    const int64_t f = fa + warp + (int64_t)kWarps * j;
+    const Cursor cu = locate(f, a, vp.n_sessions);
+    m.q = cu.s * vp.h_kv + cu.g;
+    m.s = cu.s;
+    m.i = cu.i;
+    if (MODE == 1) {
+      int L = vp.view_len[m.q];
+      L = L < 0 ? 0 : (L > Lcap ? Lcap : L);
+      m.valid = max(0, min(32, L - 32 * cu.i));
+      m.ysrc = m.q * Lcap + 32 * cu.i;
+    } else {
+      const int id = vp.kept[(int64_t)m.q * vp.budget + cu.i];
+      const int prev = cu.i > 0 ? vp.kept[(int64_t)m.q * vp.budget + cu.i - 1] : -1;
+      if (id >= 0 && id < a.n_blk[cu.s] && id > prev) {  // kept ids ascend within a list
+        const int32_t page = vp.bt[(int64_t)cu.s * vp.max_blocks + id];
+        if (page >= 0 && page < vp.n_pages) {
+          m.valid = block_tokens(id, a, cu.s);
+          m.ysrc = (int)(((int64_t)page * vp.h_kv + cu.g) * 32);
         } else {
-          id = vp.kept[(int64_t)q * vp.budget + cj.i];
-          if (id >= 0 && id < a.n_blk[cj.s]) {
-            const int32_t page = vp.bt[(int64_t)cj.s * vp.max_blocks + id];
-            if (page >= 0 && page < vp.n_pages) {
-              valid = block_tokens(id, a, cj.s);
-              src_off = (((int64_t)page * vp.h_kv + cj.g) * 32) * D;
-            } else {
-              atomicOr(vp.status, KVM_DEV_BAD_PAGE);
-            }
-          } else {
-            atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
-          }
-        }
-      }
-      const int nb = (int)(fb - f0 < 32 ? fb - f0 : 32);
-      for (int j = 0; j < nb; ++j) {
-        int vj = __shfl_sync(0xffffffffu, valid, j);
-        const int64_t oj = __shfl_sync(0xffffffffu, src_off, j);
-        const int idj = __shfl_sync(0xffffffffu, id, j);
-        const int ij = __shfl_sync(0xffffffffu, cj.i, j);
-        if (MODE != 1 && vj > 0) {  // kept ids must ascend within a list
-          if (ij > 0 && idj <= prev_id) {
-            vj = 0;
-            if (lane == 0) atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
-          }
-        }
-        if (MODE != 1) prev_id = vj > 0 ? idj : prev_id;
-        if (lane == 0) {
-          const int st = (int)(k % NS);
-          bool ok = true;
-          if (k >= NS) ok = mbar_wait(&empty_bar[st], (uint32_t)((k / NS - 1) & 1), vp.status);
-          if (!ok || abort_flag) {
-            abort_flag = 1;
-          } else {
-            meta[st] = vj;
-            if (vj > 0) {
-              mbar_arrive_expect_tx(&full_bar[st], 2 * Q::PAGE);
-              bulk_g2s(kbuf + st * 32 * D, vp.k_src + oj, Q::PAGE, &full_bar[st]);
-              bulk_g2s(vbuf + st * 32 * D, vp.v_src + oj, Q::PAGE, &full_bar[st]);
-            } else {
-              mbar_arrive(&full_bar[st]);
-            }
-          }
-        }
-        ++k;
-        if (__shfl_sync(0xffffffffu, (int)abort_flag, 0)) break;
-      }
-      if (__shfl_sync(0xffffffffu, (int)abort_flag, 0)) break;
-      // the warp advances its cursor by 32 blocks
-      for (int j = 0; j < nb; ++j) advance(cur, a, vp.n_sessions, vp.h_kv);
-    }
-    if (lane == 0 && abort_flag) {
-      // drain: the last phase issued on each stage may still have copies in flight
-      const int64_t k_issued = k;
-      for (int64_t j = (k_issued > NS ? k_issued - NS : (int64_t)0); j < k_issued; ++j)
-        mbar_wait(&full_bar[j % NS], (uint32_t)((j / NS) & 1), vp.status);
-    }
-  } else {
-    // ------------------------------------------------------------ consumer warps
-    const int tw = lane / CP;             // token within the warp
-    const int cp = lane % CP;             // chunk pair
-    const int r = warp * TPW + tw;        // token row within the page
-    float2 off[8];                        // cos/sin of r * theta_i for this lane's 8 frequencies
-#pragma unroll
-    for (int u = 0; u < 8; ++u) off[u] = vp.rope_off[r * (D / 2) + 8 * cp + u];
-
-    float qr[G][16];  // rotated, scaled query slice: [0..8) first half, [8..16) second half
-    float m[G], lsum[G], acc[G][PVD];
-    Cursor cur = locate(fa, a, vp.n_sessions, vp.h_kv);
-    int seg_q = -1;
-    const int64_t n = fb - fa;
-
-    auto flush = [&](int q) {
-      // per-warp l: sum over the warp's tokens
-#pragma unroll
-      for (int hh = 0; hh < G; ++hh) {
-        float l = lsum[hh];
-#pragma unroll
-        for (int o = CP; o < 32; o <<= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-        float* w = mscr + (warp * G + hh) * (2 + D);
-        if (lane == 0) {
-          w[0] = m[hh];
-          w[1] = l;
-        }
-#pragma unroll
-        for (int d = 0; d < PVD; ++d) w[2 + lane * PVD + d] = acc[hh][d];
-      }
-      named_sync(1, NCT);
-      float* rec = vp.rec + (int64_t)(c + q) * G * (2 + D);
-      for (int idx = tid; idx < G * D; idx += NCT) {
-        const int hh = idx / D, dim = idx % D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) M = fmaxf(M, mscr[(w * G + hh) * (2 + D)]);
-        float av = 0.f, lv = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-          for (int w = 0; w < NCW; ++w) {
-            const float* ws = mscr + (w * G + hh) * (2 + D);
-            const float sc = fast_exp2(ws[0] - M);
-            av = fmaf(ws[2 + dim], sc, av);
-            lv = fmaf(ws[1], sc, lv);
-          }
-        }
-        rec[hh * (2 + D) + 2 + dim] = av;
-        if (dim == 0) {
-          rec[hh * (2 + D)] = M;
-          rec[hh * (2 + D) + 1] = lv;
-        }
-      }
-      named_sync(1, NCT);
-    };
-
-    auto begin_segment = [&](const Cursor& cs) {
-      const int q = cs.s * vp.h_kv + cs.g;
-      const int nk = a.n_keep[cs.s];
-      int L;
-      if (MODE == 1) {
-        L = vp.view_len[q];
-        if (L < 0 || L > 32 * vp.budget) {  // caller-supplied: clamp so the RoPE table read stays in range
-          if (tid == 0) atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
-          L = L < 0 ? 0 : 32 * vp.budget;
+          atomicOr(vp.status, KVM_DEV_BAD_PAGE);
         }
       } else {
-        const int last = vp.kept[(int64_t)q * vp.budget + nk - 1];
-        L = 32 * (nk - 1) + ((last >= 0 && last < a.n_blk[cs.s]) ? block_tokens(last, a, cs.s) : 32);
-        if (cs.i == 0 && tid == 0) vp.view_len[q] = L;
+        atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
       }
-      if (kAttend) {
-        // RoPE(q, L): cos/sin of L*theta_i composed from slot L/32 and offset L%32
-        const float2* bb = vp.rope_base + (int64_t)(L >> 5) * (D / 2) + 8 * cp;
-        const float2* oo = vp.rope_off + (L & 31) * (D / 2) + 8 * cp;
-        float cs_[8], sn_[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) rope_cs(bb[u], oo[u], cs_[u], sn_[u]);
-#pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          const uint16_t* qh = vp.q + ((int64_t)cs.s * vp.h_q + cs.g * G + hh) * D;
-          const uint4 w1 = *reinterpret_cast<const uint4*>(qh + 8 * cp);
-          const uint4 w2 = *reinterpret_cast<const uint4*>(qh + D / 2 + 8 * cp);
-          const uint32_t a1[4] = {w1.x, w1.y, w1.z, w1.w}, a2[4] = {w2.x, w2.y, w2.z, w2.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int v = 2 * u + e;
-              const float x1 = e ? bf16hi(a1[u]) : bf16lo(a1[u]);
-              const float x2 = e ? bf16hi(a2[u]) : bf16lo(a2[u]);
-              qr[hh][v] = (x1 * cs_[v] - x2 * sn_[v]) * vp.q_scale;
-              qr[hh][8 + v] = (x2 * cs_[v] + x1 * sn_[v]) * vp.q_scale;
-            }
-          }
-          m[hh] = -INFINITY;
-          lsum[hh] = 0.f;
-#pragma unroll
-          for (int d = 0; d < PVD; ++d) acc[hh][d] = 0.f;
-        }
-      }
-      return q;
-    };
-
-    bool aborted = false;
-    for (int64_t k = 0; k < n; ++k) {
-      const int st = (int)(k % NS);
-      const bool ok = mbar_wait(&full_bar[st], (uint32_t)((k / NS) & 1), vp.status);
-      int bad;
-      asm volatile(
-          "{\n\t.reg .pred p, q;\n\tsetp.eq.u32 p, %1, 0;\n\t"
-          "bar.red.or.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-          : "=r"(bad)
-          : "r"((uint32_t)ok), "r"(NCT)
-          : "memory");
-      if (bad) {
-        aborted = true;
-        abort_flag = 1;
-        break;
-      }
-      if (cur.i == 0 || seg_q < 0) {
-        if (kAttend && seg_q >= 0) flush(seg_q);  // a share with only skipped blocks leaves a neutral record
-        seg_q = begin_segment(cur);
-      }
-      const int valid = meta[st];
-      if (valid > 0) {
-        const uint16_t* kp = kbuf + st * 32 * D + r * D;
-        const uint16_t* vpg = vbuf + st * 32 * D + r * D;
-        const uint4 k1 = *reinterpret_cast<const uint4*>(kp + 8 * cp);
-        const uint4 k2 = *reinterpret_cast<const uint4*>(kp + D / 2 + 8 * cp);
-        float y1[8], y2[8];
-        const uint32_t ka[4] = {k1.x, k1.y, k1.z, k1.w}, kb[4] = {k2.x, k2.y, k2.z, k2.w};
-        if (kWrite) {
-          const int64_t j = (int64_t)cur.i * 32 + r;  // view position
-          const float2* bb = vp.rope_base + (int64_t)cur.i * (D / 2) + 8 * cp;
-          uint32_t o1[4], o2[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            float f1[2], f2[2];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int v = 2 * u + e;
-              float cs_, sn_;
-              rope_cs(bb[v], off[v], cs_, sn_);
-              const float x1 = e ? bf16hi(ka[u]) : bf16lo(ka[u]);
-              const float x2 = e ? bf16hi(kb[u]) : bf16lo(kb[u]);
-              f1[e] = fmaf(x1, cs_, -x2 * sn_);
-              f2[e] = fmaf(x2, cs_, x1 * sn_);
-              // fp32 tables put |error| <= 3e-7 (|x1| + |x2|) on f; that stays below one bf16 ulp of the
-              // result unless the rotation cancels (|f| < ~8e-5 (|x1| + |x2|)).  Those pairs are redone in
-              // float-float from hi/lo tables, so the stored key is always within one ulp of the exact rotation.
-              const float tau = 0x1p-12f * (fabsf(x1) + fabsf(x2));
-              if (fminf(fabsf(f1[e]), fabsf(f2[e])) < tau) {
-                rotate_exact(x1, x2, vp.rope_base_hl[(int64_t)cur.i * (D / 2) + 8 * cp + v],
-                             vp.rope_off_hl[r * (D / 2) + 8 * cp + v], f1[e], f2[e]);
-              }
-            }
-            o1[u] = pack_bf16x2(f1[0], f1[1]);
-            o2[u] = pack_bf16x2(f2[0], f2[1]);
-            y1[2 * u] = bf16lo(o1[u]);
-            y1[2 * u + 1] = bf16hi(o1[u]);
-            y2[2 * u] = bf16lo(o2[u]);
-            y2[2 * u + 1] = bf16hi(o2[u]);
-          }
-          if (r < valid) {
-            const int q = seg_q;
-            uint16_t* kd = vp.k_view + ((int64_t)q * vp.budget * 32 + j) * D;
-            uint16_t* vd = vp.v_view + ((int64_t)q * vp.budget * 32 + j) * D;
-            *reinterpret_cast<uint4*>(kd + 8 * cp) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-            *reinterpret_cast<uint4*>(kd + D / 2 + 8 * cp) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
-            *reinterpret_cast<uint4*>(vd + 8 * cp) = *reinterpret_cast<const uint4*>(vpg + 8 * cp);
-            *reinterpret_cast<uint4*>(vd + D / 2 + 8 * cp) = *reinterpret_cast<const uint4*>(vpg + D / 2 + 8 * cp);
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            y1[2 * u] = bf16lo(ka[u]);
-            y1[2 * u + 1] = bf16hi(ka[u]);
-            y2[2 * u] = bf16lo(kb[u]);
-            y2[2 * u + 1] = bf16hi(kb[u]);
-          }
-        }
-        if (kAttend) {
-          float sc[G];
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            float d0 = 0.f;
-#pragma unroll
-            for (int v = 0; v < 8; ++v) d0 = fmaf(qr[hh][v], y1[v], d0);
-#pragma unroll
-            for (int v = 0; v < 8; ++v) d0 = fmaf(qr[hh][8 + v], y2[v], d0);
-#pragma unroll
-            for (int o = 1; o < CP; o <<= 1) d0 += __shfl_xor_sync(0xffffffffu, d0, o);
-            sc[hh] = r < valid ? d0 : -INFINITY;
-          }
-          float* pw = pbuf + warp * TPW * 8;
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            float bm = sc[hh];
-#pragma unroll
-            for (int o = CP; o < 32; o <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-            const float mn = fmaxf(m[hh], bm);
-            float corr = 1.f, p = 0.f;
-            if (mn != -INFINITY) {
-              corr = fast_exp2(m[hh] - mn);  // 0 when m was -inf
-              p = fast_exp2(sc[hh] - mn);    // 0 for rows past `valid`
-            }
-            m[hh] = mn;
-            lsum[hh] = fmaf(lsum[hh], corr, p);
-#pragma unroll
-            for (int d = 0; d < PVD; ++d) acc[hh][d] *= corr;
-            if (cp == 0) pw[tw * 8 + hh] = p;
-          }
-          __syncwarp();
-          // P.V over the warp's tokens: lane owns dims [PVD*lane, PVD*lane + PVD)
-#pragma unroll
-          for (int t = 0; t < TPW; ++t) {
-            if (warp * TPW + t >= valid) break;  // rows past the tail may hold any bits
-            const uint16_t* vrow = vbuf + st * 32 * D + (warp * TPW + t) * D + PVD * lane;
-            float vv[PVD];
-            if constexpr (PVD == 4) {
-              const uint2 w = *reinterpret_cast<const uint2*>(vrow);
-              vv[0] = bf16lo(w.x);
-              vv[1] = bf16hi(w.x);
-              vv[2] = bf16lo(w.y);
-              vv[3] = bf16hi(w.y);
-            } else {
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(vrow);
-              vv[0] = bf16lo(w);
-              vv[1] = bf16hi(w);
-            }
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-              const float p = pw[t * 8 + hh];
-#pragma unroll
-              for (int d = 0; d < PVD; ++d) acc[hh][d] = fmaf(p, vv[d], acc[hh][d]);
-            }
-          }
-          __syncwarp();
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[st]);
-      advance(cur, a, vp.n_sessions, vp.h_kv);
     }
-    if (!aborted && kAttend && seg_q >= 0) flush(seg_q);
+    return m;
+  };
+  auto bcast = [&](const BlockMeta& m, int src) {
+    BlockMeta r;
+    r.q = __shfl_sync(0xffffffffu, m.q, src);
+    r.s = __shfl_sync(0xffffffffu, m.s, src);
+    r.i = __shfl_sync(0xffffffffu, m.i, src);
+    r.valid = __shfl_sync(0xffffffffu, m.valid, src);
+    r.ysrc = __shfl_sync(0xffffffffu, m.ysrc, src);
+    return r;
+  };
+  auto issue_k = [&](const BlockMeta& m) {
+    if (lane == 0) {
+      if (m.valid > 0) {
+        mbar_arrive_expect_tx(&full_k[warp], Q::PAGE);
+#pragma unroll
+        for (int b = 0; b < Q::BOXES; ++b) tma_load_2d(kbuf + b * Q::BOX, &tm_ksrc, 64 * b, m.ysrc, &full_k[warp]);
+      } else {
+        mbar_arrive(&full_k[warp]);
+      }
+    }
+  };
+  auto issue_v = [&](const BlockMeta& m) {
+    if (lane == 0) {
+      if (m.valid > 0) {
+        mbar_arrive_expect_tx(&full_v[warp], Q::PAGE);
+#pragma unroll
+        for (int b = 0; b < Q::BOXES; ++b) tma_load_2d(vbuf + b * Q::BOX, &tm_vsrc, 64 * b, m.ysrc, &full_v[warp]);
+      } else {
+        mbar_arrive(&full_v[warp]);
+      }
+    }
+  };
+
+  // ------------------------------------------------------------ attention state of this warp
+  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group (query head) and column pair
+  uint32_t qa[Q::KS][4];                     // query A fragments: rows 0..7 bf16 hi, rows 8..15 bf16 residual
+  float o[Q::NO][4];                         // output accumulators: [0..1] hi part, [2..3] residual part
+  float m_run = -INFINITY, l_run = 0.f;      // head gq, log2 domain; l is this thread's partial sum
+  int seg = -1, last_written = seg_first - 1;
+
+  auto write_record = [&](int sq, bool neutral) {
+    if (!kAttend) return;
+    float l = neutral ? 0.f : l_run;
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (gq >= G) return;
+    float* rec = vp.rec + (((int64_t)(c + sq) * kWarps + warp) * G + gq) * (2 + D);
+    if (tq == 0) {
+      rec[0] = neutral ? -INFINITY : m_run;
+      rec[1] = l;
+    }
+#pragma unroll
+    for (int n = 0; n < Q::NO; ++n) {
+      rec[2 + 8 * n + 2 * tq] = neutral ? 0.f : o[n][0] + o[n][2];
+      rec[2 + 8 * n + 2 * tq + 1] = neutral ? 0.f : o[n][1] + o[n][3];
+    }
+  };
+  auto neutral_upto = [&](int sq_end) {  // neutral records for segments (last_written, sq_end)
+    for (int sq = last_written + 1; sq < sq_end; ++sq) write_record(sq, true);
+    if (sq_end - 1 > last_written) last_written = sq_end - 1;
+  };
+
+  auto begin_segment = [&](const BlockMeta& m) {
+    const int nk = a.n_keep[m.s];
+    int L;
+    if (MODE == 1) {
+      L = vp.view_len[m.q];
+      if (L < 0 || L > Lcap) {  // caller-supplied: clamp so the table reads stay in range
+        if (lane == 0) atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
+        L = L < 0 ? 0 : Lcap;
+      }
+    } else {
+      const int last = vp.kept[(int64_t)m.q * vp.budget + nk - 1];
+      L = 32 * (nk - 1) + ((last >= 0 && last < a.n_blk[m.s]) ? block_tokens(last, a, m.s) : 32);
+      if (m.i == 0 && lane == 0) vp.view_len[m.q] = L;
+    }
+    if (!kAttend) return;
+    // RoPE(q, L) for this thread's fragment elements: head gq, dims 16kk + 2tq + {0,1,8,9} (kk < KS/2),
+    // each paired with the same dim + d/2, which sits in k-step kk + KS/2 at the same place
+    const int g = m.q % vp.h_kv;
+    const float2* bb = vp.rope_base + (int64_t)(L >> 5) * (D / 2);
+    const float2* oo = vp.rope_off + (L & 31) * (D / 2);
+    const uint16_t* qh = vp.q + ((int64_t)m.s * vp.h_q + g * G + (gq < G ? gq : 0)) * D;
+#pragma unroll
+    for (int kk = 0; kk < Q::KS / 2; ++kk) {
+      float y1[4], y2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int dim = 16 * kk + 2 * tq + (e & 1) + 8 * (e >> 1);
+        const float x1 = __uint_as_float((uint32_t)qh[dim] << 16);
+        const float x2 = __uint_as_float((uint32_t)qh[dim + D / 2] << 16);
+        const float2 o2 = oo[dim];
+        float cs, sn;
+        rope_cs(bb[dim], o2.x, o2.y, cs, sn);
+        y1[e] = gq < G ? (x1 * cs - x2 * sn) * vp.q_scale : 0.f;
+        y2[e] = gq < G ? (x2 * cs + x1 * sn) * vp.q_scale : 0.f;
+      }
+      split2(y1[0], y1[1], qa[kk][0], qa[kk][1]);
+      split2(y1[2], y1[3], qa[kk][2], qa[kk][3]);
+      split2(y2[0], y2[1], qa[kk + Q::KS / 2][0], qa[kk + Q::KS / 2][1]);
+      split2(y2[2], y2[3], qa[kk + Q::KS / 2][2], qa[kk + Q::KS / 2][3]);
+    }
+#pragma unroll
+    for (int n = 0; n < Q::NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m_run = -INFINITY;
+    l_run = 0.f;
+  };
+
+  // ------------------------------------------------------------ main loop over this warp's blocks
+  BlockMeta batch = resolve(0);
+  BlockMeta cur = bcast(batch, 0);
+  if (nblk_w > 0) {
+    issue_k(cur);
+    issue_v(cur);
   }
-  __syncthreads();
+  bool aborted = false;
+  for (int64_t j = 0; j < nblk_w; ++j) {
+    const uint32_t phase = (uint32_t)(j & 1);
+    // metadata of the next block (the batch is refilled every 32 blocks)
+    BlockMeta nxt{-1, 0, 0, 0, 0};
+    if (j + 1 < nblk_w) {
+      if (((j + 1) & 31) == 0) batch = resolve(j + 1);
+      nxt = bcast(batch, (int)((j + 1) & 31));
+    }
+    if (cur.q != seg) {
+      if (seg >= 0) {
+        write_record(seg, false);
+        last_written = seg;
+      }
+      neutral_upto(cur.q);
+      seg = cur.q;
+      begin_segment(cur);
+    }
+    const int valid = cur.valid;
+    const int64_t ydst = (int64_t)cur.q * Lcap + 32 * cur.i;
+
+    // ---- K: wait, rotate in place, store (the abort decision is made by the whole warp)
+    if (__any_sync(0xffffffffu, !mbar_wait(&full_k[warp], phase, vp.status))) {
+      aborted = true;
+      break;
+    }
+    if (valid > 0 && kWrite) {
+      const int cc = lane % Q::CPR;
+      float2 bb[8];
+      {
+        const float4* bp = reinterpret_cast<const float4*>(vp.rope_base + (int64_t)cur.i * (D / 2) + 8 * cc);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float4 t = __ldg(bp + u);
+          bb[2 * u] = make_float2(t.x, t.y);
+          bb[2 * u + 1] = make_float2(t.z, t.w);
+        }
+      }
+#pragma unroll 2
+      for (int pass = 0; pass < Q::PASSES; ++pass) {
+        const int r = lane / Q::CPR + Q::RPP * pass;
+        const uint32_t a1 = kaddr + chunk_off(r, cc), a2 = kaddr + chunk_off(r, cc + D / 16);
+        const uint4 w1 = lds128(a1), w2 = lds128(a2);
+        const uint32_t xa[4] = {w1.x, w1.y, w1.z, w1.w}, xb[4] = {w2.x, w2.y, w2.z, w2.w};
+        uint32_t oa[4], ob[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float4 ofs = off_s[(r * 4 + u) * Q::CPR + cc];
+          float f1[2], f2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int v = 2 * u + e;
+            float cs, sn;
+            rope_cs(bb[v], e ? ofs.z : ofs.x, e ? ofs.w : ofs.y, cs, sn);
+            const float x1 = e ? bf16hi(xa[u]) : bf16lo(xa[u]);
+            const float x2 = e ? bf16hi(xb[u]) : bf16lo(xb[u]);
+            f1[e] = fmaf(x1, cs, -x2 * sn);
+            f2[e] = fmaf(x2, cs, x1 * sn);
+            // fp32 tables put |error| <= 3e-7 (|x1| + |x2|) on f, below one bf16 ulp of the result unless
+            // the rotation cancels; those pairs are redone in float-float so every stored key is within
+            // one ulp of the exact rotation.
+            const float tau = 0x1p-12f * (fabsf(x1) + fabsf(x2));
+            if (fminf(fabsf(f1[e]), fabsf(f2[e])) < tau)
+              rotate_exact(x1, x2, vp.rope_base_hl[(int64_t)cur.i * (D / 2) + 8 * cc + v],
+                           vp.rope_off_hl[r * (D / 2) + 8 * cc + v], f1[e], f2[e]);
+          }
+          oa[u] = pack_bf16x2(f1[0], f1[1]);
+          ob[u] = pack_bf16x2(f2[0], f2[1]);
+        }
+        sts128(a1, make_uint4(oa[0], oa[1], oa[2], oa[3]));
+        sts128(a2, make_uint4(ob[0], ob[1], ob[2], ob[3]));
+        if (valid < 32 && r < valid) {  // partial block: plain stores of the rows present
+          uint16_t* kd = vp.k_view + (ydst + r) * D;
+          *reinterpret_cast<uint4*>(kd + 8 * cc) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+          *reinterpret_cast<uint4*>(kd + D / 2 + 8 * cc) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (valid == 32 && lane == 0) {
+#pragma unroll
+        for (int b = 0; b < Q::BOXES; ++b) tma_store_2d(&tm_kdst, 64 * b, (int)ydst, kbuf + b * Q::BOX);
+        bulk_commit();
+      }
+    }
+
+    // ---- scores S = q . K^T for the block's 32 tokens (4 n-tiles of 8)
+    float sc[4][4];
+#pragma unroll
+    for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+    if (kAttend && valid > 0) {
+#pragma unroll
+      for (int kk = 0; kk < Q::KS; ++kk) {
+#pragma unroll
+        for (int np = 0; np < 2; ++np) {
+          const int tok = 16 * np + (lane & 7) + 8 * (lane >> 4);
+          const int chk = 2 * kk + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kaddr + chunk_off(tok, chk), b0, b1, b2, b3);
+          mma_16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+          mma_16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+        }
+      }
+    }
+    // the K page is no longer needed: once its store has read it, fetch the next block's K
+    __syncwarp();
+    if (lane == 0) {
+      bulk_wait_read_all();
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (j + 1 < nblk_w) issue_k(nxt);
+
+    // ---- V: wait, store, P.V
+    if (__any_sync(0xffffffffu, !mbar_wait(&full_v[warp], phase, vp.status))) {
+      aborted = true;
+      break;
+    }
+    if (valid > 0 && kWrite) {
+      if (valid == 32) {
+        if (lane == 0) {
+#pragma unroll
+          for (int b = 0; b < Q::BOXES; ++b) tma_store_2d(&tm_vdst, 64 * b, (int)ydst, vbuf + b * Q::BOX);
+          bulk_commit();
+        }
+      } else {
+        const int cc = lane % Q::CPR;
+#pragma unroll 1
+        for (int pass = 0; pass < Q::PASSES; ++pass) {
+          const int r = lane / Q::CPR + Q::RPP * pass;
+          if (r < valid) {
+            uint16_t* vd = vp.v_view + (ydst + r) * D;
+            *reinterpret_cast<uint4*>(vd + 8 * cc) = lds128(vaddr + chunk_off(r, cc));
+            *reinterpret_cast<uint4*>(vd + D / 2 + 8 * cc) = lds128(vaddr + chunk_off(r, cc + D / 16));
+          }
+        }
+      }
+    }
+    if (kAttend && valid > 0) {
+      if (valid < 32) {  // rows past the tail may hold any bits: zero them before P.V
+        __syncwarp();
+        const int cc = lane % Q::CPR;
+#pragma unroll 1
+        for (int pass = 0; pass < Q::PASSES; ++pass) {
+          const int r = lane / Q::CPR + Q::RPP * pass;
+          if (r >= valid) {
+            sts128(vaddr + chunk_off(r, cc), make_uint4(0, 0, 0, 0));
+            sts128(vaddr + chunk_off(r, cc + D / 16), make_uint4(0, 0, 0, 0));
+          }
+        }
+        __syncwarp();
+      }
+      // online softmax for head gq over this block
+      float s[8], bm = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < 4; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int tok = 8 * n + 2 * tq + e;
+          const float v = sc[n][e] + sc[n][2 + e];
+          s[2 * n + e] = tok < valid ? v : -INFINITY;
+          bm = fmaxf(bm, s[2 * n + e]);
+        }
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+      if (bm > m_run + 8.f) {  // raise the reference only when it grows by more than 8 (a factor 256)
+        const float corr = fast_exp2(m_run - bm);  // 0 when m_run was -inf
+        l_run *= corr;
+#pragma unroll
+        for (int n = 0; n < Q::NO; ++n) {
+          o[n][0] *= corr;
+          o[n][1] *= corr;
+          o[n][2] *= corr;
+          o[n][3] *= corr;
+        }
+        m_run = bm;
+      }
+      uint32_t ph[4], pl[4];  // P for n-tiles 0..3: bf16 hi and residual, packed pairs
+#pragma unroll
+      for (int n = 0; n < 4; ++n) {
+        const float p0 = fast_exp2(s[2 * n] - m_run), p1 = fast_exp2(s[2 * n + 1] - m_run);
+        l_run += p0 + p1;
+        split2(p0, p1, ph[n], pl[n]);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+        for (int np = 0; np < Q::NO / 2; ++np) {
+          const int tok = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
+          const int chk = 2 * np + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vaddr + chunk_off(tok, chk), b0, b1, b2, b3);
+          mma_16816(o[2 * np], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b0, b1);
+          mma_16816(o[2 * np + 1], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b2, b3);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      bulk_wait_read_all();
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (j + 1 < nblk_w) issue_v(nxt);
+    cur = nxt;
+  }
+  if (aborted) {
+    // drain: copies already issued for this warp's stage must land before the CTA exits
+    if (lane == 0) {
+      bulk_wait_all();
+      mbar_wait(&full_k[warp], 0, vp.status);
+      mbar_wait(&full_k[warp], 1, vp.status);
+      mbar_wait(&full_v[warp], 0, vp.status);
+      mbar_wait(&full_v[warp], 1, vp.status);
+    }
+    return;
+  }
+  if (seg >= 0) {
+    write_record(seg, false);
+    last_written = seg;
+  }
+  neutral_upto(seg_last + 1);
+  if (lane == 0) bulk_wait_all();
 }
 
 // Merges the partial records of each (session, query head) and writes out;
@@ -528,54 +615,27 @@ __global__ void combine_kernel(const ViewParams vp, const SessionArgs a, int att
   const int c0 = cta_of(start, vp.total, vp.P), c1 = cta_of(end, vp.total, vp.P);
   // CTAs between c0 and c1 with an empty share wrote no record: skip them
   auto empty = [&](int c) { return cta_begin(c, vp.total, vp.P) >= cta_begin(c + 1, vp.total, vp.P); };
+  auto rec = [&](int c, int w) { return vp.rec + (((int64_t)(c + q) * kWarps + w) * G + hh) * (2 + D); };
   float M = -INFINITY;
   for (int c = c0; c <= c1; ++c)
-    if (!empty(c)) M = fmaxf(M, vp.rec[((int64_t)(c + q) * G + hh) * (2 + D)]);
+    if (!empty(c))
+      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, rec(c, w)[0]);
   for (int dim = threadIdx.x; dim < D; dim += blockDim.x) {
     float av = 0.f, lv = 0.f;
     if (M != -INFINITY) {
       for (int c = c0; c <= c1; ++c) {
         if (empty(c)) continue;
-        const float* rc = vp.rec + ((int64_t)(c + q) * G + hh) * (2 + D);
-        const float sc = exp2f(rc[0] - M);
-        av = fmaf(rc[2 + dim], sc, av);
-        lv = fmaf(rc[1], sc, lv);
+        for (int w = 0; w < kWarps; ++w) {
+          const float* rc = rec(c, w);
+          if (rc[0] == -INFINITY) continue;
+          const float sc = exp2f(rc[0] - M);
+          av = fmaf(rc[2 + dim], sc, av);
+          lv = fmaf(rc[1], sc, lv);
+        }
       }
     }
     vp.out[((int64_t)s * vp.h_q + h) * D + dim] = lv > 0.f ? av / lv : 0.f;
   }
-}
-
-template <int D, int G>
-cudaError_t launch_dg(const Ctx& c, int mode, const ViewParams& vp, const SessionArgs& a, cudaStream_t st) {
-  using Q = Geo<D>;
-  const size_t smem = (size_t)Q::NSTAGE * 2 * Q::PAGE + (size_t)Q::NCW * G * (2 + D) * 4 +
-                      (size_t)Q::NCW * Q::TPW * 8 * 4;
-  cudaError_t e = cudaSuccess;
-  if (vp.total > 0) {
-    void (*kern)(const ViewParams, const SessionArgs) =
-        mode == 0 ? view_kernel<D, G, 0> : (mode == 1 ? view_kernel<D, G, 1> : view_kernel<D, G, 2>);
-    if ((e = ensure_smem(kern, c.device, smem)) != cudaSuccess) return e;
-    kern<<<vp.P, Q::NT, smem, st>>>(vp, a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  combine_kernel<D, G><<<vp.n_sessions * vp.h_q, D, 0, st>>>(vp, a, mode != 0);
-  return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t launch_d(const Ctx& c, int mode, const ViewParams& vp, const SessionArgs& a, cudaStream_t st) {
-  switch (c.group) {
-    case 1: return launch_dg<D, 1>(c, mode, vp, a, st);
-    case 2: return launch_dg<D, 2>(c, mode, vp, a, st);
-    case 3: return launch_dg<D, 3>(c, mode, vp, a, st);
-    case 4: return launch_dg<D, 4>(c, mode, vp, a, st);
-    case 5: return launch_dg<D, 5>(c, mode, vp, a, st);
-    case 6: return launch_dg<D, 6>(c, mode, vp, a, st);
-    case 7: return launch_dg<D, 7>(c, mode, vp, a, st);
-    case 8: return launch_dg<D, 8>(c, mode, vp, a, st);
-  }
-  return cudaErrorInvalidValue;
 }
 
 // RoPE tables computed in fp64: base[slot][i] = (cos, sin)(32*slot*theta_i), off[r][i] = (cos, sin)(r*theta_i),
@@ -605,6 +665,71 @@ __global__ void rope_table_kernel(float2* base, int n_slots, float2* off, float4
   }
 }
 
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over rows of d bf16 values: boxes of 64 columns x 32 rows, 128-byte swizzle.
+cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, int d) {
+  memset(m, 0, sizeof(*m));
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  if (rows < 32) rows = 32;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const Ctx& c, int mode, const CUtensorMap* maps, const ViewParams& vp, const SessionArgs& a,
+                      cudaStream_t st) {
+  using Q = Geo<D>;
+  const size_t smem = (size_t)kWarps * 2 * Q::PAGE + (size_t)32 * 4 * Q::CPR * sizeof(float4) + 1024;
+  cudaError_t e = cudaSuccess;
+  if (vp.total > 0) {
+    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ViewParams,
+                 const SessionArgs) =
+        mode == 0 ? view_kernel<D, G, 0> : (mode == 1 ? view_kernel<D, G, 1> : view_kernel<D, G, 2>);
+    if ((e = ensure_smem(kern, c.device, smem)) != cudaSuccess) return e;
+    kern<<<vp.P, kWarps * 32, smem, st>>>(maps[0], maps[1], maps[2], maps[3], vp, a);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  combine_kernel<D, G><<<vp.n_sessions * vp.h_q, D, 0, st>>>(vp, a, mode != 0);
+  return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const Ctx& c, int mode, const CUtensorMap* maps, const ViewParams& vp, const SessionArgs& a,
+                     cudaStream_t st) {
+  switch (c.group) {
+    case 1: return launch_dg<D, 1>(c, mode, maps, vp, a, st);
+    case 2: return launch_dg<D, 2>(c, mode, maps, vp, a, st);
+    case 3: return launch_dg<D, 3>(c, mode, maps, vp, a, st);
+    case 4: return launch_dg<D, 4>(c, mode, maps, vp, a, st);
+    case 5: return launch_dg<D, 5>(c, mode, maps, vp, a, st);
+    case 6: return launch_dg<D, 6>(c, mode, maps, vp, a, st);
+    case 7: return launch_dg<D, 7>(c, mode, maps, vp, a, st);
+    case 8: return launch_dg<D, 8>(c, mode, maps, vp, a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,
@@ -612,11 +737,9 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
                         const uint16_t* q, uint16_t* k_view, uint16_t* v_view, int32_t* view_len, float* out,
                         cudaStream_t st) {
   ViewParams vp;
-  vp.k_src = k_src;
-  vp.v_src = v_src;
-  vp.n_pages = n_pages;
   vp.bt = bt;
   vp.max_blocks = c.p.max_blocks;
+  vp.n_pages = n_pages;
   vp.kept = kept;
   vp.q = q;
   vp.k_view = k_view;
@@ -636,13 +759,30 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
   vp.n_sessions = n_sessions;
   vp.P = c.view_ctas;
   vp.q_scale = (float)(1.4426950408889634 / sqrt((double)c.p.d));
-  return c.p.d == 128 ? launch_d<128>(c, mode, vp, a, st) : launch_d<64>(c, mode, vp, a, st);
+  // tensor maps: sources (pool pages, or the view for mode 1) and destinations (the view)
+  const uint64_t view_rows = (uint64_t)n_sessions * c.p.h_kv * 32 * c.budget;
+  const uint64_t pool_rows = (uint64_t)n_pages * c.p.h_kv * 32;
+  if (pool_rows > 0x7FFFFFFFull || view_rows > 0x7FFFFFFFull) return cudaErrorInvalidValue;
+  CUtensorMap maps[4];
+  cudaError_t e;
+  if (mode == 1) {
+    if ((e = make_map(&maps[0], k_src, view_rows, c.p.d)) != cudaSuccess) return e;
+    if ((e = make_map(&maps[1], v_src, view_rows, c.p.d)) != cudaSuccess) return e;
+    maps[2] = maps[0];
+    maps[3] = maps[1];
+  } else {
+    if ((e = make_map(&maps[0], k_src, pool_rows, c.p.d)) != cudaSuccess) return e;
+    if ((e = make_map(&maps[1], v_src, pool_rows, c.p.d)) != cudaSuccess) return e;
+    if ((e = make_map(&maps[2], k_view, view_rows, c.p.d)) != cudaSuccess) return e;
+    if ((e = make_map(&maps[3], v_view, view_rows, c.p.d)) != cudaSuccess) return e;
+  }
+  return c.p.d == 128 ? launch_d<128>(c, mode, maps, vp, a, st) : launch_d<64>(c, mode, maps, vp, a, st);
 }
 
 cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st) {
   rope_table_kernel<<<256, 256, 0, st>>>(reinterpret_cast<float2*>(c.rope_base), c.budget + 1,
-                                         reinterpret_cast<float2*>(c.rope_off),
-                                         c.rope_base_hl, c.rope_off_hl, c.p.d, (double)c.p.rope_theta);
+                                         reinterpret_cast<float2*>(c.rope_off), c.rope_base_hl, c.rope_off_hl, c.p.d,
+                                         (double)c.p.rope_theta);
   return cudaGetLastError();
 }
 
