@@ -22,7 +22,9 @@
  * --------------------------------
  * - bf16 tensors are passed as uint16_t bit patterns.  fp32 is float.
  * - Unless a parameter says "host", every pointer is DEVICE memory owned by the
- *   caller (for example a PyTorch tensor); the library never frees it.
+ *   caller (for example a PyTorch tensor); the library never frees it.  K/V
+ *   pools, views, queries, the index and attention outputs must be 16-byte
+ *   aligned; int32 arrays 4-byte aligned (KVM_ERR_INVALID_ARG otherwise).
  * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *   stream).  Every call only enqueues work on it and returns; nothing
  *   synchronises the host except kvm_create, kvm_destroy and kvm_device_status.
@@ -209,7 +211,9 @@ kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint
 /*
  * Reads (and optionally clears) the device status word after synchronising
  * `stream`.  *out receives the KVM_DEV_* bits.  Returns KVM_OK when the word
- * is zero, KVM_ERR_DEVICE or KVM_ERR_TIMEOUT otherwise.
+ * is zero, KVM_ERR_DEVICE or KVM_ERR_TIMEOUT otherwise.  A timed-out view
+ * call leaves its attention outputs unwritten; clearing a non-zero word also
+ * resets the context's per-call merge state, so the context can be reused.
  */
 kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* stream);
 

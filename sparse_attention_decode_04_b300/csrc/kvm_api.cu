@@ -151,12 +151,14 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   const size_t S = (size_t)p->max_sessions;
   const size_t sz_e = S * p->h_kv * (size_t)p->max_blocks * c.group * sizeof(float);
   const size_t sz_part = S * p->h_q * (size_t)c.max_tiles * sizeof(float2);
-  const size_t sz_rec = ((size_t)c.view_ctas + S * p->h_kv) * kvm::kViewWarps * c.group * (2 + p->d) * sizeof(float);
+  const size_t sz_rec =
+      ((size_t)c.view_ctas + S * p->h_kv) * (kvm::kViewWarps + 1) * c.group * (4 + p->d) * sizeof(float);
+  const size_t sz_cnt = S * p->h_kv * sizeof(uint32_t);
   const size_t sz_base = (size_t)(budget + 1) * (p->d / 2) * sizeof(float2);
   const size_t sz_off = (size_t)32 * (p->d / 2) * sizeof(float2);
-  constexpr int kBufs = 8;
+  constexpr int kBufs = 9;
   void* ptrs[kBufs] = {};
-  const size_t sizes[kBufs] = {sz_e, sz_part, sz_rec, sz_base, sz_off, 256, 2 * sz_base, 2 * sz_off};
+  const size_t sizes[kBufs] = {sz_e, sz_part, sz_rec, sz_base, sz_off, 256, sz_base, sz_off, sz_cnt};
   for (int i = 0; i < kBufs && e == cudaSuccess; ++i) e = cudaMalloc(&ptrs[i], sizes[i]);
   if (e != cudaSuccess) {
     for (void* q : ptrs)
@@ -170,8 +172,9 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   c.rope_base = (float*)ptrs[3];
   c.rope_off = (float*)ptrs[4];
   c.status = (uint32_t*)ptrs[5];
-  c.rope_base_hl = (float4*)ptrs[6];
-  c.rope_off_hl = (float4*)ptrs[7];
+  c.rope_base_lo = (float*)ptrs[6];
+  c.rope_off_lo = (float*)ptrs[7];
+  c.seg_count = (uint32_t*)ptrs[8];
   for (size_t s : sizes) c.bytes += s;
   if (p->max_queries > 1) {
     c.step_blk_cap_pad = (p->max_blocks + 255) / 256 * 256;
@@ -194,6 +197,7 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
     }
   }
   e = cudaMemset(c.status, 0, 256);
+  if (e == cudaSuccess) e = cudaMemset(c.seg_count, 0, sz_cnt);
   if (e == cudaSuccess) e = kvm::launch_rope_tables(c, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
@@ -211,8 +215,8 @@ kvm_status kvm_destroy(kvm_ctx* ctx) {
   cudaGetDevice(&prev);
   if (prev != c.device) cudaSetDevice(c.device);
   cudaError_t e = cudaDeviceSynchronize();
-  void* ptrs[13] = {c.e_buf,      c.part,       c.rec,      c.rope_base, c.rope_off,   c.status,  c.rope_base_hl,
-                    c.rope_off_hl, c.step_kpk,   c.step_qpk, c.step_part, c.step_stats, c.step_gs};
+  void* ptrs[14] = {c.e_buf,      c.part,       c.rec,      c.rope_base, c.rope_off,   c.status,  c.rope_base_lo,
+                    c.rope_off_lo, c.step_kpk,   c.step_qpk, c.step_part, c.step_stats, c.step_gs, c.seg_count};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   if (prev >= 0 && prev != c.device) cudaSetDevice(prev);
@@ -295,8 +299,8 @@ static kvm_status view_call(kvm_ctx* ctx, int mode, const uint16_t* k_src, const
   if (mode != 0 && (!q || !out)) return fail(KVM_ERR_INVALID_ARG, "NULL q or out");
   if (mode != 1 && n_pages < 1) return fail(KVM_ERR_INVALID_ARG, "n_pages=%lld must be >= 1", (long long)n_pages);
   if (!aligned(k_src, 16) || !aligned(v_src, 16) || !aligned(k_view, 16) || !aligned(v_view, 16) ||
-      !aligned(q, 16) || !aligned(out, 4) || !aligned(view_len, 4) || !aligned(kept_ids, 4))
-    return fail(KVM_ERR_INVALID_ARG, "K/V/q buffers must be 16-byte aligned");
+      !aligned(q, 16) || !aligned(out, 16) || !aligned(view_len, 4) || !aligned(kept_ids, 4))
+    return fail(KVM_ERR_INVALID_ARG, "K/V/q/out buffers must be 16-byte aligned");
   SessionArgs a;
   if (mode == 1) {
     // the view lengths live on the device: walk every slot of each view, skip the empty ones
@@ -347,6 +351,9 @@ kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* s
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
   if (e == cudaSuccess) e = cudaMemcpy(out, ctx->c.status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && clear) e = cudaMemset(ctx->c.status, 0, sizeof(uint32_t));
+  // a stopped view kernel may have left segment arrival counters behind: clearing restarts them
+  if (e == cudaSuccess && clear && *out != 0)
+    e = cudaMemset(ctx->c.seg_count, 0, sizeof(uint32_t) * ctx->c.p.max_sessions * ctx->c.p.h_kv);
   if (e != cudaSuccess) return cuda_fail(e, "kvm_device_status");
   if (*out == 0) return KVM_OK;
   if (*out & KVM_DEV_TIMEOUT) return fail(KVM_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", *out);

@@ -12,7 +12,7 @@ namespace kvm {
 constexpr int kBlock = 32;            // tokens per block / page
 constexpr int kMaxGroup = 8;          // query heads per KV head
 constexpr int kMaxSessionsHost = 64;  // sessions per call (kernel-parameter arrays)
-constexpr int kViewWarps = 8;         // warps (and attention-record slots) per view-kernel CTA
+constexpr int kViewWarps = 5;         // consumer warps (attention-record slots) per view-kernel CTA
 
 // Per-session values passed by value to the kernels (they size the grids, so
 // they live on the host; passing them as kernel parameters keeps every call
@@ -37,11 +37,12 @@ struct Ctx {
   // scratch (device)
   float* e_buf = nullptr;      // [S][h_kv][max_blocks][group] exp(s - tile max), log2 domain
   float2* part = nullptr;      // [S][h_q][max_tiles] (tile max, tile sum) in log2 domain
-  float* rec = nullptr;        // [view_ctas + S*h_kv][kViewWarps][group][2 + d] attention partials
+  float* rec = nullptr;        // [view_ctas + S*h_kv][kViewWarps + 1][group][4 + d] attention partials
+  uint32_t* seg_count = nullptr;  // [S*h_kv] CTAs of a view call done with each segment (0 between calls)
   float* rope_base = nullptr;  // [budget + 1][d/2][2] cos/sin of 32*slot*theta_i
   float* rope_off = nullptr;   // [32][d/2][2] cos/sin of r*theta_i
-  float4* rope_base_hl = nullptr;  // the same tables as fp32 hi/lo pairs (cos_h, cos_l, sin_h, sin_l)
-  float4* rope_off_hl = nullptr;   // read only on the cancellation fallback
+  float* rope_base_lo = nullptr;  // [budget + 1][d/2][2] what the fp32 rounding of rope_base dropped
+  float* rope_off_lo = nullptr;   // [32][d/2][2] the same for rope_off (read on the cancellation fallback)
   uint32_t* status = nullptr;  // device status word
   int64_t max_tiles = 0;
   // step-level (multi-query) scoring scratch, allocated when max_queries > 1

@@ -14,30 +14,42 @@
 //   mode 2  fused:       pages -> views + attention partials (each page read once)
 // Work: the flat list of kept blocks over (session, KV head).  A persistent grid
 // of one CTA per SM takes equal contiguous shares, so every SM streams the same
-// number of pages.  Inside a CTA, eight warps each own one shared-memory stage
-// (a K page and a V page) and take every eighth block of the share; warps never
-// wait on one another.  Per block, a warp:
-//   - receives the K and V pages by TMA tiled loads (64-column boxes) with the
-//     128-byte swizzle, so the ldmatrix reads below are free of bank conflicts;
-//   - rotates K in place at view positions 32*i + r (cos/sin composed in fp32
-//     from a per-slot and a per-offset table, both filled in fp64; pairs whose
-//     rotation cancels are redone in float-float), rounds to bf16, and writes
-//     the rotated K and the untouched V to the view with TMA tiled stores;
-//   - computes the scores with mma.sync (m16n8k16, bf16 -> fp32): A rows 0..7
-//     hold the rotated, scaled query heads rounded to bf16 and rows 8..15 their
-//     bf16 residuals, so one MMA gives both halves and their sum is an
-//     fp32-accurate score;
-//   - keeps an online softmax per head in the log2 domain (the running maximum
-//     is raised only when it grows by more than 8, so rescaling is rare);
-//   - accumulates P.V with mma.sync, P split the same way into bf16 + residual.
-// The next block's K page is fetched as soon as the scores are done, its V page
-// as soon as P.V is done, so the copies overlap the rest of the block's work.
-// Each warp writes one partial record (max, sum, output) per segment (session,
-// KV head) of its CTA's share — a neutral record for a segment it had no block
-// of — at index ((cta + segment) * 8 + warp), which is unique.  The combine
-// kernel merges the records of each (session, query head).
-// Every mbarrier wait is bounded; a timeout sets KVM_DEV_TIMEOUT and the warp
-// drains its copies and stops.
+// number of pages.  Each CTA is warp-specialised:
+//   - a producer warp resolves 32 blocks at a time (kept id -> page, one lane
+//     each, the next 32 resolved while the current 32 are issued) and keeps a
+//     ring of NS shared-memory stages full: per block one stage receives the K
+//     and V pages by TMA tiled loads (64-column boxes, 128-byte swizzle) and,
+//     when writing a view, the block's rows of the RoPE base tables by 1-D bulk
+//     copies, all completing on the stage's `full` mbarrier;
+//   - five consumer warps take every fifth block of the share.  Block j uses
+//     stage j mod NS with NS a multiple of five, so each consumer owns NS/5
+//     stages and meets their rounds strictly in order: a wait on a stage's
+//     barrier is never more than one phase ahead, which the parity waits need.  Per block a
+//     consumer rotates K in place at view positions 32*i + r (cos/sin composed
+//     in fp32 from the staged per-slot row and a per-offset table held in
+//     shared memory, both filled in fp64; pairs whose rotation cancels are
+//     redone in float-float from the hi/lo halves), rounds to bf16 and writes
+//     the rotated K and the untouched V to the view with TMA tiled stores; then
+//     computes the scores with mma.sync (m16n8k16, bf16 -> fp32; A rows 0..7
+//     hold the rotated, scaled query heads rounded to bf16, rows 8..15 their
+//     bf16 residuals, so one MMA gives an fp32-accurate score), keeps an
+//     online softmax per head in the log2 domain (the running maximum is
+//     raised only when it grows by more than 8) and accumulates P.V with
+//     mma.sync, P split the same way; finally it frees the stage on its
+//     `empty` mbarrier once its stores have read the stage.
+// No consumer ever reads global memory on the per-block path.  Each consumer
+// writes one partial record (max, sum, output) per segment (session, KV head)
+// of its CTA's share — a neutral record for a segment it had no block of — in
+// the record group (cta + segment), which is unique to the pair.  At the end
+// the CTA folds its consumers' records of each segment into one CTA record
+// (log-sum-exp), then counts itself in on each of its segments with one
+// atomic add; the CTA that arrives last on a segment (no CTA ever waits)
+// merges that segment's CTA records with batched independent loads and writes
+// the G output rows, then resets the segment's counter for the next call.
+// Every mbarrier wait is bounded; a timeout sets KVM_DEV_TIMEOUT, the warp
+// stops, the producer waits (bounded) for its copies in flight, and the CTA
+// does not count itself in, so the outputs of its segments are left unwritten
+// (the status word says why).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <string.h>
@@ -50,7 +62,8 @@
 namespace kvm {
 namespace {
 
-constexpr int kWarps = kViewWarps;
+constexpr int kConsumers = kViewWarps;          // consumer warps (attention-record slots) per CTA
+constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
 
 struct ViewParams {
   const int32_t* bt;
@@ -62,13 +75,15 @@ struct ViewParams {
   uint16_t* v_view;
   int32_t* view_len;
   float* rec;
-  const float2* rope_base;     // [budget + 1][d/2]
+  uint32_t* seg_count;         // [n_sessions * h_kv] arrival counters (zero between calls)
+  const float2* rope_base;     // [budget + 1][d/2] (cos, sin) rounded to fp32
+  const float2* rope_base_lo;  // [budget + 1][d/2] what the rounding dropped (cos, sin)
   const float2* rope_off;      // [32][d/2]
-  const float4* rope_base_hl;  // hi/lo copies, read only on the cancellation fallback
-  const float4* rope_off_hl;
+  const float2* rope_off_lo;   // [32][d/2]
   float* out;
   uint32_t* status;
   int64_t total;  // kept blocks over all (session, KV head)
+  int any_empty;  // some session keeps no block
   int budget;
   int h_kv;
   int h_q;
@@ -76,6 +91,10 @@ struct ViewParams {
   int P;  // CTAs
   float q_scale;  // log2(e) / sqrt(d)
 };
+
+// Attention record of one (CTA, segment, warp, query head): max, sum, 2 pad, output[D] (16-byte aligned).
+template <int D>
+constexpr int kRecFloats = 4 + D;
 
 template <int D>
 struct Geo {
@@ -87,6 +106,14 @@ struct Geo {
   static constexpr int PASSES = CPR;            // rotation passes per page
   static constexpr int KS = D / 16;             // MMA k-steps over the head dimension
   static constexpr int NO = D / 8;              // output n-tiles
+  static constexpr int NS = kConsumers * (D == 128 ? 2 : 4);  // pipeline stages, NS / kConsumers per consumer
+  static constexpr uint32_t TAB = D / 2 * 8;     // bytes of one table row ((cos, sin) per pair)
+  // shared memory, from the 1024-byte-aligned base
+  static constexpr uint32_t OFF_TAB = NS * 2 * PAGE;             // [NS][hi row | lo row] base table rows
+  static constexpr uint32_t OFF_OFFHI = OFF_TAB + NS * 2 * TAB;  // [32][4][CPR] float4 offset table (hi)
+  static constexpr uint32_t OFF_OFFLO = OFF_OFFHI + 32 * TAB;    // [32][d/2] float2 offset table (lo)
+  static constexpr uint32_t OFF_META = OFF_OFFLO + 32 * TAB;     // [NS] int: tokens of the staged block
+  static constexpr uint32_t BYTES = OFF_META + NS * 4 + 1024;    // + alignment slack
 };
 
 __device__ __forceinline__ int64_t cta_begin(int c, int64_t total, int P) { return (int64_t)c * total / P; }
@@ -98,12 +125,14 @@ __device__ __forceinline__ int cta_of(int64_t f, int64_t total, int P) {
 struct Cursor {
   int s, g, i;
 };
+// (session, KV head, slot) of flat block f; a session's share is h_kv * n_keep < 2^31 blocks.
 __device__ __forceinline__ Cursor locate(int64_t f, const SessionArgs& a, int n_sessions) {
   int s = 0;
   while (s + 1 < n_sessions && a.seg_base[s + 1] <= f) ++s;
-  const int64_t local = f - a.seg_base[s];
+  const int local = (int)(f - a.seg_base[s]);
   const int nk = a.n_keep[s];
-  return Cursor{s, (int)(local / nk), (int)(local % nk)};
+  const int g = local / nk;
+  return Cursor{s, g, local - g * nk};
 }
 
 // Tokens of kept block `id` present in session s's history.
@@ -154,6 +183,16 @@ __device__ __forceinline__ void rotate_exact(float x1, float x2, float4 b, float
   y2 = r2.h + r2.l;
 }
 
+__device__ __forceinline__ float4 lds128f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float2 lds64f(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -173,478 +212,544 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = pack_bf16x2(x0 - bf16lo(hi), x1 - bf16hi(hi));
 }
 
-struct BlockMeta {
-  int q;      // segment = s * h_kv + g
-  int s;
-  int i;      // index in the segment's kept list (view slot)
-  int valid;  // tokens present (0: skipped)
-  int ysrc;   // source tile row
-};
-
 template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+__global__ void __launch_bounds__(kThreads, 1)
     view_kernel(const __grid_constant__ CUtensorMap tm_ksrc, const __grid_constant__ CUtensorMap tm_vsrc,
                 const __grid_constant__ CUtensorMap tm_kdst, const __grid_constant__ CUtensorMap tm_vdst,
                 const ViewParams vp, const SessionArgs a) {
   using Q = Geo<D>;
   constexpr bool kWrite = MODE != 1;
   constexpr bool kAttend = MODE != 0;
+  constexpr int NS = Q::NS;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  // 1024-byte aligned stages: [warp][K page | V page]; then the offset table [32][4][CPR] float4
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
-  float4* off_s = reinterpret_cast<float4*>(smem + kWarps * 2 * Q::PAGE);
-  __shared__ __align__(8) uint64_t full_k[kWarps], full_v[kWarps];
+  const uint32_t sbase = smem_addr(smem);
+  int* meta = reinterpret_cast<int*>(smem + Q::OFF_META);
+  __shared__ __align__(8) uint64_t full[NS], empty[NS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
+  if (vp.any_empty) {
+    // sessions with no kept block (empty history): zero output rows and view lengths
+    const int64_t per_s = (int64_t)vp.h_q * D, n_out = vp.n_sessions * per_s;
+    for (int64_t idx = (int64_t)c * blockDim.x + tid; idx < n_out; idx += (int64_t)vp.P * blockDim.x) {
+      const int s = (int)(idx / per_s), hd = (int)(idx % per_s);
+      if (a.n_keep[s] != 0) continue;
+      if (kAttend) vp.out[idx] = 0.f;
+      if (hd % (G * D) == 0) vp.view_len[s * vp.h_kv + hd / (G * D)] = 0;
+    }
+  }
   const int64_t fa = cta_begin(c, vp.total, vp.P), fb = cta_begin(c + 1, vp.total, vp.P);
   if (fa >= fb) return;
+  const int64_t nb = fb - fa;  // blocks of this CTA
   const int Lcap = 32 * vp.budget;
 
   if (kWrite) {
-    for (int idx = tid; idx < 32 * 4 * Q::CPR; idx += kWarps * 32) {
+    // offset tables: hi as [r][u][cc] float4 (the pairs 8cc+2u, 8cc+2u+1 of row r), lo as [r][d/2] float2
+    float4* off_hi = reinterpret_cast<float4*>(smem + Q::OFF_OFFHI);
+    float2* off_lo = reinterpret_cast<float2*>(smem + Q::OFF_OFFLO);
+    for (int idx = tid; idx < 32 * 4 * Q::CPR; idx += kThreads) {
       const int r = idx / (4 * Q::CPR), u = (idx / Q::CPR) % 4, cc = idx % Q::CPR;
       const float2 o0 = vp.rope_off[r * (D / 2) + 8 * cc + 2 * u];
       const float2 o1 = vp.rope_off[r * (D / 2) + 8 * cc + 2 * u + 1];
-      off_s[idx] = make_float4(o0.x, o0.y, o1.x, o1.y);
+      off_hi[idx] = make_float4(o0.x, o0.y, o1.x, o1.y);
     }
+    for (int idx = tid; idx < 32 * (D / 2); idx += kThreads) off_lo[idx] = vp.rope_off_lo[idx];
   }
-  if (lane == 0) {
-    mbar_init(&full_k[warp], 1);
-    mbar_init(&full_v[warp], 1);
+  if (tid == 0) {
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], 1);
+    }
     mbar_fence_init();
   }
   __syncthreads();
 
-  unsigned char* kbuf = smem + warp * 2 * Q::PAGE;
-  unsigned char* vbuf = kbuf + Q::PAGE;
-  const uint32_t kaddr = smem_addr(kbuf), vaddr = smem_addr(vbuf);
   const Cursor firstc = locate(fa, a, vp.n_sessions), lastc = locate(fb - 1, a, vp.n_sessions);
   const int seg_first = firstc.s * vp.h_kv + firstc.g;
   const int seg_last = lastc.s * vp.h_kv + lastc.g;
+  bool aborted = false;
+  int64_t issued = 0;  // producer: blocks whose copies were issued
 
-  // ------------------------------------------------------------ per-block metadata, 32 blocks at a time
-  // lane l describes this warp's block number jb + l: flat index fa + warp + 8 * (jb + l)
-  const int64_t nblk_w = (fb - fa - warp + kWarps - 1) / kWarps;  // blocks this warp processes (may be <= 0)
-  auto resolve = [&](int64_t jb) -> BlockMeta {
-    BlockMeta m{-1, 0, 0, 0, 0};
-    const int64_t j = jb + lane;
-    if (j >= nblk_w) return m;
-    const int64_t f = fa + warp + (int64_t)kWarps * j;
-    const Cursor cu = locate(f, a, vp.n_sessions);
-    m.q = cu.s * vp.h_kv + cu.g;
-    m.s = cu.s;
-    m.i = cu.i;
-    if (MODE == 1) {
-      int L = vp.view_len[m.q];
-      L = L < 0 ? 0 : (L > Lcap ? Lcap : L);
-      m.valid = max(0, min(32, L - 32 * cu.i));
-      m.ysrc = m.q * Lcap + 32 * cu.i;
-    } else {
-      const int id = vp.kept[(int64_t)m.q * vp.budget + cu.i];
-      const int prev = cu.i > 0 ? vp.kept[(int64_t)m.q * vp.budget + cu.i - 1] : -1;
-      if (id >= 0 && id < a.n_blk[cu.s] && id > prev) {  // kept ids ascend within a list
-        const int32_t page = vp.bt[(int64_t)cu.s * vp.max_blocks + id];
-        if (page >= 0 && page < vp.n_pages) {
-          m.valid = block_tokens(id, a, cu.s);
-          m.ysrc = (int)(((int64_t)page * vp.h_kv + cu.g) * 32);
+  static_assert(NS % kConsumers == 0, "each consumer owns whole stages");
+  if (warp == kConsumers) {
+    // ============================================================ producer
+    // lane l resolves block jb + l: tokens present (0 = skip), source tile row, view slot
+    auto resolve = [&](int64_t jb, int& valid, int& ysrc, int& slot) {
+      valid = 0;
+      ysrc = 0;
+      slot = 0;
+      const int64_t j = jb + lane;
+      if (j >= nb) return;
+      const Cursor cu = locate(fa + j, a, vp.n_sessions);
+      const int q = cu.s * vp.h_kv + cu.g;
+      slot = cu.i;
+      if (MODE == 1) {
+        int L = vp.view_len[q];
+        L = L < 0 ? 0 : (L > Lcap ? Lcap : L);  // caller-supplied: the consumer reports a bad value
+        valid = max(0, min(32, L - 32 * cu.i));
+        ysrc = q * Lcap + 32 * cu.i;
+      } else {
+        const int id = vp.kept[(int64_t)q * vp.budget + cu.i];
+        const int prev = cu.i > 0 ? vp.kept[(int64_t)q * vp.budget + cu.i - 1] : -1;
+        if (id >= 0 && id < a.n_blk[cu.s] && id > prev) {  // kept ids ascend within a list
+          const int32_t page = vp.bt[(int64_t)cu.s * vp.max_blocks + id];
+          if (page >= 0 && page < vp.n_pages) {
+            valid = block_tokens(id, a, cu.s);
+            ysrc = (int)(((int64_t)page * vp.h_kv + cu.g) * 32);
+          } else {
+            atomicOr(vp.status, KVM_DEV_BAD_PAGE);
+          }
         } else {
-          atomicOr(vp.status, KVM_DEV_BAD_PAGE);
+          atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
+        }
+      }
+    };
+    int v_cur, y_cur, i_cur;
+    resolve(0, v_cur, y_cur, i_cur);
+    for (int64_t jb = 0; jb < nb && !aborted; jb += 32) {
+      int v_nxt = 0, y_nxt = 0, i_nxt = 0;
+      if (jb + 32 < nb) resolve(jb + 32, v_nxt, y_nxt, i_nxt);  // in flight while this batch is issued
+      const int cnt = (int)(nb - jb < 32 ? nb - jb : 32);
+      for (int l = 0; l < cnt; ++l) {
+        const int valid = __shfl_sync(0xffffffffu, v_cur, l);
+        const int ysrc = __shfl_sync(0xffffffffu, y_cur, l);
+        const int slot = __shfl_sync(0xffffffffu, i_cur, l);
+        const int64_t jj = jb + l;
+        const int st = (int)(jj % NS);
+        const uint32_t round = (uint32_t)(jj / NS);
+        int ok = 1;
+        if (lane == 0) {
+          if (round > 0) ok = mbar_wait(&empty[st], (round - 1) & 1, vp.status);
+          if (ok) {
+            meta[st] = valid;
+            unsigned char* kdst = smem + st * 2 * Q::PAGE;
+            if (valid > 0) {
+              mbar_arrive_expect_tx(&full[st], 2 * Q::PAGE + (kWrite ? 2 * Q::TAB : 0));
+#pragma unroll
+              for (int b = 0; b < Q::BOXES; ++b) {
+                tma_load_2d(kdst + b * Q::BOX, &tm_ksrc, 64 * b, ysrc, &full[st]);
+                tma_load_2d(kdst + Q::PAGE + b * Q::BOX, &tm_vsrc, 64 * b, ysrc, &full[st]);
+              }
+              if (kWrite) {
+                unsigned char* tdst = smem + Q::OFF_TAB + st * 2 * Q::TAB;
+                bulk_g2s(tdst, vp.rope_base + (int64_t)slot * (D / 2), Q::TAB, &full[st]);
+                bulk_g2s(tdst + Q::TAB, vp.rope_base_lo + (int64_t)slot * (D / 2), Q::TAB, &full[st]);
+              }
+            } else {
+              mbar_arrive(&full[st]);
+            }
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+          aborted = true;
+          break;
+        }
+        issued = jj + 1;
+      }
+      v_cur = v_nxt;
+      y_cur = y_nxt;
+      i_cur = i_nxt;
+    }
+  } else {
+    // ============================================================ consumers
+    const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group (query head) and column pair
+    uint32_t qa[Q::KS][4];                     // query A fragments: rows 0..7 bf16 hi, rows 8..15 bf16 residual
+    float o[Q::NO][4];                         // output accumulators: [0..1] hi part, [2..3] residual part
+    float m_run = -INFINITY, l_run = 0.f;      // head gq, log2 domain; l is this thread's partial sum
+    int seg = -1, last_written = seg_first - 1;
+
+    auto write_record = [&](int sq, bool neutral) {
+      if (!kAttend) return;
+      float l = neutral ? 0.f : l_run;
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      if (gq >= G) return;
+      float* rec = vp.rec + (((int64_t)(c + sq) * (kConsumers + 1) + warp) * G + gq) * kRecFloats<D>;
+      if (tq == 0) *reinterpret_cast<float2*>(rec) = make_float2(neutral ? -INFINITY : m_run, l);
+#pragma unroll
+      for (int n = 0; n < Q::NO; ++n)
+        *reinterpret_cast<float2*>(rec + 4 + 8 * n + 2 * tq) =
+            neutral ? make_float2(0.f, 0.f) : make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+    };
+    auto neutral_upto = [&](int sq_end) {  // neutral records for segments (last_written, sq_end)
+      for (int sq = last_written + 1; sq < sq_end; ++sq) write_record(sq, true);
+      if (sq_end - 1 > last_written) last_written = sq_end - 1;
+    };
+
+    auto begin_segment = [&](const Cursor& cu, int q) {
+      const int nk = a.n_keep[cu.s];
+      int L;
+      if (MODE == 1) {
+        L = vp.view_len[q];
+        if (L < 0 || L > Lcap) {  // caller-supplied: clamp so the table reads stay in range
+          if (lane == 0) atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
+          L = L < 0 ? 0 : Lcap;
         }
       } else {
-        atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
+        const int last = vp.kept[(int64_t)q * vp.budget + nk - 1];
+        L = 32 * (nk - 1) + ((last >= 0 && last < a.n_blk[cu.s]) ? block_tokens(last, a, cu.s) : 32);
+        if (cu.i == 0 && lane == 0) vp.view_len[q] = L;
       }
-    }
-    return m;
-  };
-  auto bcast = [&](const BlockMeta& m, int src) {
-    BlockMeta r;
-    r.q = __shfl_sync(0xffffffffu, m.q, src);
-    r.s = __shfl_sync(0xffffffffu, m.s, src);
-    r.i = __shfl_sync(0xffffffffu, m.i, src);
-    r.valid = __shfl_sync(0xffffffffu, m.valid, src);
-    r.ysrc = __shfl_sync(0xffffffffu, m.ysrc, src);
-    return r;
-  };
-  auto issue_k = [&](const BlockMeta& m) {
-    if (lane == 0) {
-      if (m.valid > 0) {
-        mbar_arrive_expect_tx(&full_k[warp], Q::PAGE);
+      if (!kAttend) return;
+      // RoPE(q, L) for this thread's fragment elements: head gq, dims 16kk + 2tq + {0,1,8,9} (kk < KS/2),
+      // each paired with the same dim + d/2, which sits in k-step kk + KS/2 at the same place
+      const float2* bb = vp.rope_base + (int64_t)(L >> 5) * (D / 2);
+      const float2* oo = vp.rope_off + (L & 31) * (D / 2);
+      const uint16_t* qh = vp.q + ((int64_t)cu.s * vp.h_q + cu.g * G + (gq < G ? gq : 0)) * D;
 #pragma unroll
-        for (int b = 0; b < Q::BOXES; ++b) tma_load_2d(kbuf + b * Q::BOX, &tm_ksrc, 64 * b, m.ysrc, &full_k[warp]);
-      } else {
-        mbar_arrive(&full_k[warp]);
-      }
-    }
-  };
-  auto issue_v = [&](const BlockMeta& m) {
-    if (lane == 0) {
-      if (m.valid > 0) {
-        mbar_arrive_expect_tx(&full_v[warp], Q::PAGE);
+      for (int kk = 0; kk < Q::KS / 2; ++kk) {
+        float y1[4], y2[4];
 #pragma unroll
-        for (int b = 0; b < Q::BOXES; ++b) tma_load_2d(vbuf + b * Q::BOX, &tm_vsrc, 64 * b, m.ysrc, &full_v[warp]);
-      } else {
-        mbar_arrive(&full_v[warp]);
+        for (int e = 0; e < 4; ++e) {
+          const int dim = 16 * kk + 2 * tq + (e & 1) + 8 * (e >> 1);
+          const float x1 = __uint_as_float((uint32_t)qh[dim] << 16);
+          const float x2 = __uint_as_float((uint32_t)qh[dim + D / 2] << 16);
+          const float2 o2 = oo[dim];
+          float cs, sn;
+          rope_cs(bb[dim], o2.x, o2.y, cs, sn);
+          y1[e] = gq < G ? (x1 * cs - x2 * sn) * vp.q_scale : 0.f;
+          y2[e] = gq < G ? (x2 * cs + x1 * sn) * vp.q_scale : 0.f;
+        }
+        split2(y1[0], y1[1], qa[kk][0], qa[kk][1]);
+        split2(y1[2], y1[3], qa[kk][2], qa[kk][3]);
+        split2(y2[0], y2[1], qa[kk + Q::KS / 2][0], qa[kk + Q::KS / 2][1]);
+        split2(y2[2], y2[3], qa[kk + Q::KS / 2][2], qa[kk + Q::KS / 2][3]);
       }
-    }
-  };
+#pragma unroll
+      for (int n = 0; n < Q::NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+      m_run = -INFINITY;
+      l_run = 0.f;
+    };
 
-  // ------------------------------------------------------------ attention state of this warp
-  const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group (query head) and column pair
-  uint32_t qa[Q::KS][4];                     // query A fragments: rows 0..7 bf16 hi, rows 8..15 bf16 residual
-  float o[Q::NO][4];                         // output accumulators: [0..1] hi part, [2..3] residual part
-  float m_run = -INFINITY, l_run = 0.f;      // head gq, log2 domain; l is this thread's partial sum
-  int seg = -1, last_written = seg_first - 1;
-
-  auto write_record = [&](int sq, bool neutral) {
-    if (!kAttend) return;
-    float l = neutral ? 0.f : l_run;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    if (gq >= G) return;
-    float* rec = vp.rec + (((int64_t)(c + sq) * kWarps + warp) * G + gq) * (2 + D);
-    if (tq == 0) {
-      rec[0] = neutral ? -INFINITY : m_run;
-      rec[1] = l;
-    }
-#pragma unroll
-    for (int n = 0; n < Q::NO; ++n) {
-      rec[2 + 8 * n + 2 * tq] = neutral ? 0.f : o[n][0] + o[n][2];
-      rec[2 + 8 * n + 2 * tq + 1] = neutral ? 0.f : o[n][1] + o[n][3];
-    }
-  };
-  auto neutral_upto = [&](int sq_end) {  // neutral records for segments (last_written, sq_end)
-    for (int sq = last_written + 1; sq < sq_end; ++sq) write_record(sq, true);
-    if (sq_end - 1 > last_written) last_written = sq_end - 1;
-  };
-
-  auto begin_segment = [&](const BlockMeta& m) {
-    const int nk = a.n_keep[m.s];
-    int L;
-    if (MODE == 1) {
-      L = vp.view_len[m.q];
-      if (L < 0 || L > Lcap) {  // caller-supplied: clamp so the table reads stay in range
-        if (lane == 0) atomicOr(vp.status, KVM_DEV_BAD_BLOCK);
-        L = L < 0 ? 0 : Lcap;
+    for (int64_t jj = warp; jj < nb; jj += kConsumers) {
+      const int st = (int)(jj % NS);
+      const uint32_t phase = (uint32_t)((jj / NS) & 1);
+      const Cursor cu = locate(fa + jj, a, vp.n_sessions);
+      const int q = cu.s * vp.h_kv + cu.g;
+      if (q != seg) {
+        if (seg >= 0) {
+          write_record(seg, false);
+          last_written = seg;
+        }
+        neutral_upto(q);
+        seg = q;
+        begin_segment(cu, q);
       }
-    } else {
-      const int last = vp.kept[(int64_t)m.q * vp.budget + nk - 1];
-      L = 32 * (nk - 1) + ((last >= 0 && last < a.n_blk[m.s]) ? block_tokens(last, a, m.s) : 32);
-      if (m.i == 0 && lane == 0) vp.view_len[m.q] = L;
-    }
-    if (!kAttend) return;
-    // RoPE(q, L) for this thread's fragment elements: head gq, dims 16kk + 2tq + {0,1,8,9} (kk < KS/2),
-    // each paired with the same dim + d/2, which sits in k-step kk + KS/2 at the same place
-    const int g = m.q % vp.h_kv;
-    const float2* bb = vp.rope_base + (int64_t)(L >> 5) * (D / 2);
-    const float2* oo = vp.rope_off + (L & 31) * (D / 2);
-    const uint16_t* qh = vp.q + ((int64_t)m.s * vp.h_q + g * G + (gq < G ? gq : 0)) * D;
-#pragma unroll
-    for (int kk = 0; kk < Q::KS / 2; ++kk) {
-      float y1[4], y2[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int dim = 16 * kk + 2 * tq + (e & 1) + 8 * (e >> 1);
-        const float x1 = __uint_as_float((uint32_t)qh[dim] << 16);
-        const float x2 = __uint_as_float((uint32_t)qh[dim + D / 2] << 16);
-        const float2 o2 = oo[dim];
-        float cs, sn;
-        rope_cs(bb[dim], o2.x, o2.y, cs, sn);
-        y1[e] = gq < G ? (x1 * cs - x2 * sn) * vp.q_scale : 0.f;
-        y2[e] = gq < G ? (x2 * cs + x1 * sn) * vp.q_scale : 0.f;
+      const int64_t ydst = (int64_t)q * Lcap + 32 * cu.i;
+      const uint32_t kaddr = sbase + st * 2 * Q::PAGE, vaddr = kaddr + Q::PAGE;
+      if (__any_sync(0xffffffffu, !mbar_wait(&full[st], phase, vp.status))) {
+        aborted = true;
+        break;
       }
-      split2(y1[0], y1[1], qa[kk][0], qa[kk][1]);
-      split2(y1[2], y1[3], qa[kk][2], qa[kk][3]);
-      split2(y2[0], y2[1], qa[kk + Q::KS / 2][0], qa[kk + Q::KS / 2][1]);
-      split2(y2[2], y2[3], qa[kk + Q::KS / 2][2], qa[kk + Q::KS / 2][3]);
-    }
-#pragma unroll
-    for (int n = 0; n < Q::NO; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    m_run = -INFINITY;
-    l_run = 0.f;
-  };
+      const int valid = meta[st];
 
-  // ------------------------------------------------------------ main loop over this warp's blocks
-  BlockMeta batch = resolve(0);
-  BlockMeta cur = bcast(batch, 0);
-  if (nblk_w > 0) {
-    issue_k(cur);
-    issue_v(cur);
-  }
-  bool aborted = false;
-  for (int64_t j = 0; j < nblk_w; ++j) {
-    const uint32_t phase = (uint32_t)(j & 1);
-    // metadata of the next block (the batch is refilled every 32 blocks)
-    BlockMeta nxt{-1, 0, 0, 0, 0};
-    if (j + 1 < nblk_w) {
-      if (((j + 1) & 31) == 0) batch = resolve(j + 1);
-      nxt = bcast(batch, (int)((j + 1) & 31));
-    }
-    if (cur.q != seg) {
-      if (seg >= 0) {
-        write_record(seg, false);
-        last_written = seg;
-      }
-      neutral_upto(cur.q);
-      seg = cur.q;
-      begin_segment(cur);
-    }
-    const int valid = cur.valid;
-    const int64_t ydst = (int64_t)cur.q * Lcap + 32 * cur.i;
-
-    // ---- K: wait, rotate in place, store (the abort decision is made by the whole warp)
-    if (__any_sync(0xffffffffu, !mbar_wait(&full_k[warp], phase, vp.status))) {
-      aborted = true;
-      break;
-    }
-    if (valid > 0 && kWrite) {
-      const int cc = lane % Q::CPR;
-      float2 bb[8];
-      {
-        const float4* bp = reinterpret_cast<const float4*>(vp.rope_base + (int64_t)cur.i * (D / 2) + 8 * cc);
+      // ---- K: rotate in place at view positions 32*i + r, store K and V to the view
+      if (valid > 0 && kWrite) {
+        const int cc = lane % Q::CPR;
+        const uint32_t tab_hi = sbase + Q::OFF_TAB + st * 2 * Q::TAB, tab_lo = tab_hi + Q::TAB;
+        const uint32_t offhi = sbase + Q::OFF_OFFHI, offlo = sbase + Q::OFF_OFFLO;
+        float2 bb[8];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float4 t = __ldg(bp + u);
+          const float4 t = lds128f(tab_hi + (8 * cc + 2 * u) * 8);
           bb[2 * u] = make_float2(t.x, t.y);
           bb[2 * u + 1] = make_float2(t.z, t.w);
         }
-      }
 #pragma unroll 2
-      for (int pass = 0; pass < Q::PASSES; ++pass) {
-        const int r = lane / Q::CPR + Q::RPP * pass;
-        const uint32_t a1 = kaddr + chunk_off(r, cc), a2 = kaddr + chunk_off(r, cc + D / 16);
-        const uint4 w1 = lds128(a1), w2 = lds128(a2);
-        const uint32_t xa[4] = {w1.x, w1.y, w1.z, w1.w}, xb[4] = {w2.x, w2.y, w2.z, w2.w};
-        uint32_t oa[4], ob[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 ofs = off_s[(r * 4 + u) * Q::CPR + cc];
-          float f1[2], f2[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int v = 2 * u + e;
-            float cs, sn;
-            rope_cs(bb[v], e ? ofs.z : ofs.x, e ? ofs.w : ofs.y, cs, sn);
-            const float x1 = e ? bf16hi(xa[u]) : bf16lo(xa[u]);
-            const float x2 = e ? bf16hi(xb[u]) : bf16lo(xb[u]);
-            f1[e] = fmaf(x1, cs, -x2 * sn);
-            f2[e] = fmaf(x2, cs, x1 * sn);
-            // fp32 tables put |error| <= 3e-7 (|x1| + |x2|) on f, below one bf16 ulp of the result unless
-            // the rotation cancels; those pairs are redone in float-float so every stored key is within
-            // one ulp of the exact rotation.
-            const float tau = 0x1p-12f * (fabsf(x1) + fabsf(x2));
-            if (fminf(fabsf(f1[e]), fabsf(f2[e])) < tau)
-              rotate_exact(x1, x2, vp.rope_base_hl[(int64_t)cur.i * (D / 2) + 8 * cc + v],
-                           vp.rope_off_hl[r * (D / 2) + 8 * cc + v], f1[e], f2[e]);
-          }
-          oa[u] = pack_bf16x2(f1[0], f1[1]);
-          ob[u] = pack_bf16x2(f2[0], f2[1]);
-        }
-        sts128(a1, make_uint4(oa[0], oa[1], oa[2], oa[3]));
-        sts128(a2, make_uint4(ob[0], ob[1], ob[2], ob[3]));
-        if (valid < 32 && r < valid) {  // partial block: plain stores of the rows present
-          uint16_t* kd = vp.k_view + (ydst + r) * D;
-          *reinterpret_cast<uint4*>(kd + 8 * cc) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-          *reinterpret_cast<uint4*>(kd + D / 2 + 8 * cc) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-        }
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (valid == 32 && lane == 0) {
-#pragma unroll
-        for (int b = 0; b < Q::BOXES; ++b) tma_store_2d(&tm_kdst, 64 * b, (int)ydst, kbuf + b * Q::BOX);
-        bulk_commit();
-      }
-    }
-
-    // ---- scores S = q . K^T for the block's 32 tokens (4 n-tiles of 8)
-    float sc[4][4];
-#pragma unroll
-    for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-    if (kAttend && valid > 0) {
-#pragma unroll
-      for (int kk = 0; kk < Q::KS; ++kk) {
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          const int tok = 16 * np + (lane & 7) + 8 * (lane >> 4);
-          const int chk = 2 * kk + ((lane >> 3) & 1);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kaddr + chunk_off(tok, chk), b0, b1, b2, b3);
-          mma_16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-          mma_16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-        }
-      }
-    }
-    // the K page is no longer needed: once its store has read it, fetch the next block's K
-    __syncwarp();
-    if (lane == 0) {
-      bulk_wait_read_all();
-      fence_proxy_async_smem();
-    }
-    __syncwarp();
-    if (j + 1 < nblk_w) issue_k(nxt);
-
-    // ---- V: wait, store, P.V
-    if (__any_sync(0xffffffffu, !mbar_wait(&full_v[warp], phase, vp.status))) {
-      aborted = true;
-      break;
-    }
-    if (valid > 0 && kWrite) {
-      if (valid == 32) {
-        if (lane == 0) {
-#pragma unroll
-          for (int b = 0; b < Q::BOXES; ++b) tma_store_2d(&tm_vdst, 64 * b, (int)ydst, vbuf + b * Q::BOX);
-          bulk_commit();
-        }
-      } else {
-        const int cc = lane % Q::CPR;
-#pragma unroll 1
         for (int pass = 0; pass < Q::PASSES; ++pass) {
           const int r = lane / Q::CPR + Q::RPP * pass;
-          if (r < valid) {
+          const uint32_t a1 = kaddr + chunk_off(r, cc), a2 = kaddr + chunk_off(r, cc + D / 16);
+          const uint4 w1 = lds128(a1), w2 = lds128(a2);
+          const uint32_t xa[4] = {w1.x, w1.y, w1.z, w1.w}, xb[4] = {w2.x, w2.y, w2.z, w2.w};
+          // all eight pairs branch-free, then one (rare) fix-up pass over the pairs whose rotation cancels
+          float f1[8], f2[8];
+          uint32_t redo = 0;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float4 ofs = lds128f(offhi + ((r * 4 + u) * Q::CPR + cc) * 16);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int v = 2 * u + e;
+              float cs, sn;
+              rope_cs(bb[v], e ? ofs.z : ofs.x, e ? ofs.w : ofs.y, cs, sn);
+              const float x1 = e ? bf16hi(xa[u]) : bf16lo(xa[u]);
+              const float x2 = e ? bf16hi(xb[u]) : bf16lo(xb[u]);
+              f1[v] = fmaf(x1, cs, -x2 * sn);
+              f2[v] = fmaf(x2, cs, x1 * sn);
+              // fp32 tables put |error| <= 3e-7 (|x1| + |x2|) on f, below one bf16 ulp of the result unless
+              // the rotation cancels; those pairs are redone in float-float so every stored key is within
+              // one ulp of the exact rotation.
+              redo |= (fminf(fabsf(f1[v]), fabsf(f2[v])) < 0x1p-12f * (fabsf(x1) + fabsf(x2))) ? (1u << v) : 0u;
+            }
+          }
+          if (redo) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              if (!(redo >> v & 1)) continue;
+              const float x1 = (v & 1) ? bf16hi(xa[v / 2]) : bf16lo(xa[v / 2]);
+              const float x2 = (v & 1) ? bf16hi(xb[v / 2]) : bf16lo(xb[v / 2]);
+              const float2 bl = lds64f(tab_lo + (8 * cc + v) * 8);
+              const float2 ol = lds64f(offlo + (r * (D / 2) + 8 * cc + v) * 8);
+              const float4 oh4 = lds128f(offhi + ((r * 4 + v / 2) * Q::CPR + cc) * 16);
+              const float2 oh = (v & 1) ? make_float2(oh4.z, oh4.w) : make_float2(oh4.x, oh4.y);
+              rotate_exact(x1, x2, make_float4(bb[v].x, bl.x, bb[v].y, bl.y), make_float4(oh.x, ol.x, oh.y, ol.y),
+                           f1[v], f2[v]);
+            }
+          }
+          uint32_t oa[4], ob[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            oa[u] = pack_bf16x2(f1[2 * u], f1[2 * u + 1]);
+            ob[u] = pack_bf16x2(f2[2 * u], f2[2 * u + 1]);
+          }
+          sts128(a1, make_uint4(oa[0], oa[1], oa[2], oa[3]));
+          sts128(a2, make_uint4(ob[0], ob[1], ob[2], ob[3]));
+          if (valid < 32 && r < valid) {  // partial block: plain stores of the rows present
+            uint16_t* kd = vp.k_view + (ydst + r) * D;
+            *reinterpret_cast<uint4*>(kd + 8 * cc) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+            *reinterpret_cast<uint4*>(kd + D / 2 + 8 * cc) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
             uint16_t* vd = vp.v_view + (ydst + r) * D;
             *reinterpret_cast<uint4*>(vd + 8 * cc) = lds128(vaddr + chunk_off(r, cc));
             *reinterpret_cast<uint4*>(vd + D / 2 + 8 * cc) = lds128(vaddr + chunk_off(r, cc + D / 16));
           }
         }
-      }
-    }
-    if (kAttend && valid > 0) {
-      if (valid < 32) {  // rows past the tail may hold any bits: zero them before P.V
+        fence_proxy_async_smem();
         __syncwarp();
-        const int cc = lane % Q::CPR;
-#pragma unroll 1
-        for (int pass = 0; pass < Q::PASSES; ++pass) {
-          const int r = lane / Q::CPR + Q::RPP * pass;
-          if (r >= valid) {
-            sts128(vaddr + chunk_off(r, cc), make_uint4(0, 0, 0, 0));
-            sts128(vaddr + chunk_off(r, cc + D / 16), make_uint4(0, 0, 0, 0));
+        if (valid == 32 && lane == 0) {
+#pragma unroll
+          for (int b = 0; b < Q::BOXES; ++b) {
+            tma_store_2d(&tm_kdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + b * Q::BOX);
+            tma_store_2d(&tm_vdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + Q::PAGE + b * Q::BOX);
+          }
+          bulk_commit();
+        }
+      }
+
+      if (kAttend && valid > 0) {
+        // ---- scores S = q . K^T for the block's 32 tokens (4 n-tiles of 8)
+        float sc[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < Q::KS; ++kk) {
+#pragma unroll
+          for (int np = 0; np < 2; ++np) {
+            const int tok = 16 * np + (lane & 7) + 8 * (lane >> 4);
+            const int chk = 2 * kk + ((lane >> 3) & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kaddr + chunk_off(tok, chk), b0, b1, b2, b3);
+            mma_16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+            mma_16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
           }
         }
-        __syncwarp();
-      }
-      // online softmax for head gq over this block
-      float s[8], bm = -INFINITY;
-#pragma unroll
-      for (int n = 0; n < 4; ++n)
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int tok = 8 * n + 2 * tq + e;
-          const float v = sc[n][e] + sc[n][2 + e];
-          s[2 * n + e] = tok < valid ? v : -INFINITY;
-          bm = fmaxf(bm, s[2 * n + e]);
+        if (valid < 32) {  // rows past the tail may hold any bits: zero them before P.V
+          __syncwarp();
+          const int cc = lane % Q::CPR;
+#pragma unroll 1
+          for (int pass = 0; pass < Q::PASSES; ++pass) {
+            const int r = lane / Q::CPR + Q::RPP * pass;
+            if (r >= valid) {
+              sts128(vaddr + chunk_off(r, cc), make_uint4(0, 0, 0, 0));
+              sts128(vaddr + chunk_off(r, cc + D / 16), make_uint4(0, 0, 0, 0));
+            }
+          }
+          __syncwarp();
         }
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-      if (bm > m_run + 8.f) {  // raise the reference only when it grows by more than 8 (a factor 256)
-        const float corr = fast_exp2(m_run - bm);  // 0 when m_run was -inf
-        l_run *= corr;
+        // online softmax for head gq over this block
+        float s[8], bm = -INFINITY;
 #pragma unroll
-        for (int n = 0; n < Q::NO; ++n) {
-          o[n][0] *= corr;
-          o[n][1] *= corr;
-          o[n][2] *= corr;
-          o[n][3] *= corr;
+        for (int n = 0; n < 4; ++n)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int tok = 8 * n + 2 * tq + e;
+            const float v = sc[n][e] + sc[n][2 + e];
+            s[2 * n + e] = tok < valid ? v : -INFINITY;
+            bm = fmaxf(bm, s[2 * n + e]);
+          }
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+        if (bm > m_run + 8.f) {  // raise the reference only when it grows by more than 8 (a factor 256)
+          const float corr = fast_exp2(m_run - bm);  // 0 when m_run was -inf
+          l_run *= corr;
+#pragma unroll
+          for (int n = 0; n < Q::NO; ++n) {
+            o[n][0] *= corr;
+            o[n][1] *= corr;
+            o[n][2] *= corr;
+            o[n][3] *= corr;
+          }
+          m_run = bm;
         }
-        m_run = bm;
-      }
-      uint32_t ph[4], pl[4];  // P for n-tiles 0..3: bf16 hi and residual, packed pairs
+        uint32_t ph[4], pl[4];  // P for n-tiles 0..3: bf16 hi and residual, packed pairs
 #pragma unroll
-      for (int n = 0; n < 4; ++n) {
-        const float p0 = fast_exp2(s[2 * n] - m_run), p1 = fast_exp2(s[2 * n + 1] - m_run);
-        l_run += p0 + p1;
-        split2(p0, p1, ph[n], pl[n]);
-      }
+        for (int n = 0; n < 4; ++n) {
+          const float p0 = fast_exp2(s[2 * n] - m_run), p1 = fast_exp2(s[2 * n + 1] - m_run);
+          l_run += p0 + p1;
+          split2(p0, p1, ph[n], pl[n]);
+        }
 #pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
+        for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
-        for (int np = 0; np < Q::NO / 2; ++np) {
-          const int tok = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
-          const int chk = 2 * np + (lane >> 4);
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vaddr + chunk_off(tok, chk), b0, b1, b2, b3);
-          mma_16816(o[2 * np], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b0, b1);
-          mma_16816(o[2 * np + 1], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b2, b3);
+          for (int np = 0; np < Q::NO / 2; ++np) {
+            const int tok = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
+            const int chk = 2 * np + (lane >> 4);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vaddr + chunk_off(tok, chk), b0, b1, b2, b3);
+            mma_16816(o[2 * np], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b0, b1);
+            mma_16816(o[2 * np + 1], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b2, b3);
+          }
         }
       }
-    }
-    __syncwarp();
-    if (lane == 0) {
-      bulk_wait_read_all();
+      // ---- free the stage once this warp's view stores have read it
       fence_proxy_async_smem();
-    }
-    __syncwarp();
-    if (j + 1 < nblk_w) issue_v(nxt);
-    cur = nxt;
-  }
-  if (aborted) {
-    // drain: copies already issued for this warp's stage must land before the CTA exits
-    if (lane == 0) {
-      bulk_wait_all();
-      mbar_wait(&full_k[warp], 0, vp.status);
-      mbar_wait(&full_k[warp], 1, vp.status);
-      mbar_wait(&full_v[warp], 0, vp.status);
-      mbar_wait(&full_v[warp], 1, vp.status);
-    }
-    return;
-  }
-  if (seg >= 0) {
-    write_record(seg, false);
-    last_written = seg;
-  }
-  neutral_upto(seg_last + 1);
-  if (lane == 0) bulk_wait_all();
-}
-
-// Merges the partial records of each (session, query head) and writes out;
-// also writes view_len = 0 for empty kept lists.
-template <int D, int G>
-__global__ void combine_kernel(const ViewParams vp, const SessionArgs a, int attend) {
-  const int s = blockIdx.x / vp.h_q, h = blockIdx.x % vp.h_q;
-  const int g = h / G, hh = h % G;
-  const int q = s * vp.h_kv + g;
-  const int nk = a.n_keep[s];
-  if (nk == 0) {
-    if (attend)
-      for (int dim = threadIdx.x; dim < D; dim += blockDim.x) vp.out[((int64_t)s * vp.h_q + h) * D + dim] = 0.f;
-    if (hh == 0 && threadIdx.x == 0 && vp.view_len) vp.view_len[q] = 0;
-    return;
-  }
-  if (!attend) return;
-  const int64_t start = a.seg_base[s] + (int64_t)g * nk, end = start + nk - 1;
-  const int c0 = cta_of(start, vp.total, vp.P), c1 = cta_of(end, vp.total, vp.P);
-  // CTAs between c0 and c1 with an empty share wrote no record: skip them
-  auto empty = [&](int c) { return cta_begin(c, vp.total, vp.P) >= cta_begin(c + 1, vp.total, vp.P); };
-  auto rec = [&](int c, int w) { return vp.rec + (((int64_t)(c + q) * kWarps + w) * G + hh) * (2 + D); };
-  float M = -INFINITY;
-  for (int c = c0; c <= c1; ++c)
-    if (!empty(c))
-      for (int w = 0; w < kWarps; ++w) M = fmaxf(M, rec(c, w)[0]);
-  for (int dim = threadIdx.x; dim < D; dim += blockDim.x) {
-    float av = 0.f, lv = 0.f;
-    if (M != -INFINITY) {
-      for (int c = c0; c <= c1; ++c) {
-        if (empty(c)) continue;
-        for (int w = 0; w < kWarps; ++w) {
-          const float* rc = rec(c, w);
-          if (rc[0] == -INFINITY) continue;
-          const float sc = exp2f(rc[0] - M);
-          av = fmaf(rc[2 + dim], sc, av);
-          lv = fmaf(rc[1], sc, lv);
-        }
+      __syncwarp();
+      if (lane == 0) {
+        bulk_wait_read_all();
+        mbar_arrive(&empty[st]);
       }
     }
-    vp.out[((int64_t)s * vp.h_q + h) * D + dim] = lv > 0.f ? av / lv : 0.f;
+    if (!aborted) {
+      if (seg >= 0) {
+        write_record(seg, false);
+        last_written = seg;
+      }
+      neutral_upto(seg_last + 1);
+    }
+  }
+
+  if (lane == 0) bulk_wait_all();  // this warp's view stores are complete
+  __threadfence();                 // this thread's records are visible GPU-wide before the CTA counts itself in
+  if (__syncthreads_or(aborted)) {
+    if (warp == kConsumers && lane == 0) {
+      // copies still in flight into a stage must land before the CTA exits: wait (bounded) for the
+      // last round issued on each stage
+      for (int st = 0; st < NS; ++st)
+        if (issued > st) mbar_wait(&full[st], (uint32_t)(((issued - 1 - st) / NS) & 1), vp.status);
+    }
+    return;
+  }
+  if (!kAttend) return;
+
+  // ------------------------------------------------------------ merge
+  // Records: per (CTA c, segment sq) a group of kConsumers + 1 slots at ((c + sq) * (kConsumers + 1)) * G;
+  // slot w < kConsumers holds consumer w's partial state, slot kConsumers the CTA's merged state.
+  // 1. the CTA folds its consumers' records of each of its segments into its CTA record (one round of
+  //    independent loads per thread: thread i owns head i / (D/4), dims 4 * (i % (D/4)) .. + 3)
+  constexpr int kSlots = kConsumers + 1;
+  constexpr int Q4 = D / 4;
+  const bool all_live = vp.total >= vp.P;  // then no CTA share is empty
+  auto live_cta = [&](int cc) { return all_live || cta_begin(cc, vp.total, vp.P) < cta_begin(cc + 1, vp.total, vp.P); };
+  auto rec_at = [&](int cc, int sq, int slot, int h) {
+    return vp.rec + ((((int64_t)(cc + sq) * kSlots + slot) * G) + h) * kRecFloats<D>;
+  };
+  for (int item = tid; item < (seg_last - seg_first + 1) * G * Q4; item += kThreads) {
+    const int sq = seg_first + item / (G * Q4), h = (item / Q4) % G, d4 = item % Q4;
+    float2 ml[kConsumers];
+    float4 ov[kConsumers];
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) {
+      const float* r = rec_at(c, sq, w, h);
+      ml[w] = __ldcg(reinterpret_cast<const float2*>(r));
+      ov[w] = __ldcg(reinterpret_cast<const float4*>(r + 4) + d4);
+    }
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, ml[w].x);
+    float lv = 0.f;
+    float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kConsumers; ++w) {
+        const float sc = ml[w].x == -INFINITY ? 0.f : exp2f(ml[w].x - M);
+        lv = fmaf(ml[w].y, sc, lv);
+        av.x = fmaf(ov[w].x, sc, av.x);
+        av.y = fmaf(ov[w].y, sc, av.y);
+        av.z = fmaf(ov[w].z, sc, av.z);
+        av.w = fmaf(ov[w].w, sc, av.w);
+      }
+    }
+    float* r = rec_at(c, sq, kConsumers, h);
+    if (d4 == 0) *reinterpret_cast<float2*>(r) = make_float2(M, lv);
+    reinterpret_cast<float4*>(r + 4)[d4] = av;
+  }
+  __threadfence();
+  __syncthreads();
+  // 2. count this CTA in on each of its segments (one atomic per segment, in parallel); the CTA that
+  //    completes a segment merges it
+  __shared__ int s_last[64];
+  for (int sq0 = seg_first; sq0 <= seg_last; sq0 += 64) {
+    const int n_here = min(64, seg_last - sq0 + 1);
+    if (tid < n_here) {
+      const int sq = sq0 + tid;
+      const int s = sq / vp.h_kv, g = sq % vp.h_kv;
+      const int nk = a.n_keep[s];
+      const int64_t start = a.seg_base[s] + (int64_t)g * nk;
+      const int c0 = cta_of(start, vp.total, vp.P), c1 = cta_of(start + nk - 1, vp.total, vp.P);
+      uint32_t n_cov = 0;
+      if (all_live)
+        n_cov = c1 - c0 + 1;
+      else
+        for (int cc = c0; cc <= c1; ++cc) n_cov += live_cta(cc);
+      const uint32_t prev = atomicAdd(&vp.seg_count[sq], 1u);
+      s_last[tid] = prev + 1 == n_cov;
+      if (prev + 1 == n_cov) vp.seg_count[sq] = 0;  // every CTA of the segment has counted: ready for the next call
+    }
+    __syncthreads();
+    // 3. merge of the CTA records of each completed segment, 8 CTAs per round of independent loads
+    for (int k = 0; k < n_here; ++k) {
+      if (!s_last[k]) continue;
+      __threadfence();
+      const int sq = sq0 + k;
+      const int s = sq / vp.h_kv, g = sq % vp.h_kv;
+      const int nk = a.n_keep[s];
+      const int64_t start = a.seg_base[s] + (int64_t)g * nk;
+      const int c0 = cta_of(start, vp.total, vp.P), c1 = cta_of(start + nk - 1, vp.total, vp.P);
+      for (int i = tid; i < G * Q4; i += kThreads) {
+        const int h = i / Q4, d4 = i % Q4;
+        float m_acc = -INFINITY, l_acc = 0.f;
+        float4 o_acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int cb = c0; cb <= c1; cb += 8) {
+          float2 ml[8];
+          float4 ov[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int cc = cb + u;
+            const bool live = cc <= c1 && live_cta(cc);
+            ml[u] = make_float2(-INFINITY, 0.f);
+            ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (live) {
+              const float* r = rec_at(cc, sq, kConsumers, h);
+              ml[u] = __ldcg(reinterpret_cast<const float2*>(r));
+              ov[u] = __ldcg(reinterpret_cast<const float4*>(r + 4) + d4);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (ml[u].x == -INFINITY) continue;  // neutral record or no CTA
+            const float mn = fmaxf(m_acc, ml[u].x);
+            const float a0 = exp2f(m_acc - mn), a1 = exp2f(ml[u].x - mn);  // a0 = 0 while m_acc is -inf
+            l_acc = fmaf(l_acc, a0, ml[u].y * a1);
+            o_acc.x = fmaf(o_acc.x, a0, ov[u].x * a1);
+            o_acc.y = fmaf(o_acc.y, a0, ov[u].y * a1);
+            o_acc.z = fmaf(o_acc.z, a0, ov[u].z * a1);
+            o_acc.w = fmaf(o_acc.w, a0, ov[u].w * a1);
+            m_acc = mn;
+          }
+        }
+        const float inv = l_acc > 0.f ? 1.f / l_acc : 0.f;
+        reinterpret_cast<float4*>(vp.out + ((int64_t)s * vp.h_q + g * G + h) * D)[d4] =
+            make_float4(o_acc.x * inv, o_acc.y * inv, o_acc.z * inv, o_acc.w * inv);
+      }
+    }
+    __syncthreads();  // s_last is re-written for the next 64 segments
   }
 }
 
 // RoPE tables computed in fp64: base[slot][i] = (cos, sin)(32*slot*theta_i), off[r][i] = (cos, sin)(r*theta_i),
-// theta_i = rope_theta^(-2i/d); stored as fp32 and as fp32 hi/lo pairs (value = hi + lo to ~2^-48).
-__device__ __forceinline__ float4 hilo(double c, double s) {
-  const float ch = (float)c, sh = (float)s;
-  return make_float4(ch, (float)(c - (double)ch), sh, (float)(s - (double)sh));
-}
-__global__ void rope_table_kernel(float2* base, int n_slots, float2* off, float4* base_hl, float4* off_hl, int d,
+// theta_i = rope_theta^(-2i/d); each stored as the fp32 rounding (hi) and the fp32 rounding of what that
+// dropped (lo), so hi + lo holds the value to ~2^-48.
+__global__ void rope_table_kernel(float2* base, float2* base_lo, int n_slots, float2* off, float2* off_lo, int d,
                                   double rope_theta) {
   const int half = d / 2;
   const int64_t n = (int64_t)(n_slots + 32) * half;
@@ -652,15 +757,17 @@ __global__ void rope_table_kernel(float2* base, int n_slots, float2* off, float4
     const int64_t row = idx / half;
     const int i = (int)(idx % half);
     const double inv_freq = pow(rope_theta, -2.0 * i / d);
+    const bool is_base = row < n_slots;
     double sn, cs;
-    if (row < n_slots) {
-      sincos(32.0 * (double)row * inv_freq, &sn, &cs);
-      base[row * half + i] = make_float2((float)cs, (float)sn);
-      base_hl[row * half + i] = hilo(cs, sn);
+    sincos((is_base ? 32.0 * (double)row : (double)(row - n_slots)) * inv_freq, &sn, &cs);
+    const float ch = (float)cs, sh = (float)sn;
+    const float2 hi = make_float2(ch, sh), lo = make_float2((float)(cs - (double)ch), (float)(sn - (double)sh));
+    if (is_base) {
+      base[row * half + i] = hi;
+      base_lo[row * half + i] = lo;
     } else {
-      sincos((double)(row - n_slots) * inv_freq, &sn, &cs);
-      off[(row - n_slots) * half + i] = make_float2((float)cs, (float)sn);
-      off_hl[(row - n_slots) * half + i] = hilo(cs, sn);
+      off[(row - n_slots) * half + i] = hi;
+      off_lo[(row - n_slots) * half + i] = lo;
     }
   }
 }
@@ -700,17 +807,14 @@ template <int D, int G>
 cudaError_t launch_dg(const Ctx& c, int mode, const CUtensorMap* maps, const ViewParams& vp, const SessionArgs& a,
                       cudaStream_t st) {
   using Q = Geo<D>;
-  const size_t smem = (size_t)kWarps * 2 * Q::PAGE + (size_t)32 * 4 * Q::CPR * sizeof(float4) + 1024;
-  cudaError_t e = cudaSuccess;
-  if (vp.total > 0) {
-    void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ViewParams,
-                 const SessionArgs) =
-        mode == 0 ? view_kernel<D, G, 0> : (mode == 1 ? view_kernel<D, G, 1> : view_kernel<D, G, 2>);
-    if ((e = ensure_smem(kern, c.device, smem)) != cudaSuccess) return e;
-    kern<<<vp.P, kWarps * 32, smem, st>>>(maps[0], maps[1], maps[2], maps[3], vp, a);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  combine_kernel<D, G><<<vp.n_sessions * vp.h_q, D, 0, st>>>(vp, a, mode != 0);
+  static_assert(Q::BYTES <= 227 * 1024, "view kernel shared memory");
+  if (vp.total == 0 && !vp.any_empty) return cudaSuccess;
+  void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ViewParams,
+               const SessionArgs) =
+      mode == 0 ? view_kernel<D, G, 0> : (mode == 1 ? view_kernel<D, G, 1> : view_kernel<D, G, 2>);
+  cudaError_t e = ensure_smem(kern, c.device, Q::BYTES);
+  if (e != cudaSuccess) return e;
+  kern<<<vp.P, kThreads, Q::BYTES, st>>>(maps[0], maps[1], maps[2], maps[3], vp, a);
   return cudaGetLastError();
 }
 
@@ -746,13 +850,16 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
   vp.v_view = v_view;
   vp.view_len = view_len;
   vp.rec = c.rec;
+  vp.seg_count = c.seg_count;
   vp.rope_base = reinterpret_cast<const float2*>(c.rope_base);
   vp.rope_off = reinterpret_cast<const float2*>(c.rope_off);
-  vp.rope_base_hl = c.rope_base_hl;
-  vp.rope_off_hl = c.rope_off_hl;
+  vp.rope_base_lo = reinterpret_cast<const float2*>(c.rope_base_lo);
+  vp.rope_off_lo = reinterpret_cast<const float2*>(c.rope_off_lo);
   vp.out = out;
   vp.status = c.status;
   vp.total = a.seg_base[n_sessions];
+  vp.any_empty = 0;
+  for (int s = 0; s < n_sessions; ++s) vp.any_empty |= a.n_keep[s] == 0;
   vp.budget = c.budget;
   vp.h_kv = c.p.h_kv;
   vp.h_q = c.p.h_q;
@@ -780,9 +887,10 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
 }
 
 cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st) {
-  rope_table_kernel<<<256, 256, 0, st>>>(reinterpret_cast<float2*>(c.rope_base), c.budget + 1,
-                                         reinterpret_cast<float2*>(c.rope_off), c.rope_base_hl, c.rope_off_hl, c.p.d,
-                                         (double)c.p.rope_theta);
+  rope_table_kernel<<<256, 256, 0, st>>>(reinterpret_cast<float2*>(c.rope_base),
+                                         reinterpret_cast<float2*>(c.rope_base_lo), c.budget + 1,
+                                         reinterpret_cast<float2*>(c.rope_off), reinterpret_cast<float2*>(c.rope_off_lo),
+                                         c.p.d, (double)c.p.rope_theta);
   return cudaGetLastError();
 }
 

@@ -212,3 +212,30 @@ def test_bad_page_is_reported_not_faulted():
     assert K.kvm_device_status(ctx) == 0          # cleared
     assert torch.isfinite(dev.out).all()
     ctx.close()
+
+
+def test_repeated_view_calls_give_identical_outputs():
+    # the attention merge counts CTAs per segment in the context and must start from zero on every call
+    w = synth.WORKLOADS["gqa40x8_256k"].with_(n_tok=40000)
+    li = synth.layer_inputs(w, 0)
+    ctx = K.Context.for_workload(w)
+    dev = LayerOnDevice(w, li, ctx)
+    dev.index_build()
+    dev.score_select()
+    dev.fused()
+    torch.cuda.synchronize()
+    first = dev.out.clone()
+    for _ in range(3):
+        dev.out.fill_(float("nan"))
+        dev.fused()
+        torch.cuda.synchronize()
+        assert torch.equal(dev.out, first)
+    # the unfused attention over the view written by the fused call reads the same bytes
+    for _ in range(2):
+        dev.out.fill_(float("nan"))
+        dev.attend()
+        torch.cuda.synchronize()
+        assert torch.allclose(dev.out, first, atol=1e-5, rtol=0)
+    assert K.kvm_device_status(ctx) == 0
+    assert compare_layer(w, li, dev, heads=[0, 7]) >= 1
+    ctx.close()
