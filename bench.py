@@ -405,7 +405,7 @@ def run_kvm(args, w):
             "hbm_gbps": round(gbs, 1), "must_touch_bytes_per_layer": bytes_layer,
             "hbm_frac_of_measured": round(bytes_layer / (us_layer * 1e-6) / 1e9 / peak, 4),
             "stages_us_per_layer": stage_us, "ms_per_step_eager_untimed": round(eager_ms, 4),
-            "roofline": {"bound": "hbm", "kernel": "kvm_materialize_attn (view kernel + combine)",
+            "roofline": {"bound": "hbm", "kernel": "kvm_materialize_attn (view_kernel: gather + re-RoPE + view write + attention + merge)",
                          "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes_per_launch": vb},

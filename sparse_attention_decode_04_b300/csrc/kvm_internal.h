@@ -12,7 +12,7 @@ namespace kvm {
 constexpr int kBlock = 32;            // tokens per block / page
 constexpr int kMaxGroup = 8;          // query heads per KV head
 constexpr int kMaxSessionsHost = 64;  // sessions per call (kernel-parameter arrays)
-constexpr int kViewWarps = 5;         // consumer warps (attention-record slots) per view-kernel CTA
+constexpr int kViewWarps = 2;         // attention warps (attention-record slots) per view-kernel CTA
 
 // Per-session values passed by value to the kernels (they size the grids, so
 // they live on the host; passing them as kernel parameters keeps every call

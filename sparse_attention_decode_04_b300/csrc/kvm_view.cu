@@ -21,27 +21,32 @@
 //     and V pages by TMA tiled loads (64-column boxes, 128-byte swizzle) and,
 //     when writing a view, the block's rows of the RoPE base tables by 1-D bulk
 //     copies, all completing on the stage's `full` mbarrier;
-//   - five consumer warps take every fifth block of the share.  Block j uses
-//     stage j mod NS with NS a multiple of five, so each consumer owns NS/5
-//     stages and meets their rounds strictly in order: a wait on a stage's
-//     barrier is never more than one phase ahead, which the parity waits need.  Per block a
-//     consumer rotates K in place at view positions 32*i + r (cos/sin composed
-//     in fp32 from the staged per-slot row and a per-offset table held in
-//     shared memory, both filled in fp64; pairs whose rotation cancels are
-//     redone in float-float from the hi/lo halves), rounds to bf16 and writes
-//     the rotated K and the untouched V to the view with TMA tiled stores; then
-//     computes the scores with mma.sync (m16n8k16, bf16 -> fp32; A rows 0..7
-//     hold the rotated, scaled query heads rounded to bf16, rows 8..15 their
-//     bf16 residuals, so one MMA gives an fp32-accurate score), keeps an
-//     online softmax per head in the log2 domain (the running maximum is
-//     raised only when it grows by more than 8) and accumulates P.V with
-//     mma.sync, P split the same way; finally it frees the stage on its
-//     `empty` mbarrier once its stores have read the stage.
-// No consumer ever reads global memory on the per-block path.  Each consumer
+//   - four rotation warps take every fourth block of the share: each rotates
+//     K in place at view positions 32*i + r (cos/sin composed in fp32 from the
+//     staged per-slot row and the per-offset values, which a lane keeps in
+//     registers because it always rotates the same (row, pair) slots; both
+//     tables filled in fp64; pairs whose rotation cancels are redone in
+//     float-float from the hi/lo halves), rounds to bf16, writes the rotated K and the
+//     untouched V to the view with TMA tiled stores, marks the stage `rotated`
+//     and frees its share of the stage once the stores have read it;
+//   - two attention warps take every other block: each waits for the rotated
+//     page, computes the scores with mma.sync (m16n8k16, bf16 -> fp32; A rows
+//     0..7 hold the rotated, scaled query heads rounded to bf16, rows 8..15
+//     their bf16 residuals, so one MMA gives an fp32-accurate score), keeps an
+//     online softmax per head in the log2 domain (the running maximum is raised
+//     only when it grows by more than 8) and accumulates P.V with mma.sync, P
+//     split the same way, then frees its share of the stage.
+// NS is a multiple of both warp counts, so every rotation and every attention
+// warp owns whole stages and meets their rounds strictly in order: a wait on a
+// stage barrier is never more than one phase ahead, which the parity waits
+// need.  The 7 warps fit two per SM sub-partition, so every warp may hold up
+// to 255 registers; the rotation (about four times the attention's work per
+// block) gets four warps.
+// No warp reads global memory on the per-block path.  Each attention warp
 // writes one partial record (max, sum, output) per segment (session, KV head)
 // of its CTA's share — a neutral record for a segment it had no block of — in
 // the record group (cta + segment), which is unique to the pair.  At the end
-// the CTA folds its consumers' records of each segment into one CTA record
+// the CTA folds its attention warps' records of each segment into one CTA record
 // (log-sum-exp), then counts itself in on each of its segments with one
 // atomic add; the CTA that arrives last on a segment (no CTA ever waits)
 // merges that segment's CTA records with batched independent loads and writes
@@ -62,8 +67,10 @@
 namespace kvm {
 namespace {
 
-constexpr int kConsumers = kViewWarps;          // consumer warps (attention-record slots) per CTA
-constexpr int kThreads = (kConsumers + 1) * 32;  // + one producer warp
+constexpr int kRot = 4;                      // rotation warps per CTA (warps 0 .. kRot-1)
+constexpr int kAttn = kViewWarps;            // attention warps per CTA (attention-record slots)
+constexpr int kProducer = kRot + kAttn;      // warp index of the producer
+constexpr int kThreads = (kRot + kAttn + 1) * 32;
 
 struct ViewParams {
   const int32_t* bt;
@@ -106,13 +113,11 @@ struct Geo {
   static constexpr int PASSES = CPR;            // rotation passes per page
   static constexpr int KS = D / 16;             // MMA k-steps over the head dimension
   static constexpr int NO = D / 8;              // output n-tiles
-  static constexpr int NS = kConsumers * (D == 128 ? 2 : 4);  // pipeline stages, NS / kConsumers per consumer
+  static constexpr int NS = D == 128 ? 12 : 24;  // pipeline stages: a multiple of kRot and of kAttn
   static constexpr uint32_t TAB = D / 2 * 8;     // bytes of one table row ((cos, sin) per pair)
   // shared memory, from the 1024-byte-aligned base
   static constexpr uint32_t OFF_TAB = NS * 2 * PAGE;             // [NS][hi row | lo row] base table rows
-  static constexpr uint32_t OFF_OFFHI = OFF_TAB + NS * 2 * TAB;  // [32][4][CPR] float4 offset table (hi)
-  static constexpr uint32_t OFF_OFFLO = OFF_OFFHI + 32 * TAB;    // [32][d/2] float2 offset table (lo)
-  static constexpr uint32_t OFF_META = OFF_OFFLO + 32 * TAB;     // [NS] int: tokens of the staged block
+  static constexpr uint32_t OFF_META = OFF_TAB + NS * 2 * TAB;  // [NS] int: tokens of the staged block
   static constexpr uint32_t BYTES = OFF_META + NS * 4 + 1024;    // + alignment slack
 };
 
@@ -225,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_addr(smem);
   int* meta = reinterpret_cast<int*>(smem + Q::OFF_META);
-  __shared__ __align__(8) uint64_t full[NS], empty[NS];
+  __shared__ __align__(8) uint64_t full[NS], rotated[NS], empty[NS];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
@@ -244,22 +249,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t nb = fb - fa;  // blocks of this CTA
   const int Lcap = 32 * vp.budget;
 
-  if (kWrite) {
-    // offset tables: hi as [r][u][cc] float4 (the pairs 8cc+2u, 8cc+2u+1 of row r), lo as [r][d/2] float2
-    float4* off_hi = reinterpret_cast<float4*>(smem + Q::OFF_OFFHI);
-    float2* off_lo = reinterpret_cast<float2*>(smem + Q::OFF_OFFLO);
-    for (int idx = tid; idx < 32 * 4 * Q::CPR; idx += kThreads) {
-      const int r = idx / (4 * Q::CPR), u = (idx / Q::CPR) % 4, cc = idx % Q::CPR;
-      const float2 o0 = vp.rope_off[r * (D / 2) + 8 * cc + 2 * u];
-      const float2 o1 = vp.rope_off[r * (D / 2) + 8 * cc + 2 * u + 1];
-      off_hi[idx] = make_float4(o0.x, o0.y, o1.x, o1.y);
-    }
-    for (int idx = tid; idx < 32 * (D / 2); idx += kThreads) off_lo[idx] = vp.rope_off_lo[idx];
-  }
   if (tid == 0) {
     for (int st = 0; st < NS; ++st) {
       mbar_init(&full[st], 1);
-      mbar_init(&empty[st], 1);
+      mbar_init(&rotated[st], 1);
+      mbar_init(&empty[st], (kWrite ? 1 : 0) + (kAttend ? 1 : 0));  // the stage's rotation and attention warps
     }
     mbar_fence_init();
   }
@@ -271,8 +265,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool aborted = false;
   int64_t issued = 0;  // producer: blocks whose copies were issued
 
-  static_assert(NS % kConsumers == 0, "each consumer owns whole stages");
-  if (warp == kConsumers) {
+  static_assert(NS % kRot == 0 && NS % kAttn == 0, "each rotation and each attention warp owns whole stages");
+  if (warp == kProducer) {
     // ============================================================ producer
     // lane l resolves block jb + l: tokens present (0 = skip), source tile row, view slot
     auto resolve = [&](int64_t jb, int& valid, int& ysrc, int& slot) {
@@ -286,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       slot = cu.i;
       if (MODE == 1) {
         int L = vp.view_len[q];
-        L = L < 0 ? 0 : (L > Lcap ? Lcap : L);  // caller-supplied: the consumer reports a bad value
+        L = L < 0 ? 0 : (L > Lcap ? Lcap : L);  // caller-supplied: the attention warp reports a bad value
         valid = max(0, min(32, L - 32 * cu.i));
         ysrc = q * Lcap + 32 * cu.i;
       } else {
@@ -351,8 +345,158 @@ __global__ void __launch_bounds__(kThreads, 1)
       y_cur = y_nxt;
       i_cur = i_nxt;
     }
-  } else {
-    // ============================================================ consumers
+  } else if (warp < kRot) {
+    // ============================================================ rotation warps
+    if (kWrite) {
+      // A lane always rotates the same pairs of every block: rows r = lane / CPR + RPP * pass, pairs
+      // k = 8 cc + v (v < 8) with cc = lane % CPR.  Their offset cos/sin (r * theta_k, block-independent)
+      // stay in registers for the whole kernel: of[pass][u] holds pairs 2u and 2u + 1.
+      const int cc = lane % Q::CPR;
+      float4 of[Q::PASSES][4];
+#pragma unroll
+      for (int pass = 0; pass < Q::PASSES; ++pass)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2* t = vp.rope_off + (lane / Q::CPR + Q::RPP * pass) * (D / 2) + 8 * cc + 2 * u;
+          const float2 o0 = __ldg(t), o1 = __ldg(t + 1);
+          of[pass][u] = make_float4(o0.x, o0.y, o1.x, o1.y);
+        }
+      for (int64_t jj = warp; jj < nb; jj += kRot) {
+        const int st = (int)(jj % NS);
+        const uint32_t phase = (uint32_t)((jj / NS) & 1);
+        const Cursor cu = locate(fa + jj, a, vp.n_sessions);
+        const int q = cu.s * vp.h_kv + cu.g;
+        const int64_t ydst = (int64_t)q * Lcap + 32 * cu.i;
+        const uint32_t vaddr = sbase + st * 2 * Q::PAGE + Q::PAGE;
+        if (__any_sync(0xffffffffu, !mbar_wait(&full[st], phase, vp.status))) {
+          aborted = true;
+          break;
+        }
+        const int valid = meta[st];
+        if (cu.i == 0 && lane == 0) {  // the segment's view length, written by the rotation warp of its block 0
+          const int nk = a.n_keep[cu.s];
+          const int last = vp.kept[(int64_t)q * vp.budget + nk - 1];
+          vp.view_len[q] = 32 * (nk - 1) + ((last >= 0 && last < a.n_blk[cu.s]) ? block_tokens(last, a, cu.s) : 32);
+        }
+        if (valid > 0) {
+            unsigned char* kst = smem + st * 2 * Q::PAGE;
+            uint4* kq = reinterpret_cast<uint4*>(kst);  // the stage's K page as 16-byte chunks
+            const float4* __restrict__ tabh = reinterpret_cast<const float4*>(smem + Q::OFF_TAB + st * 2 * Q::TAB);
+            float2 bb[8];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float4 t = tabh[4 * cc + u];
+              bb[2 * u] = make_float2(t.x, t.y);
+              bb[2 * u + 1] = make_float2(t.z, t.w);
+            }
+            // one pass = row r = lane / CPR + RPP * pass, chunks cc and cc + d/16 (8 pairs); the next pass's
+            // operands are loaded before this pass's results are stored.
+            // Accuracy: with the fp32 tables (each within 2^-24 relative of the fp64 value) the composed cos/sin
+            // are within 4 * 2^-24 of exact and the rotated f within 2^-24 (5 (|x1| + |x2|) + |f|), less than one
+            // bf16 ulp of f (> 2^-8 |f|) whenever |f| >= 2^-13 (|x1| + |x2|).  Pairs below that (the rotation
+            // cancels) keep their original bits in the stage, are flagged, and are redone in float-float after
+            // the passes, so every stored key is within one ulp of the exact rotation.
+            uint4 wa = kq[chunk_off(lane / Q::CPR, cc) >> 4], wb = kq[chunk_off(lane / Q::CPR, cc + D / 16) >> 4];
+            uint64_t redo_all = 0;  // bit 8 * pass + v
+#pragma unroll
+            for (int pass = 0; pass < Q::PASSES; ++pass) {
+              const int r = lane / Q::CPR + Q::RPP * pass;
+              uint4 wa_n = wa, wb_n = wb;
+              if (pass + 1 < Q::PASSES) {
+                const int rn = r + Q::RPP;
+                wa_n = kq[chunk_off(rn, cc) >> 4];
+                wb_n = kq[chunk_off(rn, cc + D / 16) >> 4];
+              }
+              const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
+              uint32_t oa[4], ob[4], redo = 0;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                float f1[2], f2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int v = 2 * u + e;
+                  float cs, sn;
+                  rope_cs(bb[v], e ? of[pass][u].z : of[pass][u].x, e ? of[pass][u].w : of[pass][u].y, cs, sn);
+                  const float x1 = e ? bf16hi(xa[u]) : bf16lo(xa[u]);
+                  const float x2 = e ? bf16hi(xb[u]) : bf16lo(xb[u]);
+                  f1[e] = fmaf(x1, cs, -x2 * sn);
+                  f2[e] = fmaf(x2, cs, x1 * sn);
+                  redo |= (fminf(fabsf(f1[e]), fabsf(f2[e])) < 0x1p-13f * (fabsf(x1) + fabsf(x2))) ? (1u << v) : 0u;
+                }
+                oa[u] = pack_bf16x2(f1[0], f1[1]);
+                ob[u] = pack_bf16x2(f2[0], f2[1]);
+              }
+              if (redo) {  // flagged pairs keep their original bits until the fix-up below
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const uint32_t m = ((redo >> (2 * u)) & 1u ? 0x0000FFFFu : 0u) | ((redo >> (2 * u + 1)) & 1u ? 0xFFFF0000u : 0u);
+                  oa[u] = (oa[u] & ~m) | (xa[u] & m);
+                  ob[u] = (ob[u] & ~m) | (xb[u] & m);
+                }
+                redo_all |= (uint64_t)redo << (8 * pass);
+              }
+              kq[chunk_off(r, cc) >> 4] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+              kq[chunk_off(r, cc + D / 16) >> 4] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+              wa = wa_n;
+              wb = wb_n;
+            }
+            if (redo_all) {  // rare: float-float rotation of the flagged pairs, read back from the stage
+              const float2* tabl = reinterpret_cast<const float2*>(smem + Q::OFF_TAB + st * 2 * Q::TAB + Q::TAB);
+              const float2* tabh2 = reinterpret_cast<const float2*>(tabh);
+#pragma unroll 1
+              for (uint64_t m = redo_all; m; m &= m - 1) {
+                const int bit = __ffsll((long long)m) - 1, pass = bit >> 3, v = bit & 7, k = 8 * cc + v;
+                const int r = lane / Q::CPR + Q::RPP * pass;
+                uint16_t* e1 = reinterpret_cast<uint16_t*>(kst + chunk_off(r, cc)) + v;
+                uint16_t* e2 = reinterpret_cast<uint16_t*>(kst + chunk_off(r, cc + D / 16)) + v;
+                const float x1 = __uint_as_float((uint32_t)*e1 << 16), x2 = __uint_as_float((uint32_t)*e2 << 16);
+                const float2 bh = tabh2[k], bl = tabl[k];
+                const float2 oh = __ldg(vp.rope_off + r * (D / 2) + k), ol = __ldg(vp.rope_off_lo + r * (D / 2) + k);
+                float y1, y2;
+                rotate_exact(x1, x2, make_float4(bh.x, bl.x, bh.y, bl.y), make_float4(oh.x, ol.x, oh.y, ol.y), y1, y2);
+                const uint32_t y = pack_bf16x2(y1, y2);
+                *e1 = (uint16_t)(y & 0xFFFFu);
+                *e2 = (uint16_t)(y >> 16);
+              }
+            }
+            if (valid < 32) {  // partial block: plain stores of the rows present, from the stage
+              __syncwarp();
+#pragma unroll 1
+              for (int pass = 0; pass < Q::PASSES; ++pass) {
+                const int r = lane / Q::CPR + Q::RPP * pass;
+                if (r < valid) {
+                  uint16_t* kd = vp.k_view + (ydst + r) * D;
+                  uint16_t* vd = vp.v_view + (ydst + r) * D;
+                  *reinterpret_cast<uint4*>(kd + 8 * cc) = kq[chunk_off(r, cc) >> 4];
+                  *reinterpret_cast<uint4*>(kd + D / 2 + 8 * cc) = kq[chunk_off(r, cc + D / 16) >> 4];
+                  *reinterpret_cast<uint4*>(vd + 8 * cc) = lds128(vaddr + chunk_off(r, cc));
+                  *reinterpret_cast<uint4*>(vd + D / 2 + 8 * cc) = lds128(vaddr + chunk_off(r, cc + D / 16));
+                }
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (valid == 32 && lane == 0) {
+#pragma unroll
+              for (int b = 0; b < Q::BOXES; ++b) {
+                tma_store_2d(&tm_kdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + b * Q::BOX);
+                tma_store_2d(&tm_vdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + Q::PAGE + b * Q::BOX);
+              }
+              bulk_commit();
+            }
+        }
+        // the attention warp may read the rotated page now; the stage is free once the view stores read it
+        if (lane == 0) {
+          if (kAttend) mbar_arrive(&rotated[st]);
+          bulk_wait_read_all();
+          mbar_arrive(&empty[st]);
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp < kProducer) {
+    // ============================================================ attention warps
+    const int aw = warp - kRot;               // attention-record slot
     const int gq = lane >> 2, tq = lane & 3;  // MMA fragment row group (query head) and column pair
     uint32_t qa[Q::KS][4];                     // query A fragments: rows 0..7 bf16 hi, rows 8..15 bf16 residual
     float o[Q::NO][4];                         // output accumulators: [0..1] hi part, [2..3] residual part
@@ -360,12 +504,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     int seg = -1, last_written = seg_first - 1;
 
     auto write_record = [&](int sq, bool neutral) {
-      if (!kAttend) return;
       float l = neutral ? 0.f : l_run;
       l += __shfl_xor_sync(0xffffffffu, l, 1);
       l += __shfl_xor_sync(0xffffffffu, l, 2);
       if (gq >= G) return;
-      float* rec = vp.rec + (((int64_t)(c + sq) * (kConsumers + 1) + warp) * G + gq) * kRecFloats<D>;
+      float* rec = vp.rec + (((int64_t)(c + sq) * (kAttn + 1) + aw) * G + gq) * kRecFloats<D>;
       if (tq == 0) *reinterpret_cast<float2*>(rec) = make_float2(neutral ? -INFINITY : m_run, l);
 #pragma unroll
       for (int n = 0; n < Q::NO; ++n)
@@ -389,9 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const int last = vp.kept[(int64_t)q * vp.budget + nk - 1];
         L = 32 * (nk - 1) + ((last >= 0 && last < a.n_blk[cu.s]) ? block_tokens(last, a, cu.s) : 32);
-        if (cu.i == 0 && lane == 0) vp.view_len[q] = L;
       }
-      if (!kAttend) return;
       // RoPE(q, L) for this thread's fragment elements: head gq, dims 16kk + 2tq + {0,1,8,9} (kk < KS/2),
       // each paired with the same dim + d/2, which sits in k-step kk + KS/2 at the same place
       const float2* bb = vp.rope_base + (int64_t)(L >> 5) * (D / 2);
@@ -422,206 +563,120 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run = 0.f;
     };
 
-    for (int64_t jj = warp; jj < nb; jj += kConsumers) {
-      const int st = (int)(jj % NS);
-      const uint32_t phase = (uint32_t)((jj / NS) & 1);
-      const Cursor cu = locate(fa + jj, a, vp.n_sessions);
-      const int q = cu.s * vp.h_kv + cu.g;
-      if (q != seg) {
+    if (kAttend) {
+      for (int64_t jj = aw; jj < nb; jj += kAttn) {
+        const int st = (int)(jj % NS);
+        const uint32_t phase = (uint32_t)((jj / NS) & 1);
+        const Cursor cu = locate(fa + jj, a, vp.n_sessions);
+        const int q = cu.s * vp.h_kv + cu.g;
+        if (q != seg) {
+          if (seg >= 0) {
+            write_record(seg, false);
+            last_written = seg;
+          }
+          neutral_upto(q);
+          seg = q;
+          begin_segment(cu, q);
+        }
+        const uint32_t kaddr = sbase + st * 2 * Q::PAGE, vaddr = kaddr + Q::PAGE;
+        // the rotated page (fused) or the view page as loaded (attention over a given view)
+        if (__any_sync(0xffffffffu, !mbar_wait(kWrite ? &rotated[st] : &full[st], phase, vp.status))) {
+          aborted = true;
+          break;
+        }
+        const int valid = meta[st];
+        if (valid > 0) {
+            // ---- scores S = q . K^T for the block's 32 tokens (4 n-tiles of 8)
+            float sc[4][4];
+#pragma unroll
+            for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < Q::KS; ++kk) {
+#pragma unroll
+              for (int np = 0; np < 2; ++np) {
+                const int tok = 16 * np + (lane & 7) + 8 * (lane >> 4);
+                const int chk = 2 * kk + ((lane >> 3) & 1);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(kaddr + chunk_off(tok, chk), b0, b1, b2, b3);
+                mma_16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
+                mma_16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
+              }
+            }
+            if (valid < 32) {  // rows past the tail may hold any bits: zero them before P.V
+              __syncwarp();
+              const int cc = lane % Q::CPR;
+#pragma unroll 1
+              for (int pass = 0; pass < Q::PASSES; ++pass) {
+                const int r = lane / Q::CPR + Q::RPP * pass;
+                if (r >= valid) {
+                  sts128(vaddr + chunk_off(r, cc), make_uint4(0, 0, 0, 0));
+                  sts128(vaddr + chunk_off(r, cc + D / 16), make_uint4(0, 0, 0, 0));
+                }
+              }
+              __syncwarp();
+            }
+            // online softmax for head gq over this block
+            float s[8], bm = -INFINITY;
+#pragma unroll
+            for (int n = 0; n < 4; ++n)
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int tok = 8 * n + 2 * tq + e;
+                const float v = sc[n][e] + sc[n][2 + e];
+                s[2 * n + e] = tok < valid ? v : -INFINITY;
+                bm = fmaxf(bm, s[2 * n + e]);
+              }
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+            bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+            if (bm > m_run + 8.f) {  // raise the reference only when it grows by more than 8 (a factor 256)
+              const float corr = fast_exp2(m_run - bm);  // 0 when m_run was -inf
+              l_run *= corr;
+#pragma unroll
+              for (int n = 0; n < Q::NO; ++n) {
+                o[n][0] *= corr;
+                o[n][1] *= corr;
+                o[n][2] *= corr;
+                o[n][3] *= corr;
+              }
+              m_run = bm;
+            }
+            uint32_t ph[4], pl[4];  // P for n-tiles 0..3: bf16 hi and residual, packed pairs
+#pragma unroll
+            for (int n = 0; n < 4; ++n) {
+              const float p0 = fast_exp2(s[2 * n] - m_run), p1 = fast_exp2(s[2 * n + 1] - m_run);
+              l_run += p0 + p1;
+              split2(p0, p1, ph[n], pl[n]);
+            }
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+              for (int np = 0; np < Q::NO / 2; ++np) {
+                const int tok = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int chk = 2 * np + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(vaddr + chunk_off(tok, chk), b0, b1, b2, b3);
+                mma_16816(o[2 * np], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b0, b1);
+                mma_16816(o[2 * np + 1], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b2, b3);
+              }
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+      }
+      if (!aborted) {
         if (seg >= 0) {
           write_record(seg, false);
           last_written = seg;
         }
-        neutral_upto(q);
-        seg = q;
-        begin_segment(cu, q);
+        neutral_upto(seg_last + 1);
       }
-      const int64_t ydst = (int64_t)q * Lcap + 32 * cu.i;
-      const uint32_t kaddr = sbase + st * 2 * Q::PAGE, vaddr = kaddr + Q::PAGE;
-      if (__any_sync(0xffffffffu, !mbar_wait(&full[st], phase, vp.status))) {
-        aborted = true;
-        break;
-      }
-      const int valid = meta[st];
-
-      // ---- K: rotate in place at view positions 32*i + r, store K and V to the view
-      if (valid > 0 && kWrite) {
-        const int cc = lane % Q::CPR;
-        const uint32_t tab_hi = sbase + Q::OFF_TAB + st * 2 * Q::TAB, tab_lo = tab_hi + Q::TAB;
-        const uint32_t offhi = sbase + Q::OFF_OFFHI, offlo = sbase + Q::OFF_OFFLO;
-        float2 bb[8];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float4 t = lds128f(tab_hi + (8 * cc + 2 * u) * 8);
-          bb[2 * u] = make_float2(t.x, t.y);
-          bb[2 * u + 1] = make_float2(t.z, t.w);
-        }
-#pragma unroll 2
-        for (int pass = 0; pass < Q::PASSES; ++pass) {
-          const int r = lane / Q::CPR + Q::RPP * pass;
-          const uint32_t a1 = kaddr + chunk_off(r, cc), a2 = kaddr + chunk_off(r, cc + D / 16);
-          const uint4 w1 = lds128(a1), w2 = lds128(a2);
-          const uint32_t xa[4] = {w1.x, w1.y, w1.z, w1.w}, xb[4] = {w2.x, w2.y, w2.z, w2.w};
-          // all eight pairs branch-free, then one (rare) fix-up pass over the pairs whose rotation cancels
-          float f1[8], f2[8];
-          uint32_t redo = 0;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float4 ofs = lds128f(offhi + ((r * 4 + u) * Q::CPR + cc) * 16);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int v = 2 * u + e;
-              float cs, sn;
-              rope_cs(bb[v], e ? ofs.z : ofs.x, e ? ofs.w : ofs.y, cs, sn);
-              const float x1 = e ? bf16hi(xa[u]) : bf16lo(xa[u]);
-              const float x2 = e ? bf16hi(xb[u]) : bf16lo(xb[u]);
-              f1[v] = fmaf(x1, cs, -x2 * sn);
-              f2[v] = fmaf(x2, cs, x1 * sn);
-              // fp32 tables put |error| <= 3e-7 (|x1| + |x2|) on f, below one bf16 ulp of the result unless
-              // the rotation cancels; those pairs are redone in float-float so every stored key is within
-              // one ulp of the exact rotation.
-              redo |= (fminf(fabsf(f1[v]), fabsf(f2[v])) < 0x1p-12f * (fabsf(x1) + fabsf(x2))) ? (1u << v) : 0u;
-            }
-          }
-          if (redo) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              if (!(redo >> v & 1)) continue;
-              const float x1 = (v & 1) ? bf16hi(xa[v / 2]) : bf16lo(xa[v / 2]);
-              const float x2 = (v & 1) ? bf16hi(xb[v / 2]) : bf16lo(xb[v / 2]);
-              const float2 bl = lds64f(tab_lo + (8 * cc + v) * 8);
-              const float2 ol = lds64f(offlo + (r * (D / 2) + 8 * cc + v) * 8);
-              const float4 oh4 = lds128f(offhi + ((r * 4 + v / 2) * Q::CPR + cc) * 16);
-              const float2 oh = (v & 1) ? make_float2(oh4.z, oh4.w) : make_float2(oh4.x, oh4.y);
-              rotate_exact(x1, x2, make_float4(bb[v].x, bl.x, bb[v].y, bl.y), make_float4(oh.x, ol.x, oh.y, ol.y),
-                           f1[v], f2[v]);
-            }
-          }
-          uint32_t oa[4], ob[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            oa[u] = pack_bf16x2(f1[2 * u], f1[2 * u + 1]);
-            ob[u] = pack_bf16x2(f2[2 * u], f2[2 * u + 1]);
-          }
-          sts128(a1, make_uint4(oa[0], oa[1], oa[2], oa[3]));
-          sts128(a2, make_uint4(ob[0], ob[1], ob[2], ob[3]));
-          if (valid < 32 && r < valid) {  // partial block: plain stores of the rows present
-            uint16_t* kd = vp.k_view + (ydst + r) * D;
-            *reinterpret_cast<uint4*>(kd + 8 * cc) = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-            *reinterpret_cast<uint4*>(kd + D / 2 + 8 * cc) = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-            uint16_t* vd = vp.v_view + (ydst + r) * D;
-            *reinterpret_cast<uint4*>(vd + 8 * cc) = lds128(vaddr + chunk_off(r, cc));
-            *reinterpret_cast<uint4*>(vd + D / 2 + 8 * cc) = lds128(vaddr + chunk_off(r, cc + D / 16));
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (valid == 32 && lane == 0) {
-#pragma unroll
-          for (int b = 0; b < Q::BOXES; ++b) {
-            tma_store_2d(&tm_kdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + b * Q::BOX);
-            tma_store_2d(&tm_vdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + Q::PAGE + b * Q::BOX);
-          }
-          bulk_commit();
-        }
-      }
-
-      if (kAttend && valid > 0) {
-        // ---- scores S = q . K^T for the block's 32 tokens (4 n-tiles of 8)
-        float sc[4][4];
-#pragma unroll
-        for (int n = 0; n < 4; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < Q::KS; ++kk) {
-#pragma unroll
-          for (int np = 0; np < 2; ++np) {
-            const int tok = 16 * np + (lane & 7) + 8 * (lane >> 4);
-            const int chk = 2 * kk + ((lane >> 3) & 1);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4(kaddr + chunk_off(tok, chk), b0, b1, b2, b3);
-            mma_16816(sc[2 * np], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b0, b1);
-            mma_16816(sc[2 * np + 1], qa[kk][0], qa[kk][1], qa[kk][2], qa[kk][3], b2, b3);
-          }
-        }
-        if (valid < 32) {  // rows past the tail may hold any bits: zero them before P.V
-          __syncwarp();
-          const int cc = lane % Q::CPR;
-#pragma unroll 1
-          for (int pass = 0; pass < Q::PASSES; ++pass) {
-            const int r = lane / Q::CPR + Q::RPP * pass;
-            if (r >= valid) {
-              sts128(vaddr + chunk_off(r, cc), make_uint4(0, 0, 0, 0));
-              sts128(vaddr + chunk_off(r, cc + D / 16), make_uint4(0, 0, 0, 0));
-            }
-          }
-          __syncwarp();
-        }
-        // online softmax for head gq over this block
-        float s[8], bm = -INFINITY;
-#pragma unroll
-        for (int n = 0; n < 4; ++n)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int tok = 8 * n + 2 * tq + e;
-            const float v = sc[n][e] + sc[n][2 + e];
-            s[2 * n + e] = tok < valid ? v : -INFINITY;
-            bm = fmaxf(bm, s[2 * n + e]);
-          }
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
-        bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-        if (bm > m_run + 8.f) {  // raise the reference only when it grows by more than 8 (a factor 256)
-          const float corr = fast_exp2(m_run - bm);  // 0 when m_run was -inf
-          l_run *= corr;
-#pragma unroll
-          for (int n = 0; n < Q::NO; ++n) {
-            o[n][0] *= corr;
-            o[n][1] *= corr;
-            o[n][2] *= corr;
-            o[n][3] *= corr;
-          }
-          m_run = bm;
-        }
-        uint32_t ph[4], pl[4];  // P for n-tiles 0..3: bf16 hi and residual, packed pairs
-#pragma unroll
-        for (int n = 0; n < 4; ++n) {
-          const float p0 = fast_exp2(s[2 * n] - m_run), p1 = fast_exp2(s[2 * n + 1] - m_run);
-          l_run += p0 + p1;
-          split2(p0, p1, ph[n], pl[n]);
-        }
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-          for (int np = 0; np < Q::NO / 2; ++np) {
-            const int tok = 16 * ks + (lane & 7) + 8 * ((lane >> 3) & 1);
-            const int chk = 2 * np + (lane >> 4);
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vaddr + chunk_off(tok, chk), b0, b1, b2, b3);
-            mma_16816(o[2 * np], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b0, b1);
-            mma_16816(o[2 * np + 1], ph[2 * ks], pl[2 * ks], ph[2 * ks + 1], pl[2 * ks + 1], b2, b3);
-          }
-        }
-      }
-      // ---- free the stage once this warp's view stores have read it
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        bulk_wait_read_all();
-        mbar_arrive(&empty[st]);
-      }
-    }
-    if (!aborted) {
-      if (seg >= 0) {
-        write_record(seg, false);
-        last_written = seg;
-      }
-      neutral_upto(seg_last + 1);
     }
   }
 
   if (lane == 0) bulk_wait_all();  // this warp's view stores are complete
   __threadfence();                 // this thread's records are visible GPU-wide before the CTA counts itself in
   if (__syncthreads_or(aborted)) {
-    if (warp == kConsumers && lane == 0) {
+    if (warp == kProducer && lane == 0) {
       // copies still in flight into a stage must land before the CTA exits: wait (bounded) for the
       // last round issued on each stage
       for (int st = 0; st < NS; ++st)
@@ -632,11 +687,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!kAttend) return;
 
   // ------------------------------------------------------------ merge
-  // Records: per (CTA c, segment sq) a group of kConsumers + 1 slots at ((c + sq) * (kConsumers + 1)) * G;
-  // slot w < kConsumers holds consumer w's partial state, slot kConsumers the CTA's merged state.
-  // 1. the CTA folds its consumers' records of each of its segments into its CTA record (one round of
+  // Records: per (CTA c, segment sq) a group of kAttn + 1 slots at ((c + sq) * (kAttn + 1)) * G;
+  // slot w < kAttn holds attention warp w's partial state, slot kAttn the CTA's merged state.
+  // 1. the CTA folds its attention warps' records of each of its segments into its CTA record (one round of
   //    independent loads per thread: thread i owns head i / (D/4), dims 4 * (i % (D/4)) .. + 3)
-  constexpr int kSlots = kConsumers + 1;
+  constexpr int kSlots = kAttn + 1;
   constexpr int Q4 = D / 4;
   const bool all_live = vp.total >= vp.P;  // then no CTA share is empty
   auto live_cta = [&](int cc) { return all_live || cta_begin(cc, vp.total, vp.P) < cta_begin(cc + 1, vp.total, vp.P); };
@@ -645,22 +700,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   for (int item = tid; item < (seg_last - seg_first + 1) * G * Q4; item += kThreads) {
     const int sq = seg_first + item / (G * Q4), h = (item / Q4) % G, d4 = item % Q4;
-    float2 ml[kConsumers];
-    float4 ov[kConsumers];
+    float2 ml[kAttn];
+    float4 ov[kAttn];
 #pragma unroll
-    for (int w = 0; w < kConsumers; ++w) {
+    for (int w = 0; w < kAttn; ++w) {
       const float* r = rec_at(c, sq, w, h);
       ml[w] = __ldcg(reinterpret_cast<const float2*>(r));
       ov[w] = __ldcg(reinterpret_cast<const float4*>(r + 4) + d4);
     }
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, ml[w].x);
+    for (int w = 0; w < kAttn; ++w) M = fmaxf(M, ml[w].x);
     float lv = 0.f;
     float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kConsumers; ++w) {
+      for (int w = 0; w < kAttn; ++w) {
         const float sc = ml[w].x == -INFINITY ? 0.f : exp2f(ml[w].x - M);
         lv = fmaf(ml[w].y, sc, lv);
         av.x = fmaf(ov[w].x, sc, av.x);
@@ -669,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         av.w = fmaf(ov[w].w, sc, av.w);
       }
     }
-    float* r = rec_at(c, sq, kConsumers, h);
+    float* r = rec_at(c, sq, kAttn, h);
     if (d4 == 0) *reinterpret_cast<float2*>(r) = make_float2(M, lv);
     reinterpret_cast<float4*>(r + 4)[d4] = av;
   }
@@ -719,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ml[u] = make_float2(-INFINITY, 0.f);
             ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (live) {
-              const float* r = rec_at(cc, sq, kConsumers, h);
+              const float* r = rec_at(cc, sq, kAttn, h);
               ml[u] = __ldcg(reinterpret_cast<const float2*>(r));
               ov[u] = __ldcg(reinterpret_cast<const float4*>(r + 4) + d4);
             }
