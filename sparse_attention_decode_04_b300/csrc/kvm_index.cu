@@ -6,10 +6,12 @@
 // accumulated in fp32.
 //
 // One warp per (session, KV head, block touched by the append).  Lane l owns
-// d/32 consecutive dimensions; the warp walks the block's rows in token order,
-// so every load instruction reads one contiguous 2*d-byte key row.  A partial
+// d/32 consecutive dimensions; every load instruction reads one contiguous
+// 2*d-byte key row, and all rows of the block are in flight at once.  A partial
 // last block is averaged over the tokens present.  Rows are independent, so
 // re-running an append over the same tokens rewrites the same values.
+#include <type_traits>
+
 #include "kvm_device.cuh"
 #include "kvm_internal.h"
 
@@ -39,21 +41,33 @@ __global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_
     return;
   }
   const uint16_t* src = k_pool + ((int64_t)page * h_kv + g) * (int64_t)(kBlock * D) + lane * PER;
+  // all rows of the block are loaded before any is summed (one memory round trip), then added in token
+  // order, so the result does not depend on how the history was split into appends
+  using Vec = typename std::conditional<PER == 4, uint2, uint32_t>::type;
+  Vec w[kBlock];
+#pragma unroll
+  for (int t = 0; t < kBlock; ++t) {
+    if (t < nv) {
+      w[t] = __ldg(reinterpret_cast<const Vec*>(src + t * D));
+    } else {
+      if constexpr (PER == 4) w[t] = make_uint2(0u, 0u); else w[t] = 0u;
+    }
+  }
   float acc[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) acc[i] = 0.f;
-#pragma unroll 8
-  for (int t = 0; t < nv; ++t) {
-    if constexpr (PER == 4) {
-      const uint2 w = __ldg(reinterpret_cast<const uint2*>(src + t * D));
-      acc[0] += bf16lo(w.x);
-      acc[1] += bf16hi(w.x);
-      acc[2] += bf16lo(w.y);
-      acc[3] += bf16hi(w.y);
-    } else {
-      const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(src + t * D));
-      acc[0] += bf16lo(w);
-      acc[1] += bf16hi(w);
+#pragma unroll
+  for (int t = 0; t < kBlock; ++t) {
+    if (t < nv) {
+      if constexpr (PER == 4) {
+        acc[0] += bf16lo(w[t].x);
+        acc[1] += bf16hi(w[t].x);
+        acc[2] += bf16lo(w[t].y);
+        acc[3] += bf16hi(w[t].y);
+      } else {
+        acc[0] += bf16lo(w[t]);
+        acc[1] += bf16hi(w[t]);
+      }
     }
   }
   float* dst = index + (((int64_t)s * h_kv + g) * max_blocks + b) * D + lane * PER;

@@ -117,6 +117,7 @@ extern "C" kvm_status kvm_score_select_noalloc(const kvm_params* p, const uint16
   a.seg_base[n_sessions] = base;
 
   cudaError_t e = cudaGetDevice(&c.device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, c.device);
   unsigned char* scratch = nullptr;
   if (e == cudaSuccess) e = scratch_address(c.device, &scratch);
   if (e != cudaSuccess)

@@ -15,9 +15,13 @@
 //   each CTA owns 1/C of the blocks.  From the tiles' partials it forms the
 //   softmax normalisers, Gs[b] = sum_h e[b][h] * exp(m_tile - M_h) / Z_h, and
 //   then runs an exact 3-pass radix select (11/11/10 bits) over the
-//   candidates, histograms merged through distributed shared memory, followed
-//   by a cluster-wide stable compaction: ascending ids, equal scores resolved
-//   toward the lower id.
+//   candidates: per pass each CTA builds its slice's histogram with
+//   shared-memory atomics, one cluster barrier, and every CTA pulls the C
+//   histograms through distributed shared memory (16-byte loads, 4 bins each)
+//   and scans the merged counts itself (double-buffered histograms, so one
+//   barrier a pass).
+//   A stable compaction follows (one exchange of per-CTA tie / kept counts):
+//   ascending ids, equal scores resolved toward the lower id.
 #include <cooperative_groups.h>
 
 #include "kvm_device.cuh"
@@ -173,8 +177,14 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   }
 }
 
-// Block-wide exclusive scan of one int per thread (kSelectThreads threads); returns the total via *total.
-__device__ int block_exclusive_scan(int v, int* scratch, int* total) {
+struct RadixResult {
+  uint32_t digit;
+  int krem;
+};
+
+// Block-wide exclusive scan of one int per thread for NT threads; returns the total via *total.
+template <int NT>
+__device__ int block_exclusive_scan_n(int v, int* scratch, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -185,7 +195,7 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   if (lane == 31) scratch[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    int w = lane < kSelectThreads / 32 ? scratch[lane] : 0;
+    int w = lane < NT / 32 ? scratch[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
@@ -195,21 +205,17 @@ __device__ int block_exclusive_scan(int v, int* scratch, int* total) {
   }
   __syncthreads();
   const int before = (warp > 0 ? scratch[32 + warp - 1] : 0) + x - v;
-  *total = scratch[32 + kSelectThreads / 32 - 1];
+  *total = scratch[32 + NT / 32 - 1];
   __syncthreads();
   return before;
 }
-
-struct RadixResult {
-  uint32_t digit;
-  int krem;
-};
 
 template <int G>
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     const float* __restrict__ e_buf, const float2* __restrict__ part, int64_t max_tiles, int64_t max_blocks,
     int h_kv, int h_q, SessionArgs a, int rows_per_tile, int n_sink, int n_recent, int top_k, int budget,
     int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores, const float* __restrict__ gs_in) {
+  constexpr int NT = kSelectThreads;
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
   const int C = (int)cluster.num_blocks();
@@ -217,11 +223,11 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
   uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw);        // [slice_cap]
   float* coef = reinterpret_cast<float*>(key + slice_cap);       // [tiles in slice][G]
   __shared__ float s_M[G], s_invZ[G];
-  __shared__ int hist[kRadixBins];
-  __shared__ int tot[kRadixBins];
+  __shared__ __align__(16) int hist[2][kRadixBins];  // double-buffered: pass p builds hist[p & 1] while others may read the other
   __shared__ int scan_scratch[64];
   __shared__ RadixResult res;
-  __shared__ int cta_count;
+  __shared__ int cnt[2];               // this CTA's (equal to T, kept otherwise) counts, read by higher ranks
+  __shared__ int sums[NT];             // per-thread merged bin counts, then the counts above each thread
 
   const int s = blockIdx.z, g = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_blk = a.n_blk[s];
@@ -235,161 +241,215 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     const float* src = gs_in + ((int64_t)s * h_kv + g) * max_blocks;
     float* gs_dst = (group_scores && group_scores != gs_in) ? group_scores + ((int64_t)s * h_kv + g) * max_blocks
                                                               : nullptr;
-    for (int b = lo + tid; b < hi; b += kSelectThreads) {
+    for (int b = lo + tid; b < hi; b += NT) {
       const float gs = src[b];
       key[b - lo] = order_key(gs);
       if (gs_dst) gs_dst[b] = gs;
     }
-    __syncthreads();
   } else {
-  // 1. softmax normalisers of the group's heads (every CTA computes them the same way)
-  if (warp < G) {
-    const float2* p = part + ((int64_t)s * h_q + g * G + warp) * max_tiles;
-    float M = -INFINITY;
-    for (int t = lane; t < n_tiles; t += 32) M = fmaxf(M, p[t].x);
+    // 1. softmax normalisers of the group's heads (every CTA computes them the same way)
+    if (warp < G) {
+      const float2* p = part + ((int64_t)s * h_q + g * G + warp) * max_tiles;
+      float M = -INFINITY;
+      for (int t = lane; t < n_tiles; t += 32) M = fmaxf(M, p[t].x);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    float Z = 0.f;
-    for (int t = lane; t < n_tiles; t += 32) Z += p[t].y * expf(p[t].x - M);
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      float Z = 0.f;
+      for (int t = lane; t < n_tiles; t += 32) Z += p[t].y * expf(p[t].x - M);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-    if (lane == 0) {
-      s_M[warp] = M;
-      s_invZ[warp] = 1.f / Z;
+      for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
+      if (lane == 0) {
+        s_M[warp] = M;
+        s_invZ[warp] = 1.f / Z;
+      }
+    }
+    __syncthreads();
+    // 2. per-tile coefficients exp(m_tile - M) / Z for the tiles overlapping this slice
+    const int t0 = lo / rows_per_tile;
+    const int nt = hi > lo ? (hi - 1) / rows_per_tile - t0 + 1 : 0;
+    for (int i = tid; i < nt * G; i += NT) {
+      const int t = t0 + i / G, h = i % G;
+      const float2 p = part[((int64_t)s * h_q + g * G + h) * max_tiles + t];
+      coef[i] = expf(p.x - s_M[h]) * s_invZ[h];
+    }
+    __syncthreads();
+    // 3. group scores of the slice
+    const float* e_src = e_buf + ((int64_t)s * h_kv + g) * max_blocks * G;
+    float* gs_dst = group_scores ? group_scores + ((int64_t)s * h_kv + g) * max_blocks : nullptr;
+#pragma unroll 4
+    for (int b = lo + tid; b < hi; b += NT) {
+      const float* cf = coef + (b / rows_per_tile - t0) * G;
+      float gs = 0.f;
+#pragma unroll
+      for (int h = 0; h < G; ++h) gs = fmaf(e_src[(int64_t)b * G + h], cf[h], gs);
+      key[b - lo] = order_key(gs);
+      if (gs_dst) gs_dst[b] = gs;
     }
   }
   __syncthreads();
-  // 2. per-tile coefficients exp(m_tile - M) / Z for the tiles overlapping this slice
-  const int t0 = lo / rows_per_tile;
-  const int nt = hi > lo ? (hi - 1) / rows_per_tile - t0 + 1 : 0;
-  for (int i = tid; i < nt * G; i += kSelectThreads) {
-    const int t = t0 + i / G, h = i % G;
-    const float2 p = part[((int64_t)s * h_q + g * G + h) * max_tiles + t];
-    coef[i] = expf(p.x - s_M[h]) * s_invZ[h];
-  }
-  __syncthreads();
-  // 3. group scores of the slice
-  const float* e_src = e_buf + ((int64_t)s * h_kv + g) * max_blocks * G;
-  float* gs_dst = group_scores ? group_scores + ((int64_t)s * h_kv + g) * max_blocks : nullptr;
-  for (int b = lo + tid; b < hi; b += kSelectThreads) {
-    const float* cf = coef + (b / rows_per_tile - t0) * G;
-    float gs = 0.f;
-#pragma unroll
-    for (int h = 0; h < G; ++h) gs = fmaf(e_src[(int64_t)b * G + h], cf[h], gs);
-    key[b - lo] = order_key(gs);
-    if (gs_dst) gs_dst[b] = gs;
-  }
-  __syncthreads();
-  }
 
   if (n_blk <= budget) {  // every block is kept (uniform across the cluster)
-    for (int b = lo + tid; b < hi; b += kSelectThreads) kept_row[b] = b;
+    for (int b = lo + tid; b < hi; b += NT) kept_row[b] = b;
     if (crank == 0)
-      for (int i = n_blk + tid; i < budget; i += kSelectThreads) kept_row[i] = -1;
+      for (int i = n_blk + tid; i < budget; i += NT) kept_row[i] = -1;
     return;  // no distributed shared memory access on this path
   }
   const int cand_lo = n_sink, cand_hi = n_blk - n_recent;  // candidates [cand_lo, cand_hi)
+  const int len = hi - lo;
+  const int n_iter = (len + NT - 1) / NT;
 
-  // 4. exact radix select of the top_k-th largest candidate key
+  // 4. exact radix select of the top_k-th largest candidate key (11 + 11 + 10 bits).  Each CTA builds the
+  //    histogram of its slice; after one cluster barrier every CTA pulls all C histograms (independent
+  //    loads) and scans the merged counts itself, so all CTAs reach the same digit without a second barrier.
   uint32_t prefix = 0, pmask = 0;
   int krem = top_k;
-#pragma unroll
+#pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
     const int nb = pass == 2 ? 1024 : 2048;
-    for (int i = tid; i < kRadixBins; i += kSelectThreads) hist[i] = 0;
+    int* h = hist[pass & 1];
+    for (int i = tid; i < kRadixBins; i += NT) h[i] = 0;
     __syncthreads();
-    const int clo = max(lo, cand_lo), chi = min(hi, cand_hi);
-    for (int b = clo + tid; b < chi; b += kSelectThreads) {
-      const uint32_t k = key[b - lo];
-      if ((k & pmask) == prefix) atomicAdd(&hist[(k >> shift) & (nb - 1)], 1);
+#pragma unroll 4
+    for (int j = 0; j < n_iter; ++j) {
+      const int b = lo + tid + j * NT;
+      int d = -1;
+      if (b < hi && b >= cand_lo && b < cand_hi) {
+        const uint32_t k = key[b - lo];
+        if ((k & pmask) == prefix) d = (int)((k >> shift) & (uint32_t)(nb - 1));
+      }
+      if (d >= 0) atomicAdd(&h[d], 1);
     }
-    cluster.sync();
-    if (crank == 0) {
-      // merged histogram; each thread owns 4 consecutive bins
-      int local[4], sum = 0;
+    cluster.sync();  // every slice's histogram is complete (and the previous pass's pulls are done)
+    // merged counts of this thread's 4 bins (one 16-byte remote load per rank), then keys in bins owned by
+    // higher threads (reversed scan)
+    int local[4] = {0, 0, 0, 0}, sum = 0;
+    if (4 * tid < nb) {
+      int4 parts[8];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int bin = 4 * tid + j;
-        int v = 0;
-        if (bin < nb)
-          for (int r = 0; r < C; ++r) v += cluster.map_shared_rank(hist, r)[bin];
-        local[j] = v;
-        sum += v;
-      }
-      // suffix sums over threads: count of keys in bins owned by higher threads
-      // keys in bins owned by higher threads: an exclusive scan in reversed thread order
-      int rev_total;
-      tot[tid] = sum;
-      __syncthreads();
-      const int mine = tot[kSelectThreads - 1 - tid];
-      const int excl = block_exclusive_scan(mine, scan_scratch, &rev_total);
-      // thread tid' = kSelectThreads-1-tid owns `mine`; keys above tid' = excl
-      tot[kSelectThreads - 1 - tid] = excl;
-      __syncthreads();
-      int above = tot[tid];
-      for (int j = 3; j >= 0; --j) {
-        const int bin = 4 * tid + j;
-        if (bin < nb && local[j] > 0 && above < krem && krem <= above + local[j]) {
-          res.digit = (uint32_t)bin;
-          res.krem = krem - above;
+      for (int r = 0; r < 8; ++r)
+        if (r < C) parts[r] = *reinterpret_cast<const int4*>(cluster.map_shared_rank(h, r) + 4 * tid);
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+        if (r < C) {
+          local[0] += parts[r].x;
+          local[1] += parts[r].y;
+          local[2] += parts[r].z;
+          local[3] += parts[r].w;
         }
-        above += local[j];
-      }
+      sum = local[0] + local[1] + local[2] + local[3];
     }
-    cluster.sync();
-    const RadixResult r = *cluster.map_shared_rank(&res, 0);
-    prefix |= r.digit << shift;
+    const int rev = NT - 1 - tid;
+    sums[tid] = sum;
+    __syncthreads();
+    int total;
+    const int excl_rev = block_exclusive_scan_n<NT>(sums[rev], scan_scratch, &total);
+    sums[rev] = excl_rev;  // keys in bins owned by threads above `rev`
+    __syncthreads();
+    int above = sums[tid];
+#pragma unroll
+    for (int jb = 3; jb >= 0; --jb) {
+      const int bin = 4 * tid + jb;
+      if (bin < nb && local[jb] > 0 && above < krem && krem <= above + local[jb]) {
+        res.digit = (uint32_t)bin;
+        res.krem = krem - above;
+      }
+      above += local[jb];
+    }
+    __syncthreads();
+    prefix |= res.digit << shift;
     pmask |= (uint32_t)(nb - 1) << shift;
-    krem = r.krem;
+    krem = res.krem;
+    __syncthreads();  // res and sums are rewritten by the next pass
   }
   const uint32_t T = prefix;
-  const int need_eq = krem;  // how many keys equal to T are taken (lowest ids first)
+  const int need_eq = krem;  // how many keys equal to T are taken (lowest ids first, over the whole cluster)
 
-  // 5. stable compaction: each thread owns a contiguous run of the slice
-  const int len = hi - lo;
-  const int per = (len + kSelectThreads - 1) / kSelectThreads;
-  const int u0 = lo + min(len, tid * per), u1 = lo + min(len, (tid + 1) * per);
+  // 5. stable compaction.  Warp w owns slice positions [w * 32 * n_iter, (w + 1) * 32 * n_iter), lane-interleaved
+  //    (conflict-free shared-memory reads); block order is kept within and across warps and CTAs.
   auto is_cand = [&](int b) { return b >= cand_lo && b < cand_hi; };
-  int n_eq = 0;
-  for (int b = u0; b < u1; ++b) n_eq += (is_cand(b) && key[b - lo] == T);
-  int cta_eq;
-  const int eq_off = block_exclusive_scan(n_eq, scan_scratch, &cta_eq);
-  if (tid == 0) cta_count = cta_eq;
-  cluster.sync();
-  int eq_base = 0;
-  for (int r = 0; r < crank; ++r) eq_base += *cluster.map_shared_rank(&cta_count, r);
-  cluster.sync();  // everyone has read cta_count before it is reused
-  int n_keep_local = 0, e_i = eq_base + eq_off;
-  for (int b = u0; b < u1; ++b) {
-    bool keep;
-    if (!is_cand(b)) {
-      keep = true;
-    } else {
-      const uint32_t k = key[b - lo];
-      keep = k > T || (k == T && e_i < need_eq);
-      e_i += (k == T);
+  const int wbase = lo + warp * 32 * n_iter;
+  int eq_w = 0, gt_w = 0, nc_w = 0;
+  for (int j = 0; j < n_iter; ++j) {
+    const int b = wbase + j * 32 + lane;
+    bool eq = false, gt = false, nc = false;
+    if (b < hi) {
+      if (!is_cand(b)) {
+        nc = true;
+      } else {
+        const uint32_t k = key[b - lo];
+        eq = k == T;
+        gt = k > T;
+      }
     }
-    n_keep_local += keep;
+    eq_w += __popc(__ballot_sync(0xffffffffu, eq));
+    gt_w += __popc(__ballot_sync(0xffffffffu, gt));
+    nc_w += __popc(__ballot_sync(0xffffffffu, nc));
   }
-  int cta_keep;
-  const int keep_off = block_exclusive_scan(n_keep_local, scan_scratch, &cta_keep);
-  if (tid == 0) cta_count = cta_keep;
+  int eq_cta, other_cta;
+  const int eq_before = block_exclusive_scan_n<NT>(lane == 0 ? eq_w : 0, scan_scratch, &eq_cta);
+  block_exclusive_scan_n<NT>(lane == 0 ? gt_w + nc_w : 0, scan_scratch, &other_cta);
+  if (tid == 0) {
+    cnt[0] = eq_cta;
+    cnt[1] = other_cta;
+  }
   cluster.sync();
-  int keep_base = 0;
-  for (int r = 0; r < crank; ++r) keep_base += *cluster.map_shared_rank(&cta_count, r);
-  int pos = keep_base + keep_off;
-  e_i = eq_base + eq_off;
-  for (int b = u0; b < u1; ++b) {
-    bool keep;
-    if (!is_cand(b)) {
-      keep = true;
-    } else {
-      const uint32_t k = key[b - lo];
-      keep = k > T || (k == T && e_i < need_eq);
-      e_i += (k == T);
+  // counts of the lower ranks: ties before this CTA, and kept blocks before it
+  int eq_base = 0, keep_base = 0;
+  for (int r = 0; r < crank; ++r) {
+    const int* rc = cluster.map_shared_rank(cnt, r);
+    const int e_r = rc[0], o_r = rc[1];
+    const int taken = max(0, min(e_r, need_eq - eq_base));
+    keep_base += o_r + taken;
+    eq_base += e_r;
+  }
+  // per warp: ties before the warp (within the cluster) and kept blocks before the warp
+  const int eq_warp0 = eq_base + __shfl_sync(0xffffffffu, eq_before, 0);
+  int keep_w = 0;
+  {
+    int eq_run = eq_warp0;
+    for (int j = 0; j < n_iter; ++j) {
+      const int b = wbase + j * 32 + lane;
+      bool keep = false, eq = false;
+      if (b < hi) {
+        if (!is_cand(b)) {
+          keep = true;
+        } else {
+          const uint32_t k = key[b - lo];
+          eq = k == T;
+          keep = k > T;
+        }
+      }
+      const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+      if (eq) keep = eq_run + __popc(eqm & ((1u << lane) - 1)) < need_eq;
+      eq_run += __popc(eqm);
+      keep_w += __popc(__ballot_sync(0xffffffffu, keep));
     }
-    if (keep) kept_row[pos++] = b;
+  }
+  int keep_cta;
+  const int keep_before = block_exclusive_scan_n<NT>(lane == 0 ? keep_w : 0, scan_scratch, &keep_cta);
+  int pos = keep_base + __shfl_sync(0xffffffffu, keep_before, 0);
+  {
+    int eq_run = eq_warp0;
+    for (int j = 0; j < n_iter; ++j) {
+      const int b = wbase + j * 32 + lane;
+      bool keep = false, eq = false;
+      if (b < hi) {
+        if (!is_cand(b)) {
+          keep = true;
+        } else {
+          const uint32_t k = key[b - lo];
+          eq = k == T;
+          keep = k > T;
+        }
+      }
+      const unsigned eqm = __ballot_sync(0xffffffffu, eq);
+      if (eq) keep = eq_run + __popc(eqm & ((1u << lane) - 1)) < need_eq;
+      eq_run += __popc(eqm);
+      const unsigned km = __ballot_sync(0xffffffffu, keep);
+      if (keep) kept_row[pos + __popc(km & ((1u << lane) - 1))] = b;
+      pos += __popc(km);
+    }
   }
   cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
@@ -435,10 +495,14 @@ cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_
     // nothing to score: every kept list is empty
     return cudaMemsetAsync(kept, 0xFF, sizeof(int32_t) * (size_t)n_sessions * c.p.h_kv * c.budget, st);
   }
-  // rows per score tile: about 512 tiles over the call, 32..1024 rows each
-  int64_t want = rows / 512;
-  int rpt = kStageRows;
-  while (rpt < want && rpt < 1024) rpt <<= 1;
+  // rows per score tile: one wave of two CTAs per SM over the call (a multiple of 32 rows, 32..4096)
+  (void)rows;
+  const int64_t units = (int64_t)c.p.h_kv * n_sessions;
+  const int64_t sms = c.num_sms > 0 ? c.num_sms : 1;
+  const int64_t tiles_per_head = (2 * sms + units - 1) / units;
+  int64_t rpt64 = (max_blk + tiles_per_head - 1) / tiles_per_head;
+  rpt64 = (rpt64 + kStageRows - 1) / kStageRows * kStageRows;
+  const int rpt = (int)(rpt64 < kStageRows ? kStageRows : (rpt64 > 4096 ? 4096 : rpt64));
   const int tiles = (max_blk + rpt - 1) / rpt;
   const size_t smem_a = (size_t)kStages * kStageRows * D * 4 + (size_t)rpt * G * 4;
   auto ka = score_tile_kernel<D, G>;
