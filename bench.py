@@ -11,7 +11,8 @@ Metric: step latency per layer (us) and the HBM GB/s of the bytes each layer
 must touch (index read + appended keys + kept K/V read + view write).
 
     python bench.py [--steps K] [--warmup W] [--gpus N] [--impl kvm|reference]
-                    [--workload NAME] [--no-e2e] [--no-cpu-baseline]
+                    [--workload NAME] [--layers N] [--no-e2e] [--no-cpu-baseline]
+                    [--profile-step]
 
 --impl reference times the CPU oracle on a bounded sample of the same workload
 (one KV head of one layer per step) on the host's cores.
@@ -385,12 +386,18 @@ def run_kvm(args, w):
                "kind": "oracle", "sample": desc}
 
     traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        with open(tr_path) as f:
-            tr = json.load(f).get(w.name)
-        if tr and tr.get("source_hash") == K_source_hash():
-            traffic = tr.get("bytes_per_launch")
+    prof_dir = os.path.join(ROOT, "profiles")
+    want_hash = K_source_hash()
+    for fn in sorted(os.listdir(prof_dir)) if os.path.isdir(prof_dir) else []:
+        if not fn.endswith(".md"):
+            continue
+        with open(os.path.join(prof_dir, fn)) as f:
+            for ln in f:
+                parts = ln.split()
+                if len(parts) >= 5 and parts[0] == "traffic" and parts[1] == w.name:
+                    kv = dict(p.split("=", 1) for p in parts[3:] if "=" in p)
+                    if kv.get("source_hash") == want_hash:
+                        traffic = int(kv["bytes_per_launch"])
 
     if rank == 0:
         line = {
@@ -436,6 +443,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvm", choices=["kvm", "reference"])
     ap.add_argument("--workload", default="ws1m_16layer", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--layers", type=int, default=None,
+                    help="run only this many layers of the workload (profiling captures; each layer's launches are "
+                         "the full-size ones)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -448,6 +458,8 @@ def main():
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     w = synth.WORKLOADS[args.workload]
+    if args.layers is not None:
+        w = w.with_(n_layers=max(1, min(args.layers, w.n_layers)))
     if args.impl == "reference":
         run_reference(args, w)
     else:
