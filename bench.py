@@ -57,6 +57,22 @@ def view_call_bytes(w: synth.Workload) -> int:
     return 4 * w.h_kv * w.view_tokens * w.d * 2 * w.n_sessions
 
 
+def max_over_ranks(values, world: int, device):
+    """Each timing's maximum over all ranks (every rank calls this; identity on one rank)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def job_gbps(bytes_per_rank_layer: int, us_layer_slowest: float, world: int) -> float:
+    """Whole-job GB/s: every rank moved its own bytes in the slowest rank's time (weak scaling)."""
+    return bytes_per_rank_layer * world / (us_layer_slowest * 1e-6) / 1e9
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -317,14 +333,11 @@ def run_kvm(args, w):
     stage_us = {name: round(ms * 1e3 / L, 2) for name, ms in stage_ms.items()}
     eager_ms = timed(step, max(1, min(args.steps, 3)))
 
-    if world > 1:
-        t = torch.tensor([step_ms, eager_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms, eager_ms = float(t[0]), float(t[1])
+    step_ms, eager_ms = max_over_ranks([step_ms, eager_ms], world, dev)
 
     us_layer = step_ms * 1e3 / L
     bytes_layer = must_touch_bytes(w)
-    gbs = bytes_layer / (us_layer * 1e-6) / 1e9 * world
+    gbs = job_gbps(bytes_layer, us_layer, world)
     peak, peak_kind = load_peaks()
     vb = view_call_bytes(w)
     view_us = stage_us.get("materialize_attn") or us_layer

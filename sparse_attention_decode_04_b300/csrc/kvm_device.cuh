@@ -202,6 +202,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Kernels of the decode path are launched with programmatic stream serialisation: the next kernel on the
+// stream may be scheduled while this one still runs.  Every kernel therefore calls griddep_wait() before it
+// reads anything an earlier kernel wrote and before it writes any output, and calls it on every path (so a
+// kernel never completes before its predecessor, which keeps the ordering transitive).  Without a
+// programmatic predecessor both instructions are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_
                                                                    float* __restrict__ index,
                                                                    uint32_t* __restrict__ status) {
   constexpr int PER = D / 32;  // dims per lane
+  griddep_wait();
   const int s = blockIdx.z, g = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t bi = (int64_t)blockIdx.x * kWarps + warp;
@@ -86,13 +87,10 @@ cudaError_t launch_index_append(const Ctx& c, const uint16_t* k_pool, int64_t n_
                                 cudaStream_t st) {
   if (max_count <= 0) return cudaSuccess;
   dim3 grid((max_count + kWarps - 1) / kWarps, c.p.h_kv, n_sessions);
-  if (c.p.d == 128)
-    index_append_kernel<128><<<grid, kWarps * 32, 0, st>>>(k_pool, n_pages, bt, c.p.max_blocks, c.p.h_kv, a,
-                                                            index, c.status);
-  else
-    index_append_kernel<64><<<grid, kWarps * 32, 0, st>>>(k_pool, n_pages, bt, c.p.max_blocks, c.p.h_kv, a,
-                                                           index, c.status);
-  return cudaGetLastError();
+  return c.p.d == 128 ? launch_pdl(index_append_kernel<128>, grid, dim3(kWarps * 32), 0, st, 1, k_pool, n_pages, bt,
+                                    c.p.max_blocks, c.p.h_kv, a, index, c.status)
+                       : launch_pdl(index_append_kernel<64>, grid, dim3(kWarps * 32), 0, st, 1, k_pool, n_pages, bt,
+                                    c.p.max_blocks, c.p.h_kv, a, index, c.status);
 }
 
 }  // namespace kvm

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "kvm.h"
 
 namespace kvm {
@@ -84,6 +86,33 @@ cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st);
 
 // Sets the message kvm_last_error() returns on this thread (kvm_api.cu).
 void set_last_error(const char* msg);
+
+// Launches `kernel` on `st` with programmatic stream serialisation (the kernel must call griddep_wait()
+// before touching its predecessor's data; see kvm_device.cuh), and an optional cluster of `cluster_x` CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_x,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on `device`.
 // The limit only ever grows, and each (kernel, device) pair is configured once

@@ -51,6 +51,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   __shared__ float red[kScoreThreads / 32][G];
   __shared__ float tile_max[G];
 
+  griddep_wait();
   const int s = blockIdx.z, g = blockIdx.y, tile = blockIdx.x;
   const int64_t n_blk = a.n_blk[s];
   const int64_t r0 = (int64_t)tile * rows_per_tile;
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     int h_kv, int h_q, SessionArgs a, int rows_per_tile, int n_sink, int n_recent, int top_k, int budget,
     int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores, const float* __restrict__ gs_in) {
   constexpr int NT = kSelectThreads;
+  griddep_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
   const int C = (int)cluster.num_blocks();
@@ -465,21 +467,9 @@ cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, in
   auto kb = select_kernel<G>;
   cudaError_t e;
   if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(C, c.p.h_kv, n_sessions);
-  cfg.blockDim = dim3(kSelectThreads);
-  cfg.dynamicSmemBytes = smem_b;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = C;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kb, (const float*)c.e_buf, (const float2*)c.part, c.max_tiles, c.p.max_blocks,
-                            c.p.h_kv, c.p.h_q, a, rpt, c.p.n_sink, c.p.n_recent, c.p.top_k, c.budget, slice_cap,
-                            kept, group_scores, gs_in);
+  return launch_pdl(kb, dim3(C, c.p.h_kv, n_sessions), dim3(kSelectThreads), smem_b, st, C, (const float*)c.e_buf,
+                    (const float2*)c.part, c.max_tiles, c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.p.n_sink,
+                    c.p.n_recent, c.p.top_k, c.budget, slice_cap, kept, group_scores, gs_in);
 }
 
 template <int D, int G>
@@ -508,9 +498,10 @@ cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_
   auto ka = score_tile_kernel<D, G>;
   cudaError_t e = ensure_smem(ka, c.device, smem_a);
   if (e != cudaSuccess) return e;
-  ka<<<dim3(tiles, c.p.h_kv, n_sessions), kScoreThreads, smem_a, st>>>(
-      q, index, c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.e_buf, c.part, c.max_tiles, head_scores, c.status);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_pdl(ka, dim3(tiles, c.p.h_kv, n_sessions), dim3(kScoreThreads), smem_a, st, 1, q, index,
+                      c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.e_buf, c.part, c.max_tiles, head_scores,
+                      c.status)) != cudaSuccess)
+    return e;
 
   return launch_select<G>(c, n_sessions, a, rpt, max_blk, kept, group_scores, nullptr, st);
 }

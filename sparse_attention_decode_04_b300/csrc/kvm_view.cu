@@ -234,6 +234,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
+  if (tid == 0) {
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&rotated[st], 1);
+      mbar_init(&empty[st], (kWrite ? 1 : 0) + (kAttend ? 1 : 0));  // the stage's rotation and attention warps
+    }
+    mbar_fence_init();
+  }
+  griddep_wait();  // kept ids, views and outputs belong to the stream order from here on
   if (vp.any_empty) {
     // sessions with no kept block (empty history): zero output rows and view lengths
     const int64_t per_s = (int64_t)vp.h_q * D, n_out = vp.n_sessions * per_s;
@@ -249,14 +258,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t nb = fb - fa;  // blocks of this CTA
   const int Lcap = 32 * vp.budget;
 
-  if (tid == 0) {
-    for (int st = 0; st < NS; ++st) {
-      mbar_init(&full[st], 1);
-      mbar_init(&rotated[st], 1);
-      mbar_init(&empty[st], (kWrite ? 1 : 0) + (kAttend ? 1 : 0));  // the stage's rotation and attention warps
-    }
-    mbar_fence_init();
-  }
   __syncthreads();
 
   const Cursor firstc = locate(fa, a, vp.n_sessions), lastc = locate(fb - 1, a, vp.n_sessions);
@@ -869,8 +870,7 @@ cudaError_t launch_dg(const Ctx& c, int mode, const CUtensorMap* maps, const Vie
       mode == 0 ? view_kernel<D, G, 0> : (mode == 1 ? view_kernel<D, G, 1> : view_kernel<D, G, 2>);
   cudaError_t e = ensure_smem(kern, c.device, Q::BYTES);
   if (e != cudaSuccess) return e;
-  kern<<<vp.P, kThreads, Q::BYTES, st>>>(maps[0], maps[1], maps[2], maps[3], vp, a);
-  return cudaGetLastError();
+  return launch_pdl(kern, dim3(vp.P), dim3(kThreads), Q::BYTES, st, 1, maps[0], maps[1], maps[2], maps[3], vp, a);
 }
 
 template <int D>
