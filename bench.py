@@ -4,9 +4,10 @@ Default workload (ws1m_16layer): 40 query heads / 8 KV heads, d = 128, a
 1,048,576-token history per layer with 16 layers resident in HBM (64 GiB of
 bf16 K/V pages + 2 GiB fp32 Mean-K index), a 65,536-token view per layer
 (4 sink + 32 recent + 2012 top-k blocks), one decode query per layer.  One
-step = for each of the 16 layers, in order:
-    kvm_index_append (the step's 512 new tokens) -> kvm_score_select
-    -> kvm_materialize_attn (gather + re-RoPE view, decode attention).
+step = the step's 512 new tokens appended to every layer's index (kvm_index_append, on a side
+stream: no layer's append depends on an earlier layer), then for each of the 16 layers, in order:
+    kvm_score_select (after that layer's append) -> kvm_materialize_attn (gather + re-RoPE view,
+    decode attention).
 Metric: step latency per layer (us) and the HBM GB/s of the bytes each layer
 must touch (index read + appended keys + kept K/V read + view write).
 
@@ -253,11 +254,35 @@ def run_kvm(args, w):
         K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer], qs[layer], k_view,
                                v_view, view_len, outs[layer])
 
-    def step():
+    # The step's new tokens have their keys for every layer when the step starts, so no layer's index append
+    # waits on an earlier layer's output: all appends go to a side stream at the start of the step, and each
+    # layer's scoring waits only for its own append.
+    app_stream = torch.cuda.Stream()
+    app_done = [torch.cuda.Event() for _ in range(L)]
+
+    def appends_ahead(before_append=None):
+        app_stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(app_stream):
+            for layer in range(L):
+                if before_append is not None:
+                    before_append(layer)
+                call_append(layer)
+                app_done[layer].record(app_stream)
+
+    def layers_after_appends(select_fn, view_fn):
+        main = torch.cuda.current_stream()
         for layer in range(L):
-            call_append(layer)
-            call_select(layer)
-            call_view(layer)
+            if w.append_tok:
+                main.wait_event(app_done[layer])
+            select_fn(layer)
+            view_fn(layer)
+        if w.append_tok:
+            main.wait_stream(app_stream)
+
+    def step():
+        if w.append_tok:
+            appends_ahead()
+        layers_after_appends(call_select, call_view)
 
     stage_fns = {"index_append": call_append, "score_select": call_select, "materialize_attn": call_view}
 
@@ -361,18 +386,23 @@ def run_kvm(args, w):
         h2d = q_host.numel() * 2 + (sum(t.numel() * 2 for t in new_k) * 2 if new_k else 0)
         d2h = out_host.numel() * 4
 
+        def copy_new_pages(layer):
+            if new_k:
+                p0 = first_new_page[0]
+                kp[layer][p0:p0 + app_blocks].copy_(new_k[layer], non_blocking=True)
+                vp[layer][p0:p0 + app_blocks].copy_(new_v[layer], non_blocking=True)
+
         def e2e_step():
             q_dev.copy_(q_host, non_blocking=True)
-            for layer in range(L):
-                if new_k:
-                    p0 = first_new_page[0]
-                    kp[layer][p0:p0 + app_blocks].copy_(new_k[layer], non_blocking=True)
-                    vp[layer][p0:p0 + app_blocks].copy_(new_v[layer], non_blocking=True)
-                if w.append_tok:
-                    K.kvm_index_append(ctx, kp[layer], n_pages, bt, [n_hist] * S, [w.append_tok] * S, index[layer])
-                K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept[layer])
-                K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer], q_dev[layer], k_view,
-                                       v_view, view_len, outs[layer])
+            if w.append_tok:
+                appends_ahead(copy_new_pages)   # H2D of the new pages + appends, on the side stream
+            else:
+                for layer in range(L):
+                    copy_new_pages(layer)
+            layers_after_appends(
+                lambda layer: K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept[layer]),
+                lambda layer: K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer],
+                                                     q_dev[layer], k_view, v_view, view_len, outs[layer]))
             for layer in range(L):
                 out_host[layer].copy_(outs[layer], non_blocking=True)
 

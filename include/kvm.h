@@ -30,8 +30,12 @@
  *   synchronises the host except kvm_create, kvm_destroy and kvm_device_status.
  * - Block size is fixed: 32 tokens per block, one block per physical page.
  * - One context serves one device (the device current at kvm_create) and one
- *   head geometry.  Calls on one context must not run concurrently on
+ *   head geometry.  kvm_score_select, kvm_materialize, kvm_decode_attn and
+ *   kvm_materialize_attn on one context must not run concurrently on
  *   different streams: they share the context's scratch buffers.
+ *   kvm_index_append uses no scratch (only the status word, which it updates
+ *   atomically), so appends may run on another stream alongside them, e.g.
+ *   every layer's append at the start of a decode step.
  * - Layouts (all row-major, innermost last):
  *     pool (K or V) of one layer   [n_pages][h_kv][32][d]            bf16 (a page = 32 tokens, all KV heads)
  *     block_table                  [n_sessions][max_blocks]          int32: block -> page

@@ -752,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (prev + 1 == n_cov) vp.seg_count[sq] = 0;  // every CTA of the segment has counted: ready for the next call
     }
     __syncthreads();
-    // 3. merge of the CTA records of each completed segment, 8 CTAs per round of independent loads
+    // 3. merge of the CTA records of each completed segment, up to 24 CTAs per round of independent loads
     for (int k = 0; k < n_here; ++k) {
       if (!s_last[k]) continue;
       __threadfence();
@@ -765,33 +765,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int h = i / Q4, d4 = i % Q4;
         float m_acc = -INFINITY, l_acc = 0.f;
         float4 o_acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int cb = c0; cb <= c1; cb += 8) {
-          float2 ml[8];
-          float4 ov[8];
+        constexpr int kBatch = 24;  // records loaded together (one round of independent loads)
+        for (int cb = c0; cb <= c1; cb += kBatch) {
+          float2 ml[kBatch];
+          float4 ov[kBatch];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+          for (int u = 0; u < kBatch; ++u) {
             const int cc = cb + u;
-            const bool live = cc <= c1 && live_cta(cc);
             ml[u] = make_float2(-INFINITY, 0.f);
             ov[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (live) {
+            if (cc <= c1 && live_cta(cc)) {
               const float* r = rec_at(cc, sq, kAttn, h);
               ml[u] = __ldcg(reinterpret_cast<const float2*>(r));
               ov[u] = __ldcg(reinterpret_cast<const float4*>(r + 4) + d4);
             }
           }
+          float mb = m_acc;
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            if (ml[u].x == -INFINITY) continue;  // neutral record or no CTA
-            const float mn = fmaxf(m_acc, ml[u].x);
-            const float a0 = exp2f(m_acc - mn), a1 = exp2f(ml[u].x - mn);  // a0 = 0 while m_acc is -inf
-            l_acc = fmaf(l_acc, a0, ml[u].y * a1);
-            o_acc.x = fmaf(o_acc.x, a0, ov[u].x * a1);
-            o_acc.y = fmaf(o_acc.y, a0, ov[u].y * a1);
-            o_acc.z = fmaf(o_acc.z, a0, ov[u].z * a1);
-            o_acc.w = fmaf(o_acc.w, a0, ov[u].w * a1);
-            m_acc = mn;
+          for (int u = 0; u < kBatch; ++u) mb = fmaxf(mb, ml[u].x);
+          if (mb == -INFINITY) continue;  // only neutral records so far
+          const float a0 = exp2f(m_acc - mb);  // 0 while m_acc is -inf
+          l_acc *= a0;
+          o_acc.x *= a0;
+          o_acc.y *= a0;
+          o_acc.z *= a0;
+          o_acc.w *= a0;
+#pragma unroll
+          for (int u = 0; u < kBatch; ++u) {
+            const float a1 = exp2f(ml[u].x - mb);  // 0 for neutral records (m = -inf)
+            l_acc = fmaf(ml[u].y, a1, l_acc);
+            o_acc.x = fmaf(ov[u].x, a1, o_acc.x);
+            o_acc.y = fmaf(ov[u].y, a1, o_acc.y);
+            o_acc.z = fmaf(ov[u].z, a1, o_acc.z);
+            o_acc.w = fmaf(ov[u].w, a1, o_acc.w);
           }
+          m_acc = mb;
         }
         const float inv = l_acc > 0.f ? 1.f / l_acc : 0.f;
         reinterpret_cast<float4*>(vp.out + ((int64_t)s * vp.h_q + g * G + h) * D)[d4] =
