@@ -8,7 +8,8 @@
 //
 // Kernel A (score_tile_kernel), grid (tiles, h_kv, sessions):
 //   streams a tile of index rows of one KV head through shared memory with
-//   1-D bulk copies (4-stage mbarrier pipeline), computes the G scores of
+//   1-D bulk copies (5-stage mbarrier pipeline; one warp polls, one CTA
+//   barrier per stage), computes the G scores of
 //   each row with 8 lanes per row and shuffle reductions, then writes
 //   e[b][h] = exp(s[b][h] - m_tile[h]) and the tile's (m_tile, sum e) per head.
 // Kernel B (select_kernel), grid (C, h_kv, sessions), clusters of C CTAs:
@@ -34,7 +35,7 @@ namespace {
 
 constexpr int kScoreThreads = 256;  // 8 warps, 4 rows each per stage
 constexpr int kStageRows = 32;
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kSelectThreads = 512;
 constexpr int kRadixBins = 2048;
 
@@ -98,11 +99,15 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   int k = 0;
   bool aborted = false;
   for (; k < nstage; ++k) {
-    const bool ok = mbar_wait(&full_bar[k % kStages], (k / kStages) & 1, status);
+    // warp 0 alone polls the stage's barrier; the CTA barrier then releases everyone, and (being past every
+    // warp's work on stage k - 1) lets thread 0 refill that stage
+    bool ok = true;
+    if (warp == 0) ok = mbar_wait(&full_bar[k % kStages], (k / kStages) & 1, status);
     if (__syncthreads_or(!ok)) {
       aborted = true;
       break;
     }
+    if (tid == 0 && k >= 1 && k - 1 + kStages < nstage) issue(k - 1 + kStages);
     const int rows = min(kStageRows, nrows - k * kStageRows);
     const bool valid_row = rsel < rows;  // all lanes compute (uniform shuffles); only valid rows store
     const float* row = stage_buf + (k % kStages) * kStageRows * D + (valid_row ? rsel : 0) * D;
@@ -137,16 +142,17 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
         }
       }
     }
-    __syncthreads();  // every warp is done with this stage buffer
-    if (tid == 0 && k + kStages < nstage) issue(k + kStages);
   }
   if (aborted) {
-    // drain the copies still in flight into this CTA's shared memory (bounded), then leave
+    // drain the copies still in flight into this CTA's shared memory (bounded), then leave: stages k .. issued-1
+    const int issued = min(k == 0 ? kStages : k - 1 + kStages, nstage);
     if (tid == 0)
-      for (int j = k; j < min(k + kStages, nstage); ++j) mbar_wait(&full_bar[j % kStages], (j / kStages) & 1, status);
+      for (int j = k; j < issued; ++j) mbar_wait(&full_bar[j % kStages], (j / kStages) & 1, status);
     __syncthreads();
     return;
   }
+  __syncthreads();  // every warp is done with the last stage (s_tile complete)
+  griddep_launch_dependents();  // the selection may be scheduled while this epilogue runs
 
   // Tile max per head: lanes with the same `sub` hold partial maxima.
   float m = run_max;
@@ -366,6 +372,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
   }
   const uint32_t T = prefix;
   const int need_eq = krem;  // how many keys equal to T are taken (lowest ids first, over the whole cluster)
+  griddep_launch_dependents();  // the view kernel may be scheduled while the compaction runs
 
   // 5. stable compaction.  Warp w owns slice positions [w * 32 * n_iter, (w + 1) * 32 * n_iter), lane-interleaved
   //    (conflict-free shared-memory reads); block order is kept within and across warps and CTAs.

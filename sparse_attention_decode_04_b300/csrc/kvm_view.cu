@@ -242,7 +242,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_fence_init();
   }
-  griddep_wait();  // kept ids, views and outputs belong to the stream order from here on
+  // A rotation lane always rotates the same pairs of every block: rows r = lane / CPR + RPP * pass, pairs
+  // k = 8 cc + v (v < 8) with cc = lane % CPR.  Their offset cos/sin (r * theta_k, block-independent, from the
+  // context's table) stay in registers for the whole kernel: of[pass][u] holds pairs 2u and 2u + 1.  They are
+  // loaded before the wait on the preceding kernel, which wrote none of them.
+  float4 of[Q::PASSES][4];
+  if (kWrite && warp < kRot) {
+    const int cc = lane % Q::CPR;
+#pragma unroll
+    for (int pass = 0; pass < Q::PASSES; ++pass)
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float2* t = vp.rope_off + (lane / Q::CPR + Q::RPP * pass) * (D / 2) + 8 * cc + 2 * u;
+        const float2 o0 = __ldg(t), o1 = __ldg(t + 1);
+        of[pass][u] = make_float4(o0.x, o0.y, o1.x, o1.y);
+      }
+  }
+  griddep_wait();  // kept ids, queries, views and outputs belong to the stream order from here on
   if (vp.any_empty) {
     // sessions with no kept block (empty history): zero output rows and view lengths
     const int64_t per_s = (int64_t)vp.h_q * D, n_out = vp.n_sessions * per_s;
@@ -349,19 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kRot) {
     // ============================================================ rotation warps
     if (kWrite) {
-      // A lane always rotates the same pairs of every block: rows r = lane / CPR + RPP * pass, pairs
-      // k = 8 cc + v (v < 8) with cc = lane % CPR.  Their offset cos/sin (r * theta_k, block-independent)
-      // stay in registers for the whole kernel: of[pass][u] holds pairs 2u and 2u + 1.
       const int cc = lane % Q::CPR;
-      float4 of[Q::PASSES][4];
-#pragma unroll
-      for (int pass = 0; pass < Q::PASSES; ++pass)
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2* t = vp.rope_off + (lane / Q::CPR + Q::RPP * pass) * (D / 2) + 8 * cc + 2 * u;
-          const float2 o0 = __ldg(t), o1 = __ldg(t + 1);
-          of[pass][u] = make_float4(o0.x, o0.y, o1.x, o1.y);
-        }
       for (int64_t jj = warp; jj < nb; jj += kRot) {
         const int st = (int)(jj % NS);
         const uint32_t phase = (uint32_t)((jj / NS) & 1);
@@ -674,6 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  griddep_launch_dependents();     // the next kernel may be scheduled while this one merges and drains
   if (lane == 0) bulk_wait_all();  // this warp's view stores are complete
   __threadfence();                 // this thread's records are visible GPU-wide before the CTA counts itself in
   if (__syncthreads_or(aborted)) {
