@@ -248,7 +248,11 @@ def run_kvm(args, w):
             K.kvm_index_append(ctx, kp[layer], n_pages, bt, [n_hist] * S, [w.append_tok] * S, index[layer])
 
     def call_select(layer):
-        K.kvm_score_select(ctx, qs[layer], 1, index[layer], n_tok, kept[layer])
+        if args.selection == "kvmem":
+            K.kvm_score_select(ctx, qs[layer], 1, index[layer], n_tok, kept[layer])
+        else:  # the pages' controls at the same budget
+            control = K.CONTROL_RECENT_ONLY if args.selection == "recent" else K.CONTROL_WITHDRAWN_AVERAGE
+            K.kvm_select_control(ctx, control, qs[layer], index[layer], n_tok, kept[layer])
 
     def call_view(layer):
         K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer], qs[layer], k_view,
@@ -400,7 +404,8 @@ def run_kvm(args, w):
                 for layer in range(L):
                     copy_new_pages(layer)
             layers_after_appends(
-                lambda layer: K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept[layer]),
+                lambda layer: (K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept[layer])
+                               if args.selection == "kvmem" else call_select(layer)),
                 lambda layer: K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer],
                                                      q_dev[layer], k_view, v_view, view_len, outs[layer]))
             for layer in range(L):
@@ -457,7 +462,7 @@ def run_kvm(args, w):
             "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": w.name, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d, "history_tokens": w.n_tok,
                        "layers": L, "sessions_per_gpu": S, "view_tokens": w.view_tokens, "append_tokens": w.append_tok,
-                       "kv_dtype": "bf16", "cuda_graph": graph is not None,
+                       "kv_dtype": "bf16", "cuda_graph": graph is not None, "selection": args.selection,
                        "l2": "inputs larger than L2 (index 128 MiB + K/V pool 4 GiB per layer), no flush",
                        "parallelism": f"replicas x{world}"},
             "hbm_gbps": round(gbs, 1), "must_touch_bytes_per_layer": bytes_layer,
@@ -494,6 +499,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvm", choices=["kvm", "reference"])
     ap.add_argument("--workload", default="ws1m_16layer", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--selection", default="kvmem", choices=["kvmem", "recent", "withdrawn"],
+                    help="kvmem (the method) or one of the pages' controls at the same budget: recent-only, or the "
+                         "withdrawn head-averaged scoring")
     ap.add_argument("--layers", type=int, default=None,
                     help="run only this many layers of the workload (profiling captures; each layer's launches are "
                          "the full-size ones)")

@@ -213,6 +213,29 @@ kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint
                                 void* stream);
 
 /*
+ * Selection controls (the comparisons the pages report next to the method).
+ * KVMEM reproduction README, "Local reproduction" (a recent-only control at
+ * the same block budget) and "2026-09-08 validation correction" (the
+ * withdrawn scoring averaged the GQA query heads before the softmax).
+ *   KVM_CONTROL_RECENT_ONLY       kept = the last min(n_blk, budget) blocks of
+ *                                 each history, ascending; q, index and
+ *                                 group_scores are not used (may be NULL).
+ *   KVM_CONTROL_WITHDRAWN_AVERAGE per KV head g: q_bar = mean of the group's
+ *                                 query heads (unweighted, not re-normalised),
+ *                                 s[b] = <q_bar, index[g][b]>/sqrt(d),
+ *                                 Gs[g][b] = softmax_b(s)[b]; then the same
+ *                                 sink / recent / top_k selection as
+ *                                 kvm_score_select.
+ * Arguments and layouts are those of kvm_score_select with one query token
+ * (n_q = 1); group_scores (nullable) receives the control's Gs.
+ */
+#define KVM_CONTROL_RECENT_ONLY 1
+#define KVM_CONTROL_WITHDRAWN_AVERAGE 2
+kvm_status kvm_select_control(kvm_ctx* ctx, int32_t control, const uint16_t* q, const float* index,
+                              const int64_t* n_tok, int32_t n_sessions, int32_t* kept_ids, float* group_scores,
+                              void* stream);
+
+/*
  * Reads (and optionally clears) the device status word after synchronising
  * `stream`.  *out receives the KVM_DEV_* bits.  Returns KVM_OK when the word
  * is zero, KVM_ERR_DEVICE or KVM_ERR_TIMEOUT otherwise.  A timed-out view

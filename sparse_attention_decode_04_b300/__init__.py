@@ -22,6 +22,7 @@ KVM_OK = 0
 STATUS_NAMES = {0: "KVM_OK", 1: "KVM_ERR_INVALID_ARG", 2: "KVM_ERR_SHAPE", 3: "KVM_ERR_BUDGET", 4: "KVM_ERR_CUDA",
                 5: "KVM_ERR_TIMEOUT", 6: "KVM_ERR_DEVICE"}
 DEV_BAD_PAGE, DEV_BAD_BLOCK, DEV_TIMEOUT = 0x1, 0x2, 0x4
+CONTROL_RECENT_ONLY, CONTROL_WITHDRAWN_AVERAGE = 1, 2
 
 
 class KvmError(RuntimeError):
@@ -62,8 +63,9 @@ def lib() -> ctypes.CDLL:
         L.kvm_decode_attn.argtypes = [P, P, P, P, P, i32, P, P]
         L.kvm_materialize_attn.argtypes = [P, P, P, i64, P, P, i32, P, P, P, P, P, P, P]
         L.kvm_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
+        L.kvm_select_control.argtypes = [P, i32, P, P, P, i32, P, P, P]
         for name in ("kvm_create", "kvm_destroy", "kvm_index_append", "kvm_score_select", "kvm_materialize",
-                     "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status"):
+                     "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status", "kvm_select_control"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -143,6 +145,13 @@ def kvm_score_select(ctx: Context, q, n_q: int, index, n_tok, kept_ids, group_sc
     n = len(n_tok)
     _check(lib().kvm_score_select(ctx.handle, _ptr(q), int(n_q), _ptr(index), _i64(n_tok), n, _ptr(kept_ids),
                                   _ptr(group_scores), _ptr(head_scores), _stream(stream)))
+
+
+def kvm_select_control(ctx: Context, control: int, q, index, n_tok, kept_ids, group_scores=None, stream=None):
+    """The selection controls: CONTROL_RECENT_ONLY (q, index unused) or CONTROL_WITHDRAWN_AVERAGE."""
+    n = len(n_tok)
+    _check(lib().kvm_select_control(ctx.handle, int(control), _ptr(q), _ptr(index), _i64(n_tok), n, _ptr(kept_ids),
+                                    _ptr(group_scores), _stream(stream)))
 
 
 def kvm_materialize(ctx: Context, k_pool, v_pool, n_pages: int, block_table, n_tok, kept_ids, k_view, v_view,

@@ -284,6 +284,31 @@ kvm_status kvm_score_select(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const 
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_score_select launch");
 }
 
+kvm_status kvm_select_control(kvm_ctx* ctx, int32_t control, const uint16_t* q, const float* index,
+                              const int64_t* n_tok, int32_t n_sessions, int32_t* kept_ids, float* group_scores,
+                              void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if (control != KVM_CONTROL_RECENT_ONLY && control != KVM_CONTROL_WITHDRAWN_AVERAGE)
+    return fail(KVM_ERR_INVALID_ARG, "unknown selection control %d", control);
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_sessions == 0) return KVM_OK;
+  if (!kept_ids) return fail(KVM_ERR_INVALID_ARG, "kvm_select_control: kept_ids is NULL");
+  if (control == KVM_CONTROL_WITHDRAWN_AVERAGE) {
+    if (!q || !index) return fail(KVM_ERR_INVALID_ARG, "kvm_select_control: NULL q or index");
+    if (!aligned(q, 16) || !aligned(index, 16) || !aligned(group_scores, 4))
+      return fail(KVM_ERR_INVALID_ARG, "q and index must be 16-byte aligned, outputs 4-byte aligned");
+  }
+  if (!aligned(kept_ids, 4)) return fail(KVM_ERR_INVALID_ARG, "kept_ids must be 4-byte aligned");
+  SessionArgs a;
+  if ((s = history_args(c, n_tok, n_sessions, &a)) != KVM_OK) return s;
+  cudaError_t e = kvm::launch_select_control(c, control, q, index, n_sessions, a, kept_ids,
+                                             control == KVM_CONTROL_WITHDRAWN_AVERAGE ? group_scores : nullptr,
+                                             (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_select_control launch");
+}
+
 static kvm_status view_call(kvm_ctx* ctx, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,
                             const int32_t* block_table, const int64_t* n_tok, int32_t n_sessions,
                             const int32_t* kept_ids, const uint16_t* q, uint16_t* k_view, uint16_t* v_view,

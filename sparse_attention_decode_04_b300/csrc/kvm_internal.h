@@ -69,6 +69,10 @@ cudaError_t launch_score_select(const Ctx& c, const uint16_t* q, int n_q, const 
                                 const SessionArgs& a, int32_t* kept, float* group_scores, float* head_scores,
                                 cudaStream_t st);
 
+// kvm_score.cu: the selection controls (recent-only; withdrawn head-averaged scoring)
+cudaError_t launch_select_control(const Ctx& c, int control, const uint16_t* q, const float* index, int n_sessions,
+                                  const SessionArgs& a, int32_t* kept, float* group_scores, cudaStream_t st);
+
 // kvm_step_score.cu: step-level scores of n_q > 1 query tokens (tcgen05) into gs_out [S][h_kv][max_blocks]
 cudaError_t launch_step_scores(const Ctx& c, const uint16_t* q, int n_q, const float* index, int n_sessions,
                                const SessionArgs& a, float* gs_out, cudaStream_t st);

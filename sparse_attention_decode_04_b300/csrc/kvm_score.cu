@@ -43,7 +43,9 @@ template <int D, int G>
 __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
     const uint16_t* __restrict__ q, const float* __restrict__ index, int64_t max_blocks, int h_kv, int h_q,
     SessionArgs a, int rows_per_tile, float* __restrict__ e_buf, float2* __restrict__ part, int64_t max_tiles,
-    float* __restrict__ head_scores, uint32_t* __restrict__ status) {
+    float* __restrict__ head_scores, uint32_t* __restrict__ status, int q_heads, int avg_group) {
+  // q_heads: query heads per session in q.  avg_group > 0 (with G == 1): the withdrawn scoring, one score row
+  // per KV head from the unweighted mean of its avg_group query heads (taken in fp32).
   constexpr int NV = D / 32;  // float4 chunks per lane per row
   extern __shared__ __align__(128) unsigned char smem_raw[];
   float* stage_buf = reinterpret_cast<float*>(smem_raw);                   // [kStages][32][D]
@@ -82,16 +84,34 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   // Query slice of this lane, scaled by 1/sqrt(d): dims 4*sub + 32*i + {0..3}.
   float qv[G][NV * 4];
   const float inv_sqrt_d = __frsqrt_rn((float)D);
+  if (G == 1 && avg_group > 0) {
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    const uint16_t* qh = q + ((int64_t)s * h_q + g * G + h) * D;
+    for (int j = 0; j < NV * 4; ++j) qv[0][j] = 0.f;
+    for (int h = 0; h < avg_group; ++h) {
+      const uint16_t* qh = q + ((int64_t)s * q_heads + g * avg_group + h) * D;
 #pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh + 4 * sub + 32 * i));
-      qv[h][4 * i + 0] = bf16lo(w.x) * inv_sqrt_d;
-      qv[h][4 * i + 1] = bf16hi(w.x) * inv_sqrt_d;
-      qv[h][4 * i + 2] = bf16lo(w.y) * inv_sqrt_d;
-      qv[h][4 * i + 3] = bf16hi(w.y) * inv_sqrt_d;
+      for (int i = 0; i < NV; ++i) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh + 4 * sub + 32 * i));
+        qv[0][4 * i + 0] += bf16lo(w.x);
+        qv[0][4 * i + 1] += bf16hi(w.x);
+        qv[0][4 * i + 2] += bf16lo(w.y);
+        qv[0][4 * i + 3] += bf16hi(w.y);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NV * 4; ++j) qv[0][j] = qv[0][j] / (float)avg_group * inv_sqrt_d;
+  } else {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const uint16_t* qh = q + ((int64_t)s * q_heads + g * G + h) * D;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh + 4 * sub + 32 * i));
+        qv[h][4 * i + 0] = bf16lo(w.x) * inv_sqrt_d;
+        qv[h][4 * i + 1] = bf16hi(w.x) * inv_sqrt_d;
+        qv[h][4 * i + 2] = bf16lo(w.y) * inv_sqrt_d;
+        qv[h][4 * i + 3] = bf16hi(w.y) * inv_sqrt_d;
+      }
     }
   }
   float run_max = -INFINITY;  // lane (sub == h) tracks head h over its rows
@@ -465,7 +485,8 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
 
 template <int G>
 cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, int rpt, int max_blk, int32_t* kept,
-                          float* group_scores, const float* gs_in, cudaStream_t st) {
+                          float* group_scores, const float* gs_in, cudaStream_t st, int part_heads = -1) {
+  if (part_heads < 0) part_heads = c.p.h_q;  // score rows per session in the tile partials
   int C = (max_blk + 4095) / 4096;
   C = C < 1 ? 1 : (C > 8 ? 8 : C);
   const int slice_cap = (max_blk + C - 1) / C;
@@ -475,8 +496,48 @@ cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, in
   cudaError_t e;
   if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
   return launch_pdl(kb, dim3(C, c.p.h_kv, n_sessions), dim3(kSelectThreads), smem_b, st, C, (const float*)c.e_buf,
-                    (const float2*)c.part, c.max_tiles, c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.p.n_sink,
+                    (const float2*)c.part, c.max_tiles, c.p.max_blocks, c.p.h_kv, part_heads, a, rpt, c.p.n_sink,
                     c.p.n_recent, c.p.top_k, c.budget, slice_cap, kept, group_scores, gs_in);
+}
+
+// Rows per score tile: one wave of two CTAs per SM over the call (a multiple of 32 rows, 32..4096).
+int rows_per_tile(const Ctx& c, int n_sessions, int max_blk) {
+  const int64_t units = (int64_t)c.p.h_kv * n_sessions;
+  const int64_t sms = c.num_sms > 0 ? c.num_sms : 1;
+  const int64_t tiles_per_head = (2 * sms + units - 1) / units;
+  int64_t rpt64 = (max_blk + tiles_per_head - 1) / tiles_per_head;
+  rpt64 = (rpt64 + kStageRows - 1) / kStageRows * kStageRows;
+  return (int)(rpt64 < kStageRows ? kStageRows : (rpt64 > 4096 ? 4096 : rpt64));
+}
+
+// The withdrawn scoring (a control): one softmax per KV head over the scores of the group's averaged query.
+template <int D>
+cudaError_t launch_withdrawn(const Ctx& c, const uint16_t* q, const float* index, int n_sessions, const SessionArgs& a,
+                             int32_t* kept, float* group_scores, cudaStream_t st) {
+  int max_blk = 0;
+  for (int s = 0; s < n_sessions; ++s) max_blk = max(max_blk, a.n_blk[s]);
+  if (max_blk == 0) return cudaMemsetAsync(kept, 0xFF, sizeof(int32_t) * (size_t)n_sessions * c.p.h_kv * c.budget, st);
+  const int rpt = rows_per_tile(c, n_sessions, max_blk);
+  const int tiles = (max_blk + rpt - 1) / rpt;
+  const size_t smem_a = (size_t)kStages * kStageRows * D * 4 + (size_t)rpt * 4;
+  auto ka = score_tile_kernel<D, 1>;
+  cudaError_t e = ensure_smem(ka, c.device, smem_a);
+  if (e != cudaSuccess) return e;
+  // partial rows are indexed per KV head here (h_kv score rows per session)
+  if ((e = launch_pdl(ka, dim3(tiles, c.p.h_kv, n_sessions), dim3(kScoreThreads), smem_a, st, 1, q, index,
+                      c.p.max_blocks, c.p.h_kv, c.p.h_kv, a, rpt, c.e_buf, c.part, c.max_tiles, (float*)nullptr,
+                      c.status, c.p.h_q, c.group)) != cudaSuccess)
+    return e;
+  return launch_select<1>(c, n_sessions, a, rpt, max_blk, kept, group_scores, nullptr, st, c.p.h_kv);
+}
+
+// The recent-only control: the last min(n_blk, budget) blocks, ascending, -1 padded.
+__global__ void recent_only_kernel(int32_t* __restrict__ kept, int h_kv, int budget, SessionArgs a) {
+  griddep_wait();
+  const int g = blockIdx.x, s = blockIdx.y;
+  const int n_keep = a.n_keep[s], n_blk = a.n_blk[s];
+  int32_t* row = kept + ((int64_t)s * h_kv + g) * budget;
+  for (int i = threadIdx.x; i < budget; i += blockDim.x) row[i] = i < n_keep ? n_blk - n_keep + i : -1;
 }
 
 template <int D, int G>
@@ -492,14 +553,8 @@ cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_
     // nothing to score: every kept list is empty
     return cudaMemsetAsync(kept, 0xFF, sizeof(int32_t) * (size_t)n_sessions * c.p.h_kv * c.budget, st);
   }
-  // rows per score tile: one wave of two CTAs per SM over the call (a multiple of 32 rows, 32..4096)
   (void)rows;
-  const int64_t units = (int64_t)c.p.h_kv * n_sessions;
-  const int64_t sms = c.num_sms > 0 ? c.num_sms : 1;
-  const int64_t tiles_per_head = (2 * sms + units - 1) / units;
-  int64_t rpt64 = (max_blk + tiles_per_head - 1) / tiles_per_head;
-  rpt64 = (rpt64 + kStageRows - 1) / kStageRows * kStageRows;
-  const int rpt = (int)(rpt64 < kStageRows ? kStageRows : (rpt64 > 4096 ? 4096 : rpt64));
+  const int rpt = rows_per_tile(c, n_sessions, max_blk);
   const int tiles = (max_blk + rpt - 1) / rpt;
   const size_t smem_a = (size_t)kStages * kStageRows * D * 4 + (size_t)rpt * G * 4;
   auto ka = score_tile_kernel<D, G>;
@@ -507,7 +562,7 @@ cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_
   if (e != cudaSuccess) return e;
   if ((e = launch_pdl(ka, dim3(tiles, c.p.h_kv, n_sessions), dim3(kScoreThreads), smem_a, st, 1, q, index,
                       c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.e_buf, c.part, c.max_tiles, head_scores,
-                      c.status)) != cudaSuccess)
+                      c.status, c.p.h_q, 0)) != cudaSuccess)
     return e;
 
   return launch_select<G>(c, n_sessions, a, rpt, max_blk, kept, group_scores, nullptr, st);
@@ -548,6 +603,14 @@ cudaError_t launch_select_given(const Ctx& c, const float* gs, int n_sessions, c
     case 8: return launch_select<8>(c, n_sessions, a, kStageRows, max_blk, kept, group_scores_out, gs, st);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_select_control(const Ctx& c, int control, const uint16_t* q, const float* index, int n_sessions,
+                                  const SessionArgs& a, int32_t* kept, float* group_scores, cudaStream_t st) {
+  if (control == KVM_CONTROL_RECENT_ONLY)
+    return launch_pdl(recent_only_kernel, dim3(c.p.h_kv, n_sessions), dim3(256), 0, st, 1, kept, c.p.h_kv, c.budget, a);
+  return c.p.d == 128 ? launch_withdrawn<128>(c, q, index, n_sessions, a, kept, group_scores, st)
+                      : launch_withdrawn<64>(c, q, index, n_sessions, a, kept, group_scores, st);
 }
 
 cudaError_t launch_score_select(const Ctx& c, const uint16_t* q, int n_q, const float* index, int n_sessions,
