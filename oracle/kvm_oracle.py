@@ -286,6 +286,34 @@ def decode_attention(q_bits, k_view_bits, v_view_bits, theta: float) -> np.ndarr
     return p @ v
 
 
+def step_view_attention(q_steps_bits, k_view_bits, v_view_bits, theta: float) -> np.ndarray:
+    """Attention of a step's T query tokens (the group's heads) over the view: [T][G][d].
+
+    [REVIEW] "Strengths" (recall scheduled once per agent step) and [README]
+    "Local reproduction" (the view replaces full attention).  READING: the
+    step's tokens are the history's last T tokens, so token t sits at view
+    position p_t = L - T + t (the recent blocks of the view hold them); its
+    query is rotated at p_t and attends the view slots j <= p_t (causal within
+    the step); softmax scale 1/sqrt(d).
+    """
+    q = bf16_to_f64(q_steps_bits)                 # [T][G][d]
+    T, g, d = q.shape
+    k = bf16_to_f64(k_view_bits)
+    v = bf16_to_f64(v_view_bits)
+    L = k.shape[0]
+    if L < T:
+        raise ValueError("the view must hold the step's tokens")
+    out = np.zeros((T, g, d))
+    for t in range(T):
+        pos = L - T + t
+        qr = rope(q[t], pos, theta)
+        s = qr @ k[:pos + 1].T / np.sqrt(d)
+        p = np.exp(s - s.max(axis=1, keepdims=True))
+        p /= p.sum(axis=1, keepdims=True)
+        out[t] = p @ v[:pos + 1]
+    return out
+
+
 # --------------------------------------------------------------------------- one layer
 def kvmem_layer(k_pool, v_pool, page_of, q_bits, n_tok: int, n_sink: int, n_recent: int, top_k: int,
                 theta: float, attend: bool = True, heads=None):

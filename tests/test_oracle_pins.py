@@ -290,3 +290,68 @@ def test_clean_variant_recovers_every_planted_block():
     # GQA geometry, 4 planted topics per KV head: signal <mu_b, sum mu> ~ 32 against cross-talk std ~ 5.7.
     w2 = synth.WORKLOADS["gqa40x8_256k"].with_(n_tok=32768, top_k=64, n_planted=4, eps_scale=0.1, q_noise_var=0.0)
     assert _recovered(w2) == [4] * 8
+
+
+# --------------------------------------------------------------------------- step attention over the view
+def test_step_attention_is_causal_within_the_step():
+    rng = np.random.default_rng(3)
+    T, G, d, L = 5, 2, 16, 40
+    q = rand_bf16((T, G, d))
+    k = rand_bf16((L, d))
+    v = rand_bf16((L, d))
+    out = O.step_view_attention(q, k, v, 1e4)
+    # slots after a token's own position never reach it; its own slot and earlier ones do
+    for t in range(T):
+        pos = L - T + t
+        v2 = v.copy()
+        v2[pos + 1:] = O.f64_to_bf16(rng.normal(size=(L - pos - 1, d)))
+        out2 = O.step_view_attention(q, k, v2, 1e4)
+        assert np.array_equal(out2[t], out[t])
+        v3 = v.copy()
+        v3[pos] = O.f64_to_bf16(rng.normal(size=d) + 3.0)
+        assert not np.allclose(O.step_view_attention(q, k, v3, 1e4)[t], out[t])
+
+
+def test_step_attention_positions_match_decode_attention_by_relative_distance():
+    """Token t of the step (query at view position p, keys at 0..p) and decode attention over slots 0..p
+    (query at p + 1) see the same relative distances once the keys are moved one position on (RoPE
+    composition).  The moved keys are re-rounded to bf16, hence the loose tolerance; an off-by-one in the
+    step's positions changes high-frequency logits by about a radian and fails it."""
+    T, G, d, L = 3, 2, 16, 24
+    q = rand_bf16((T, G, d))
+    k = rand_bf16((L, d))
+    v = rand_bf16((L, d))
+    out = O.step_view_attention(q, k, v, 1e4)
+    for t in range(T):
+        pos = L - T + t
+        moved = O.f64_to_bf16(O.rope(O.bf16_to_f64(k[:pos + 1]), np.ones(pos + 1), 1e4))
+        ref = O.decode_attention(q[t], moved, v[:pos + 1], 1e4)
+        assert np.allclose(out[t], ref, atol=2e-2)
+
+
+def test_step_attention_uniform_keys_average_the_causal_window():
+    T, G, d, L = 4, 3, 8, 12
+    q = rand_bf16((T, G, d))
+    k = np.zeros((L, d), dtype=np.uint16)                 # zero keys: every logit is 0
+    v = rand_bf16((L, d))
+    out = O.step_view_attention(q, k, v, 1e4)
+    vf = O.bf16_to_f64(v)
+    for t in range(T):
+        pos = L - T + t
+        assert np.allclose(out[t], np.broadcast_to(vf[:pos + 1].mean(axis=0), (G, d)), atol=1e-14)
+
+
+def test_step_attention_matches_library_softmax_hand_case():
+    # T = 2, L = 2, d = 2, theta irrelevant at position 0 for token 0 (RoPE at 0 is the identity)
+    q = O.f64_to_bf16([[[1.0, 0.0]], [[0.0, 2.0]]])      # [T][G=1][d]
+    k = O.f64_to_bf16([[2.0, 0.0], [0.0, 1.0]])
+    v = O.f64_to_bf16([[1.0, -1.0], [3.0, 5.0]])
+    out = O.step_view_attention(q, k, v, 1e4)
+    assert np.allclose(out[0, 0], [1.0, -1.0], atol=1e-15)   # token 0 sees slot 0 only
+    # token 1 at position 1: q rotated by angle 1 * theta^0 = 1 rad on the (0, 1) pair
+    c, s_ = np.cos(1.0), np.sin(1.0)
+    qr = np.array([0.0 * c - 2.0 * s_, 2.0 * c + 0.0 * s_])
+    logits = np.array([qr @ [2.0, 0.0], qr @ [0.0, 1.0]]) / np.sqrt(2.0)
+    w = np.exp(logits - logits.max())
+    w /= w.sum()
+    assert np.allclose(out[1, 0], w @ np.array([[1.0, -1.0], [3.0, 5.0]]), atol=1e-14)
