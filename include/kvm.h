@@ -17,6 +17,8 @@
  *   4. kvm_decode_attn    single-token attention over the view.
  *   kvm_materialize_attn  3 + 4 in one pass (the view is written once and never
  *                         re-read from HBM).
+ *   kvm_step_attn         attention of a whole step's query tokens over the
+ *                         view (tensor cores), after a multi-query selection.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -30,8 +32,8 @@
  *   synchronises the host except kvm_create, kvm_destroy and kvm_device_status.
  * - Block size is fixed: 32 tokens per block, one block per physical page.
  * - One context serves one device (the device current at kvm_create) and one
- *   head geometry.  kvm_score_select, kvm_materialize, kvm_decode_attn and
- *   kvm_materialize_attn on one context must not run concurrently on
+ *   head geometry.  kvm_score_select, kvm_materialize, kvm_decode_attn,
+ *   kvm_materialize_attn and kvm_step_attn on one context must not run concurrently on
  *   different streams: they share the context's scratch buffers.
  *   kvm_index_append uses no scratch (only the status word, which it updates
  *   atomically), so appends may run on another stream alongside them, e.g.
@@ -82,6 +84,7 @@ typedef enum {
 #define KVM_DEV_BAD_PAGE 0x1u    /* block_table entry outside [0, n_pages)          */
 #define KVM_DEV_BAD_BLOCK 0x2u   /* kept id outside [0, n_blk) or not ascending     */
 #define KVM_DEV_TIMEOUT 0x4u     /* a pipeline wait exceeded its iteration limit    */
+#define KVM_DEV_BAD_VIEW 0x8u    /* kvm_step_attn: view_len outside [n_q, 32*budget] */
 
 typedef struct kvm_ctx kvm_ctx; /* opaque */
 
@@ -95,7 +98,7 @@ typedef struct {
   float rope_theta;     /* RoPE base (rotate-half pairing, full head dimension)        */
   int64_t max_blocks;   /* block capacity per session (block-table row, index rows)    */
   int32_t max_sessions; /* sessions per call, 1..64                                    */
-  int32_t max_queries;  /* query tokens per session in one kvm_score_select, >= 1      */
+  int32_t max_queries;  /* query tokens per session in one kvm_score_select or kvm_step_attn, >= 1 */
 } kvm_params;
 
 /* Human-readable name of a status code (static storage). */
@@ -211,6 +214,29 @@ kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint
                                 int32_t n_sessions, const int32_t* kept_ids, const uint16_t* q,
                                 uint16_t* k_view, uint16_t* v_view, int32_t* view_len, float* out,
                                 void* stream);
+
+/*
+ * Attention of a step's n_q query tokens over the view, on the tensor cores.
+ * Evolve review of KVMem, "Strengths" (recall once per agent step) and KVMEM
+ * reproduction README, "Local reproduction" (the view replaces full
+ * attention).  The step's tokens are the history's last n_q tokens, so they
+ * sit in the view's last slots: token t is at view position
+ * p_t = L - n_q + t (L = view_len[s][g]) and attends the slots j <= p_t:
+ *   out[s][t][h] = sum_{j<=p_t} softmax_j(<RoPE(q[s][t][h], p_t), k_view[g][j]>/sqrt(d)) v_view[g][j]
+ * Products are fp32-accurate (each bf16 MMA operand that is not already bf16
+ * -- the rotated query and the probabilities -- is split into a bf16 part
+ * and its bf16 residual); accumulation is fp32.
+ *   q          [n_sessions][n_q][h_q][d] bf16, post-q-norm, pre-RoPE
+ *   k_view, v_view, view_len as written by kvm_materialize
+ *   out        [n_sessions][n_q][h_q][d] fp32 (16-byte aligned)
+ * Needs a context created with max_queries > 1 (it owns the packed operand
+ * scratch) and 1 <= n_q <= max_queries, n_q <= 32*budget (KVM_ERR_SHAPE
+ * otherwise).  A view_len outside [n_q, 32*budget] sets KVM_DEV_BAD_VIEW;
+ * that head's outputs are then undefined.
+ */
+kvm_status kvm_step_attn(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const uint16_t* k_view,
+                         const uint16_t* v_view, const int32_t* view_len, int32_t n_sessions, float* out,
+                         void* stream);
 
 /*
  * Selection controls (the comparisons the pages report next to the method).

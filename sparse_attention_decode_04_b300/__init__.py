@@ -21,7 +21,7 @@ BLOCK = 32
 KVM_OK = 0
 STATUS_NAMES = {0: "KVM_OK", 1: "KVM_ERR_INVALID_ARG", 2: "KVM_ERR_SHAPE", 3: "KVM_ERR_BUDGET", 4: "KVM_ERR_CUDA",
                 5: "KVM_ERR_TIMEOUT", 6: "KVM_ERR_DEVICE"}
-DEV_BAD_PAGE, DEV_BAD_BLOCK, DEV_TIMEOUT = 0x1, 0x2, 0x4
+DEV_BAD_PAGE, DEV_BAD_BLOCK, DEV_TIMEOUT, DEV_BAD_VIEW = 0x1, 0x2, 0x4, 0x8
 CONTROL_RECENT_ONLY, CONTROL_WITHDRAWN_AVERAGE = 1, 2
 
 
@@ -64,8 +64,10 @@ def lib() -> ctypes.CDLL:
         L.kvm_materialize_attn.argtypes = [P, P, P, i64, P, P, i32, P, P, P, P, P, P, P]
         L.kvm_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
         L.kvm_select_control.argtypes = [P, i32, P, P, P, i32, P, P, P]
+        L.kvm_step_attn.argtypes = [P, P, i32, P, P, P, i32, P, P]
         for name in ("kvm_create", "kvm_destroy", "kvm_index_append", "kvm_score_select", "kvm_materialize",
-                     "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status", "kvm_select_control"):
+                     "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status", "kvm_select_control",
+                     "kvm_step_attn"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -173,6 +175,12 @@ def kvm_materialize_attn(ctx: Context, k_pool, v_pool, n_pages: int, block_table
     _check(lib().kvm_materialize_attn(ctx.handle, _ptr(k_pool), _ptr(v_pool), int(n_pages), _ptr(block_table),
                                       _i64(n_tok), n, _ptr(kept_ids), _ptr(q), _ptr(k_view), _ptr(v_view),
                                       _ptr(view_len), _ptr(out), _stream(stream)))
+
+
+def kvm_step_attn(ctx: Context, q, n_q: int, k_view, v_view, view_len, n_sessions: int, out, stream=None):
+    """Attention of a step's n_q query tokens (the history's last n_q tokens) over the view."""
+    _check(lib().kvm_step_attn(ctx.handle, _ptr(q), int(n_q), _ptr(k_view), _ptr(v_view), _ptr(view_len),
+                               int(n_sessions), _ptr(out), _stream(stream)))
 
 
 def kvm_device_status(ctx: Context, clear: bool = True, stream=None) -> int:

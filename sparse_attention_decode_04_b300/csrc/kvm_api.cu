@@ -180,16 +180,25 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
     c.step_blk_cap_pad = (p->max_blocks + 255) / 256 * 256;
     c.step_rows_cap_pad = (int)(((int64_t)p->max_queries * c.group + 255) / 256 * 256);
     const size_t SG = S * p->h_kv;
-    const size_t sz[5] = {SG * c.step_blk_cap_pad * p->d * 2, SG * c.step_rows_cap_pad * p->d * 2,
+    c.attn_l_pad = ((int64_t)kvm::kBlock * c.budget + 63) / 64 * 64;
+    const size_t sz[8] = {SG * c.step_blk_cap_pad * p->d * 2,
+                          SG * c.step_rows_cap_pad * p->d * 2,
                           SG * kvm::kStepMaxRanges * c.step_rows_cap_pad * sizeof(float2),
-                          SG * c.step_rows_cap_pad * sizeof(float2), SG * p->max_blocks * sizeof(float)};
-    void* q5[5] = {};
-    for (int i = 0; i < 5 && e == cudaSuccess; ++i) e = cudaMalloc(&q5[i], sz[i]);
+                          SG * c.step_rows_cap_pad * sizeof(float2),
+                          SG * p->max_blocks * sizeof(float),
+                          2 * SG * c.step_rows_cap_pad * p->d * 2,
+                          SG * c.attn_l_pad * p->d * 2,
+                          SG * c.attn_l_pad * p->d * 2};
+    void* q5[8] = {};
+    for (int i = 0; i < 8 && e == cudaSuccess; ++i) e = cudaMalloc(&q5[i], sz[i]);
     c.step_kpk = (uint16_t*)q5[0];
     c.step_qpk = (uint16_t*)q5[1];
     c.step_part = (float2*)q5[2];
     c.step_stats = (float2*)q5[3];
     c.step_gs = (float*)q5[4];
+    c.attn_q = (uint16_t*)q5[5];
+    c.attn_kpk = (uint16_t*)q5[6];
+    c.attn_vtpk = (uint16_t*)q5[7];
     for (size_t b : sz) c.bytes += b;
     if (e != cudaSuccess) {
       kvm_destroy(ctx);
@@ -215,8 +224,9 @@ kvm_status kvm_destroy(kvm_ctx* ctx) {
   cudaGetDevice(&prev);
   if (prev != c.device) cudaSetDevice(c.device);
   cudaError_t e = cudaDeviceSynchronize();
-  void* ptrs[14] = {c.e_buf,      c.part,       c.rec,      c.rope_base, c.rope_off,   c.status,  c.rope_base_lo,
-                    c.rope_off_lo, c.step_kpk,   c.step_qpk, c.step_part, c.step_stats, c.step_gs, c.seg_count};
+  void* ptrs[17] = {c.e_buf,      c.part,       c.rec,      c.rope_base, c.rope_off,   c.status,  c.rope_base_lo,
+                    c.rope_off_lo, c.step_kpk,   c.step_qpk, c.step_part, c.step_stats, c.step_gs, c.seg_count,
+                    c.attn_q,      c.attn_kpk,   c.attn_vtpk};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   if (prev >= 0 && prev != c.device) cudaSetDevice(prev);
@@ -369,6 +379,27 @@ kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint
                    view_len, out, stream);
 }
 
+kvm_status kvm_step_attn(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const uint16_t* k_view,
+                         const uint16_t* v_view, const int32_t* view_len, int32_t n_sessions, float* out,
+                         void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_sessions == 0) return KVM_OK;
+  if (!q || !k_view || !v_view || !view_len || !out)
+    return fail(KVM_ERR_INVALID_ARG, "kvm_step_attn: NULL pointer argument");
+  if (n_q < 1 || n_q > c.p.max_queries)
+    return fail(KVM_ERR_SHAPE, "n_q=%d outside [1, max_queries=%d]", n_q, c.p.max_queries);
+  if (!c.attn_kpk) return fail(KVM_ERR_SHAPE, "kvm_step_attn needs a context created with max_queries > 1");
+  if ((int64_t)n_q > (int64_t)kvm::kBlock * c.budget)
+    return fail(KVM_ERR_SHAPE, "n_q=%d exceeds the view capacity %d", n_q, kvm::kBlock * c.budget);
+  if (!aligned(q, 16) || !aligned(k_view, 16) || !aligned(v_view, 16) || !aligned(out, 16) || !aligned(view_len, 4))
+    return fail(KVM_ERR_INVALID_ARG, "q, k_view, v_view and out must be 16-byte aligned");
+  cudaError_t e = kvm::launch_step_attn(c, q, n_q, k_view, v_view, view_len, n_sessions, out, (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_step_attn launch");
+}
+
 kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* stream) {
   kvm_status s = check_ctx(ctx);
   if (s != KVM_OK) return s;
@@ -382,7 +413,7 @@ kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* s
   if (e != cudaSuccess) return cuda_fail(e, "kvm_device_status");
   if (*out == 0) return KVM_OK;
   if (*out & KVM_DEV_TIMEOUT) return fail(KVM_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", *out);
-  return fail(KVM_ERR_DEVICE, "device status 0x%x (bad page / block id)", *out);
+  return fail(KVM_ERR_DEVICE, "device status 0x%x (bad page, block id or view length)", *out);
 }
 
 }  // extern "C"

@@ -71,6 +71,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
+// mbar_wait by all 32 lanes of a warp with one verdict for the warp: lanes that go on to warp-collective
+// instructions (tcgen05.ld, shuffles) must not split when a wait gives up just as the phase completes.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
+}
+
 // 1-D bulk copy global -> this CTA's shared memory, completing on `bar`.
 // dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

@@ -55,6 +55,11 @@ struct Ctx {
   float2* step_part = nullptr;   // row (max, sum) per column range [S*h_kv][kStepMaxRanges][rows]
   float2* step_stats = nullptr;  // row (max, 1/sum) [S*h_kv][rows]
   float* step_gs = nullptr;      // group scores when the caller does not ask for them [S][h_kv][max_blocks]
+  // step attention over the view (multi-query), allocated when max_queries > 1
+  int64_t attn_l_pad = 0;         // 32 * budget rounded up to 64 (view tokens per packed head)
+  uint16_t* attn_q = nullptr;     // rotated, scaled query rows, bf16 part then residual: [2][S*h_kv][rows][d]
+  uint16_t* attn_kpk = nullptr;   // view keys, core-matrix order [S*h_kv][attn_l_pad][d]
+  uint16_t* attn_vtpk = nullptr;  // view values transposed per 64-token tile [S*h_kv][attn_l_pad / 64][d][64]
 };
 
 constexpr int kStepMaxRanges = 64;
@@ -79,6 +84,10 @@ cudaError_t launch_step_scores(const Ctx& c, const uint16_t* q, int n_q, const f
 // kvm_score.cu: the cluster top-k on given group scores
 cudaError_t launch_select_given(const Ctx& c, const float* gs, int n_sessions, const SessionArgs& a, int32_t* kept,
                                 float* group_scores_out, cudaStream_t st);
+
+// kvm_step_attn.cu: attention of n_q step tokens over the view (tcgen05); out [S][n_q][h_q][d] fp32
+cudaError_t launch_step_attn(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* k_view, const uint16_t* v_view,
+                             const int32_t* view_len, int n_sessions, float* out, cudaStream_t st);
 
 // kvm_view.cu — mode: 0 materialise, 1 attend over a view, 2 fused
 cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,

@@ -1,0 +1,408 @@
+// Attention of a step's query tokens over the execution view, on the
+// 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Evolve review of KVMem, "Strengths": recall is scheduled once per agent
+// step; KVMEM reproduction README, "Local reproduction": the view replaces
+// full attention.  The step's T tokens are the history's last T tokens, so
+// token t sits at view position p_t = L - T + t (the view's recent blocks hold
+// it); its query, rotated at p_t, attends the view slots j <= p_t.  Per KV
+// head g the R = T*G query rows (row r = t*G + hh) form a dense
+// R x L x d contraction twice (scores, then P.V):
+//   pack    queries rotated at p_t and scaled by log2(e)/sqrt(d), split into a
+//           bf16 part and its bf16 residual; K and V^T of the view re-laid out
+//           in the no-swizzle K-major core-matrix layout (8 rows x 16 bytes per
+//           core matrix), so every operand tile is one contiguous bulk copy;
+//   attend  per 128 query rows, over 64-token tiles of the view:
+//             S  = Q_hi K^T + Q_lo K^T          (one fp32 TMEM accumulator)
+//             P  = exp2(S - m) per row          (online softmax in registers)
+//             O += P_hi V + P_lo V              (fp32 TMEM accumulator)
+//           with the split operands giving fp32-accurate products on bf16 MMAs.
+// Warp roles: warp 0 issues the bulk copies, warp 1 owns TMEM and issues the
+// MMAs (S of the next tile is issued before P.V of this one, into a second S
+// buffer), warps 2..5 own one query row per thread (each warp can only read
+// its quarter of the 128 TMEM lanes): they read S, keep the running maximum
+// (raised only when it grows by more than 8, then O is rescaled in TMEM),
+// write P to shared memory and finally O / l to the output.
+// Every mbarrier wait is bounded.
+#include "kvm_device.cuh"
+#include "kvm_internal.h"
+
+namespace kvm {
+namespace {
+
+constexpr int kThreads = 192;  // 6 warps
+constexpr int kRows = 128;     // query rows per CTA (MMA M)
+constexpr int kTile = 64;      // view tokens per tile (S: N = 64; P.V: K = 64)
+constexpr uint32_t kTmemCols = 256;  // S[2] x 64 columns + O 128 columns
+
+// Element (r, c) of a [rows][cols] bf16 matrix in the K-major core-matrix layout (cols = K).
+__device__ __forceinline__ int64_t cm_index(int64_t r, int c, int cols) {
+  return ((r >> 3) * (cols >> 3) + (c >> 3)) * 64 + (r & 7) * 8 + (c & 7);
+}
+
+// The view length the kernels work with: a length outside [n_q, Lcap] is reported by the query packing and
+// clamped into that range, so every access stays inside the view buffers.
+__device__ __forceinline__ int clamp_view_len(int L, int n_q, int Lcap) { return L < n_q ? n_q : (L > Lcap ? Lcap : L); }
+
+// Query rows of KV head (s, g): rotated at p_t, scaled, split -> hi / lo packed [rows_pad][D].
+template <int D>
+__global__ void step_pack_q_kernel(const uint16_t* __restrict__ q, const int32_t* __restrict__ view_len, int n_q,
+                                   int h_q, int h_kv, int group, int rows_pad, int Lcap,
+                                   const float2* __restrict__ rope_base, const float2* __restrict__ rope_off,
+                                   float q_scale, uint16_t* __restrict__ q_hi, uint16_t* __restrict__ q_lo,
+                                   uint32_t* __restrict__ status) {
+  griddep_wait();
+  const int sg = blockIdx.y, s = sg / h_kv, g = sg % h_kv;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;  // (row, pair i < D/2)
+  if (idx >= rows_pad * (D / 2)) return;
+  const int row = idx / (D / 2), i = idx % (D / 2);
+  float y1 = 0.f, y2 = 0.f;
+  if (row < n_q * group) {
+    const int L0 = view_len[sg];
+    if ((L0 < n_q || L0 > Lcap) && i == 0) atomicOr(status, KVM_DEV_BAD_VIEW);
+    const int L = clamp_view_len(L0, n_q, Lcap);
+    const int t = row / group, hh = row % group;
+    const int pos = L - n_q + t;
+    const uint16_t* qh = q + (((int64_t)s * n_q + t) * h_q + g * group + hh) * D;
+    const float x1 = __uint_as_float((uint32_t)qh[i] << 16), x2 = __uint_as_float((uint32_t)qh[i + D / 2] << 16);
+    const float2 b = rope_base[(int64_t)(pos >> 5) * (D / 2) + i], o = rope_off[(pos & 31) * (D / 2) + i];
+    const float cs = fmaf(b.x, o.x, -b.y * o.y), sn = fmaf(b.y, o.x, b.x * o.y);
+    y1 = (x1 * cs - x2 * sn) * q_scale;
+    y2 = (x2 * cs + x1 * sn) * q_scale;
+  }
+  const uint32_t h = pack_bf16x2(y1, y2);
+  const uint32_t l = pack_bf16x2(y1 - bf16lo(h), y2 - bf16hi(h));
+  uint16_t* dh = q_hi + (int64_t)sg * rows_pad * D;
+  uint16_t* dl = q_lo + (int64_t)sg * rows_pad * D;
+  dh[cm_index(row, i, D)] = (uint16_t)(h & 0xFFFFu);
+  dh[cm_index(row, i + D / 2, D)] = (uint16_t)(h >> 16);
+  dl[cm_index(row, i, D)] = (uint16_t)(l & 0xFFFFu);
+  dl[cm_index(row, i + D / 2, D)] = (uint16_t)(l >> 16);
+}
+
+// One 64-token tile of the view of KV head (s, g): K packed [tokens][D], V^T packed [D][tokens]; tokens past
+// the view length are zero (their probabilities are zero, and zero values keep P.V finite).
+template <int D>
+__global__ void __launch_bounds__(256) step_pack_kv_kernel(const uint16_t* __restrict__ k_view,
+                                                           const uint16_t* __restrict__ v_view,
+                                                           const int32_t* __restrict__ view_len, int n_q, int Lcap,
+                                                           int64_t l_pad, uint16_t* __restrict__ k_pk,
+                                                           uint16_t* __restrict__ vt_pk) {
+  griddep_wait();
+  __shared__ __align__(16) uint16_t vs[kTile][D];
+  const int sg = blockIdx.y, tile = blockIdx.x;
+  const int L = clamp_view_len(view_len[sg], n_q, Lcap);
+  const int tok0 = tile * kTile;
+  if (tok0 >= L) return;  // never read by the attention kernel
+  const uint16_t* ksrc = k_view + (int64_t)sg * Lcap * D;
+  const uint16_t* vsrc = v_view + (int64_t)sg * Lcap * D;
+  uint16_t* kdst = k_pk + ((int64_t)sg * l_pad + tok0) * D;
+  uint16_t* vdst = vt_pk + ((int64_t)sg * (l_pad / kTile) + tile) * kTile * D;
+  // 16-byte chunks in packed order (8 token rows of one core matrix are consecutive), so the writes are contiguous
+  for (int c = threadIdx.x; c < kTile * (D / 8); c += blockDim.x) {
+    const int rr = c & 7, c8 = (c >> 3) % (D / 8), r = (c / D) * 8 + rr;
+    const int tok = tok0 + r;
+    uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
+    if (tok < L) {
+      kw = __ldg(reinterpret_cast<const uint4*>(ksrc + (int64_t)tok * D + 8 * c8));
+      vw = __ldg(reinterpret_cast<const uint4*>(vsrc + (int64_t)tok * D + 8 * c8));
+    }
+    *reinterpret_cast<uint4*>(kdst + (int64_t)c * 8) = kw;
+    *reinterpret_cast<uint4*>(&vs[r][8 * c8]) = vw;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x; c < D * (kTile / 8); c += blockDim.x) {  // 16-byte chunks (dim, 8 tokens), dim fastest
+    const int dd = c % D, t8 = c / D;
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      w[u] = (uint32_t)vs[8 * t8 + 2 * u][dd] | ((uint32_t)vs[8 * t8 + 2 * u + 1][dd] << 16);
+    *reinterpret_cast<uint4*>(vdst + cm_index(dd, 8 * t8, kTile)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+struct AttnBars {
+  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, drain;
+};
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
+               ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// grid (rows_pad / 128, 1, S * h_kv)
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
+    const uint16_t* __restrict__ q_hi, const uint16_t* __restrict__ q_lo, const uint16_t* __restrict__ k_pk,
+    const uint16_t* __restrict__ vt_pk, const int32_t* __restrict__ view_len, int n_q, int rows_pad, int Lcap,
+    int64_t l_pad, int h_kv, int h_q, float* __restrict__ out, uint32_t* __restrict__ status) {
+  constexpr uint32_t Q_BYTES = kRows * D * 2, KV_BYTES = kTile * D * 2, P_BYTES = kRows * kTile * 2;
+  constexpr uint32_t SBO_Q = D / 8 * 128, SBO_P = kTile / 8 * 128, LBO = 128;
+  constexpr uint32_t IDESC_S = idesc_bf16_f32(kRows, kTile), IDESC_O = idesc_bf16_f32(kRows, D);
+  extern __shared__ __align__(1024) unsigned char smem[];
+  unsigned char* qh_s = smem;
+  unsigned char* ql_s = qh_s + Q_BYTES;
+  unsigned char* k_s = ql_s + Q_BYTES;      // [2] tiles
+  unsigned char* v_s = k_s + 2 * KV_BYTES;  // [2] tiles (V^T)
+  unsigned char* ph_s = v_s + 2 * KV_BYTES;
+  unsigned char* pl_s = ph_s + P_BYTES;
+  __shared__ AttnBars bars;
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int abort_flag;
+
+  griddep_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int sg = blockIdx.z, s = sg / h_kv, g = sg % h_kv;
+  const int row0 = blockIdx.x * kRows;
+  const int L = clamp_view_len(view_len[sg], n_q, Lcap);
+  // tiles up to the last view position any row of this CTA attends (the step's token rows are ordered by t)
+  const int last_row = min(n_q * G, row0 + kRows) - 1;
+  const int nt = (L - n_q + last_row / G + kTile) / kTile;
+
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    abort_flag = 0;
+    mbar_init(&bars.q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.kv_full[i], 1);
+      mbar_init(&bars.kv_empty[i], 1);
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_free[i], 4);
+    }
+    mbar_init(&bars.p_full, 4);
+    mbar_init(&bars.pv_done, 1);
+    mbar_init(&bars.drain, 1);
+    mbar_fence_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const uint32_t tm_o = tmem + 2 * kTile;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    mbar_arrive_expect_tx(&bars.q_full, 2 * Q_BYTES);
+    bulk_g2s(qh_s, q_hi + ((int64_t)sg * rows_pad + row0) * D, Q_BYTES, &bars.q_full);
+    bulk_g2s(ql_s, q_lo + ((int64_t)sg * rows_pad + row0) * D, Q_BYTES, &bars.q_full);
+    int j = 0;
+    for (; j < nt && !abort_flag; ++j) {
+      const int st = j & 1;
+      if (j >= 2 && !mbar_wait(&bars.kv_empty[st], ((j >> 1) - 1) & 1, status)) {
+        abort_flag = 1;
+        break;
+      }
+      mbar_arrive_expect_tx(&bars.kv_full[st], 2 * KV_BYTES);
+      bulk_g2s(k_s + st * KV_BYTES, k_pk + ((int64_t)sg * l_pad + (int64_t)j * kTile) * D, KV_BYTES, &bars.kv_full[st]);
+      bulk_g2s(v_s + st * KV_BYTES, vt_pk + ((int64_t)sg * (l_pad / kTile) + j) * kTile * D, KV_BYTES,
+               &bars.kv_full[st]);
+    }
+    // copies in flight must land before the CTA can exit
+    mbar_wait(&bars.q_full, 0, status);
+    for (int i = max(0, j - 2); i < j; ++i) mbar_wait(&bars.kv_full[i & 1], (i >> 1) & 1, status);
+  } else if (warp == 1 && lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t qh_a = smem_addr(qh_s), ql_a = smem_addr(ql_s), ph_a = smem_addr(ph_s), pl_a = smem_addr(pl_s);
+    auto issue_s = [&](int j) -> bool {
+      const int st = j & 1;
+      if (!mbar_wait(&bars.kv_full[st], (j >> 1) & 1, status)) return false;
+      if (j >= 2 && !mbar_wait(&bars.s_free[st], ((j >> 1) - 1) & 1, status)) return false;
+      tc_fence_after();
+      const uint32_t k_a = smem_addr(k_s + st * KV_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16(tmem + st * kTile, smem_desc(qh_a + kk * 256, LBO, SBO_Q), smem_desc(k_a + kk * 256, LBO, SBO_Q),
+                 IDESC_S, kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_bf16(tmem + st * kTile, smem_desc(ql_a + kk * 256, LBO, SBO_Q), smem_desc(k_a + kk * 256, LBO, SBO_Q),
+                 IDESC_S, 1);
+      mma_commit(&bars.s_full[st]);
+      return true;
+    };
+    bool ok = mbar_wait(&bars.q_full, 0, status) && (nt == 0 || issue_s(0));
+    int j = 0;
+    for (; ok && j < nt && !abort_flag; ++j) {
+      const int st = j & 1;
+      if (j + 1 < nt && !issue_s(j + 1)) {
+        ok = false;
+        break;
+      }
+      if (!mbar_wait(&bars.p_full, j & 1, status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t v_a = smem_addr(v_s + st * KV_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_bf16(tm_o, smem_desc(ph_a + kk * 256, LBO, SBO_P), smem_desc(v_a + kk * 256, LBO, SBO_P), IDESC_O,
+                 (j > 0 || kk > 0));
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        mma_bf16(tm_o, smem_desc(pl_a + kk * 256, LBO, SBO_P), smem_desc(v_a + kk * 256, LBO, SBO_P), IDESC_O, 1);
+      mma_commit(&bars.pv_done);
+      mma_commit(&bars.kv_empty[st]);
+    }
+    if (!ok) abort_flag = 1;
+    // every issued MMA has completed before TMEM is released
+    mma_commit(&bars.drain);
+    mbar_wait(&bars.drain, 0, status);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ softmax / epilogue, one query row per thread
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
+    const int row = row0 + r;
+    const bool valid_row = row < n_q * G;
+    const int t = row / G, hh = row % G;
+    const int pos = L - n_q + t;  // this row's view position; it attends slots <= pos
+    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int st = j & 1;
+      if (__any_sync(0xffffffffu, abort_flag) || !mbar_wait_warp(&bars.s_full[st], (j >> 1) & 1, status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[2][32];
+      tmem_ld32(tmem + lane_base + st * kTile, sv[0]);
+      tmem_ld32(tmem + lane_base + st * kTile + 32, sv[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.s_free[st]);
+      float x[kTile], mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kTile; ++c) {
+        const int tok = j * kTile + c;
+        x[c] = (valid_row && tok <= pos) ? __uint_as_float(sv[c >> 5][c & 31]) : -INFINITY;
+        mt = fmaxf(mt, x[c]);
+      }
+      // raise the reference only when it grows by more than 8 (a factor 256): O is then rescaled in TMEM
+      const float m_new = (mt > m + 8.f) ? mt : m;
+      const float corr = m_new == m ? 1.f : fast_exp2(m - m_new);  // 0 while m was -inf
+      if (j > 0 && !mbar_wait_warp(&bars.pv_done, (j - 1) & 1, status)) {  // P buffer free, O quiescent
+        ok = false;
+        break;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+        tc_fence_after();
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t ov[32];
+          tmem_ld32(tm_o + lane_base + cc * 32, ov);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
+          tmem_st32(tm_o + lane_base + cc * 32, ov);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      l *= corr;
+      m = m_new;
+      // P = exp2(S - m), split into bf16 + residual, written in the core-matrix layout (rows x 64 tokens)
+#pragma unroll
+      for (int c8 = 0; c8 < kTile / 8; ++c8) {
+        uint32_t wh[4], wl[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float p0 = x[8 * c8 + 2 * u] == -INFINITY ? 0.f : fast_exp2(x[8 * c8 + 2 * u] - m);
+          const float p1 = x[8 * c8 + 2 * u + 1] == -INFINITY ? 0.f : fast_exp2(x[8 * c8 + 2 * u + 1] - m);
+          l += p0 + p1;
+          wh[u] = pack_bf16x2(p0, p1);
+          wl[u] = pack_bf16x2(p0 - bf16lo(wh[u]), p1 - bf16hi(wh[u]));
+        }
+        const int64_t e = cm_index(r, 8 * c8, kTile) * 2;
+        *reinterpret_cast<uint4*>(ph_s + e) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4*>(pl_s + e) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.p_full);
+    }
+    if (!ok) abort_flag = 1;
+    if (ok && nt > 0 && mbar_wait_warp(&bars.pv_done, (nt - 1) & 1, status)) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* dst = out + (((int64_t)s * n_q + t) * h_q + g * G + hh) * D;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t ov[32];
+        tmem_ld32(tm_o + lane_base + cc * 32, ov);
+        tmem_wait_ld();
+        if (valid_row) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(dst + cc * 32 + i) =
+                make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
+                            __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, int G>
+cudaError_t launch_dg(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* k_view, const uint16_t* v_view,
+                      const int32_t* view_len, int n_sessions, float* out, cudaStream_t st) {
+  const int SG = n_sessions * c.p.h_kv;
+  const int rows_pad = (n_q * G + kRows - 1) / kRows * kRows;  // query rows per KV head, padded to the CTA tile
+  const int Lcap = 32 * c.budget;
+  const int64_t l_pad = c.attn_l_pad;
+  cudaError_t e;
+  const int nqp = rows_pad * (D / 2);
+  if ((e = launch_pdl(step_pack_q_kernel<D>, dim3((nqp + 255) / 256, SG), dim3(256), 0, st, 1, q, view_len, n_q,
+                      c.p.h_q, c.p.h_kv, G, rows_pad, Lcap, reinterpret_cast<const float2*>(c.rope_base),
+                      reinterpret_cast<const float2*>(c.rope_off), (float)(1.4426950408889634 / sqrt((double)D)),
+                      c.attn_q, c.attn_q + (int64_t)SG * rows_pad * D, c.status)) != cudaSuccess)
+    return e;
+  if ((e = launch_pdl(step_pack_kv_kernel<D>, dim3((unsigned)(l_pad / kTile), SG), dim3(256), 0, st, 1, k_view, v_view,
+                      view_len, n_q, Lcap, l_pad, c.attn_kpk, c.attn_vtpk)) != cudaSuccess)
+    return e;
+  const size_t smem = 2 * (size_t)kRows * D * 2 + 4 * (size_t)kTile * D * 2 + 2 * (size_t)kRows * kTile * 2 + 1024;
+  auto ka = step_attn_kernel<D, G>;
+  if ((e = ensure_smem(ka, c.device, smem)) != cudaSuccess) return e;
+  return launch_pdl(ka, dim3(rows_pad / kRows, 1, SG), dim3(kThreads), smem, st, 1, (const uint16_t*)c.attn_q,
+                    (const uint16_t*)(c.attn_q + (int64_t)SG * rows_pad * D), (const uint16_t*)c.attn_kpk, (const uint16_t*)c.attn_vtpk, view_len,
+                    n_q, rows_pad, Lcap, l_pad, c.p.h_kv, c.p.h_q, out, c.status);
+}
+
+template <int D>
+cudaError_t launch_d(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* k_view, const uint16_t* v_view,
+                     const int32_t* view_len, int n_sessions, float* out, cudaStream_t st) {
+  switch (c.group) {
+    case 1: return launch_dg<D, 1>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+    case 2: return launch_dg<D, 2>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+    case 3: return launch_dg<D, 3>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+    case 4: return launch_dg<D, 4>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+    case 5: return launch_dg<D, 5>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+    case 6: return launch_dg<D, 6>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+    case 7: return launch_dg<D, 7>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+    case 8: return launch_dg<D, 8>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_step_attn(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* k_view, const uint16_t* v_view,
+                             const int32_t* view_len, int n_sessions, float* out, cudaStream_t st) {
+  return c.p.d == 128 ? launch_d<128>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st)
+                      : launch_d<64>(c, q, n_q, k_view, v_view, view_len, n_sessions, out, st);
+}
+
+}  // namespace kvm

@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
     float m = -INFINITY, z = 0.f;
     for (int j = 0; j < nt; ++j) {
       const int st = j & 1;
-      if (abort_flag || !mbar_wait(&bars.d_full[st], (j >> 1) & 1, status)) {
+      if (__any_sync(0xffffffffu, abort_flag) || !mbar_wait_warp(&bars.d_full[st], (j >> 1) & 1, status)) {
         abort_flag = 1;
         break;
       }
@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
     float acc = 0.f;
     for (int j = 0; j < nchunk; ++j) {
       const int st = j & 1;
-      if (abort_flag || !mbar_wait(&bars.d_full[st], (j >> 1) & 1, status)) {
+      if (__any_sync(0xffffffffu, abort_flag) || !mbar_wait_warp(&bars.d_full[st], (j >> 1) & 1, status)) {
         abort_flag = 1;
         break;
       }

@@ -28,7 +28,8 @@ def declared_functions():
 def test_every_declared_symbol_is_exported(lib):
     names = declared_functions()
     assert {"kvm_create", "kvm_destroy", "kvm_index_append", "kvm_score_select", "kvm_materialize",
-            "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status"} <= set(names)
+            "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status", "kvm_step_attn",
+            "kvm_select_control"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} is declared in kvm.h but not exported"
 
@@ -66,6 +67,7 @@ def test_calls_reject_null_context(lib):
     assert lib.kvm_materialize(None, None, None, 1, None, n, 1, None, None, None, None, None) == 1
     assert lib.kvm_decode_attn(None, None, None, None, None, 1, None, None) == 1
     assert lib.kvm_materialize_attn(None, None, None, 1, None, n, 1, None, None, None, None, None, None, None) == 1
+    assert lib.kvm_step_attn(None, None, 4, None, None, None, 1, None, None) == 1
     out = ctypes.c_uint32(0)
     assert lib.kvm_device_status(None, ctypes.byref(out), 0, None) == 1
     assert lib.kvm_destroy(None) == 0
