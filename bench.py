@@ -39,6 +39,8 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "select+materialize+attend step µs and HBM GB/s at 1M-token history, per layer"
+STEP_METRIC = ("step-level select+materialize+attend µs per layer: 256 query tokens scored together over a "
+               "1M-token history, then their causal attention over the 65,536-token view")
 BLOCK = 32
 
 
@@ -151,6 +153,19 @@ def _oracle_child(name: str, reps: int, warmup: int):
     qg = q[G * g:G * (g + 1)]
     times, n_keep = [], 0
     static_idx = None if w.append_tok else O.mean_k_index(keys)  # no append: the index is state, as on the GPU
+    if w.n_q > 1:  # a step of n_q query tokens: step scores, select, materialise, step attention
+        qs = synth.queries(w, 0)[0][:, G * g:G * (g + 1)]
+        for i in range(warmup + reps):
+            t0 = time.perf_counter()
+            gs = O.step_group_scores(qs, static_idx[None])[0]
+            ids = O.select_blocks(gs, w.n_blk, w.n_sink, w.n_recent, w.top_k)
+            kv, vv = O.materialize(keys, vals, ids, w.n_tok, w.rope_theta)
+            O.step_view_attention(qs, kv, vv, w.rope_theta)
+            n_keep = len(ids)
+            if i >= warmup:
+                times.append(time.perf_counter() - t0)
+        print(json.dumps({"seconds": statistics.median(times), "n_keep": n_keep, "reps": len(times)}), flush=True)
+        return
     for i in range(warmup + reps):
         t0 = time.perf_counter()
         idx = O.index_append(hist_index, keys, n_hist, w.append_tok) if w.append_tok else static_idx
@@ -175,9 +190,15 @@ def oracle_sample(w: synth.Workload, reps: int, warmup: int):
     r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", w.name, str(reps), str(warmup)],
                        capture_output=True, text=True, env=env, check=True)
     res = json.loads(r.stdout.strip().splitlines()[-1])
-    desc = (f"oracle (numpy fp64, 1 thread) on KV head 0 of layer 0 of {w.name}: append {w.append_tok} tokens, "
-            f"score {w.n_blk} blocks for {w.group} query heads, select, materialise {res['n_keep']} blocks, attend; "
-            f"per-layer value = {w.h_kv * w.n_sessions} (session, KV head) units x that time")
+    if w.n_q > 1:
+        desc = (f"oracle (numpy fp64, 1 thread) on KV head 0 of layer 0 of {w.name}: step scores of {w.n_q} tokens x "
+                f"{w.group} query heads over {w.n_blk} blocks, select, materialise {res['n_keep']} blocks, causal "
+                f"attention of the {w.n_q} tokens over the view; per-layer value = {w.h_kv * w.n_sessions} "
+                f"(session, KV head) units x that time")
+    else:
+        desc = (f"oracle (numpy fp64, 1 thread) on KV head 0 of layer 0 of {w.name}: append {w.append_tok} tokens, "
+                f"score {w.n_blk} blocks for {w.group} query heads, select, materialise {res['n_keep']} blocks, "
+                f"attend; per-layer value = {w.h_kv * w.n_sessions} (session, KV head) units x that time")
     return res["seconds"], 1, desc
 
 
@@ -188,7 +209,8 @@ def run_reference(args, w):
     per_head_s, threads, desc = oracle_sample(w, args.steps, args.warmup)
     us_layer = per_head_s * w.h_kv * w.n_sessions * 1e6
     gbs = must_touch_bytes(w) / (us_layer * 1e-6) / 1e9
-    line = {"impl": "reference", "metric": METRIC, "value": round(us_layer, 1), "unit": "us/layer",
+    line = {"impl": "reference", "metric": METRIC if w.n_q == 1 else STEP_METRIC, "value": round(us_layer, 1),
+            "unit": "us/layer",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_layer * w.n_layers / 1e3, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "sample": "1 KV head of 1 layer per step"},
@@ -482,6 +504,197 @@ def run_kvm(args, w):
         dist.destroy_process_group()
 
 
+def step_attn_flops(w: synth.Workload) -> int:
+    """Algorithmic FLOPs of one kvm_step_attn call: per (query row, attended slot) a d-long dot product for the
+    score and a d-long accumulation of the value, 2 FLOPs per multiply-add; token t attends L - n_q + t + 1 slots."""
+    L, T = w.view_tokens, w.n_q
+    attended = sum(L - T + t + 1 for t in range(T))
+    return 4 * w.d * w.h_q * attended * w.n_sessions
+
+
+def step_score_flops(w: synth.Workload) -> int:
+    """Algorithmic FLOPs of the step scores: one (n_q * h_q) x n_blk x d contraction (2 FLOPs per multiply-add)."""
+    return 2 * w.n_q * w.h_q * w.n_blk * w.d * w.n_sessions
+
+
+def run_kvm_step(args, w):
+    """One layer of a step of n_q query tokens: step scores + select, materialise, step attention."""
+    import torch
+
+    import sparse_attention_decode_04_b300 as K
+    from synth import device as synth_dev
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    S = w.n_sessions
+    ctx = K.Context.for_workload(w)
+    bt = torch.from_numpy(synth.block_table(w)).to(dev)
+    kp = torch.empty((w.n_pages, w.h_kv, BLOCK, w.d), dtype=torch.bfloat16, device=dev)
+    vp = torch.empty_like(kp)
+    synth_dev.fill_kv_pool(w, 0, bt, kp.view(torch.int16), vp.view(torch.int16))
+    q_np = synth.queries(w, 0)                                          # [S][n_q][h_q][d]
+    q = torch.from_numpy(q_np.view(np.int16)).to(dev).view(torch.bfloat16).contiguous()
+    index = torch.zeros((S, w.h_kv, w.n_blk, w.d), dtype=torch.float32, device=dev)
+    n_tok = [w.n_tok] * S
+    K.kvm_index_append(ctx, kp, w.n_pages, bt, [0] * S, n_tok, index)
+    kept = torch.empty((S, w.h_kv, ctx.budget), dtype=torch.int32, device=dev)
+    k_view = torch.empty((S, w.h_kv, BLOCK * ctx.budget, w.d), dtype=torch.bfloat16, device=dev)
+    v_view = torch.empty_like(k_view)
+    view_len = torch.empty((S, w.h_kv), dtype=torch.int32, device=dev)
+    out = torch.empty((S, w.n_q, w.h_q, w.d), dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+
+    def call_select(q_in=q):
+        K.kvm_score_select(ctx, q_in, w.n_q, index, n_tok, kept)
+
+    def call_materialize():
+        K.kvm_materialize(ctx, kp, vp, w.n_pages, bt, n_tok, kept, k_view, v_view, view_len)
+
+    def call_attn(q_in=q):
+        K.kvm_step_attn(ctx, q_in, w.n_q, k_view, v_view, view_len, S, out)
+
+    def step():
+        call_select()
+        call_materialize()
+        call_attn()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    if args.profile_step:
+        torch.cuda.profiler.start()
+        step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        if rank == 0:
+            print(json.dumps({"profile_step": w.name}), flush=True)
+        return
+
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    graph = capture(step)
+    stage_graphs = {"score_select": capture(call_select), "materialize": capture(call_materialize),
+                    "step_attn": capture(call_attn)}
+    for _ in range(max(1, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    def timed(fn, reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    gpu_index = local
+    if os.environ.get("CUDA_VISIBLE_DEVICES"):
+        try:
+            gpu_index = int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])
+        except ValueError:
+            gpu_index = local
+    sampler = ClockSampler(gpu_index)
+    with sampler:
+        time.sleep(0.3)
+        step_ms = timed(graph.replay, args.steps)
+        stage_ms = {name: timed(g.replay, args.steps) for name, g in stage_graphs.items()}
+    st = K.kvm_device_status(ctx)
+    if st != 0:
+        raise RuntimeError(f"device status 0x{st:x} after the timed region")
+    step_ms = max_over_ranks([step_ms], world, dev)[0]
+
+    # end to end with host buffers: H2D of the step's queries, D2H of the attention output
+    q_host = torch.from_numpy(q_np.view(np.int16)).view(torch.bfloat16).pin_memory()
+    q_dev = torch.empty_like(q)
+    out_host = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q_dev.copy_(q_host, non_blocking=True)
+        call_select(q_dev)
+        call_materialize()
+        call_attn(q_dev)
+        out_host.copy_(out, non_blocking=True)
+
+    e2e_graph = capture(e2e_step)
+    for _ in range(2):
+        e2e_graph.replay()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    e2e_ms = timed(e2e_graph.replay, args.steps)
+    e2e_ms = max(e2e_ms, (time.perf_counter() - wall0) * 1e3 / args.steps)
+
+    peak_tf = None
+    pk = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk):
+        with open(pk) as f:
+            peak_tf, peak_kind = float(json.load(f)["bf16_tflops"]), "measured (cuBLAS bf16 burst)"
+    if peak_tf is None:
+        peak_tf, peak_kind = 1800.0, "fallback"
+    attn_flops = step_attn_flops(w)
+    attn_us = stage_ms["step_attn"] * 1e3
+    achieved = attn_flops / (attn_us * 1e-6) / 1e12
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        per_head_s, threads, desc = oracle_sample(w, 1, 0)
+        cpu = {"value": round(per_head_s * w.h_kv * S * 1e6, 1), "unit": "us/layer", "cores": threads,
+               "kind": "oracle", "sample": desc}
+    if rank == 0:
+        line = {
+            "metric": STEP_METRIC, "value": round(step_ms * 1e3, 2), "unit": "us/layer", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 MMA (split operands), f32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": w.name, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d, "history_tokens": w.n_tok,
+                       "query_tokens": w.n_q, "sessions_per_gpu": S, "view_tokens": w.view_tokens,
+                       "kv_dtype": "bf16", "cuda_graph": True,
+                       "l2": "inputs larger than L2 (K/V pool 4 GiB, index 128 MiB, view 256 MiB), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
+            "roofline": {"bound": "tensor", "kernel": "kvm_step_attn (query packing + view packing + tcgen05 "
+                                                      "attention, timed together)",
+                         "achieved": round(achieved, 1), "peak": peak_tf, "peak_kind": peak_kind, "unit": "TFLOP/s",
+                         "frac": round(achieved / peak_tf, 4), "traffic": None,
+                         "algorithmic_flops_per_launch": attn_flops,
+                         "issued_mma_flops_per_launch": 2 * attn_flops},
+            "step_scores": {"algorithmic_flops": step_score_flops(w),
+                            "tflops_per_s": round(step_score_flops(w) / (stage_ms["score_select"] * 1e-3) / 1e12, 1)},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_ms * 1e3, 2), "unit": "us/layer", "h2d_bytes_per_step": q_host.numel() * 2,
+                    "d2h_bytes_per_step": out_host.numel() * 4, "cuda_graph": True},
+            # per step: step scores 5 + select 1, view kernel 1, step attention 3; timed as the whole-step graph
+            # and again as the three stage graphs
+            "gpu_launches": 20 * args.steps,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def K_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -521,6 +734,8 @@ def main():
         w = w.with_(n_layers=max(1, min(args.layers, w.n_layers)))
     if args.impl == "reference":
         run_reference(args, w)
+    elif w.n_q > 1:
+        run_kvm_step(args, w)
     else:
         run_kvm(args, w)
 

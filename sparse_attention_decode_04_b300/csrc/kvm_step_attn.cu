@@ -19,10 +19,12 @@
 //           with the split operands giving fp32-accurate products on bf16 MMAs.
 // Warp roles: warp 0 issues the bulk copies, warp 1 owns TMEM and issues the
 // MMAs (S of the next tile is issued before P.V of this one, into a second S
-// buffer), warps 2..5 own one query row per thread (each warp can only read
-// its quarter of the 128 TMEM lanes): they read S, keep the running maximum
-// (raised only when it grows by more than 8, then O is rescaled in TMEM),
-// write P to shared memory and finally O / l to the output.
+// buffer), warps 2..9 run the softmax in two streams (even and odd tiles), each
+// thread owning one query row of its stream (a warp can only read its quarter
+// of the 128 TMEM lanes).  A stream reads S, keeps its running maximum (raised
+// only when it grows by more than 8, then its accumulator is rescaled in TMEM)
+// and writes P to shared memory; at the end the two streams' states are merged
+// and O / l is written to the output.
 // Every mbarrier wait is bounded.
 #include "kvm_device.cuh"
 #include "kvm_internal.h"
@@ -30,10 +32,12 @@
 namespace kvm {
 namespace {
 
-constexpr int kThreads = 192;  // 6 warps
-constexpr int kRows = 128;     // query rows per CTA (MMA M)
-constexpr int kTile = 64;      // view tokens per tile (S: N = 64; P.V: K = 64)
-constexpr uint32_t kTmemCols = 256;  // S[2] x 64 columns + O 128 columns
+constexpr int kSoftWarps = 8;                   // two per TMEM lane quarter
+constexpr int kThreads = 64 + 32 * kSoftWarps;  // producer, MMA issuer, softmax warps
+constexpr int kRows = 128;                      // query rows per CTA (MMA M)
+constexpr int kTile = 64;                       // view tokens per tile (S: N = 64; P.V: K = 64)
+static_assert(kTile == 64, "the softmax reductions are written for 64-token tiles");
+constexpr uint32_t kTmemCols = 512;             // S[2] x 64 columns + O_0, O_1 (128 columns each), padded
 
 // Element (r, c) of a [rows][cols] bf16 matrix in the K-major core-matrix layout (cols = K).
 __device__ __forceinline__ int64_t cm_index(int64_t r, int c, int cols) {
@@ -121,8 +125,12 @@ __global__ void __launch_bounds__(256) step_pack_kv_kernel(const uint16_t* __res
   }
 }
 
+constexpr int kStages = 3;  // K tile stages and V tile stages in shared memory
+
 struct AttnBars {
-  uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done, drain;
+  uint64_t q_full, k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], drain;
+  uint64_t xch[4];  // per lane quarter: both softmax warps have published their row state
 };
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -132,7 +140,22 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+template <int D>
+constexpr size_t attn_smem_bytes() {
+  return 2 * (size_t)kRows * D * 2 + 2 * (size_t)kStages * kTile * D * 2 + 4 * (size_t)kRows * kTile * 2;
+}
+// dynamic + static (barriers and the row exchange buffer, under 3 KiB) within the 227 KiB a CTA may use
+static_assert(attn_smem_bytes<128>() + 3 * 1024 <= 227 * 1024, "step attention: shared memory per CTA");
+
 // grid (rows_pad / 128, 1, S * h_kv)
+//
+// Pipeline of tile j (stream j & 1 owns S buffer, P buffer, accumulator O and softmax warps; K/V tiles
+// rotate over kStages stages):
+//   MMA issuer:  [S(j) read] S(j+2) = Q K(j+2)^T  ->  [P(j) written]  ->  O_(j&1) += P(j) V(j)
+//   softmax of stream j & 1:  [S(j) done] read S(j), free it; [P.V(j-2) done] rescale O if the maximum rose,
+//                write P(j)
+// so each stream's softmax overlaps the other stream's MMAs.  Every barrier is waited on at most one phase
+// behind its newest completed phase (each buffer's next phase needs a step the waiter has not taken).
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
     const uint16_t* __restrict__ q_hi, const uint16_t* __restrict__ q_lo, const uint16_t* __restrict__ k_pk,
@@ -141,16 +164,16 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
   constexpr uint32_t Q_BYTES = kRows * D * 2, KV_BYTES = kTile * D * 2, P_BYTES = kRows * kTile * 2;
   constexpr uint32_t SBO_Q = D / 8 * 128, SBO_P = kTile / 8 * 128, LBO = 128;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(kRows, kTile), IDESC_O = idesc_bf16_f32(kRows, D);
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem[];  // no-swizzle operands need 16-byte alignment
   unsigned char* qh_s = smem;
   unsigned char* ql_s = qh_s + Q_BYTES;
-  unsigned char* k_s = ql_s + Q_BYTES;      // [2] tiles
-  unsigned char* v_s = k_s + 2 * KV_BYTES;  // [2] tiles (V^T)
-  unsigned char* ph_s = v_s + 2 * KV_BYTES;
-  unsigned char* pl_s = ph_s + P_BYTES;
+  unsigned char* k_s = ql_s + Q_BYTES;            // [kStages] tiles
+  unsigned char* v_s = k_s + kStages * KV_BYTES;  // [kStages] tiles (V^T)
+  unsigned char* p_s = v_s + kStages * KV_BYTES;  // [2 buffers][hi, lo] probability tiles
   __shared__ AttnBars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ float xval[2][2][kRows];  // [max, sum][stream][row]: each stream's softmax state at the end
 
   griddep_wait();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -168,14 +191,19 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
   if (tid == 0) {
     abort_flag = 0;
     mbar_init(&bars.q_full, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars.kv_full[i], 1);
-      mbar_init(&bars.kv_empty[i], 1);
-      mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_free[i], 4);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&bars.k_full[i], 1);
+      mbar_init(&bars.k_empty[i], 1);
+      mbar_init(&bars.v_full[i], 1);
+      mbar_init(&bars.v_empty[i], 1);
     }
-    mbar_init(&bars.p_full, 4);
-    mbar_init(&bars.pv_done, 1);
+    for (int i = 0; i < 2; ++i) {  // one of each per stream (tile parity)
+      mbar_init(&bars.s_full[i], 1);
+      mbar_init(&bars.s_free[i], kSoftWarps / 2);
+      mbar_init(&bars.p_full[i], kSoftWarps / 2);
+      mbar_init(&bars.pv_done[i], 1);
+    }
+    for (int i = 0; i < 4; ++i) mbar_init(&bars.xch[i], 2);
     mbar_init(&bars.drain, 1);
     mbar_fence_init();
   }
@@ -183,71 +211,91 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tm_o = tmem + 2 * kTile;
+  const uint32_t tm_o = tmem + 2 * kTile;  // O_0 (even tiles), then O_1 (odd tiles)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
+    // K tiles run two tiles ahead of V tiles (scores are computed two tiles ahead of P.V)
     mbar_arrive_expect_tx(&bars.q_full, 2 * Q_BYTES);
     bulk_g2s(qh_s, q_hi + ((int64_t)sg * rows_pad + row0) * D, Q_BYTES, &bars.q_full);
     bulk_g2s(ql_s, q_lo + ((int64_t)sg * rows_pad + row0) * D, Q_BYTES, &bars.q_full);
-    int j = 0;
-    for (; j < nt && !abort_flag; ++j) {
-      const int st = j & 1;
-      if (j >= 2 && !mbar_wait(&bars.kv_empty[st], ((j >> 1) - 1) & 1, status)) {
-        abort_flag = 1;
-        break;
+    int nk = 0, nv = 0;  // tiles whose K / V copy was issued
+    for (int i = 0; i < nt + 2 && !abort_flag; ++i) {
+      if (i < nt) {
+        const int sk = i % kStages;
+        if (i >= kStages && !mbar_wait(&bars.k_empty[sk], (i / kStages - 1) & 1, status)) {
+          abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars.k_full[sk], KV_BYTES);
+        bulk_g2s(k_s + sk * KV_BYTES, k_pk + ((int64_t)sg * l_pad + (int64_t)i * kTile) * D, KV_BYTES,
+                 &bars.k_full[sk]);
+        nk = i + 1;
       }
-      mbar_arrive_expect_tx(&bars.kv_full[st], 2 * KV_BYTES);
-      bulk_g2s(k_s + st * KV_BYTES, k_pk + ((int64_t)sg * l_pad + (int64_t)j * kTile) * D, KV_BYTES, &bars.kv_full[st]);
-      bulk_g2s(v_s + st * KV_BYTES, vt_pk + ((int64_t)sg * (l_pad / kTile) + j) * kTile * D, KV_BYTES,
-               &bars.kv_full[st]);
+      const int jv = i - 2;
+      if (jv >= 0) {
+        const int sv = jv % kStages;
+        if (jv >= kStages && !mbar_wait(&bars.v_empty[sv], (jv / kStages - 1) & 1, status)) {
+          abort_flag = 1;
+          break;
+        }
+        mbar_arrive_expect_tx(&bars.v_full[sv], KV_BYTES);
+        bulk_g2s(v_s + sv * KV_BYTES, vt_pk + ((int64_t)sg * (l_pad / kTile) + jv) * kTile * D, KV_BYTES,
+                 &bars.v_full[sv]);
+        nv = jv + 1;
+      }
     }
     // copies in flight must land before the CTA can exit
     mbar_wait(&bars.q_full, 0, status);
-    for (int i = max(0, j - 2); i < j; ++i) mbar_wait(&bars.kv_full[i & 1], (i >> 1) & 1, status);
+    for (int i = max(0, nk - kStages); i < nk; ++i) mbar_wait(&bars.k_full[i % kStages], (i / kStages) & 1, status);
+    for (int i = max(0, nv - kStages); i < nv; ++i) mbar_wait(&bars.v_full[i % kStages], (i / kStages) & 1, status);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t qh_a = smem_addr(qh_s), ql_a = smem_addr(ql_s), ph_a = smem_addr(ph_s), pl_a = smem_addr(pl_s);
+    const uint32_t qh_a = smem_addr(qh_s), ql_a = smem_addr(ql_s), p_a = smem_addr(p_s);
+    // S(j) into the S buffer of stream j & 1, once that stream's softmax has read S(j - 2)
     auto issue_s = [&](int j) -> bool {
-      const int st = j & 1;
-      if (!mbar_wait(&bars.kv_full[st], (j >> 1) & 1, status)) return false;
-      if (j >= 2 && !mbar_wait(&bars.s_free[st], ((j >> 1) - 1) & 1, status)) return false;
+      const int sk = j % kStages, sb = j & 1;
+      if (!mbar_wait(&bars.k_full[sk], (j / kStages) & 1, status)) return false;
+      if (j >= 2 && !mbar_wait(&bars.s_free[sb], ((j >> 1) - 1) & 1, status)) return false;
       tc_fence_after();
-      const uint32_t k_a = smem_addr(k_s + st * KV_BYTES);
+      const uint32_t k_a = smem_addr(k_s + sk * KV_BYTES);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_bf16(tmem + st * kTile, smem_desc(qh_a + kk * 256, LBO, SBO_Q), smem_desc(k_a + kk * 256, LBO, SBO_Q),
+        mma_bf16(tmem + sb * kTile, smem_desc(qh_a + kk * 256, LBO, SBO_Q), smem_desc(k_a + kk * 256, LBO, SBO_Q),
                  IDESC_S, kk > 0);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_bf16(tmem + st * kTile, smem_desc(ql_a + kk * 256, LBO, SBO_Q), smem_desc(k_a + kk * 256, LBO, SBO_Q),
+        mma_bf16(tmem + sb * kTile, smem_desc(ql_a + kk * 256, LBO, SBO_Q), smem_desc(k_a + kk * 256, LBO, SBO_Q),
                  IDESC_S, 1);
-      mma_commit(&bars.s_full[st]);
+      mma_commit(&bars.s_full[sb]);
+      mma_commit(&bars.k_empty[sk]);
       return true;
     };
-    bool ok = mbar_wait(&bars.q_full, 0, status) && (nt == 0 || issue_s(0));
-    int j = 0;
-    for (; ok && j < nt && !abort_flag; ++j) {
-      const int st = j & 1;
-      if (j + 1 < nt && !issue_s(j + 1)) {
+    bool ok = mbar_wait(&bars.q_full, 0, status);
+    for (int j = 0; ok && j < 2 && j < nt; ++j) ok = issue_s(j);
+    for (int j = 0; ok && j < nt && !abort_flag; ++j) {
+      const int sv = j % kStages, pb = j & 1;
+      // S(j + 2) as soon as the softmax has read S(j): it runs ahead of P.V(j) on the tensor pipe
+      if (j + 2 < nt && !issue_s(j + 2)) {
         ok = false;
         break;
       }
-      if (!mbar_wait(&bars.p_full, j & 1, status)) {
+      if (!mbar_wait(&bars.p_full[pb], (j >> 1) & 1, status) || !mbar_wait(&bars.v_full[sv], (j / kStages) & 1, status)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t v_a = smem_addr(v_s + st * KV_BYTES);
+      const uint32_t v_a = smem_addr(v_s + sv * KV_BYTES);
+      const uint32_t ph_a = p_a + pb * 2 * P_BYTES, pl_a = ph_a + P_BYTES;
+      const uint32_t o = tm_o + pb * D;  // this tile's stream accumulator
 #pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        mma_bf16(tm_o, smem_desc(ph_a + kk * 256, LBO, SBO_P), smem_desc(v_a + kk * 256, LBO, SBO_P), IDESC_O,
-                 (j > 0 || kk > 0));
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        mma_bf16(tm_o, smem_desc(pl_a + kk * 256, LBO, SBO_P), smem_desc(v_a + kk * 256, LBO, SBO_P), IDESC_O, 1);
-      mma_commit(&bars.pv_done);
-      mma_commit(&bars.kv_empty[st]);
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        mma_bf16(o, smem_desc(ph_a + kk * 256, LBO, SBO_P), smem_desc(v_a + kk * 256, LBO, SBO_P), IDESC_O,
+                 (j >= 2 || kk > 0));
+        mma_bf16(o, smem_desc(pl_a + kk * 256, LBO, SBO_P), smem_desc(v_a + kk * 256, LBO, SBO_P), IDESC_O, 1);
+      }
+      mma_commit(&bars.pv_done[pb]);
+      mma_commit(&bars.v_empty[sv]);
     }
     if (!ok) abort_flag = 1;
     // every issued MMA has completed before TMEM is released
@@ -255,53 +303,70 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
     mbar_wait(&bars.drain, 0, status);
   } else if (warp >= 2) {
     // ------------------------------------------------------------ softmax / epilogue, one query row per thread
-    const int quarter = warp & 3;
+    // Two streams: warps 2..5 take the even tiles, warps 6..9 the odd ones, each with its own running maximum
+    // m, sum l and accumulator (O_0 or O_1), so one stream's softmax overlaps the other's MMAs.  The streams
+    // are merged once, at the end.
+    const int quarter = warp & 3, stream = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;  // row within the tile = TMEM lane
     const int row = row0 + r;
     const bool valid_row = row < n_q * G;
     const int t = row / G, hh = row % G;
-    const int pos = L - n_q + t;  // this row's view position; it attends slots <= pos
+    const int pos = valid_row ? L - n_q + t : -1;  // this row's view position; it attends slots <= pos
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t my_o = tm_o + lane_base + stream * D;
+    const uint32_t my_s = tmem + lane_base + stream * kTile;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int st = j & 1;
-      if (__any_sync(0xffffffffu, abort_flag) || !mbar_wait_warp(&bars.s_full[st], (j >> 1) & 1, status)) {
+    for (int j = stream; j < nt; j += 2) {
+      const int ph = (j >> 1) & 1;  // phase of this stream's barriers for tile j
+      if (__any_sync(0xffffffffu, abort_flag) || !mbar_wait_warp(&bars.s_full[stream], ph, status)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sv[2][32];
-      tmem_ld32(tmem + lane_base + st * kTile, sv[0]);
-      tmem_ld32(tmem + lane_base + st * kTile + 32, sv[1]);
+      tmem_ld32(my_s, sv[0]);
+      tmem_ld32(my_s + 32, sv[1]);
       tmem_wait_ld();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_free[st]);
-      float x[kTile], mt = -INFINITY;
+      if (lane == 0) mbar_arrive(&bars.s_free[stream]);
+      const int tok0 = j * kTile;
+      float x[kTile];
+      if (__all_sync(0xffffffffu, tok0 + kTile - 1 <= pos)) {  // no masked column in this tile
 #pragma unroll
-      for (int c = 0; c < kTile; ++c) {
-        const int tok = j * kTile + c;
-        x[c] = (valid_row && tok <= pos) ? __uint_as_float(sv[c >> 5][c & 31]) : -INFINITY;
-        mt = fmaxf(mt, x[c]);
+        for (int c = 0; c < kTile; ++c) x[c] = __uint_as_float(sv[c >> 5][c & 31]);
+      } else {
+#pragma unroll
+        for (int c = 0; c < kTile; ++c) x[c] = tok0 + c <= pos ? __uint_as_float(sv[c >> 5][c & 31]) : -INFINITY;
       }
+      // tree maximum (short dependency chains)
+      float mx[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) mx[i] = fmaxf(fmaxf(x[i], x[i + 16]), fmaxf(x[i + 32], x[i + 48]));
+#pragma unroll
+      for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[i], mx[i + w]);
+      const float mt = mx[0];
       // raise the reference only when it grows by more than 8 (a factor 256): O is then rescaled in TMEM
       const float m_new = (mt > m + 8.f) ? mt : m;
       const float corr = m_new == m ? 1.f : fast_exp2(m - m_new);  // 0 while m was -inf
-      if (j > 0 && !mbar_wait_warp(&bars.pv_done, (j - 1) & 1, status)) {  // P buffer free, O quiescent
+      // P.V(j - 2), the stream's last, has read its P buffer and finished with its accumulator
+      if (j >= 2 && !mbar_wait_warp(&bars.pv_done[stream], ph ^ 1, status)) {
         ok = false;
         break;
       }
-      if (j > 0 && __any_sync(0xffffffffu, m_new != m)) {
+      if (j >= 2 && __any_sync(0xffffffffu, m_new != m)) {
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t ov[32];
-          tmem_ld32(tm_o + lane_base + cc * 32, ov);
+          tmem_ld32(my_o + cc * 32, ov);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
-          tmem_st32(tm_o + lane_base + cc * 32, ov);
+          tmem_st32(my_o + cc * 32, ov);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -309,41 +374,74 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
       l *= corr;
       m = m_new;
       // P = exp2(S - m), split into bf16 + residual, written in the core-matrix layout (rows x 64 tokens)
+      unsigned char* pbh = p_s + stream * 2 * P_BYTES;
+      unsigned char* pbl = pbh + P_BYTES;
+      const bool live = m != -INFINITY;  // padding rows: zeros
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums (short dependency chains)
 #pragma unroll
       for (int c8 = 0; c8 < kTile / 8; ++c8) {
         uint32_t wh[4], wl[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float p0 = x[8 * c8 + 2 * u] == -INFINITY ? 0.f : fast_exp2(x[8 * c8 + 2 * u] - m);
-          const float p1 = x[8 * c8 + 2 * u + 1] == -INFINITY ? 0.f : fast_exp2(x[8 * c8 + 2 * u + 1] - m);
-          l += p0 + p1;
+          const float p0 = live ? fast_exp2(x[8 * c8 + 2 * u] - m) : 0.f;
+          const float p1 = live ? fast_exp2(x[8 * c8 + 2 * u + 1] - m) : 0.f;
+          ls[u] += p0 + p1;
           wh[u] = pack_bf16x2(p0, p1);
           wl[u] = pack_bf16x2(p0 - bf16lo(wh[u]), p1 - bf16hi(wh[u]));
         }
         const int64_t e = cm_index(r, 8 * c8, kTile) * 2;
-        *reinterpret_cast<uint4*>(ph_s + e) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(pl_s + e) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        *reinterpret_cast<uint4*>(pbh + e) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
+        *reinterpret_cast<uint4*>(pbl + e) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
       }
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full);
+      if (lane == 0) mbar_arrive(&bars.p_full[stream]);
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
     }
     if (!ok) abort_flag = 1;
-    if (ok && nt > 0 && mbar_wait_warp(&bars.pv_done, (nt - 1) & 1, status)) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* dst = out + (((int64_t)s * n_q + t) * h_q + g * G + hh) * D;
+    if (ok && nt > 0) {
+      // merge the streams: O = (O_0 2^(m_0 - M) + O_1 2^(m_1 - M)) / (l_0 2^(m_0 - M) + l_1 2^(m_1 - M));
+      // a stream without tiles (nt == 1) has m = -inf and an accumulator that was never written
+      xval[0][stream][r] = m;
+      xval[1][stream][r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars.xch[quarter]);
+      const int last = (nt - 1) - ((nt - 1 - stream) & 1);  // this stream's last tile
+      ok = mbar_wait_warp(&bars.xch[quarter], 0, status) &&
+           (last < 0 || mbar_wait_warp(&bars.pv_done[stream], (last >> 1) & 1, status));
+      if (ok) {
+        // the other stream's accumulator is read too: wait for its last P.V as well
+        const int other_last = (nt - 1) - ((nt - 1 - (stream ^ 1)) & 1);
+        ok = other_last < 0 || mbar_wait_warp(&bars.pv_done[stream ^ 1], (other_last >> 1) & 1, status);
+      }
+      if (ok) {
+        tc_fence_after();
+        const float m0 = xval[0][0][r], m1 = xval[0][1][r];
+        const float M = fmaxf(m0, m1);
+        const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M), f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
+        const float lt = xval[1][0][r] * f0 + xval[1][1][r] * f1;
+        const float inv = lt > 0.f ? 1.f / lt : 0.f;
+        const float w0 = f0 * inv, w1 = f1 * inv;
+        const bool use1 = nt > 1;  // O_1 holds data only when the odd stream had a tile
+        float* dst = out + (((int64_t)s * n_q + t) * h_q + g * G + hh) * D;
+        // the two warps of a quarter split the d columns
 #pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t ov[32];
-        tmem_ld32(tm_o + lane_base + cc * 32, ov);
-        tmem_wait_ld();
-        if (valid_row) {
+        for (int cc = stream * (D / 64); cc < (stream + 1) * (D / 64); ++cc) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tm_o + lane_base + cc * 32, o0);
+          tmem_ld32(tm_o + lane_base + D + cc * 32, o1);
+          tmem_wait_ld();
+          if (valid_row) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4)
-            *reinterpret_cast<float4*>(dst + cc * 32 + i) =
-                make_float4(__uint_as_float(ov[i]) * inv, __uint_as_float(ov[i + 1]) * inv,
-                            __uint_as_float(ov[i + 2]) * inv, __uint_as_float(ov[i + 3]) * inv);
+            for (int i = 0; i < 32; i += 4) {
+              float4 v;
+              v.x = __uint_as_float(o0[i]) * w0 + (use1 ? __uint_as_float(o1[i]) * w1 : 0.f);
+              v.y = __uint_as_float(o0[i + 1]) * w0 + (use1 ? __uint_as_float(o1[i + 1]) * w1 : 0.f);
+              v.z = __uint_as_float(o0[i + 2]) * w0 + (use1 ? __uint_as_float(o1[i + 2]) * w1 : 0.f);
+              v.w = __uint_as_float(o0[i + 3]) * w0 + (use1 ? __uint_as_float(o1[i + 3]) * w1 : 0.f);
+              *reinterpret_cast<float4*>(dst + cc * 32 + i) = v;
+            }
+          }
         }
       }
     }
@@ -373,7 +471,7 @@ cudaError_t launch_dg(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* 
   if ((e = launch_pdl(step_pack_kv_kernel<D>, dim3((unsigned)(l_pad / kTile), SG), dim3(256), 0, st, 1, k_view, v_view,
                       view_len, n_q, Lcap, l_pad, c.attn_kpk, c.attn_vtpk)) != cudaSuccess)
     return e;
-  const size_t smem = 2 * (size_t)kRows * D * 2 + 4 * (size_t)kTile * D * 2 + 2 * (size_t)kRows * kTile * 2 + 1024;
+  const size_t smem = attn_smem_bytes<D>();
   auto ka = step_attn_kernel<D, G>;
   if ((e = ensure_smem(ka, c.device, smem)) != cudaSuccess) return e;
   return launch_pdl(ka, dim3(rows_pad / kRows, 1, SG), dim3(kThreads), smem, st, 1, (const uint16_t*)c.attn_q,
