@@ -124,6 +124,107 @@ def index_append(index, keys_bits, tok_begin: int, n_tok: int) -> np.ndarray:
     return new
 
 
+# --------------------------------------------------------------------------- quantised KV pages (FP8 E4M3)
+# [README] "Background and main changes" (the deployment runs the model in NVFP4) -- the pages give no
+# precision for the paged KV itself.  READING for the quantised-page variant: FP8 E4M3 codes (the OCP 8-bit
+# floating-point format: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities, exponent 15
+# with mantissa 7 is NaN, largest finite 448) with one fp32 scale per (page, KV head), for K and for V
+# separately; a value is code * scale.  Both quantisation decisions (the scale and each code) are taken in
+# fp32, the precision of the kernels.
+E4M3_MAX = 448.0
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Exact value of E4M3 codes: (-1)^s 2^(e-7) (1 + m/8) for e > 0, (-1)^s 2^-6 (m/8) for e = 0."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    e, m = (c >> 3) & 0xF, c & 7
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return np.where(c & 0x80, -mag, mag)
+
+
+_E4M3_POS = e4m3_to_f64(np.arange(127, dtype=np.uint8))   # the finite non-negative values, ascending
+
+
+def f32_to_e4m3(x) -> np.ndarray:
+    """Round (fp32) values to E4M3 codes: nearest, ties to even, magnitudes beyond 448 saturate to 448.
+
+    The spacing of E4M3 values is 2^(E-3) in the binade [2^E, 2^(E+1)) for E >= -6, and 2^-9 below 2^-6
+    (subnormals); rounding |x| on that grid with ties to even gives the nearest value, then the code is looked
+    up.  The sign is kept (negative zero included); NaN gives the NaN code 0x7F.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    _, e = np.frexp(a)                            # a = f 2^e, f in [0.5, 1): binade exponent E = e - 1
+    q = np.maximum(e - 4, -9)                     # log2 of the spacing
+    v = np.minimum(np.ldexp(np.rint(np.ldexp(a, -q)), q), E4M3_MAX)
+    v = np.where(np.isnan(a), 0.0, v)
+    code = np.searchsorted(_E4M3_POS, v).astype(np.uint8)
+    code = np.where(np.signbit(x), code | 0x80, code)
+    return np.where(np.isnan(x), 0x7F, code).astype(np.uint8)
+
+
+def quantize_page(x_bits):
+    """One page of one KV head, bf16 [32][d] -> (E4M3 codes uint8 [32][d], fp32 scale).
+
+    READING: scale = amax / 448 in fp32 (amax = the largest |x| of the page as stored, all 32 rows); each
+    code = E4M3(x / scale) with the division in fp32; a page of zeros gets scale 1.  The largest element
+    then maps to +-448 exactly.
+    """
+    x = bf16_to_f64(x_bits).astype(np.float32)
+    amax = np.float32(np.max(np.abs(x)))
+    scale = np.float32(amax / np.float32(E4M3_MAX)) if amax > 0 else np.float32(1.0)
+    return f32_to_e4m3(np.float32(x) / scale), scale
+
+
+def quantize_pool(pool_bits):
+    """Every page of a pool: (codes uint8 [n_pages][h_kv][32][d], scales fp32 [n_pages][h_kv])."""
+    pool_bits = np.asarray(pool_bits)
+    n_pages, h_kv = pool_bits.shape[:2]
+    codes = np.empty(pool_bits.shape, dtype=np.uint8)
+    scales = np.empty((n_pages, h_kv), dtype=np.float32)
+    for p in range(n_pages):
+        for g in range(h_kv):
+            codes[p, g], scales[p, g] = quantize_page(pool_bits[p, g])
+    return codes, scales
+
+
+def dequantize(codes, scale) -> np.ndarray:
+    """Values of quantised elements: the fp32 product code * scale (one rounding), as fp64."""
+    return (e4m3_to_f64(codes).astype(np.float32) * np.float32(scale)).astype(np.float64)
+
+
+def paged_dequant_tokens(codes_pool, scales, page_of, head: int, n_tok: int) -> np.ndarray:
+    """Dequantised tokens [n_tok][d] of one head, read through the block table."""
+    n_blk = -(-n_tok // BLOCK)
+    pages = np.asarray(page_of)[:n_blk]
+    vals = np.stack([dequantize(np.asarray(codes_pool)[p, head], np.asarray(scales)[p, head]) for p in pages])
+    return vals.reshape(n_blk * BLOCK, vals.shape[-1])[:n_tok]
+
+
+def mean_k_index_of(keys) -> np.ndarray:
+    """Mean-K vectors of keys given as values (fp64 [n_tok][d]): the definition of mean_k_index."""
+    k = np.asarray(keys, dtype=np.float64)
+    n_tok, d = k.shape
+    n_full = n_tok // BLOCK
+    out = np.empty((-(-n_tok // BLOCK), d))
+    out[:n_full] = k[:n_full * BLOCK].reshape(n_full, BLOCK, d).mean(axis=1)
+    if n_tok % BLOCK:
+        out[n_full] = k[n_full * BLOCK:].mean(axis=0)
+    return out
+
+
+def materialize_values(keys, values, ids, n_tok: int, theta: float):
+    """Execution view of one KV head from keys / values given as values (dequantised pages):
+    (K_view bits, V_view bits), each [L][d].  As ``materialize``, with the value view rounded to bf16
+    (nearest even) since the dequantised values are not bf16.
+    """
+    rows = view_rows(ids, n_tok)
+    k_view = f64_to_bf16(rope(np.asarray(keys, dtype=np.float64)[rows], np.arange(rows.size), theta))
+    v_view = f64_to_bf16(np.asarray(values, dtype=np.float64)[rows])
+    return k_view, v_view
+
+
 # --------------------------------------------------------------------------- step 2: scores
 def block_scores(q_bits, index) -> np.ndarray:
     """s[h, b] = <q_h, k_bar_b of h's KV head> / sqrt(d): [h_q][n_blk].

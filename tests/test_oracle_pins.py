@@ -355,3 +355,75 @@ def test_step_attention_matches_library_softmax_hand_case():
     w = np.exp(logits - logits.max())
     w /= w.sum()
     assert np.allclose(out[1, 0], w @ np.array([[1.0, -1.0], [3.0, 5.0]]), atol=1e-14)
+
+
+# ----------------------------------------------------------------------------- FP8 E4M3 pages
+def _torch_e4m3_table():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_e4m3_decode_matches_library_and_hand_values():
+    v = O.e4m3_to_f64(np.arange(256, dtype=np.uint8))
+    lib = _torch_e4m3_table()
+    assert np.array_equal(np.isnan(v), np.isnan(lib)) and np.isnan(v).sum() == 2      # 0x7F and 0xFF
+    fin = ~np.isnan(v)
+    assert np.array_equal(v[fin], lib[fin])
+    # by hand from the format: 1.0 = 2^(7-7), the largest normal 2^8 * 1.75, the smallest normal and subnormal
+    assert (v[0x38], v[0xB8], v[0x7E], v[0x08], v[0x01], v[0x07]) == (1.0, -1.0, 448.0, 2.0 ** -6, 2.0 ** -9,
+                                                                         7 * 2.0 ** -9)
+
+
+def test_e4m3_encode_is_nearest_even_by_brute_force():
+    vals = O.e4m3_to_f64(np.arange(127, dtype=np.uint8))            # finite non-negative, ascending
+    x = np.concatenate([RNG.uniform(-448, 448, 3000), RNG.uniform(-0.05, 0.05, 3000),
+                        (vals[:-1] + vals[1:]) / 2, -(vals[:-1] + vals[1:]) / 2]).astype(np.float32)
+    got = O.f32_to_e4m3(x)
+    for xi, gi in zip(x.astype(np.float64), got):
+        d = np.abs(vals - abs(xi))
+        best = np.flatnonzero(d == d.min())
+        code = best[0] if len(best) == 1 else [c for c in best if c % 2 == 0][0]   # tie: even mantissa
+        assert gi == (code | (0x80 if np.signbit(xi) else 0)), (xi, gi, code)
+    # the library's conversion agrees inside the finite range
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(got, lib)
+
+
+def test_e4m3_saturates_beyond_448():
+    assert O.f32_to_e4m3([448.0, 449.0, 463.9, 464.0, 1e6, -1e6]).tolist() == [0x7E] * 5 + [0xFE]
+
+
+def test_quantize_page_scale_and_the_largest_element():
+    x = rand_bf16((32, 64), 0.7)
+    codes, scale = O.quantize_page(x)
+    vals = O.bf16_to_f64(x)
+    amax = np.float32(np.abs(vals).max())
+    assert scale == np.float32(amax / np.float32(448.0))
+    i = np.unravel_index(np.argmax(np.abs(vals)), vals.shape)
+    assert abs(O.e4m3_to_f64(codes[i])) == 448.0
+    # every dequantised element within half a code spacing (relative 2^-4) or half a subnormal step
+    deq = O.dequantize(codes, scale)
+    assert np.all(np.abs(deq - vals) <= np.maximum(np.abs(vals) * 2.0 ** -4, 2.0 ** -10 * scale) * 1.0001)
+    zc, zs = O.quantize_page(np.zeros((32, 64), dtype=np.uint16))
+    assert zs == np.float32(1.0) and not zc.any()
+
+
+def test_representable_pages_survive_quantisation_exactly():
+    """Values that are E4M3 values times a power of two, with the largest at 448 * 2^k, have scale 2^k: the
+    dequantised pages equal the bf16 pages, so the index and the view are those of the bf16 path."""
+    k = -6
+    codes = RNG.integers(0, 127, size=(4, 32, 64)).astype(np.uint8) | (RNG.integers(0, 2, (4, 32, 64)) << 7).astype(np.uint8)
+    codes[:, 0, 0] = 0x7E                                          # the page maximum: 448
+    x = O.f64_to_bf16(O.e4m3_to_f64(codes) * 2.0 ** k)              # exact in bf16
+    pool = x[:, None]                                               # [n_pages][h_kv=1][32][d]
+    qc, qs = O.quantize_pool(pool)
+    assert np.all(qs == np.float32(2.0 ** k)) and np.array_equal(qc[:, 0], codes)
+    page_of = np.array([2, 0, 3, 1])
+    n_tok = 4 * 32 - 5
+    deq = O.paged_dequant_tokens(qc, qs, page_of, 0, n_tok)
+    bits = O.paged_tokens(pool, page_of, 0, n_tok)
+    assert np.array_equal(deq, O.bf16_to_f64(bits))
+    assert np.array_equal(O.mean_k_index_of(deq), O.mean_k_index(bits))
+    kv, vv = O.materialize_values(deq, deq, [0, 2, 3], n_tok, 1e4)
+    kb, vb = O.materialize(bits, bits, [0, 2, 3], n_tok, 1e4)
+    assert np.array_equal(kv, kb) and np.array_equal(vv, vb)
