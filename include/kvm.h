@@ -19,6 +19,11 @@
  *                         re-read from HBM).
  *   kvm_step_attn         attention of a whole step's query tokens over the
  *                         view (tensor cores), after a multi-query selection.
+ * Page tiers beyond the bf16 HBM pool:
+ *   kvm_quantize_pages, kvm_index_append_fp8, kvm_materialize_fp8
+ *                         FP8 E4M3 pages (one fp32 scale per page and KV head),
+ *                         dequantised inside the index and the gather.
+ *   kvm_materialize_host  the gather from a pool in mapped pinned host memory.
  *
  * Conventions shared by every call
  * --------------------------------
@@ -33,8 +38,10 @@
  * - Block size is fixed: 32 tokens per block, one block per physical page.
  * - One context serves one device (the device current at kvm_create) and one
  *   head geometry.  kvm_score_select, kvm_materialize, kvm_decode_attn,
- *   kvm_materialize_attn and kvm_step_attn on one context must not run concurrently on
- *   different streams: they share the context's scratch buffers.
+ *   kvm_materialize_attn and kvm_step_attn on one context must not run
+ *   concurrently on different streams: they share the context's scratch
+ *   buffers.  The index appends, kvm_quantize_pages and the gathers of
+ *   kvm_materialize_fp8 / kvm_materialize_host use no scratch.
  *   kvm_index_append uses no scratch (only the status word, which it updates
  *   atomically), so appends may run on another stream alongside them, e.g.
  *   every layer's append at the start of a decode step.
@@ -237,6 +244,61 @@ kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint
 kvm_status kvm_step_attn(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const uint16_t* k_view,
                          const uint16_t* v_view, const int32_t* view_len, int32_t n_sessions, float* out,
                          void* stream);
+
+/*
+ * Quantised KV pages.  KVMEM reproduction README, "Background and main
+ * changes" (paged KV kept beyond GPU memory; the deployment runs in NVFP4).
+ * The pages give no precision for the paged KV; this variant stores each
+ * (page, KV head) of K and of V as FP8 E4M3 codes (OCP format: bias 7, no
+ * infinities, largest finite 448) with one fp32 scale, value = code * scale:
+ *   scale = amax / 448 (fp32 division; amax over the page's 32 x d values as
+ *           stored; a page of zeros gets scale 1)
+ *   code  = E4M3(x / scale): fp32 division, nearest even, magnitudes past 448
+ *           saturate.
+ *   pool8   [n_pages][h_kv][32][d] uint8 codes (16-byte aligned)
+ *   scales  [n_pages][h_kv] fp32
+ *
+ * kvm_quantize_pages: quantises the listed pages (every KV head) of a bf16
+ * pool [n_pages][h_kv][32][d] into pool8 / scales.  pages is a device int32
+ * array of n_list page ids; an id outside [0, n_pages) sets KVM_DEV_BAD_PAGE.
+ */
+kvm_status kvm_quantize_pages(kvm_ctx* ctx, const uint16_t* pool, int64_t n_pages, const int32_t* pages,
+                              int64_t n_list, uint8_t* pool8, float* scales, void* stream);
+
+/*
+ * kvm_index_append as above, over quantised keys: each block's mean of the
+ * dequantised keys (code * scale, fp32), accumulated in fp32 in token order.
+ */
+kvm_status kvm_index_append_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const float* k_scales, int64_t n_pages,
+                                const int32_t* block_table, int32_t n_sessions, const int64_t* tok_begin,
+                                const int64_t* n_tok, float* index, void* stream);
+
+/*
+ * kvm_materialize from quantised pages: view slot j holds the j-th kept token;
+ * k_view is the dequantised key rotated at position j and rounded to bf16
+ * (nearest even), v_view the dequantised value rounded to bf16 (nearest
+ * even).  Arguments, layouts and errors otherwise as kvm_materialize; the
+ * view then feeds kvm_decode_attn or kvm_step_attn unchanged.
+ */
+kvm_status kvm_materialize_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const float* k_scales, const uint8_t* v_pool8,
+                               const float* v_scales, int64_t n_pages, const int32_t* block_table,
+                               const int64_t* n_tok, int32_t n_sessions, const int32_t* kept_ids, uint16_t* k_view,
+                               uint16_t* v_view, int32_t* view_len, void* stream);
+
+/*
+ * Host tier.  KVMEM reproduction README, "Background and main changes" and
+ * Evolve review, "Summary" (history paged across GPU and host memory).  The
+ * same outputs as kvm_materialize, with the K/V pools resident in host memory:
+ * k_pool_host / v_pool_host must be pinned and mapped into the device address
+ * space (cudaHostAlloc with cudaHostAllocMapped, or cudaHostRegister with
+ * cudaHostRegisterMapped), else KVM_ERR_INVALID_ARG.  Only the kept pages'
+ * rows cross the host link, read by the gather kernel directly (no staging
+ * copy); block_table, kept_ids and the view stay in device memory.
+ */
+kvm_status kvm_materialize_host(kvm_ctx* ctx, const uint16_t* k_pool_host, const uint16_t* v_pool_host,
+                                int64_t n_pages, const int32_t* block_table, const int64_t* n_tok,
+                                int32_t n_sessions, const int32_t* kept_ids, uint16_t* k_view, uint16_t* v_view,
+                                int32_t* view_len, void* stream);
 
 /*
  * Selection controls (the comparisons the pages report next to the method).

@@ -65,9 +65,14 @@ def lib() -> ctypes.CDLL:
         L.kvm_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), i32, P]
         L.kvm_select_control.argtypes = [P, i32, P, P, P, i32, P, P, P]
         L.kvm_step_attn.argtypes = [P, P, i32, P, P, P, i32, P, P]
+        L.kvm_quantize_pages.argtypes = [P, P, i64, P, i64, P, P, P]
+        L.kvm_index_append_fp8.argtypes = [P, P, P, i64, P, i32, P, P, P, P]
+        L.kvm_materialize_fp8.argtypes = [P, P, P, P, P, i64, P, P, i32, P, P, P, P, P]
+        L.kvm_materialize_host.argtypes = [P, P, P, i64, P, P, i32, P, P, P, P, P]
         for name in ("kvm_create", "kvm_destroy", "kvm_index_append", "kvm_score_select", "kvm_materialize",
                      "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status", "kvm_select_control",
-                     "kvm_step_attn"):
+                     "kvm_step_attn", "kvm_quantize_pages", "kvm_index_append_fp8", "kvm_materialize_fp8",
+                     "kvm_materialize_host"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -181,6 +186,36 @@ def kvm_step_attn(ctx: Context, q, n_q: int, k_view, v_view, view_len, n_session
     """Attention of a step's n_q query tokens (the history's last n_q tokens) over the view."""
     _check(lib().kvm_step_attn(ctx.handle, _ptr(q), int(n_q), _ptr(k_view), _ptr(v_view), _ptr(view_len),
                                int(n_sessions), _ptr(out), _stream(stream)))
+
+
+def kvm_quantize_pages(ctx: Context, pool, n_pages: int, pages, pool8, scales, stream=None):
+    """FP8 E4M3 codes and per-(page, KV head) fp32 scales of the listed pages (a device int32 tensor)."""
+    _check(lib().kvm_quantize_pages(ctx.handle, _ptr(pool), int(n_pages), _ptr(pages), int(pages.numel()),
+                                    _ptr(pool8), _ptr(scales), _stream(stream)))
+
+
+def kvm_index_append_fp8(ctx: Context, k_pool8, k_scales, n_pages: int, block_table, tok_begin, n_tok, index,
+                         stream=None):
+    n = len(n_tok)
+    _check(lib().kvm_index_append_fp8(ctx.handle, _ptr(k_pool8), _ptr(k_scales), int(n_pages), _ptr(block_table), n,
+                                      _i64(tok_begin), _i64(n_tok), _ptr(index), _stream(stream)))
+
+
+def kvm_materialize_fp8(ctx: Context, k_pool8, k_scales, v_pool8, v_scales, n_pages: int, block_table, n_tok,
+                        kept_ids, k_view, v_view, view_len, stream=None):
+    n = len(n_tok)
+    _check(lib().kvm_materialize_fp8(ctx.handle, _ptr(k_pool8), _ptr(k_scales), _ptr(v_pool8), _ptr(v_scales),
+                                     int(n_pages), _ptr(block_table), _i64(n_tok), n, _ptr(kept_ids), _ptr(k_view),
+                                     _ptr(v_view), _ptr(view_len), _stream(stream)))
+
+
+def kvm_materialize_host(ctx: Context, k_pool_host, v_pool_host, n_pages: int, block_table, n_tok, kept_ids,
+                         k_view, v_view, view_len, stream=None):
+    """The view from K/V pools in pinned, mapped host memory (e.g. torch.empty(..., pin_memory=True))."""
+    n = len(n_tok)
+    _check(lib().kvm_materialize_host(ctx.handle, _ptr(k_pool_host), _ptr(v_pool_host), int(n_pages),
+                                      _ptr(block_table), _i64(n_tok), n, _ptr(kept_ids), _ptr(k_view), _ptr(v_view),
+                                      _ptr(view_len), _stream(stream)))
 
 
 def kvm_device_status(ctx: Context, clear: bool = True, stream=None) -> int:

@@ -80,6 +80,27 @@ kvm_status history_args(const Ctx& c, const int64_t* n_tok, int32_t n_sessions, 
   return KVM_OK;
 }
 
+// First block and block count of each session's append, from host token ranges.
+kvm_status append_args(const Ctx& c, int32_t n_sessions, const int64_t* tok_begin, const int64_t* n_tok,
+                       SessionArgs* a, int* max_count) {
+  memset(a, 0, sizeof(*a));
+  *max_count = 0;
+  for (int i = 0; i < n_sessions; ++i) {
+    if (tok_begin[i] < 0 || n_tok[i] < 0)
+      return fail(KVM_ERR_INVALID_ARG, "session %d: negative tok_begin or n_tok", i);
+    const int64_t end = tok_begin[i] + n_tok[i];
+    if ((end + kvm::kBlock - 1) / kvm::kBlock > c.p.max_blocks)
+      return fail(KVM_ERR_SHAPE, "session %d: token %lld beyond max_blocks", i, (long long)end);
+    const int64_t b0 = tok_begin[i] / kvm::kBlock;
+    const int64_t b1 = n_tok[i] ? (end + kvm::kBlock - 1) / kvm::kBlock : b0;
+    a->n_tok[i] = end;  // tokens present after the append
+    a->aux[i] = b0;     // first block touched
+    a->count[i] = (int32_t)(b1 - b0);
+    if (a->count[i] > *max_count) *max_count = a->count[i];
+  }
+  return KVM_OK;
+}
+
 }  // namespace
 
 void kvm::set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
@@ -250,24 +271,103 @@ kvm_status kvm_index_append(kvm_ctx* ctx, const uint16_t* k_pool, int64_t n_page
   if (!aligned(k_pool, 16) || !aligned(index, 16))
     return fail(KVM_ERR_INVALID_ARG, "k_pool and index must be 16-byte aligned");
   SessionArgs a;
-  memset(&a, 0, sizeof(a));
   int max_count = 0;
-  for (int i = 0; i < n_sessions; ++i) {
-    if (tok_begin[i] < 0 || n_tok[i] < 0)
-      return fail(KVM_ERR_INVALID_ARG, "session %d: negative tok_begin or n_tok", i);
-    const int64_t end = tok_begin[i] + n_tok[i];
-    if ((end + kvm::kBlock - 1) / kvm::kBlock > c.p.max_blocks)
-      return fail(KVM_ERR_SHAPE, "session %d: token %lld beyond max_blocks", i, (long long)end);
-    const int64_t b0 = tok_begin[i] / kvm::kBlock;
-    const int64_t b1 = n_tok[i] ? (end + kvm::kBlock - 1) / kvm::kBlock : b0;
-    a.n_tok[i] = end;  // tokens present after the append
-    a.aux[i] = b0;     // first block touched
-    a.count[i] = (int32_t)(b1 - b0);
-    if (a.count[i] > max_count) max_count = a.count[i];
-  }
+  if ((s = append_args(c, n_sessions, tok_begin, n_tok, &a, &max_count)) != KVM_OK) return s;
   cudaError_t e = kvm::launch_index_append(c, k_pool, n_pages, block_table, n_sessions, a, max_count, index,
                                            (cudaStream_t)stream);
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_index_append launch");
+}
+
+kvm_status kvm_index_append_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const float* k_scales, int64_t n_pages,
+                                const int32_t* block_table, int32_t n_sessions, const int64_t* tok_begin,
+                                const int64_t* n_tok, float* index, void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_sessions == 0) return KVM_OK;
+  if (!k_pool8 || !k_scales || !block_table || !tok_begin || !n_tok || !index)
+    return fail(KVM_ERR_INVALID_ARG, "kvm_index_append_fp8: NULL pointer argument");
+  if (n_pages < 1) return fail(KVM_ERR_INVALID_ARG, "n_pages=%lld must be >= 1", (long long)n_pages);
+  if (!aligned(k_pool8, 16) || !aligned(index, 16) || !aligned(k_scales, 4))
+    return fail(KVM_ERR_INVALID_ARG, "k_pool8 and index must be 16-byte aligned, k_scales 4-byte aligned");
+  SessionArgs a;
+  int max_count = 0;
+  if ((s = append_args(c, n_sessions, tok_begin, n_tok, &a, &max_count)) != KVM_OK) return s;
+  cudaError_t e = kvm::launch_index_append_q(c, k_pool8, k_scales, n_pages, block_table, n_sessions, a, max_count,
+                                             index, (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_index_append_fp8 launch");
+}
+
+kvm_status kvm_quantize_pages(kvm_ctx* ctx, const uint16_t* pool, int64_t n_pages, const int32_t* pages,
+                              int64_t n_list, uint8_t* pool8, float* scales, void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if (n_list < 0) return fail(KVM_ERR_INVALID_ARG, "n_list=%lld is negative", (long long)n_list);
+  if (n_list == 0) return KVM_OK;
+  if (!pool || !pages || !pool8 || !scales) return fail(KVM_ERR_INVALID_ARG, "kvm_quantize_pages: NULL pointer");
+  if (n_pages < 1) return fail(KVM_ERR_INVALID_ARG, "n_pages=%lld must be >= 1", (long long)n_pages);
+  if (!aligned(pool, 16) || !aligned(pool8, 16) || !aligned(pages, 4) || !aligned(scales, 4))
+    return fail(KVM_ERR_INVALID_ARG, "pool and pool8 must be 16-byte aligned, pages and scales 4-byte aligned");
+  cudaError_t e = kvm::launch_quantize_pages(c, pool, n_pages, pages, n_list, pool8, scales, (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_quantize_pages launch");
+}
+
+static kvm_status gather_call(kvm_ctx* ctx, bool fp8, const void* k_src, const void* v_src, const float* k_scales,
+                              const float* v_scales, int64_t n_pages, const int32_t* block_table,
+                              const int64_t* n_tok, int32_t n_sessions, const int32_t* kept_ids, uint16_t* k_view,
+                              uint16_t* v_view, int32_t* view_len, void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_sessions == 0) return KVM_OK;
+  if (!k_src || !v_src || !block_table || !kept_ids || !k_view || !v_view || !view_len ||
+      (fp8 && (!k_scales || !v_scales)))
+    return fail(KVM_ERR_INVALID_ARG, "NULL pool, scales, block_table, kept_ids or view output");
+  if (n_pages < 1) return fail(KVM_ERR_INVALID_ARG, "n_pages=%lld must be >= 1", (long long)n_pages);
+  if (!aligned(k_src, 16) || !aligned(v_src, 16) || !aligned(k_view, 16) || !aligned(v_view, 16) ||
+      !aligned(view_len, 4) || !aligned(kept_ids, 4) || !aligned(k_scales, 4) || !aligned(v_scales, 4))
+    return fail(KVM_ERR_INVALID_ARG, "pools and views must be 16-byte aligned");
+  SessionArgs a;
+  if ((s = history_args(c, n_tok, n_sessions, &a)) != KVM_OK) return s;
+  cudaError_t e = kvm::launch_gather_view(c, fp8, k_src, v_src, k_scales, v_scales, n_pages, block_table, n_sessions,
+                                          a, kept_ids, k_view, v_view, view_len, (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "gather kernel launch");
+}
+
+kvm_status kvm_materialize_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const float* k_scales, const uint8_t* v_pool8,
+                               const float* v_scales, int64_t n_pages, const int32_t* block_table,
+                               const int64_t* n_tok, int32_t n_sessions, const int32_t* kept_ids, uint16_t* k_view,
+                               uint16_t* v_view, int32_t* view_len, void* stream) {
+  return gather_call(ctx, true, k_pool8, v_pool8, k_scales, v_scales, n_pages, block_table, n_tok, n_sessions,
+                     kept_ids, k_view, v_view, view_len, stream);
+}
+
+kvm_status kvm_materialize_host(kvm_ctx* ctx, const uint16_t* k_pool_host, const uint16_t* v_pool_host,
+                                int64_t n_pages, const int32_t* block_table, const int64_t* n_tok,
+                                int32_t n_sessions, const int32_t* kept_ids, uint16_t* k_view, uint16_t* v_view,
+                                int32_t* view_len, void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  // the pools must be pinned host memory mapped into the device address space; the kernel reads them through
+  // their device-side address
+  const void* dev[2] = {nullptr, nullptr};
+  const uint16_t* host[2] = {k_pool_host, v_pool_host};
+  for (int i = 0; i < 2; ++i) {
+    if (!host[i]) return fail(KVM_ERR_INVALID_ARG, "kvm_materialize_host: NULL pool");
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, host[i]);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr) {
+      cudaGetLastError();
+      return fail(KVM_ERR_INVALID_ARG, "kvm_materialize_host: %s pool is not mapped pinned host memory",
+                  i ? "V" : "K");
+    }
+    dev[i] = attr.devicePointer;
+  }
+  return gather_call(ctx, false, dev[0], dev[1], nullptr, nullptr, n_pages, block_table, n_tok, n_sessions, kept_ids,
+                     k_view, v_view, view_len, stream);
 }
 
 kvm_status kvm_score_select(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const float* index, const int64_t* n_tok,

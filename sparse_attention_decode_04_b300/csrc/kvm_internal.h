@@ -89,6 +89,17 @@ cudaError_t launch_select_given(const Ctx& c, const float* gs, int n_sessions, c
 cudaError_t launch_step_attn(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* k_view, const uint16_t* v_view,
                              const int32_t* view_len, int n_sessions, float* out, cudaStream_t st);
 
+// kvm_gather.cu: quantised (FP8 E4M3) pages and the gather of views from quantised or host-resident pages
+cudaError_t launch_quantize_pages(const Ctx& c, const uint16_t* pool, int64_t n_pages, const int32_t* pages,
+                                  int64_t n_list, uint8_t* pool8, float* scales, cudaStream_t st);
+cudaError_t launch_index_append_q(const Ctx& c, const uint8_t* k8, const float* kscale, int64_t n_pages,
+                                  const int32_t* bt, int n_sessions, const SessionArgs& a, int max_count,
+                                  float* index, cudaStream_t st);
+cudaError_t launch_gather_view(const Ctx& c, bool fp8, const void* k_src, const void* v_src, const float* k_scale,
+                               const float* v_scale, int64_t n_pages, const int32_t* bt, int n_sessions,
+                               const SessionArgs& a, const int32_t* kept, uint16_t* k_view, uint16_t* v_view,
+                               int32_t* view_len, cudaStream_t st);
+
 // kvm_view.cu — mode: 0 materialise, 1 attend over a view, 2 fused
 cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,
                         const int32_t* bt, int n_sessions, const SessionArgs& a, const int32_t* kept,

@@ -151,43 +151,6 @@ __device__ __forceinline__ uint32_t chunk_off(int r, int k) {
   return (uint32_t)((k >> 3) * (32 * 128) + r * 128 + (((k & 7) ^ (r & 7)) << 4));
 }
 
-__device__ __forceinline__ void rope_cs(const float2 b, const float c, const float s, float& co, float& sn) {
-  // cos/sin of (base + offset) from cos/sin of each (angle addition)
-  co = fmaf(b.x, c, -b.y * s);
-  sn = fmaf(b.y, c, b.x * s);
-}
-
-// Float-float (unevaluated hi + lo) arithmetic, Dekker / Knuth error-free transformations.
-struct ff {
-  float h, l;
-};
-__device__ __forceinline__ ff two_prod(float a, float b) {
-  const float p = a * b;
-  return ff{p, fmaf(a, b, -p)};
-}
-__device__ __forceinline__ ff two_sum(float a, float b) {
-  const float s = a + b, bb = s - a;
-  return ff{s, (a - (s - bb)) + (b - bb)};
-}
-// x*y - u*v for hi/lo operands, to ~2^-44 of the operand magnitudes.
-__device__ __forceinline__ ff ff_dot2(ff x, ff y, ff u, ff v) {
-  const ff p = two_prod(x.h, y.h), q = two_prod(u.h, v.h);
-  const ff s = two_sum(p.h, -q.h);
-  const float lo = s.l + (p.l - q.l) + (fmaf(x.h, y.l, x.l * y.h) - fmaf(u.h, v.l, u.l * v.h));
-  return two_sum(s.h, lo);
-}
-// Rotation of (x1, x2) by the angle whose cos/sin are composed from hi/lo base and offset tables;
-// the result is within ~2^-44 (|x1| + |x2|) of the exact rotation.
-__device__ __forceinline__ void rotate_exact(float x1, float x2, float4 b, float4 o, float& y1, float& y2) {
-  const ff cb{b.x, b.y}, sb{b.z, b.w}, co{o.x, o.y}, so{o.z, o.w};
-  const ff c = ff_dot2(cb, co, sb, so);
-  const ff s = ff_dot2(sb, co, ff{-cb.h, -cb.l}, so);
-  const ff r1 = ff_dot2(ff{x1, 0.f}, c, ff{x2, 0.f}, s);
-  const ff r2 = ff_dot2(ff{x2, 0.f}, c, ff{-x1, 0.f}, s);
-  y1 = r1.h + r1.l;
-  y2 = r2.h + r2.l;
-}
-
 __device__ __forceinline__ float4 lds128f(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
