@@ -695,6 +695,197 @@ def run_kvm_step(args, w):
         dist.destroy_process_group()
 
 
+def run_kvm_tier(args, w):
+    """The decode step with the pages in another tier: FP8 E4M3 pages in HBM (``--kv fp8``: index over the
+    dequantised keys, view gathered with dequantisation) or bf16 pages in pinned host memory (``--kv host``: the
+    view gathered over the host link; the index stays in HBM).  Per layer: [append,] score + select, gather,
+    decode attention over the view."""
+    import torch
+
+    import sparse_attention_decode_04_b300 as K
+    from synth import device as synth_dev
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    host = args.kv == "host"
+    if host:
+        w = w.with_(append_tok=0)  # new tokens' pages would be written to HBM first; the tier holds the history
+    S, L = w.n_sessions, w.n_layers
+    ctx = K.Context.for_workload(w)
+    n_pages = w.n_pages
+    n_hist = w.n_tok - w.append_tok
+    bt = torch.from_numpy(synth.block_table(w)).to(dev)
+    all_pages = torch.arange(n_pages, dtype=torch.int32, device=dev)
+    pools, index, qs, outs = [], [], [], []
+    for layer in range(L):
+        k = torch.empty((n_pages, w.h_kv, BLOCK, w.d), dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        synth_dev.fill_kv_pool(w, layer, bt, k.view(torch.int16), v.view(torch.int16))
+        idx = torch.zeros((S, w.h_kv, w.n_blk, w.d), dtype=torch.float32, device=dev)
+        if host:
+            K.kvm_index_append(ctx, k, n_pages, bt, [0] * S, [n_hist] * S, idx)
+            kh = torch.empty((n_pages, w.h_kv, BLOCK, w.d), dtype=torch.bfloat16, pin_memory=True)
+            vh = torch.empty_like(kh, pin_memory=True)
+            kh.copy_(k)
+            vh.copy_(v)
+            pools.append((kh, vh))
+        else:
+            k8 = torch.empty((n_pages, w.h_kv, BLOCK, w.d), dtype=torch.uint8, device=dev)
+            v8 = torch.empty_like(k8)
+            ks = torch.empty((n_pages, w.h_kv), dtype=torch.float32, device=dev)
+            vs = torch.empty_like(ks)
+            K.kvm_quantize_pages(ctx, k, n_pages, all_pages, k8, ks)
+            K.kvm_quantize_pages(ctx, v, n_pages, all_pages, v8, vs)
+            K.kvm_index_append_fp8(ctx, k8, ks, n_pages, bt, [0] * S, [n_hist] * S, idx)
+            pools.append((k8, ks, v8, vs))
+        torch.cuda.synchronize()
+        del k, v
+        index.append(idx)
+        q = synth.queries(w, layer)
+        qs.append(torch.from_numpy(q[:, 0].view(np.int16)).to(dev).view(torch.bfloat16).contiguous())
+        outs.append(torch.empty((S, w.h_q, w.d), dtype=torch.float32, device=dev))
+    kept = torch.empty((S, w.h_kv, ctx.budget), dtype=torch.int32, device=dev)
+    k_view = torch.empty((S, w.h_kv, BLOCK * ctx.budget, w.d), dtype=torch.bfloat16, device=dev)
+    v_view = torch.empty_like(k_view)
+    view_len = torch.empty((S, w.h_kv), dtype=torch.int32, device=dev)
+    n_tok = [w.n_tok] * S
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+
+    def call_append(layer):
+        if w.append_tok and not host:
+            k8, ks = pools[layer][0], pools[layer][1]
+            K.kvm_index_append_fp8(ctx, k8, ks, n_pages, bt, [n_hist] * S, [w.append_tok] * S, index[layer])
+
+    def call_select(layer):
+        K.kvm_score_select(ctx, qs[layer], 1, index[layer], n_tok, kept)
+
+    def call_gather(layer):
+        if host:
+            K.kvm_materialize_host(ctx, pools[layer][0], pools[layer][1], n_pages, bt, n_tok, kept, k_view, v_view,
+                                   view_len)
+        else:
+            k8, ks, v8, vs = pools[layer]
+            K.kvm_materialize_fp8(ctx, k8, ks, v8, vs, n_pages, bt, n_tok, kept, k_view, v_view, view_len)
+
+    def call_attend(layer):
+        K.kvm_decode_attn(ctx, qs[layer], k_view, v_view, view_len, S, outs[layer])
+
+    def step():
+        for layer in range(L):
+            call_append(layer)
+            call_select(layer)
+            call_gather(layer)
+            call_attend(layer)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+
+    def capture(fn):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=side):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
+    def timed(fn, reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    graph = capture(step)
+    stages = {"score_select": call_select, "gather": call_gather, "decode_attn": call_attend}
+    if w.append_tok and not host:
+        stages["index_append"] = call_append
+    stage_graphs = {n: capture(lambda fn=fn: [fn(layer) for layer in range(L)]) for n, fn in stages.items()}
+    graph.replay()
+    torch.cuda.synchronize()
+    # the host link's own copy bandwidth in this run: pinned host -> device, 1 GiB, best of 3
+    link_gbs = None
+    if host:
+        src = torch.empty(1 << 29, dtype=torch.int16, pin_memory=True)
+        dst = torch.empty(1 << 29, dtype=torch.int16, device=dev)
+        link_gbs = max(src.numel() * 2 / (timed(lambda: dst.copy_(src, non_blocking=True), 1) * 1e-3) / 1e9
+                       for _ in range(3))
+        del src, dst
+    gpu_index = local
+    if os.environ.get("CUDA_VISIBLE_DEVICES"):
+        try:
+            gpu_index = int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local])
+        except ValueError:
+            gpu_index = local
+    sampler = ClockSampler(gpu_index)
+    with sampler:
+        time.sleep(0.3)
+        step_ms = timed(graph.replay, args.steps)
+        stage_ms = {n: timed(g.replay, args.steps) for n, g in stage_graphs.items()}
+    st = K.kvm_device_status(ctx)
+    if st != 0:
+        raise RuntimeError(f"device status 0x{st:x} after the timed region")
+    step_ms = max_over_ranks([step_ms], world, dev)[0]
+    us_layer = step_ms * 1e3 / L
+    gather_us = stage_ms["gather"] * 1e3 / L
+    view_bytes = 2 * w.h_kv * w.view_tokens * w.d * 2 * S            # K and V view written (bf16)
+    if host:
+        src_bytes = 2 * w.h_kv * w.view_tokens * w.d * 2 * S         # kept bf16 rows read over the link
+        achieved = src_bytes / (gather_us * 1e-6) / 1e9
+        roof = {"bound": "host link", "kernel": "kvm_materialize_host (gather_view_kernel, bf16 source)",
+                "achieved": round(achieved, 1), "peak": round(link_gbs, 1),
+                "peak_kind": "measured in this run (pinned host -> device copy of 1 GiB)", "unit": "GB/s",
+                "frac": round(achieved / link_gbs, 4), "traffic": None, "algorithmic_bytes_per_launch": src_bytes,
+                "note": "bytes counted are the kept rows crossing the host link; the view writes go to HBM"}
+    else:
+        peak, peak_kind = load_peaks()
+        q_bytes = 2 * w.h_kv * w.view_tokens * w.d * S + 2 * w.h_kv * w.n_keep * 4 * S   # codes + scales
+        gb = q_bytes + view_bytes
+        achieved = gb / (gather_us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "kernel": "kvm_materialize_fp8 (gather_view_kernel, E4M3 source)",
+                "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None, "algorithmic_bytes_per_launch": gb}
+    if rank == 0:
+        tier = "FP8 E4M3 pages in HBM" if not host else "bf16 pages in pinned host memory"
+        line = {
+            "metric": f"select+materialize+attend step µs per layer at 1M-token history, {tier}",
+            "value": round(us_layer, 2), "unit": "us/layer", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "kv": args.kv, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d,
+                       "history_tokens": w.n_tok, "layers": L, "sessions_per_gpu": S,
+                       "view_tokens": w.view_tokens, "append_tokens": w.append_tok, "cuda_graph": True,
+                       "l2": "inputs larger than L2, no flush", "parallelism": f"replicas x{world}"},
+            "stages_us_per_layer": {n: round(v * 1e3 / L, 2) for n, v in stage_ms.items()},
+            "roofline": roof,
+            "cpu_baseline": None, "e2e": None,
+            # per layer: [append 1,] score 1 + select 1, gather 1, attention 1; the step graph and the stage graphs
+            "gpu_launches": ((1 if (w.append_tok and not host) else 0) + 4) * L * args.steps * 2,
+            "clocks": sampler.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def K_source_hash() -> str:
     import hashlib
     h = hashlib.sha256()
@@ -718,6 +909,9 @@ def main():
     ap.add_argument("--layers", type=int, default=None,
                     help="run only this many layers of the workload (profiling captures; each layer's launches are "
                          "the full-size ones)")
+    ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8", "host"],
+                    help="page tier: bf16 pages in HBM (the method), FP8 E4M3 pages in HBM, or bf16 pages in "
+                         "pinned host memory")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -736,6 +930,8 @@ def main():
         run_reference(args, w)
     elif w.n_q > 1:
         run_kvm_step(args, w)
+    elif args.kv != "bf16":
+        run_kvm_tier(args, w)
     else:
         run_kvm(args, w)
 
