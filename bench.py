@@ -887,11 +887,14 @@ def run_kvm_tier(args, w):
 
 
 def K_source_hash() -> str:
+    """Hash of the sources the view kernel is compiled from: a recorded ncu traffic figure is valid only while
+    these are unchanged."""
     import hashlib
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "sparse_attention_decode_04_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
+    files = [os.path.join(ROOT, "sparse_attention_decode_04_b300", "csrc", f)
+             for f in ("kvm_view.cu", "kvm_device.cuh", "kvm_internal.h")] + [os.path.join(ROOT, "include", "kvm.h")]
+    for f in files:
+        with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 

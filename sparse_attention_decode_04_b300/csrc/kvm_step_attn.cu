@@ -37,7 +37,7 @@ constexpr int kThreads = 64 + 32 * kSoftWarps;  // producer, MMA issuer, softmax
 constexpr int kRows = 128;                      // query rows per CTA (MMA M)
 constexpr int kTile = 64;                       // view tokens per tile (S: N = 64; P.V: K = 64)
 static_assert(kTile == 64, "the softmax reductions are written for 64-token tiles");
-constexpr uint32_t kTmemCols = 512;             // S[2] x 64 columns + O_0, O_1 (128 columns each), padded
+constexpr uint32_t kTmemCols = 512;             // S/P[4] x 64 columns + O_0, O_1 (d columns each)
 
 // Element (r, c) of a [rows][cols] bf16 matrix in the K-major core-matrix layout (cols = K).
 __device__ __forceinline__ int64_t cm_index(int64_t r, int c, int cols) {
@@ -125,11 +125,12 @@ __global__ void __launch_bounds__(256) step_pack_kv_kernel(const uint16_t* __res
   }
 }
 
-constexpr int kStages = 3;  // K tile stages and V tile stages in shared memory
+constexpr int kStages = 4;  // K tile stages and V tile stages in shared memory
+constexpr int kSP = 4;      // S/P buffers in TMEM: two per stream
 
 struct AttnBars {
   uint64_t q_full, k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], drain;
+  uint64_t s_full[kSP], p_full[kSP], pv_done[kSP], drain;
   uint64_t xch[4];  // per lane quarter: both softmax warps have published their row state
 };
 
@@ -140,36 +141,48 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// D[tmem] (+)= A * B^T for one K = 16 slice with A in tensor memory (row i in lane i, two bf16 of
+// consecutive K per 32-bit column: 8 columns per slice) and B described in shared memory.
+__device__ __forceinline__ void mma_bf16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 template <int D>
 constexpr size_t attn_smem_bytes() {
-  return 2 * (size_t)kRows * D * 2 + 2 * (size_t)kStages * kTile * D * 2 + 4 * (size_t)kRows * kTile * 2;
+  return 2 * (size_t)kRows * D * 2 + 2 * (size_t)kStages * kTile * D * 2;
 }
 // dynamic + static (barriers and the row exchange buffer, under 3 KiB) within the 227 KiB a CTA may use
 static_assert(attn_smem_bytes<128>() + 3 * 1024 <= 227 * 1024, "step attention: shared memory per CTA");
 
 // grid (rows_pad / 128, 1, S * h_kv)
 //
-// Pipeline of tile j (stream j & 1 owns S buffer, P buffer, accumulator O and softmax warps; K/V tiles
-// rotate over kStages stages):
-//   MMA issuer:  [S(j) read] S(j+2) = Q K(j+2)^T  ->  [P(j) written]  ->  O_(j&1) += P(j) V(j)
-//   softmax of stream j & 1:  [S(j) done] read S(j), free it; [P.V(j-2) done] rescale O if the maximum rose,
-//                write P(j)
-// so each stream's softmax overlaps the other stream's MMAs.  Every barrier is waited on at most one phase
-// behind its newest completed phase (each buffer's next phase needs a step the waiter has not taken).
+// Pipeline of tile j: stream j & 1 owns the softmax warps and accumulator O of tile j; S(j) and then P(j) live
+// in TMEM buffer j % 4 (two per stream); K/V tiles rotate over kStages stages:
+//   MMA issuer:  [P.V(j-2) done] S(j+2) = Q K(j+2)^T into buffer (j+2) % 4
+//                [P(j) written]  O_(j&1) += P(j) V(j), P read from TMEM
+//   softmax of stream j & 1:  [S(j) done] read S(j); [P.V(j-2) done] rescale O if the maximum rose;
+//                write P(j) over S(j) in TMEM (bf16 part in the first 32 columns, residual in the last 32)
+// so each stream's softmax overlaps the other stream's MMAs, and no probability passes through shared memory.
+// Every barrier is waited on at most one phase behind its newest completed phase (each buffer's next phase
+// needs a step the waiter has not taken).
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
     const uint16_t* __restrict__ q_hi, const uint16_t* __restrict__ q_lo, const uint16_t* __restrict__ k_pk,
     const uint16_t* __restrict__ vt_pk, const int32_t* __restrict__ view_len, int n_q, int rows_pad, int Lcap,
     int64_t l_pad, int h_kv, int h_q, float* __restrict__ out, uint32_t* __restrict__ status) {
-  constexpr uint32_t Q_BYTES = kRows * D * 2, KV_BYTES = kTile * D * 2, P_BYTES = kRows * kTile * 2;
-  constexpr uint32_t SBO_Q = D / 8 * 128, SBO_P = kTile / 8 * 128, LBO = 128;
+  constexpr uint32_t Q_BYTES = kRows * D * 2, KV_BYTES = kTile * D * 2;
+  constexpr uint32_t SBO_Q = D / 8 * 128, SBO_V = kTile / 8 * 128, LBO = 128;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(kRows, kTile), IDESC_O = idesc_bf16_f32(kRows, D);
   extern __shared__ __align__(128) unsigned char smem[];  // no-swizzle operands need 16-byte alignment
   unsigned char* qh_s = smem;
   unsigned char* ql_s = qh_s + Q_BYTES;
   unsigned char* k_s = ql_s + Q_BYTES;            // [kStages] tiles
   unsigned char* v_s = k_s + kStages * KV_BYTES;  // [kStages] tiles (V^T)
-  unsigned char* p_s = v_s + kStages * KV_BYTES;  // [2 buffers][hi, lo] probability tiles
   __shared__ AttnBars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -197,9 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
       mbar_init(&bars.v_full[i], 1);
       mbar_init(&bars.v_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {  // one of each per stream (tile parity)
+    for (int i = 0; i < kSP; ++i) {
       mbar_init(&bars.s_full[i], 1);
-      mbar_init(&bars.s_free[i], kSoftWarps / 2);
       mbar_init(&bars.p_full[i], kSoftWarps / 2);
       mbar_init(&bars.pv_done[i], 1);
     }
@@ -211,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tm_o = tmem + 2 * kTile;  // O_0 (even tiles), then O_1 (odd tiles)
+  const uint32_t tm_o = tmem + kSP * kTile;  // O_0 (even tiles), then O_1 (odd tiles)
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
@@ -251,12 +263,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
     for (int i = max(0, nv - kStages); i < nv; ++i) mbar_wait(&bars.v_full[i % kStages], (i / kStages) & 1, status);
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    const uint32_t qh_a = smem_addr(qh_s), ql_a = smem_addr(ql_s), p_a = smem_addr(p_s);
-    // S(j) into the S buffer of stream j & 1, once that stream's softmax has read S(j - 2)
+    const uint32_t qh_a = smem_addr(qh_s), ql_a = smem_addr(ql_s);
+    // S(j) into TMEM buffer j % 4 once P.V(j - 4), the last reader of that buffer, is done
     auto issue_s = [&](int j) -> bool {
-      const int sk = j % kStages, sb = j & 1;
+      const int sk = j % kStages, sb = j % kSP;
       if (!mbar_wait(&bars.k_full[sk], (j / kStages) & 1, status)) return false;
-      if (j >= 2 && !mbar_wait(&bars.s_free[sb], ((j >> 1) - 1) & 1, status)) return false;
+      if (j >= kSP && !mbar_wait(&bars.pv_done[sb], (j / kSP - 1) & 1, status)) return false;
       tc_fence_after();
       const uint32_t k_a = smem_addr(k_s + sk * KV_BYTES);
 #pragma unroll
@@ -274,25 +286,23 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
     bool ok = mbar_wait(&bars.q_full, 0, status);
     for (int j = 0; ok && j < 2 && j < nt; ++j) ok = issue_s(j);
     for (int j = 0; ok && j < nt && !abort_flag; ++j) {
-      const int sv = j % kStages, pb = j & 1;
-      // S(j + 2) as soon as the softmax has read S(j): it runs ahead of P.V(j) on the tensor pipe
+      const int sv = j % kStages, pb = j % kSP;
       if (j + 2 < nt && !issue_s(j + 2)) {
         ok = false;
         break;
       }
-      if (!mbar_wait(&bars.p_full[pb], (j >> 1) & 1, status) || !mbar_wait(&bars.v_full[sv], (j / kStages) & 1, status)) {
+      if (!mbar_wait(&bars.p_full[pb], (j / kSP) & 1, status) || !mbar_wait(&bars.v_full[sv], (j / kStages) & 1, status)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const uint32_t v_a = smem_addr(v_s + sv * KV_BYTES);
-      const uint32_t ph_a = p_a + pb * 2 * P_BYTES, pl_a = ph_a + P_BYTES;
-      const uint32_t o = tm_o + pb * D;  // this tile's stream accumulator
+      const uint32_t p_t = tmem + pb * kTile;  // P(j): bf16 part in columns 0..31, residual in 32..63
+      const uint32_t o = tm_o + (j & 1) * D;   // this tile's stream accumulator
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk) {
-        mma_bf16(o, smem_desc(ph_a + kk * 256, LBO, SBO_P), smem_desc(v_a + kk * 256, LBO, SBO_P), IDESC_O,
-                 (j >= 2 || kk > 0));
-        mma_bf16(o, smem_desc(pl_a + kk * 256, LBO, SBO_P), smem_desc(v_a + kk * 256, LBO, SBO_P), IDESC_O, 1);
+        mma_bf16_tmem_a(o, p_t + kk * 8, smem_desc(v_a + kk * 256, LBO, SBO_V), IDESC_O, (j >= 2 || kk > 0));
+        mma_bf16_tmem_a(o, p_t + kTile / 2 + kk * 8, smem_desc(v_a + kk * 256, LBO, SBO_V), IDESC_O, 1);
       }
       mma_commit(&bars.pv_done[pb]);
       mma_commit(&bars.v_empty[sv]);
@@ -314,12 +324,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
     const int pos = valid_row ? L - n_q + t : -1;  // this row's view position; it attends slots <= pos
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint32_t my_o = tm_o + lane_base + stream * D;
-    const uint32_t my_s = tmem + lane_base + stream * kTile;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = stream; j < nt; j += 2) {
-      const int ph = (j >> 1) & 1;  // phase of this stream's barriers for tile j
-      if (__any_sync(0xffffffffu, abort_flag) || !mbar_wait_warp(&bars.s_full[stream], ph, status)) {
+      const int sb = j % kSP;
+      const uint32_t my_s = tmem + lane_base + sb * kTile;
+      if (__any_sync(0xffffffffu, abort_flag) || !mbar_wait_warp(&bars.s_full[sb], (j / kSP) & 1, status)) {
         ok = false;
         break;
       }
@@ -328,9 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
       tmem_ld32(my_s, sv[0]);
       tmem_ld32(my_s + 32, sv[1]);
       tmem_wait_ld();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.s_free[stream]);
       const int tok0 = j * kTile;
       float x[kTile];
       if (__all_sync(0xffffffffu, tok0 + kTile - 1 <= pos)) {  // no masked column in this tile
@@ -352,12 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
       // raise the reference only when it grows by more than 8 (a factor 256): O is then rescaled in TMEM
       const float m_new = (mt > m + 8.f) ? mt : m;
       const float corr = m_new == m ? 1.f : fast_exp2(m - m_new);  // 0 while m was -inf
-      // P.V(j - 2), the stream's last, has read its P buffer and finished with its accumulator
-      if (j >= 2 && !mbar_wait_warp(&bars.pv_done[stream], ph ^ 1, status)) {
-        ok = false;
-        break;
-      }
       if (j >= 2 && __any_sync(0xffffffffu, m_new != m)) {
+        // the stream's accumulator must be quiescent: P.V(j - 2), its last, is done
+        if (!mbar_wait_warp(&bars.pv_done[(j - 2) % kSP], ((j - 2) / kSP) & 1, status)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -368,34 +375,27 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
           for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * corr);
           tmem_st32(my_o + cc * 32, ov);
         }
-        tmem_wait_st();
-        tc_fence_before();
       }
       l *= corr;
       m = m_new;
-      // P = exp2(S - m), split into bf16 + residual, written in the core-matrix layout (rows x 64 tokens)
-      unsigned char* pbh = p_s + stream * 2 * P_BYTES;
-      unsigned char* pbl = pbh + P_BYTES;
+      // P = exp2(S - m), split into bf16 + residual, written over S(j): two bf16 of consecutive tokens per column
       const bool live = m != -INFINITY;  // padding rows: zeros
       float ls[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums (short dependency chains)
+      uint32_t ph[kTile / 2], pl[kTile / 2];
 #pragma unroll
-      for (int c8 = 0; c8 < kTile / 8; ++c8) {
-        uint32_t wh[4], wl[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float p0 = live ? fast_exp2(x[8 * c8 + 2 * u] - m) : 0.f;
-          const float p1 = live ? fast_exp2(x[8 * c8 + 2 * u + 1] - m) : 0.f;
-          ls[u] += p0 + p1;
-          wh[u] = pack_bf16x2(p0, p1);
-          wl[u] = pack_bf16x2(p0 - bf16lo(wh[u]), p1 - bf16hi(wh[u]));
-        }
-        const int64_t e = cm_index(r, 8 * c8, kTile) * 2;
-        *reinterpret_cast<uint4*>(pbh + e) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
-        *reinterpret_cast<uint4*>(pbl + e) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+      for (int c = 0; c < kTile / 2; ++c) {
+        const float p0 = live ? fast_exp2(x[2 * c] - m) : 0.f;
+        const float p1 = live ? fast_exp2(x[2 * c + 1] - m) : 0.f;
+        ls[c & 3] += p0 + p1;
+        ph[c] = pack_bf16x2(p0, p1);
+        pl[c] = pack_bf16x2(p0 - bf16lo(ph[c]), p1 - bf16hi(ph[c]));
       }
-      fence_proxy_async_smem();
+      tmem_st32(my_s, ph);
+      tmem_st32(my_s + kTile / 2, pl);
+      tmem_wait_st();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars.p_full[stream]);
+      if (lane == 0) mbar_arrive(&bars.p_full[sb]);
       l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
     }
     if (!ok) abort_flag = 1;
@@ -407,13 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.xch[quarter]);
       const int last = (nt - 1) - ((nt - 1 - stream) & 1);  // this stream's last tile
+      const int other_last = (nt - 1) - ((nt - 1 - (stream ^ 1)) & 1);
+      // both streams' accumulators are read: wait for each stream's last P.V
       ok = mbar_wait_warp(&bars.xch[quarter], 0, status) &&
-           (last < 0 || mbar_wait_warp(&bars.pv_done[stream], (last >> 1) & 1, status));
-      if (ok) {
-        // the other stream's accumulator is read too: wait for its last P.V as well
-        const int other_last = (nt - 1) - ((nt - 1 - (stream ^ 1)) & 1);
-        ok = other_last < 0 || mbar_wait_warp(&bars.pv_done[stream ^ 1], (other_last >> 1) & 1, status);
-      }
+           (last < 0 || mbar_wait_warp(&bars.pv_done[last % kSP], (last / kSP) & 1, status)) &&
+           (other_last < 0 || mbar_wait_warp(&bars.pv_done[other_last % kSP], (other_last / kSP) & 1, status));
       if (ok) {
         tc_fence_after();
         const float m0 = xval[0][0][r], m1 = xval[0][1][r];
