@@ -789,6 +789,14 @@ def run_kvm_tier(args, w):
         step()
     torch.cuda.synchronize()
     assert K.kvm_device_status(ctx) == 0
+    if args.profile_step:
+        torch.cuda.profiler.start()
+        step()
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        if rank == 0:
+            print(json.dumps({"profile_step": w.name, "kv": args.kv}), flush=True)
+        return
     side = torch.cuda.Stream()
     side.wait_stream(stream)
 
