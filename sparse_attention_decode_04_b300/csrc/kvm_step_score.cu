@@ -27,7 +27,8 @@
 namespace kvm {
 namespace {
 
-constexpr int kThreads = 192;   // 6 warps
+constexpr int kEpiWarps = 8;    // epilogue: two warps per TMEM lane quarter, each taking half of a tile's columns
+constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA issuer, epilogue
 constexpr int kRowsM = 128;     // MMA M
 constexpr int kColsN = 256;     // MMA N
 constexpr uint32_t kTmemCols = 512;
@@ -85,7 +86,7 @@ __device__ __forceinline__ void init_bars(Bars& b) {
     mbar_init(&b.b_full[i], 1);
     mbar_init(&b.b_empty[i], 1);
     mbar_init(&b.d_full[i], 1);
-    mbar_init(&b.d_empty[i], 4);
+    mbar_init(&b.d_empty[i], kEpiWarps);
   }
   mbar_fence_init();
 }
@@ -107,6 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ float2 half_state[2][kRowsM];  // each column half's (max, sum) per row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sg = blockIdx.z, s = sg / h_kv;
@@ -171,9 +173,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
     }
     if (j > 0) mbar_wait(&bars.d_full[(j - 1) & 1], ((j - 1) >> 1) & 1, status);  // last MMAs done
   } else if (warp >= 2) {
-    // epilogue: one query row per thread
-    const int quarter = warp & 3;
-    const int row = row0 + quarter * 32 + lane;
+    // epilogue: one query row per thread, half of each tile's columns per warp
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     float m = -INFINITY, z = 0.f;
     for (int j = 0; j < nt; ++j) {
       const int st = j & 1;
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
       tc_fence_after();
       const int col0 = (j0 + j) * kColsN;
 #pragma unroll 1
-      for (int cc = 0; cc < kColsN / 32; ++cc) {
+      for (int cc = half * (kColsN / 64); cc < (half + 1) * (kColsN / 64); ++cc) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + st * kColsN + cc * 32, v);
         tmem_wait_ld();
@@ -207,10 +208,19 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.d_empty[st]);
     }
-    if (row < rows_pad) part[((int64_t)sg * n_ranges + blockIdx.y) * rows_pad + row] = make_float2(m, z);
+    half_state[half][quarter * 32 + lane] = make_float2(m, z);
   }
   tc_fence_before();
   __syncthreads();
+  if (warp >= 2 && warp < 6) {  // the two column halves of each row: (max, sum) combined
+    const int r = (warp & 3) * 32 + lane, row = row0 + r;
+    const float2 p0 = half_state[0][r], p1 = half_state[1][r];
+    const float M = fmaxf(p0.x, p1.x);
+    const float z = M == -INFINITY ? 0.f
+                                   : (p0.x == -INFINITY ? 0.f : p0.y * fast_exp2(p0.x - M)) +
+                                         (p1.x == -INFINITY ? 0.f : p1.y * fast_exp2(p1.x - M));
+    if (row < rows_pad) part[((int64_t)sg * n_ranges + blockIdx.y) * rows_pad + row] = make_float2(M, z);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -255,6 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
+  __shared__ float half_acc[2][kRowsM];  // each half's partial group score per block
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sg = blockIdx.z, s = sg / h_kv;
@@ -315,8 +326,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
     }
     if (j > 0) mbar_wait(&bars.d_full[(j - 1) & 1], ((j - 1) >> 1) & 1, status);
   } else if (warp >= 2) {
-    const int quarter = warp & 3;
-    const int blk = blk0 + quarter * 32 + lane;
+    // one block per thread, half of each tile's query rows per warp
+    const int quarter = warp & 3, half = (warp - 2) >> 2;
     float acc = 0.f;
     for (int j = 0; j < nchunk; ++j) {
       const int st = j & 1;
@@ -326,7 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int cc = 0; cc < kColsN / 32; ++cc) {
+      for (int cc = half * (kColsN / 64); cc < (half + 1) * (kColsN / 64); ++cc) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + st * kColsN + cc * 32, v);
         tmem_wait_ld();
@@ -341,10 +352,14 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars.d_empty[st]);
     }
-    if (blk < n_blk) gs_out[(int64_t)sg * max_blocks + blk] = acc;
+    half_acc[half][quarter * 32 + lane] = acc;
   }
   tc_fence_before();
   __syncthreads();
+  if (warp >= 2 && warp < 6) {  // the two halves of the query rows summed
+    const int r = (warp & 3) * 32 + lane, blk = blk0 + r;
+    if (blk < n_blk) gs_out[(int64_t)sg * max_blocks + blk] = half_acc[0][r] + half_acc[1][r];
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
