@@ -202,16 +202,19 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
     c.step_rows_cap_pad = (int)(((int64_t)p->max_queries * c.group + 255) / 256 * 256);
     const size_t SG = S * p->h_kv;
     c.attn_l_pad = ((int64_t)kvm::kBlock * c.budget + 63) / 64 * 64;
-    const size_t sz[8] = {SG * c.step_blk_cap_pad * p->d * 2,
+    c.attn_units_cap = 8 * c.num_sms;
+    const size_t sz[10] = {SG * c.step_blk_cap_pad * p->d * 2,
                           SG * c.step_rows_cap_pad * p->d * 2,
                           SG * kvm::kStepMaxRanges * c.step_rows_cap_pad * sizeof(float2),
                           SG * c.step_rows_cap_pad * sizeof(float2),
                           SG * p->max_blocks * sizeof(float),
                           2 * SG * c.step_rows_cap_pad * p->d * 2,
                           SG * c.attn_l_pad * p->d * 2,
-                          SG * c.attn_l_pad * p->d * 2};
-    void* q5[8] = {};
-    for (int i = 0; i < 8 && e == cudaSuccess; ++i) e = cudaMalloc(&q5[i], sz[i]);
+                          SG * c.attn_l_pad * p->d * 2,
+                          (size_t)c.attn_units_cap * 128 * (p->d + 2) * sizeof(float),
+                          (size_t)c.attn_units_cap * sizeof(uint32_t)};
+    void* q5[10] = {};
+    for (int i = 0; i < 10 && e == cudaSuccess; ++i) e = cudaMalloc(&q5[i], sz[i]);
     c.step_kpk = (uint16_t*)q5[0];
     c.step_qpk = (uint16_t*)q5[1];
     c.step_part = (float2*)q5[2];
@@ -220,6 +223,9 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
     c.attn_q = (uint16_t*)q5[5];
     c.attn_kpk = (uint16_t*)q5[6];
     c.attn_vtpk = (uint16_t*)q5[7];
+    c.attn_part = (float*)q5[8];
+    c.attn_cnt = (uint32_t*)q5[9];
+    if (e == cudaSuccess) e = cudaMemset(c.attn_cnt, 0, sz[9]);
     for (size_t b : sz) c.bytes += b;
     if (e != cudaSuccess) {
       kvm_destroy(ctx);
@@ -245,9 +251,9 @@ kvm_status kvm_destroy(kvm_ctx* ctx) {
   cudaGetDevice(&prev);
   if (prev != c.device) cudaSetDevice(c.device);
   cudaError_t e = cudaDeviceSynchronize();
-  void* ptrs[17] = {c.e_buf,      c.part,       c.rec,      c.rope_base, c.rope_off,   c.status,  c.rope_base_lo,
+  void* ptrs[19] = {c.e_buf,      c.part,       c.rec,      c.rope_base, c.rope_off,   c.status,  c.rope_base_lo,
                     c.rope_off_lo, c.step_kpk,   c.step_qpk, c.step_part, c.step_stats, c.step_gs, c.seg_count,
-                    c.attn_q,      c.attn_kpk,   c.attn_vtpk};
+                    c.attn_q,      c.attn_kpk,   c.attn_vtpk, c.attn_part, c.attn_cnt};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   if (prev >= 0 && prev != c.device) cudaSetDevice(prev);
@@ -510,6 +516,8 @@ kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* s
   // a stopped view kernel may have left segment arrival counters behind: clearing restarts them
   if (e == cudaSuccess && clear && *out != 0)
     e = cudaMemset(ctx->c.seg_count, 0, sizeof(uint32_t) * ctx->c.p.max_sessions * ctx->c.p.h_kv);
+  if (e == cudaSuccess && clear && *out != 0 && ctx->c.attn_cnt)
+    e = cudaMemset(ctx->c.attn_cnt, 0, sizeof(uint32_t) * ctx->c.attn_units_cap);
   if (e != cudaSuccess) return cuda_fail(e, "kvm_device_status");
   if (*out == 0) return KVM_OK;
   if (*out & KVM_DEV_TIMEOUT) return fail(KVM_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", *out);

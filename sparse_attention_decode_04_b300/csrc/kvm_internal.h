@@ -60,6 +60,9 @@ struct Ctx {
   uint16_t* attn_q = nullptr;     // rotated, scaled query rows, bf16 part then residual: [2][S*h_kv][rows][d]
   uint16_t* attn_kpk = nullptr;   // view keys, core-matrix order [S*h_kv][attn_l_pad][d]
   uint16_t* attn_vtpk = nullptr;  // view values transposed per 64-token tile [S*h_kv][attn_l_pad / 64][d][64]
+  int attn_units_cap = 0;         // (row tile, view chunk) units a split step-attention call may use
+  float* attn_part = nullptr;     // per unit: unnormalised O [128][d], then (max, sum) [128][2]
+  uint32_t* attn_cnt = nullptr;   // per (KV head, row tile): chunks done (0 between calls)
 };
 
 constexpr int kStepMaxRanges = 64;

@@ -159,7 +159,9 @@ constexpr size_t attn_smem_bytes() {
 // dynamic + static (barriers and the row exchange buffer, under 3 KiB) within the 227 KiB a CTA may use
 static_assert(attn_smem_bytes<128>() + 3 * 1024 <= 227 * 1024, "step attention: shared memory per CTA");
 
-// grid (rows_pad / 128, 1, S * h_kv)
+// grid (rows_pad / 128, chunks, S * h_kv): CTA (x, y, z) attends row tile x of KV head z over the view tiles
+// of chunk y; with more than one chunk each CTA leaves an unnormalised partial state (O, max, sum) and the CTA
+// completing a row tile merges the partials.
 //
 // Pipeline of tile j: stream j & 1 owns the softmax warps and accumulator O of tile j; S(j) and then P(j) live
 // in TMEM buffer j % 4 (two per stream); K/V tiles rotate over kStages stages:
@@ -174,7 +176,8 @@ template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
     const uint16_t* __restrict__ q_hi, const uint16_t* __restrict__ q_lo, const uint16_t* __restrict__ k_pk,
     const uint16_t* __restrict__ vt_pk, const int32_t* __restrict__ view_len, int n_q, int rows_pad, int Lcap,
-    int64_t l_pad, int h_kv, int h_q, float* __restrict__ out, uint32_t* __restrict__ status) {
+    int64_t l_pad, int h_kv, int h_q, int kv_chunk, float* __restrict__ part, uint32_t* __restrict__ cnt,
+    float* __restrict__ out, uint32_t* __restrict__ status) {
   constexpr uint32_t Q_BYTES = kRows * D * 2, KV_BYTES = kTile * D * 2;
   constexpr uint32_t SBO_Q = D / 8 * 128, SBO_V = kTile / 8 * 128, LBO = 128;
   constexpr uint32_t IDESC_S = idesc_bf16_f32(kRows, kTile), IDESC_O = idesc_bf16_f32(kRows, D);
@@ -195,7 +198,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
   const int L = clamp_view_len(view_len[sg], n_q, Lcap);
   // tiles up to the last view position any row of this CTA attends (the step's token rows are ordered by t)
   const int last_row = min(n_q * G, row0 + kRows) - 1;
-  const int nt = (L - n_q + last_row / G + kTile) / kTile;
+  const int nt_full = (L - n_q + last_row / G + kTile) / kTile;
+  // this CTA's chunk of the row tile's view tiles: [kv0, kv0 + nt)
+  const int splits = gridDim.y, kv0 = blockIdx.y * kv_chunk;
+  const int nt = min(nt_full - kv0, kv_chunk);
+  if (nt <= 0) return;  // past the view: the chunk count of this row tile does not include it
+  __shared__ int s_last;
 
   if (warp == 1) {
     tmem_alloc(&tmem_slot, kTmemCols);
@@ -240,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
           break;
         }
         mbar_arrive_expect_tx(&bars.k_full[sk], KV_BYTES);
-        bulk_g2s(k_s + sk * KV_BYTES, k_pk + ((int64_t)sg * l_pad + (int64_t)i * kTile) * D, KV_BYTES,
+        bulk_g2s(k_s + sk * KV_BYTES, k_pk + ((int64_t)sg * l_pad + (int64_t)(kv0 + i) * kTile) * D, KV_BYTES,
                  &bars.k_full[sk]);
         nk = i + 1;
       }
@@ -252,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
           break;
         }
         mbar_arrive_expect_tx(&bars.v_full[sv], KV_BYTES);
-        bulk_g2s(v_s + sv * KV_BYTES, vt_pk + ((int64_t)sg * (l_pad / kTile) + jv) * kTile * D, KV_BYTES,
+        bulk_g2s(v_s + sv * KV_BYTES, vt_pk + ((int64_t)sg * (l_pad / kTile) + kv0 + jv) * kTile * D, KV_BYTES,
                  &bars.v_full[sv]);
         nv = jv + 1;
       }
@@ -338,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
       tmem_ld32(my_s, sv[0]);
       tmem_ld32(my_s + 32, sv[1]);
       tmem_wait_ld();
-      const int tok0 = j * kTile;
+      const int tok0 = (kv0 + j) * kTile;
       float x[kTile];
       if (__all_sync(0xffffffffu, tok0 + kTile - 1 <= pos)) {  // no masked column in this tile
 #pragma unroll
@@ -419,9 +427,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
         const float f0 = m0 == -INFINITY ? 0.f : fast_exp2(m0 - M), f1 = m1 == -INFINITY ? 0.f : fast_exp2(m1 - M);
         const float lt = xval[1][0][r] * f0 + xval[1][1][r] * f1;
         const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        const float w0 = f0 * inv, w1 = f1 * inv;
+        const bool split = splits > 1;  // a chunk of the row: unnormalised partial state, merged below
+        const float w0 = split ? f0 : f0 * inv, w1 = split ? f1 : f1 * inv;
         const bool use1 = nt > 1;  // O_1 holds data only when the odd stream had a tile
-        float* dst = out + (((int64_t)s * n_q + t) * h_q + g * G + hh) * D;
+        float* pu = part + ((int64_t)(sg * gridDim.x + blockIdx.x) * splits + blockIdx.y) * (kRows * (D + 2));
+        if (split && stream == 0) *reinterpret_cast<float2*>(pu + kRows * D + 2 * r) = make_float2(M, lt);
+        float* dst = split ? pu + (int64_t)r * D : out + (((int64_t)s * n_q + t) * h_q + g * G + hh) * D;
         // the two warps of a quarter split the d columns
 #pragma unroll 1
         for (int cc = stream * (D / 64); cc < (stream + 1) * (D / 64); ++cc) {
@@ -429,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
           tmem_ld32(tm_o + lane_base + cc * 32, o0);
           tmem_ld32(tm_o + lane_base + D + cc * 32, o1);
           tmem_wait_ld();
-          if (valid_row) {
+          if (valid_row || split) {
 #pragma unroll
             for (int i = 0; i < 32; i += 4) {
               float4 v;
@@ -444,11 +455,48 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
       }
     }
   }
+  if (splits > 1) __threadfence();  // this thread's partial rows, before the chunk is counted
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if (splits > 1) {
+    // the CTA that completes a row tile's chunks merges them (no CTA waits on another)
+    const int rt_id = sg * gridDim.x + blockIdx.x;
+    const int expected = (nt_full + kv_chunk - 1) / kv_chunk;
+    if (tid == 0) s_last = atomicAdd(&cnt[rt_id], 1u) + 1 == (uint32_t)expected;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const float* pr = part + (int64_t)rt_id * splits * (kRows * (D + 2));
+      for (int item = tid; item < kRows * (D / 4); item += kThreads) {
+        const int r = item / (D / 4), c4 = item % (D / 4), row = row0 + r;
+        if (row >= n_q * G) continue;
+        float Mx = -INFINITY;
+        for (int k = 0; k < expected; ++k) Mx = fmaxf(Mx, __ldcg(pr + (int64_t)k * (kRows * (D + 2)) + kRows * D + 2 * r));
+        float Ls = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < expected; ++k) {
+          const float* pk = pr + (int64_t)k * (kRows * (D + 2));
+          const float2 ml = __ldcg(reinterpret_cast<const float2*>(pk + kRows * D + 2 * r));
+          if (ml.x == -INFINITY) continue;
+          const float w = fast_exp2(ml.x - Mx);
+          Ls += w * ml.y;
+          const float4 o = __ldcg(reinterpret_cast<const float4*>(pk + (int64_t)r * D) + c4);
+          acc.x += w * o.x;
+          acc.y += w * o.y;
+          acc.z += w * o.z;
+          acc.w += w * o.w;
+        }
+        const float inv = Ls > 0.f ? 1.f / Ls : 0.f;
+        const int t = row / G, hh = row % G;
+        reinterpret_cast<float4*>(out + (((int64_t)s * n_q + t) * h_q + g * G + hh) * D)[c4] =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+      }
+      if (tid == 0) cnt[rt_id] = 0;  // ready for the next call
+    }
   }
 }
 
@@ -472,9 +520,27 @@ cudaError_t launch_dg(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* 
   const size_t smem = attn_smem_bytes<D>();
   auto ka = step_attn_kernel<D, G>;
   if ((e = ensure_smem(ka, c.device, smem)) != cudaSuccess) return e;
-  return launch_pdl(ka, dim3(rows_pad / kRows, 1, SG), dim3(kThreads), smem, st, 1, (const uint16_t*)c.attn_q,
-                    (const uint16_t*)(c.attn_q + (int64_t)SG * rows_pad * D), (const uint16_t*)c.attn_kpk, (const uint16_t*)c.attn_vtpk, view_len,
-                    n_q, rows_pad, Lcap, l_pad, c.p.h_kv, c.p.h_q, out, c.status);
+  // Split each row tile's view tiles into chunks when the row tiles alone leave SMs idle: the chunk count
+  // minimises (CTA waves) x (chunk length + a fixed cost per chunk), within the partial-state scratch.
+  const int rt = rows_pad / kRows * SG;
+  const int tiles_max = (Lcap + kTile - 1) / kTile;
+  int splits = 1;
+  if (2 * rt <= c.attn_units_cap && rt < c.num_sms) {
+    double best = 1e30;
+    for (int sp = 1; sp <= 16 && sp * rt <= c.attn_units_cap && sp <= tiles_max; ++sp) {
+      const double waves = (double)((rt * sp + c.num_sms - 1) / c.num_sms);
+      const double cost = waves * (1.0 / sp + 0.03);
+      if (cost < best - 1e-9) {
+        best = cost;
+        splits = sp;
+      }
+    }
+  }
+  const int kv_chunk = (tiles_max + splits - 1) / splits;
+  return launch_pdl(ka, dim3(rows_pad / kRows, splits, SG), dim3(kThreads), smem, st, 1, (const uint16_t*)c.attn_q,
+                    (const uint16_t*)(c.attn_q + (int64_t)SG * rows_pad * D), (const uint16_t*)c.attn_kpk,
+                    (const uint16_t*)c.attn_vtpk, view_len, n_q, rows_pad, Lcap, l_pad, c.p.h_kv, c.p.h_q, kv_chunk,
+                    c.attn_part, c.attn_cnt, out, c.status);
 }
 
 template <int D>
