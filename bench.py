@@ -418,13 +418,23 @@ def run_kvm(args, w):
                 kp[layer][p0:p0 + app_blocks].copy_(new_k[layer], non_blocking=True)
                 vp[layer][p0:p0 + app_blocks].copy_(new_v[layer], non_blocking=True)
 
+        # The new pages' copies run on a stream of their own, back to back on the copy engine: queued behind
+        # the appends they would wait for SM room (the view kernel holds every SM while it runs).
+        copy_stream = torch.cuda.Stream()
+        copy_done = [torch.cuda.Event() for _ in range(L)]
+
         def e2e_step():
             q_dev.copy_(q_host, non_blocking=True)
-            if w.append_tok:
-                appends_ahead(copy_new_pages)   # H2D of the new pages + appends, on the side stream
-            else:
+            copy_stream.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(copy_stream):
                 for layer in range(L):
                     copy_new_pages(layer)
+                    copy_done[layer].record(copy_stream)
+            if w.append_tok:
+                appends_ahead(lambda layer: app_stream.wait_event(copy_done[layer]))
+            else:
+                for layer in range(L):
+                    torch.cuda.current_stream().wait_event(copy_done[layer])
             layers_after_appends(
                 lambda layer: (K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept[layer])
                                if args.selection == "kvmem" else call_select(layer)),
@@ -432,6 +442,7 @@ def run_kvm(args, w):
                                                      q_dev[layer], k_view, v_view, view_len, outs[layer]))
             for layer in range(L):
                 out_host[layer].copy_(outs[layer], non_blocking=True)
+            torch.cuda.current_stream().wait_stream(copy_stream)
 
         for _ in range(2):
             e2e_step()
