@@ -906,15 +906,18 @@ def run_kvm_tier(args, w):
 
 
 def K_source_hash() -> str:
-    """Hash of the sources the view kernel is compiled from: a recorded ncu traffic figure is valid only while
-    these are unchanged."""
+    """Hash of the code (comments and whitespace dropped) the view kernel is compiled from: a recorded ncu
+    traffic figure is valid only while it is unchanged."""
     import hashlib
+    import re
     h = hashlib.sha256()
     files = [os.path.join(ROOT, "sparse_attention_decode_04_b300", "csrc", f)
              for f in ("kvm_view.cu", "kvm_device.cuh", "kvm_internal.h")] + [os.path.join(ROOT, "include", "kvm.h")]
     for f in files:
-        with open(f, "rb") as fh:
-            h.update(fh.read())
+        with open(f) as fh:
+            code = re.sub(r"/\*.*?\*/", " ", fh.read(), flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

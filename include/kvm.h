@@ -333,7 +333,7 @@ kvm_status kvm_select_control(kvm_ctx* ctx, int32_t control, const uint16_t* q, 
 kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* stream);
 
 /*
- * Allocation-free score and select for one decode query.  The paper has no
+ * Allocation-free score and select for one decode query.  The method has no
  * counterpart: this entry point exists for callers that cannot allocate device
  * memory, for example a runtime whose memory pool owns every device byte, or
  * code that must not synchronise the device (cudaMalloc and cudaFree may), and

@@ -71,7 +71,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return false;
 }
 
-// mbar_wait by all 32 lanes of a warp with one verdict for the warp: lanes that go on to warp-collective
+// mbar_wait by all 32 lanes of a warp with one outcome for the warp: lanes that go on to warp-collective
 // instructions (tcgen05.ld, shuffles) must not split when a wait gives up just as the phase completes.
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* status) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, status));
