@@ -263,7 +263,8 @@ def run_kvm(args, w):
     torch.cuda.synchronize()
     assert K.kvm_device_status(ctx) == 0
     n_tok = [w.n_tok] * S
-    launches_per_layer = (1 if w.append_tok else 0) + 2 + 2
+    # [append,] score + select (recent-only: one kernel), the fused view kernel
+    launches_per_layer = (1 if w.append_tok else 0) + (1 if args.selection == "recent" else 2) + 1
 
     def call_append(layer):
         if w.append_tok:
