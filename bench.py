@@ -243,7 +243,9 @@ def run_kvm(args, w):
     n_pages = w.n_pages
     n_hist = w.n_tok - w.append_tok
     bt = torch.from_numpy(synth.block_table(w)).to(dev)
-    kp, vp, index, qs, outs = [], [], [], [], []
+    kp, vp, index, qs = [], [], [], []
+    out_all = torch.empty((L, S, w.h_q, w.d), dtype=torch.float32, device=dev)  # every layer's output, contiguous
+    outs = [out_all[layer] for layer in range(L)]
     for layer in range(L):
         k = torch.empty((n_pages, w.h_kv, BLOCK, w.d), dtype=torch.bfloat16, device=dev)
         v = torch.empty_like(k)
@@ -255,7 +257,6 @@ def run_kvm(args, w):
         idx = torch.zeros((S, w.h_kv, w.n_blk, w.d), dtype=torch.float32, device=dev)
         K.kvm_index_append(ctx, k, n_pages, bt, [0] * S, [n_hist] * S, idx)  # the history before this step
         index.append(idx)
-        outs.append(torch.empty((S, w.h_q, w.d), dtype=torch.float32, device=dev))
     kept = [torch.empty((S, w.h_kv, ctx.budget), dtype=torch.int32, device=dev) for _ in range(L)]
     k_view = torch.empty((S, w.h_kv, BLOCK * ctx.budget, w.d), dtype=torch.bfloat16, device=dev)
     v_view = torch.empty_like(k_view)
@@ -441,8 +442,7 @@ def run_kvm(args, w):
                                if args.selection == "kvmem" else call_select(layer)),
                 lambda layer: K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer],
                                                      q_dev[layer], k_view, v_view, view_len, outs[layer]))
-            for layer in range(L):
-                out_host[layer].copy_(outs[layer], non_blocking=True)
+            out_host.copy_(out_all, non_blocking=True)  # one read-back of every layer's output
             torch.cuda.current_stream().wait_stream(copy_stream)
 
         for _ in range(2):
