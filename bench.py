@@ -475,19 +475,7 @@ def run_kvm(args, w):
         cpu = {"value": round(per_head_s * w.h_kv * w.n_sessions * 1e6, 1), "unit": "us/layer", "cores": threads,
                "kind": "oracle", "sample": desc}
 
-    traffic = None
-    prof_dir = os.path.join(ROOT, "profiles")
-    want_hash = K_source_hash()
-    for fn in sorted(os.listdir(prof_dir)) if os.path.isdir(prof_dir) else []:
-        if not fn.endswith(".md"):
-            continue
-        with open(os.path.join(prof_dir, fn)) as f:
-            for ln in f:
-                parts = ln.split()
-                if len(parts) >= 5 and parts[0] == "traffic" and parts[1] == w.name:
-                    kv = dict(p.split("=", 1) for p in parts[3:] if "=" in p)
-                    if kv.get("source_hash") == want_hash:
-                        traffic = int(kv["bytes_per_launch"])
+    traffic = recorded_traffic(w.name, "view_kernel", VIEW_KERNEL_SOURCES)
 
     if rank == 0:
         line = {
@@ -763,6 +751,7 @@ def run_kvm_tier(args, w):
         q = synth.queries(w, layer)
         qs.append(torch.from_numpy(q[:, 0].view(np.int16)).to(dev).view(torch.bfloat16).contiguous())
         outs.append(torch.empty((S, w.h_q, w.d), dtype=torch.float32, device=dev))
+    torch.cuda.empty_cache()  # the bf16 pools were temporaries
     kept = torch.empty((S, w.h_kv, ctx.budget), dtype=torch.int32, device=dev)
     k_view = torch.empty((S, w.h_kv, BLOCK * ctx.budget, w.d), dtype=torch.bfloat16, device=dev)
     v_view = torch.empty_like(k_view)
@@ -880,7 +869,9 @@ def run_kvm_tier(args, w):
         achieved = gb / (gather_us * 1e-6) / 1e9
         roof = {"bound": "hbm", "kernel": "kvm_materialize_fp8 (gather_view_kernel, E4M3 source)",
                 "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": None, "algorithmic_bytes_per_launch": gb}
+                "frac": round(achieved / peak, 4),
+                "traffic": recorded_traffic(w.name + "/fp8", "gather_view_kernel", GATHER_KERNEL_SOURCES),
+                "algorithmic_bytes_per_launch": gb}
     if rank == 0:
         tier = "FP8 E4M3 pages in HBM" if not host else "bf16 pages in pinned host memory"
         line = {
@@ -906,20 +897,41 @@ def run_kvm_tier(args, w):
         dist.destroy_process_group()
 
 
-def K_source_hash() -> str:
-    """Hash of the code (comments and whitespace dropped) the view kernel is compiled from: a recorded ncu
-    traffic figure is valid only while it is unchanged."""
+VIEW_KERNEL_SOURCES = ("sparse_attention_decode_04_b300/csrc/kvm_view.cu", "sparse_attention_decode_04_b300/csrc/kvm_device.cuh",
+                       "sparse_attention_decode_04_b300/csrc/kvm_internal.h", "include/kvm.h")
+GATHER_KERNEL_SOURCES = ("sparse_attention_decode_04_b300/csrc/kvm_gather.cu",) + VIEW_KERNEL_SOURCES[1:]
+
+
+def K_source_hash(files=VIEW_KERNEL_SOURCES) -> str:
+    """Hash of the code (comments and whitespace dropped) a kernel is compiled from: a recorded ncu traffic
+    figure is valid only while it is unchanged."""
     import hashlib
     import re
     h = hashlib.sha256()
-    files = [os.path.join(ROOT, "sparse_attention_decode_04_b300", "csrc", f)
-             for f in ("kvm_view.cu", "kvm_device.cuh", "kvm_internal.h")] + [os.path.join(ROOT, "include", "kvm.h")]
     for f in files:
-        with open(f) as fh:
+        with open(os.path.join(ROOT, f)) as fh:
             code = re.sub(r"/\*.*?\*/", " ", fh.read(), flags=re.S)
         code = re.sub(r"//[^\n]*", " ", code)
         h.update(" ".join(code.split()).encode())
     return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, kernel: str, files) -> int | None:
+    """DRAM bytes per launch of `kernel` at `workload` from a `traffic` line under profiles/, if its code hash
+    still matches."""
+    prof_dir = os.path.join(ROOT, "profiles")
+    want = K_source_hash(files)
+    for fn in sorted(os.listdir(prof_dir)) if os.path.isdir(prof_dir) else []:
+        if not fn.endswith(".md"):
+            continue
+        with open(os.path.join(prof_dir, fn)) as f:
+            for ln in f:
+                parts = ln.split()
+                if len(parts) >= 5 and parts[0] == "traffic" and parts[1] == workload and parts[2] == kernel:
+                    kv = dict(p.split("=", 1) for p in parts[3:] if "=" in p)
+                    if kv.get("source_hash") == want:
+                        return int(kv["bytes_per_launch"])
+    return None
 
 
 def main():
