@@ -675,7 +675,8 @@ def run_kvm_step(args, w):
             "roofline": {"bound": "tensor", "kernel": "kvm_step_attn (query packing + view packing + tcgen05 "
                                                       "attention, timed together)",
                          "achieved": round(achieved, 1), "peak": peak_tf, "peak_kind": peak_kind, "unit": "TFLOP/s",
-                         "frac": round(achieved / peak_tf, 4), "traffic": None,
+                         "frac": round(achieved / peak_tf, 4),
+                         "traffic": recorded_traffic(w.name, "step_attn_kernel", STEP_ATTN_SOURCES),
                          "algorithmic_flops_per_launch": attn_flops,
                          "issued_mma_flops_per_launch": 2 * attn_flops},
             "step_scores": {"algorithmic_flops": step_score_flops(w),
@@ -900,6 +901,7 @@ def run_kvm_tier(args, w):
 VIEW_KERNEL_SOURCES = ("sparse_attention_decode_04_b300/csrc/kvm_view.cu", "sparse_attention_decode_04_b300/csrc/kvm_device.cuh",
                        "sparse_attention_decode_04_b300/csrc/kvm_internal.h", "include/kvm.h")
 GATHER_KERNEL_SOURCES = ("sparse_attention_decode_04_b300/csrc/kvm_gather.cu",) + VIEW_KERNEL_SOURCES[1:]
+STEP_ATTN_SOURCES = ("sparse_attention_decode_04_b300/csrc/kvm_step_attn.cu",) + VIEW_KERNEL_SOURCES[1:]
 
 
 def K_source_hash(files=VIEW_KERNEL_SOURCES) -> str:
