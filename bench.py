@@ -420,28 +420,31 @@ def run_kvm(args, w):
                 kp[layer][p0:p0 + app_blocks].copy_(new_k[layer], non_blocking=True)
                 vp[layer][p0:p0 + app_blocks].copy_(new_v[layer], non_blocking=True)
 
-        # The new pages' copies run on a stream of their own, back to back on the copy engine: queued behind
-        # the appends they would wait for SM room (the view kernel holds every SM while it runs).
+        # The new pages' copies run on a stream of their own, back to back on the copy engine, ahead of the
+        # layers that need them.
         copy_stream = torch.cuda.Stream()
         copy_done = [torch.cuda.Event() for _ in range(L)]
 
         def e2e_step():
+            main = torch.cuda.current_stream()
             q_dev.copy_(q_host, non_blocking=True)
-            copy_stream.wait_stream(torch.cuda.current_stream())
+            copy_stream.wait_stream(main)
             with torch.cuda.stream(copy_stream):
                 for layer in range(L):
                     copy_new_pages(layer)
                     copy_done[layer].record(copy_stream)
-            if w.append_tok:
-                appends_ahead(lambda layer: app_stream.wait_event(copy_done[layer]))
-            else:
-                for layer in range(L):
-                    torch.cuda.current_stream().wait_event(copy_done[layer])
-            layers_after_appends(
-                lambda layer: (K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept[layer])
-                               if args.selection == "kvmem" else call_select(layer)),
-                lambda layer: K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer],
-                                                     q_dev[layer], k_view, v_view, view_len, outs[layer]))
+            # Each layer's append runs on the main stream just before its scoring: its pages landed long before
+            # (the copies run ahead of the layers), and an append left on a side stream would wait for SM room
+            # behind the previous layer's persistent view kernel.
+            for layer in range(L):
+                main.wait_event(copy_done[layer])
+                call_append(layer)
+                if args.selection == "kvmem":
+                    K.kvm_score_select(ctx, q_dev[layer], 1, index[layer], n_tok, kept[layer])
+                else:
+                    call_select(layer)
+                K.kvm_materialize_attn(ctx, kp[layer], vp[layer], n_pages, bt, n_tok, kept[layer], q_dev[layer],
+                                       k_view, v_view, view_len, outs[layer])
             out_host.copy_(out_all, non_blocking=True)  # one read-back of every layer's output
             torch.cuda.current_stream().wait_stream(copy_stream)
 
