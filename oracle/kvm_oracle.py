@@ -415,6 +415,35 @@ def step_view_attention(q_steps_bits, k_view_bits, v_view_bits, theta: float) ->
     return out
 
 
+# --------------------------------------------------------------------------- attention-mass diagnostic
+def block_attention_mass(q_bits, keys_bits, theta: float) -> np.ndarray:
+    """Full-attention mass of each history block, summed over a group's query heads: [n_blk].
+
+    [README] "Background and main changes" (a few blocks hold most of the attention: the top 8 of about 103
+    blocks held 66.5% of it).  READING: exact attention over the whole history, the query at position
+    N = n_tok (the slot after the history, as in decode attention with every block kept) and each key at its
+    history position t, scale 1/sqrt(d); mass[b] = sum over the group's heads h and the block's tokens t of
+    softmax_t(<RoPE(q_h, N), RoPE(k_t, t)>/sqrt(d)).  Each head's weights sum to 1, so sum_b mass[b] = G.
+    """
+    q = bf16_to_f64(q_bits)                          # [G][d]
+    k = bf16_to_f64(keys_bits)                       # [n_tok][d]
+    n_tok, d = k.shape
+    qr = rope(q, n_tok, theta)
+    kr = rope(k, np.arange(n_tok), theta)
+    s = qr @ kr.T / np.sqrt(d)                       # [G][n_tok]
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    n_blk = -(-n_tok // BLOCK)
+    pad = np.zeros((p.shape[0], n_blk * BLOCK - n_tok))
+    return np.concatenate([p, pad], axis=1).reshape(p.shape[0], n_blk, BLOCK).sum(axis=(0, 2))
+
+
+def top_mass_share(mass, group: int, k: int = 8) -> float:
+    """Share of the group's attention mass held by its k largest blocks (mass sums to `group`)."""
+    m = np.sort(np.asarray(mass, dtype=np.float64))[::-1]
+    return float(m[:k].sum() / group)
+
+
 # --------------------------------------------------------------------------- one layer
 def kvmem_layer(k_pool, v_pool, page_of, q_bits, n_tok: int, n_sink: int, n_recent: int, top_k: int,
                 theta: float, attend: bool = True, heads=None):

@@ -427,3 +427,66 @@ def test_representable_pages_survive_quantisation_exactly():
     kv, vv = O.materialize_values(deq, deq, [0, 2, 3], n_tok, 1e4)
     kb, vb = O.materialize(bits, bits, [0, 2, 3], n_tok, 1e4)
     assert np.array_equal(kv, kb) and np.array_equal(vv, vb)
+
+
+# ----------------------------------------------------------------------------- attention-mass diagnostic
+def test_attention_mass_brute_force_tiny():
+    """Per-token loops with the math library: rotate each pair by hand, exponentiate, sum per block."""
+    d, G, n_tok, theta = 8, 2, 70, 100.0
+    q = rand_bf16((G, d), 1.0)
+    k = rand_bf16((n_tok, d), 1.0)
+    qv, kv = O.bf16_to_f64(q), O.bf16_to_f64(k)
+
+    def rot(x, pos):
+        out = [0.0] * d
+        for i in range(d // 2):
+            a = pos * theta ** (-2.0 * i / d)
+            out[i] = x[i] * math.cos(a) - x[i + d // 2] * math.sin(a)
+            out[i + d // 2] = x[i + d // 2] * math.cos(a) + x[i] * math.sin(a)
+        return out
+
+    want = [0.0] * 3
+    for h in range(G):
+        qr = rot(list(qv[h]), n_tok)
+        sc = [sum(a * b for a, b in zip(qr, rot(list(kv[t]), t))) / math.sqrt(d) for t in range(n_tok)]
+        mx = max(sc)
+        w = [math.exp(x - mx) for x in sc]
+        z = sum(w)
+        for t in range(n_tok):
+            want[t // 32] += w[t] / z
+    got = O.block_attention_mass(q, k, theta)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-15)
+
+
+def test_attention_mass_sums_to_group_and_uniform_keys_spread_evenly():
+    q = rand_bf16((5, 64), 1.0)
+    k = rand_bf16((32 * 9 + 11, 64), 1.0)
+    m = O.block_attention_mass(q, k, 1e4)
+    assert m.shape == (10,) and abs(m.sum() - 5.0) < 1e-12
+    # identical zero keys: every token gets 1/n_tok, so a block's mass is G * (its tokens) / n_tok
+    z = np.zeros((32 * 9 + 11, 64), dtype=np.uint16)
+    mu = O.block_attention_mass(q, z, 1e4)
+    want = 5.0 * np.array([32] * 9 + [11]) / (32 * 9 + 11)
+    assert np.allclose(mu, want, rtol=1e-12)
+
+
+def test_attention_mass_depends_on_relative_positions_only():
+    """Rotary attention sees relative positions only: the same history with the query at N + 96 and every key
+    at t + 96 (rotated by hand here) gives the same block masses."""
+    d, G, theta = 16, 2, 1e4
+    q = rand_bf16((G, d), 1.0)
+    k = rand_bf16((100, d), 1.0)
+    base = O.block_attention_mass(q, k, theta)
+    qv, kv = O.bf16_to_f64(q), O.bf16_to_f64(k)
+    qr = O.rope(qv, 100 + 96, theta)
+    kr = O.rope(kv, np.arange(100) + 96, theta)
+    s = qr @ kr.T / np.sqrt(d)
+    p = np.exp(s - s.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    shifted = np.concatenate([p, np.zeros((G, 28))], axis=1).reshape(G, 4, 32).sum(axis=(0, 2))
+    assert np.allclose(base, shifted, rtol=1e-9)
+
+
+def test_top_mass_share():
+    m = np.array([0.5, 0.1, 1.0, 0.2, 0.2])
+    assert O.top_mass_share(m, 2, k=2) == pytest.approx(0.75)
