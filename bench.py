@@ -907,6 +907,87 @@ GATHER_KERNEL_SOURCES = ("sparse_attention_decode_04_b300/csrc/kvm_gather.cu",) 
 STEP_ATTN_SOURCES = ("sparse_attention_decode_04_b300/csrc/kvm_step_attn.cu",) + VIEW_KERNEL_SOURCES[1:]
 
 
+def run_mass(args, w):
+    """The attention-mass diagnostic over every layer of the workload: per layer, the full attention of the
+    decode query over the whole history, reduced to per-block mass (one kvm_attention_mass call)."""
+    import torch
+
+    import sparse_attention_decode_04_b300 as K
+    from synth import device as synth_dev
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    rank = int(os.environ.get("RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    S, L = w.n_sessions, w.n_layers
+    ctx = K.Context.for_workload(w)
+    bt = torch.from_numpy(synth.block_table(w)).to(dev)
+    kp, qs = [], []
+    for layer in range(L):
+        k = torch.empty((w.n_pages, w.h_kv, BLOCK, w.d), dtype=torch.bfloat16, device=dev)
+        v = torch.empty_like(k)
+        synth_dev.fill_kv_pool(w, layer, bt, k.view(torch.int16), v.view(torch.int16))
+        del v
+        kp.append(k)
+        q = synth.queries(w, layer)
+        qs.append(torch.from_numpy(q[:, 0].view(np.int16)).to(dev).view(torch.bfloat16).contiguous())
+    torch.cuda.empty_cache()
+    mass = torch.zeros((L, S, w.h_kv, w.n_blk), dtype=torch.float32, device=dev)
+    n_tok = [w.n_tok] * S
+
+    def step():
+        for layer in range(L):
+            K.kvm_attention_mass(ctx, qs[layer], kp[layer], w.n_pages, bt, n_tok, mass[layer])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=side):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    with sampler:
+        time.sleep(0.3)
+        e0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    us_layer = ms * 1e3 / L
+    key_bytes = w.n_tok * w.h_kv * w.d * 2 * S  # every key of the layer read once
+    peak, peak_kind = load_peaks()
+    achieved = key_bytes / (us_layer * 1e-6) / 1e9
+    # share of each group's mass held by its 8 largest blocks (a row sums to the group size)
+    top8 = np.sort(mass.cpu().numpy().astype(np.float64), axis=-1)[..., ::-1][..., :8].sum(axis=-1) / w.group
+    shares = top8.reshape(-1)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "attention-mass diagnostic µs per layer (full attention of the decode query over the history)",
+            "value": round(us_layer, 2), "unit": "us/layer", "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": w.name, "layers": L, "sessions_per_gpu": S, "history_tokens": w.n_tok,
+                       "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d, "cuda_graph": True},
+            "roofline": {"bound": "hbm", "kernel": "kvm_attention_mass (mass_tile_kernel + mass_finalize_kernel)",
+                         "achieved": round(achieved, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": None,
+                         "algorithmic_bytes_per_launch": key_bytes},
+            "top8_share": {"mean": round(float(np.mean(shares)), 4), "min": round(float(np.min(shares)), 4),
+                           "max": round(float(np.max(shares)), 4),
+                           "note": "synthetic topic-mixture keys; the pages' 66.5% is on a real model"},
+            "gpu_launches": 2 * L * args.steps, "clocks": sampler.summary()}), flush=True)
+
+
 def K_source_hash(files=VIEW_KERNEL_SOURCES) -> str:
     """Hash of the code (comments and whitespace dropped) a kernel is compiled from: a recorded ncu traffic
     figure is valid only while it is unchanged."""
@@ -955,6 +1036,8 @@ def main():
     ap.add_argument("--kv", default="bf16", choices=["bf16", "fp8", "host"],
                     help="page tier: bf16 pages in HBM (the method), FP8 E4M3 pages in HBM, or bf16 pages in "
                          "pinned host memory")
+    ap.add_argument("--mass", action="store_true",
+                    help="time the attention-mass diagnostic (full attention over the history, per-block mass)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -971,6 +1054,8 @@ def main():
         w = w.with_(n_layers=max(1, min(args.layers, w.n_layers)))
     if args.impl == "reference":
         run_reference(args, w)
+    elif args.mass:
+        run_mass(args, w)
     elif w.n_q > 1:
         run_kvm_step(args, w)
     elif args.kv != "bf16":

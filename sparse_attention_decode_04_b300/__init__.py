@@ -69,10 +69,11 @@ def lib() -> ctypes.CDLL:
         L.kvm_index_append_fp8.argtypes = [P, P, P, i64, P, i32, P, P, P, P]
         L.kvm_materialize_fp8.argtypes = [P, P, P, P, P, i64, P, P, i32, P, P, P, P, P]
         L.kvm_materialize_host.argtypes = [P, P, P, i64, P, P, i32, P, P, P, P, P]
+        L.kvm_attention_mass.argtypes = [P, P, P, i64, P, P, i32, P, P]
         for name in ("kvm_create", "kvm_destroy", "kvm_index_append", "kvm_score_select", "kvm_materialize",
                      "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status", "kvm_select_control",
                      "kvm_step_attn", "kvm_quantize_pages", "kvm_index_append_fp8", "kvm_materialize_fp8",
-                     "kvm_materialize_host"):
+                     "kvm_materialize_host", "kvm_attention_mass"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -216,6 +217,13 @@ def kvm_materialize_host(ctx: Context, k_pool_host, v_pool_host, n_pages: int, b
     _check(lib().kvm_materialize_host(ctx.handle, _ptr(k_pool_host), _ptr(v_pool_host), int(n_pages),
                                       _ptr(block_table), _i64(n_tok), n, _ptr(kept_ids), _ptr(k_view), _ptr(v_view),
                                       _ptr(view_len), _stream(stream)))
+
+
+def kvm_attention_mass(ctx: Context, q, k_pool, n_pages: int, block_table, n_tok, mass, stream=None):
+    """Full-attention mass of every history block, summed over each KV head's query heads (a diagnostic)."""
+    n = len(n_tok)
+    _check(lib().kvm_attention_mass(ctx.handle, _ptr(q), _ptr(k_pool), int(n_pages), _ptr(block_table),
+                                    _i64(n_tok), n, _ptr(mass), _stream(stream)))
 
 
 def kvm_device_status(ctx: Context, clear: bool = True, stream=None) -> int:

@@ -12,7 +12,9 @@
 #include <utility>
 
 #include "kvm.h"
+#include "kvm_diag.h"
 #include "kvm_internal.h"
+#include "kvm_mass.h"
 
 using kvm::Ctx;
 using kvm::SessionArgs;
@@ -175,7 +177,8 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   const size_t sz_rec =
       ((size_t)c.view_ctas + S * p->h_kv) * (kvm::kViewWarps + 1) * c.group * (4 + p->d) * sizeof(float);
   const size_t sz_cnt = S * p->h_kv * sizeof(uint32_t);
-  const size_t sz_base = (size_t)(budget + 1) * (p->d / 2) * sizeof(float2);
+  // base rows cover view slots and, for the attention-mass diagnostic, every history block position
+  const size_t sz_base = (size_t)((budget > p->max_blocks ? budget : p->max_blocks) + 1) * (p->d / 2) * sizeof(float2);
   const size_t sz_off = (size_t)32 * (p->d / 2) * sizeof(float2);
   constexpr int kBufs = 9;
   void* ptrs[kBufs] = {};
@@ -235,6 +238,7 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   e = cudaMemset(c.status, 0, 256);
   if (e == cudaSuccess) e = cudaMemset(c.seg_count, 0, sz_cnt);
   if (e == cudaSuccess) e = kvm::launch_rope_tables(c, 0);
+  if (e == cudaSuccess) e = kvm::launch_mass_tables(c, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     kvm_destroy(ctx);
@@ -504,6 +508,25 @@ kvm_status kvm_step_attn(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const uin
     return fail(KVM_ERR_INVALID_ARG, "q, k_view, v_view and out must be 16-byte aligned");
   cudaError_t e = kvm::launch_step_attn(c, q, n_q, k_view, v_view, view_len, n_sessions, out, (cudaStream_t)stream);
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_step_attn launch");
+}
+
+kvm_status kvm_attention_mass(kvm_ctx* ctx, const uint16_t* q, const uint16_t* k_pool, int64_t n_pages,
+                              const int32_t* block_table, const int64_t* n_tok, int32_t n_sessions, float* mass,
+                              void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_sessions == 0) return KVM_OK;
+  if (!q || !k_pool || !block_table || !mass) return fail(KVM_ERR_INVALID_ARG, "kvm_attention_mass: NULL pointer");
+  if (n_pages < 1) return fail(KVM_ERR_INVALID_ARG, "n_pages=%lld must be >= 1", (long long)n_pages);
+  if (!aligned(q, 16) || !aligned(k_pool, 16) || !aligned(mass, 4) || !aligned(block_table, 4))
+    return fail(KVM_ERR_INVALID_ARG, "q and k_pool must be 16-byte aligned, mass and block_table 4-byte aligned");
+  SessionArgs a;
+  if ((s = history_args(c, n_tok, n_sessions, &a)) != KVM_OK) return s;
+  cudaError_t e = kvm::launch_attention_mass(c, q, k_pool, n_pages, block_table, n_sessions, a, mass,
+                                             (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_attention_mass launch");
 }
 
 kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* stream) {
