@@ -53,7 +53,7 @@ struct Ctx {
   uint16_t* step_kpk = nullptr;  // packed bf16 index [S*h_kv][step_blk_cap_pad][d] (core-matrix order)
   uint16_t* step_qpk = nullptr;  // packed bf16 query rows [S*h_kv][step_rows_cap_pad][d]
   float2* step_part = nullptr;   // row (max, sum) per column range [S*h_kv][kStepMaxRanges][rows]
-  float2* step_stats = nullptr;  // row (max, 1/sum) [S*h_kv][rows]
+  float2* step_stats = nullptr;  // row (max + log2 sum, 1/sum) [S*h_kv][rows]
   float* step_gs = nullptr;      // group scores when the caller does not ask for them [S][h_kv][max_blocks]
   // step attention over the view (multi-query), allocated when max_queries > 1
   int64_t attn_l_pad = 0;         // 32 * budget rounded up to 64 (view tokens per packed head)

@@ -184,23 +184,34 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
       }
       tc_fence_after();
       const int col0 = (j0 + j) * kColsN;
+      const bool full = col0 + kColsN <= n_blk;  // no column past the history in this tile
 #pragma unroll 1
       for (int cc = half * (kColsN / 64); cc < (half + 1) * (kColsN / 64); ++cc) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + st * kColsN + cc * 32, v);
         tmem_wait_ld();
-        float x[32], cm = -INFINITY;
+        // raw scores; the log2-domain scale (positive) is applied to the maximum and inside each exponent's FMA
+        float x[32];
+        if (full) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          x[i] = (col0 + cc * 32 + i < n_blk) ? __uint_as_float(v[i]) * scale_log2 : -INFINITY;
-          cm = fmaxf(cm, x[i]);
+          for (int i = 0; i < 32; ++i) x[i] = __uint_as_float(v[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) x[i] = (col0 + cc * 32 + i < n_blk) ? __uint_as_float(v[i]) : -INFINITY;
         }
-        const float mn = fmaxf(m, cm);
-        if (mn != -INFINITY) {
-          float acc = 0.f;
+        float mx[8];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc += fast_exp2(x[i] - mn);
-          z = z * fast_exp2(m - mn) + acc;
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(fmaxf(x[i], x[i + 8]), fmaxf(x[i + 16], x[i + 24]));
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) mx[i] = fmaxf(mx[i], mx[i + w]);
+        const float mn = fmaxf(m, mx[0] * scale_log2);
+        if (mn != -INFINITY) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int i = 0; i < 32; ++i) acc[i & 3] += fast_exp2(fmaf(x[i], scale_log2, -mn));
+          z = z * fast_exp2(m - mn) + ((acc[0] + acc[1]) + (acc[2] + acc[3]));
           m = mn;
         }
       }
@@ -227,7 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
   }
 }
 
-// Per query row: M = max over ranges, 1/Z with Z = sum z * 2^(m - M); padded rows get (+inf, 0).
+// Per query row: M = max over ranges and Z = sum z * 2^(m - M), stored as (M + log2 Z, 1/Z); padded rows get
+// (+inf, 0).
 __global__ void step_merge_kernel(const float2* __restrict__ part, int n_ranges, int rows_pad, int n_rows,
                                   float2* __restrict__ stats) {
   const int sg = blockIdx.y;
@@ -242,7 +254,8 @@ __global__ void step_merge_kernel(const float2* __restrict__ part, int n_ranges,
       const float2 p = part[((int64_t)sg * n_ranges + k) * rows_pad + row];
       if (p.x != -INFINITY) Z += p.y * exp2f(p.x - M);
     }
-    r = make_float2(M, Z > 0.f ? 1.f / Z : 0.f);
+    // (M + log2 Z, 1/Z): pass 2 folds the normaliser into the exponent
+    r = Z > 0.f ? make_float2(M + log2f(Z), 1.f / Z) : make_float2(INFINITY, 0.f);
   }
   stats[(int64_t)sg * rows_pad + row] = r;
 }
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
   extern __shared__ __align__(1024) unsigned char smem[];
   unsigned char* a_s = smem;
   unsigned char* b_s = smem + A_BYTES;
-  float2* st_s = reinterpret_cast<float2*>(smem + A_BYTES + 2 * B_BYTES);  // [rows_pad]
+  float* st_s = reinterpret_cast<float*>(smem + A_BYTES + 2 * B_BYTES);  // [rows_pad]: M + log2 Z per row
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -282,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
     abort_flag = 0;
     init_bars(bars);
   }
-  for (int i = tid; i < rows_pad; i += kThreads) st_s[i] = stats[(int64_t)sg * rows_pad + i];
+  for (int i = tid; i < rows_pad; i += kThreads) st_s[i] = stats[(int64_t)sg * rows_pad + i].x;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -341,12 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + st * kColsN + cc * 32, v);
         tmem_wait_ld();
-        const float2* sr = st_s + j * kColsN + cc * 32;
+        const float* sr = st_s + j * kColsN + cc * 32;
+        float a4[4] = {0.f, 0.f, 0.f, 0.f};  // p / Z = 2^(s c - (M + log2 Z)); short dependency chains
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float2 ms = sr[i];  // same address in every lane: broadcast
-          acc = fmaf(fast_exp2(fmaf(__uint_as_float(v[i]), scale_log2, -ms.x)), ms.y, acc);
-        }
+        for (int i = 0; i < 32; ++i)  // sr[i]: the same address in every lane (broadcast)
+          a4[i & 3] += fast_exp2(fmaf(__uint_as_float(v[i]), scale_log2, -sr[i]));
+        acc += (a4[0] + a4[1]) + (a4[2] + a4[3]);
       }
       tc_fence_before();
       __syncwarp();
