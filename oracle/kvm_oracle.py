@@ -12,9 +12,9 @@ Sources (web pages on KVMem, arXiv 2609.04852):
            (Evolve review)
 
 Every function states the passage it follows.  Where the pages leave a step
-open, the reading taken is marked READING.  Every function is pinned by the
-CPU tests in tests/test_oracle_pins.py against brute force, closed forms,
-invariants or library routines; none is "parity unpinned".
+open, the reading taken is marked READING.  The CPU tests in
+tests/test_oracle_pins.py pin each function against brute force, closed
+forms, invariants or library routines.
 
 Layouts (bf16 is carried as its uint16 bit pattern):
   pool      uint16 [n_pages][h_kv][32][d]   pre-RoPE keys / values; a page holds one block of every KV head
@@ -85,23 +85,12 @@ def mean_k_index_bf16(keys_bits) -> np.ndarray:
     """Mean-K vectors as the bf16 operand of step-level (tensor-core) scoring: uint16 [n_blk][d].
 
     READING: the step-level scoring contraction takes bf16 operands, so the
-    index is rounded to bf16 first.  That rounding is a quantisation decided in
-    floating point, so it is taken in the kernel's precision: the block's keys
-    are summed in fp32 in token order, divided by the token count in fp32, and
-    the fp32 mean is rounded to bf16 (nearest even).
+    index vector is rounded to bf16 (nearest even) first.  The oracle rounds
+    the exact mean (``mean_k_index``); a kernel that rounds its fp32 mean can
+    land one bf16 step away where the exact mean lies within the fp32 error
+    of a rounding midpoint, and the parity tests bound that effect.
     """
-    k = bf16_to_f64(keys_bits).astype(np.float32)
-    n_tok, d = k.shape
-    n_blk = -(-n_tok // BLOCK)
-    acc = np.zeros((n_blk, d), dtype=np.float32)
-    cnt = np.zeros(n_blk, dtype=np.float32)
-    for t in range(BLOCK):                       # token order within each block
-        rows = np.arange(t, n_blk * BLOCK, BLOCK)
-        rows = rows[rows < n_tok]
-        acc[rows // BLOCK] = acc[rows // BLOCK] + k[rows]
-        cnt[rows // BLOCK] += 1
-    mean32 = (acc / cnt[:, None]).astype(np.float32)
-    return f64_to_bf16(mean32.astype(np.float64))
+    return f64_to_bf16(mean_k_index(keys_bits))
 
 
 def index_append(index, keys_bits, tok_begin: int, n_tok: int) -> np.ndarray:

@@ -66,24 +66,49 @@ def test_mean_k_equals_exact_rational_mean():
             assert abs(Fraction(float(idx[b, i])) - exact) <= abs(exact) * Fraction(1, 2 ** 52)
 
 
-def test_bf16_index_operand_is_the_rounded_fp32_mean():
-    """fp32 mean within the fp32 error bound of the exact mean, then RNE to bf16 as torch does it."""
+def _bf16_nearest_even_of_rational(x: Fraction) -> int:
+    """bf16 bit pattern nearest to an exact rational, ties to the even pattern, by enumerating the
+    representable neighbours (normal range only, which the test data stays in)."""
+    if x == 0:
+        return 0
+    sign = 0x8000 if x < 0 else 0
+    a = abs(x)
+    e = 0
+    while a >= 2:
+        a /= 2
+        e += 1
+    while a < 1:
+        a *= 2
+        e -= 1
+    # a in [1, 2): neighbours 1 + m/128 and 1 + (m+1)/128
+    m = int((a - 1) * 128)
+    lo, hi = Fraction(128 + m, 128), Fraction(128 + m + 1, 128)
+    dl, dh = a - lo, hi - a
+    pick = m if dl < dh else (m + 1 if dh < dl else (m if m % 2 == 0 else m + 1))
+    if pick == 128:                      # rounded up to the next binade
+        pick, e = 0, e + 1
+    return sign | ((e + 127) << 7) | pick
+
+
+def test_bf16_index_operand_is_the_rounded_exact_mean():
+    """The bf16 operand of step scoring is the exact rational mean of each block's keys rounded to the
+    nearest bf16 (ties to even), found here by enumerating neighbours in exact arithmetic."""
     keys = rand_bf16((5 * 32 + 11, 24), scale=2.0)
     got = O.mean_k_index_bf16(keys)
-    exact = O.mean_k_index(keys)
-    vals = np.abs(O.bf16_to_f64(keys))
-    n_blk = exact.shape[0]
-    for b in range(n_blk):
-        rows = vals[b * 32:(b + 1) * 32]
-        bound = len(rows) * 2.0 ** -24 * rows.sum(axis=0) / len(rows) + 2.0 ** -24 * np.abs(exact[b])
-        # the fp32 mean the kernel forms, recomputed token by token with Python floats rounded to fp32
-        acc = np.zeros(24, dtype=np.float32)
-        for t in range(len(rows)):
-            acc = (acc + O.bf16_to_f64(keys[b * 32 + t]).astype(np.float32)).astype(np.float32)
-        mean32 = (acc / np.float32(len(rows))).astype(np.float32)
-        assert np.all(np.abs(mean32.astype(np.float64) - exact[b]) <= bound)
-        ref = torch.from_numpy(mean32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
-        assert np.array_equal(got[b], ref)
+    vals = O.bf16_to_f64(keys)
+    assert got.shape == (6, 24)
+    for b in range(6):
+        rows = range(b * 32, min(len(vals), b * 32 + 32))
+        for i in range(24):
+            exact = sum(Fraction(float(vals[t, i])) for t in rows) / len(rows)
+            assert int(got[b, i]) == _bf16_nearest_even_of_rational(exact), (b, i)
+    # a block whose exact mean sits on a midpoint: 31 keys of 1 and one of 1 + 2^-3 give a mean of
+    # 1 + 2^-8 (halfway between 1 and 1 + 2^-7) and round to the even pattern 0x3F80; 1 + 3 * 2^-3 for the
+    # odd key gives 1 + 3 * 2^-8, halfway between 0x3F81 and 0x3F82, which rounds to 0x3F82
+    tie = O.f64_to_bf16(np.array([[1.0]] * 31 + [[1.125]]))
+    assert int(O.mean_k_index_bf16(tie)[0, 0]) == 0x3F80
+    tie2 = O.f64_to_bf16(np.array([[1.0]] * 31 + [[1.375]]))
+    assert int(O.mean_k_index_bf16(tie2)[0, 0]) == 0x3F82
 
 
 def test_index_append_matches_full_build_and_is_position_free():
@@ -152,7 +177,29 @@ def test_withdrawn_averaging_is_distinguishable():
     gs = O.gqa_softmax_sum(s, 1)
     assert np.allclose(gs[0], expect, rtol=1e-13)
     wd = O.withdrawn_group_scores(q, idx)
+    # averaged query (1/2, 1/2): scores (5/2, 5/2, 0, 2.6) over sqrt(2) * sqrt(2) = 2, softmax worked by hand
+    zw = 2 * math.exp(2.5) + 1 + math.exp(2.6)
+    assert np.allclose(wd[0], [math.exp(2.5) / zw, math.exp(2.5) / zw, 1 / zw, math.exp(2.6) / zw], rtol=1e-13)
     assert int(np.argmax(gs[0])) in (0, 1) and int(np.argmax(wd[0])) == 3
+
+
+def test_withdrawn_scoring_averages_not_sums_and_keeps_groups_apart():
+    """Hand-worked vectors for two KV groups of three query heads.  The averaged query halves and thirds the
+    scores; a sum of the heads (three times the mean) or a mean over the wrong group gives another vector."""
+    q = O.f64_to_bf16([[2.0, 0.0], [1.0, 0.0], [0.0, 0.0],             # group 0: mean (1, 0)
+                       [0.0, 3.0], [0.0, 0.0], [0.0, 0.0]])            # group 1: mean (0, 1)
+    r2 = math.sqrt(2.0)
+    idx = np.array([[[r2, 0.0], [0.0, r2], [2 * r2, 0.0]],             # group 0: scores (1, 0, 2)
+                    [[0.0, r2], [r2, 0.0], [0.0, -r2]]])               # group 1: scores (1, 0, -1)
+    wd = O.withdrawn_group_scores(q, idx)
+    z0 = math.e + 1 + math.e ** 2
+    z1 = math.e + 1 + math.exp(-1)
+    want = np.array([[math.e / z0, 1 / z0, math.e ** 2 / z0], [math.e / z1, 1 / z1, math.exp(-1) / z1]])
+    assert np.allclose(wd, want, rtol=1e-14)
+    # a sum of the heads would give scores (3, 0, 6) for group 0: a different vector
+    zs = math.exp(3) + 1 + math.exp(6)
+    assert not np.allclose(wd[0], [math.exp(3) / zs, 1 / zs, math.exp(6) / zs], rtol=1e-3)
+    assert np.allclose(wd.sum(axis=1), 1.0, rtol=1e-14)                 # one softmax per KV head
 
 
 def test_step_scores_single_token_and_mass():
@@ -187,6 +234,50 @@ def test_select_tie_goes_to_lower_id():
     gs = np.zeros(20)
     gs[[7, 9, 11, 13]] = 1.0
     assert O.select_blocks(gs, 20, 1, 1, 2).tolist() == [0, 7, 9, 19]
+
+
+def brute_kth(gs, n_blk, n_sink, n_recent, top_k):
+    """The k-th largest candidate score by counting: the value v with #{c: gs_c > v} < k <= #{c: gs_c >= v}."""
+    if n_blk <= n_sink + n_recent + top_k:
+        return float("nan")
+    cands = [float(gs[b]) for b in range(n_sink, n_blk - n_recent)]
+    for v in cands:
+        above = sum(1 for x in cands if x > v)
+        at_or_above = sum(1 for x in cands if x >= v)
+        if above < top_k <= at_or_above:
+            return v
+    raise AssertionError("no k-th value")
+
+
+@pytest.mark.parametrize("n_blk,n_sink,n_recent,top_k", [
+    (60, 2, 3, 1), (60, 2, 3, 7), (60, 2, 3, 54), (60, 0, 0, 1), (60, 0, 0, 59), (40, 4, 4, 31), (40, 4, 4, 32)])
+def test_kth_candidate_score_by_counting(n_blk, n_sink, n_recent, top_k):
+    """The boundary score against a counting loop, with exact ties (values on a 0.1 grid), top_k = 1, top_k one
+    short of the candidate count, and top_k equal to it (every block kept: no boundary, NaN)."""
+    gs = np.round(RNG.uniform(0, 1, size=n_blk), 1)
+    # the forced blocks hold the largest scores: they must not be counted among the candidates
+    gs[:n_sink] = 5.0
+    gs[n_blk - n_recent:] = 7.0
+    got = O.kth_candidate_score(gs, n_blk, n_sink, n_recent, top_k)
+    want = brute_kth(gs, n_blk, n_sink, n_recent, top_k)
+    if math.isnan(want):
+        assert math.isnan(got)
+        assert len(O.select_blocks(gs, n_blk, n_sink, n_recent, top_k)) == n_blk
+        return
+    assert got == want
+    # the boundary is the smallest score among the chosen candidates
+    ids = O.select_blocks(gs, n_blk, n_sink, n_recent, top_k)
+    chosen = [b for b in ids if n_sink <= b < n_blk - n_recent]
+    assert len(chosen) == top_k and min(gs[chosen]) == got
+
+
+def test_kth_candidate_score_hand_cases():
+    gs = np.array([9.0, 0.3, 0.8, 0.8, 0.1, 0.5, 9.0])      # sink 0 and recent 6 hold the largest scores
+    assert O.kth_candidate_score(gs, 7, 1, 1, 1) == 0.8
+    assert O.kth_candidate_score(gs, 7, 1, 1, 2) == 0.8      # tie: the second 0.8
+    assert O.kth_candidate_score(gs, 7, 1, 1, 3) == 0.5
+    assert O.kth_candidate_score(gs, 7, 1, 1, 4) == 0.3
+    assert math.isnan(O.kth_candidate_score(gs, 7, 1, 1, 5))  # budget covers every block
 
 
 # ----------------------------------------------------------------------------- RoPE
