@@ -14,15 +14,21 @@
 //   e[b][h] = exp(s[b][h] - m_tile[h]) and the tile's (m_tile, sum e) per head.
 // Kernel B (select_kernel), grid (C, h_kv, sessions), clusters of C CTAs:
 //   each CTA owns 1/C of the blocks.  From the tiles' partials it forms the
-//   softmax normalisers, Gs[b] = sum_h e[b][h] * exp(m_tile - M_h) / Z_h, and
-//   then runs an exact 3-pass radix select (11/11/10 bits) over the
-//   candidates: per pass each CTA builds its slice's histogram with
-//   shared-memory atomics, one cluster barrier, and every CTA pulls the C
-//   histograms through distributed shared memory (16-byte loads, 4 bins each)
-//   and scans the merged counts itself (double-buffered histograms, so one
-//   barrier a pass).
-//   A stable compaction follows (one exchange of per-CTA tie / kept counts):
-//   ascending ids, equal scores resolved toward the lower id.
+//   softmax normalisers, Gs[b] = sum_h e[b][h] * exp(m_tile - M_h) / Z_h (the
+//   exponentials are requested before the normalisers are formed, so the two
+//   L2 round trips overlap), and builds the first radix histogram as it goes.
+//   Exact radix select over the candidates' order keys, 12 + 12 + 8 bits: per
+//   pass one cluster barrier, then a single warp locates the boundary bin over
+//   the merged counts with two rounds of distributed-shared-memory loads (64
+//   super-bin sums from every CTA, then the bins of the one super-bin that
+//   holds the boundary).  The passes stop as soon as the boundary bin holds
+//   exactly the keys still to take (all of them are kept), and after the second
+//   pass a boundary bin of at most 32 keys is settled without a third pass: its
+//   keys travel with the compaction's count exchange and every CTA ranks them.
+//   A stable compaction follows: each CTA pushes its counts (and boundary keys)
+//   into the other CTAs before one last cluster barrier, so no CTA reads
+//   another's shared memory after it.  Ids come out ascending; equal scores
+//   resolve toward the lower id.
 #include <cooperative_groups.h>
 
 #include "kvm_device.cuh"
@@ -37,7 +43,6 @@ constexpr int kScoreThreads = 256;  // 8 warps, 4 rows each per stage
 constexpr int kStageRows = 32;
 constexpr int kStages = 5;
 constexpr int kSelectThreads = 512;
-constexpr int kRadixBins = 2048;
 
 template <int D, int G>
 __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
@@ -186,12 +191,14 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
     tile_max[tid] = mm;
   }
   __syncthreads();
-  // e = exp(s - m_tile), written in place and to global in flat (row, head) order.
-  float* e_dst = e_buf + (((int64_t)s * h_kv + g) * max_blocks + r0) * G;
+  // e = exp(s - m_tile), written in place and to global head-major ([head][block]: the selection reads one
+  // head of 32 consecutive blocks per warp-wide load).
+  float* e_dst = e_buf + ((int64_t)s * h_kv + g) * G * max_blocks + r0;
   for (int i = tid; i < nrows * G; i += kScoreThreads) {
-    const float e = expf(s_tile[i] - tile_max[i % G]);
-    s_tile[i] = e;
-    e_dst[i] = e;
+    const int h = i / nrows, r = i - h * nrows;
+    const float e = expf(s_tile[r * G + h] - tile_max[h]);
+    s_tile[r * G + h] = e;
+    e_dst[(int64_t)h * max_blocks + r] = e;
   }
   __syncthreads();
   // Sum of e per head, fixed order: each warp owns heads h = warp, warp + 8, ...
@@ -204,283 +211,412 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   }
 }
 
-struct RadixResult {
-  uint32_t digit;
-  int krem;
+// Digits of the order keys: pass 0 takes bits 31..20 (sign, exponent, 3 mantissa bits), pass 1 bits 19..8,
+// pass 2 bits 7..0.  A pass's histogram is merged across the cluster in two small steps: per-CTA sums of 64
+// super-bins (each nb/64 bins) are pulled first, then the bins of the one super-bin that holds the boundary.
+constexpr int kSelBins = 4096;
+constexpr int kSelSup = 64;
+
+__device__ __forceinline__ int sel_shift(int pass) { return pass == 0 ? 20 : (pass == 1 ? 8 : 0); }
+__device__ __forceinline__ int sel_bins(int pass) { return pass == 2 ? 256 : kSelBins; }
+
+struct SelResult {
+  uint32_t digit;  // boundary bin of the pass
+  int krem;        // keys still to take inside the boundary bin
+  int count;       // keys in the boundary bin (cluster-wide)
 };
 
-// Block-wide exclusive scan of one int per thread for NT threads; returns the total via *total.
-template <int NT>
-__device__ int block_exclusive_scan_n(int v, int* scratch, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+// Warp 0: finds, over the cluster's merged counts, the bin holding the krem-th largest key of this pass.
+// sup / hist are this CTA's buffers; the same offsets are read in every CTA of the cluster.
+__device__ __forceinline__ SelResult sel_boundary(cg::cluster_group& cluster, int C, const int* sup,
+                                                  const int* hist, int nb, int krem) {
+  const int lane = threadIdx.x & 31;
+  // 1. super-bins 2*lane and 2*lane + 1, summed over the cluster (independent remote loads)
+  int c0 = 0, c1 = 0;
+  {
+    int2 v[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < C) v[r] = *reinterpret_cast<const int2*>(cluster.map_shared_rank(sup, r) + 2 * lane);
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < C) {
+        c0 += v[r].x;
+        c1 += v[r].y;
+      }
+  }
+  // keys above each of this lane's super-bins: inclusive suffix sum over the higher lanes
+  int suf = c0 + c1;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const int y = __shfl_down_sync(0xffffffffu, suf, o);
+    if (lane + o < 32) suf += y;
   }
-  if (lane == 31) scratch[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < NT / 32 ? scratch[lane] : 0;
+  const int above1 = suf - c0 - c1, above0 = above1 + c1;
+  const bool in1 = above1 < krem && krem <= above1 + c1, in0 = above0 < krem && krem <= above0 + c0;
+  const unsigned hit = __ballot_sync(0xffffffffu, in0 || in1);
+  const int src = hit ? __ffs(hit) - 1 : 0;  // exactly one lane holds the boundary super-bin
+  const int sb = __shfl_sync(0xffffffffu, in1 ? 2 * lane + 1 : 2 * lane, src);
+  const int sabove = __shfl_sync(0xffffffffu, in1 ? above1 : above0, src);
+  // 2. the bins of that super-bin (nb / 64 of them, two per lane), summed over the cluster
+  const int bw = nb / kSelSup;
+  int b0 = 0, b1 = 0;
+  if (2 * lane < bw) {
+    int2 v[8];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    scratch[32 + lane] = w;  // inclusive warp prefix
+    for (int r = 0; r < 8; ++r)
+      if (r < C) v[r] = *reinterpret_cast<const int2*>(cluster.map_shared_rank(hist, r) + sb * bw + 2 * lane);
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < C) {
+        b0 += v[r].x;
+        b1 += v[r].y;
+      }
   }
-  __syncthreads();
-  const int before = (warp > 0 ? scratch[32 + warp - 1] : 0) + x - v;
-  *total = scratch[32 + NT / 32 - 1];
-  __syncthreads();
-  return before;
+  int suf2 = b0 + b1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, suf2, o);
+    if (lane + o < 32) suf2 += y;
+  }
+  const int a1 = sabove + suf2 - b0 - b1, a0 = a1 + b1;
+  const bool j1 = b1 > 0 && a1 < krem && krem <= a1 + b1, j0 = b0 > 0 && a0 < krem && krem <= a0 + b0;
+  const unsigned hit2 = __ballot_sync(0xffffffffu, j0 || j1);
+  const int src2 = hit2 ? __ffs(hit2) - 1 : 0;
+  SelResult r;
+  r.digit = (uint32_t)__shfl_sync(0xffffffffu, sb * bw + (j1 ? 2 * lane + 1 : 2 * lane), src2);
+  r.krem = krem - __shfl_sync(0xffffffffu, j1 ? a1 : a0, src2);
+  r.count = __shfl_sync(0xffffffffu, j1 ? b1 : b0, src2);
+  return r;
 }
+
+// Loads that stay where they are written (volatile), so the exponentials are requested before the normalisers.
+__device__ __forceinline__ float ld_early(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float2 ld_early2(const float2* p) {
+  float2 v;
+  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
+  return v;
+}
+
+constexpr int kSelTilesPerLane = 10;  // tile partials a normaliser lane holds: up to 320 tiles per head
+constexpr int kSelList = 32;          // boundary keys resolved by an exchanged list instead of a third pass
 
 template <int G>
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     const float* __restrict__ e_buf, const float2* __restrict__ part, int64_t max_tiles, int64_t max_blocks,
     int h_kv, int h_q, SessionArgs a, int rows_per_tile, int n_sink, int n_recent, int top_k, int budget,
     int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores, const float* __restrict__ gs_in) {
-  constexpr int NT = kSelectThreads;
+  constexpr int NT = kSelectThreads, NW = NT / 32;
+  constexpr int J = 8;  // keys per thread whose inputs are loaded together
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw);        // [slice_cap]
+  float* coef = reinterpret_cast<float*>(key + slice_cap);       // [tiles in slice][G]
+  __shared__ __align__(16) int hist[2][kSelBins];  // pass p builds hist[p & 1]; the other may still be read remotely
+  __shared__ __align__(16) int sup[2][kSelSup];
+  __shared__ int warp_cnt[NW][2];     // per warp: blocks kept for sure, keys equal to the boundary key
+  __shared__ int warp_taken[NW];      // per warp: boundary-list keys taken (list mode)
+  __shared__ int cnts[8][2];          // pushed by the lower-ranked CTAs of the cluster: the same, per CTA
+  __shared__ uint2 blist[8][kSelList];  // list mode: each CTA's boundary-bin keys (key, block), pushed to all
+  __shared__ int blist_n[8];
+  __shared__ int taken_cnt[8];        // list mode: keys of each CTA's list that are taken
+  __shared__ int own_taken[kSelList];  // list mode: this CTA's taken blocks
+  __shared__ int own_n, own_taken_n;
+  __shared__ SelResult s_res;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < kSelBins; i += NT) hist[0][i] = 0;
+  if (tid < 8) taken_cnt[tid] = 0;
+  if (tid < NW) warp_taken[tid] = 0;
+  if (tid == 0) own_n = own_taken_n = 0;
   griddep_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
   const int C = (int)cluster.num_blocks();
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw);        // [slice_cap]
-  float* coef = reinterpret_cast<float*>(key + slice_cap);       // [tiles in slice][G]
-  __shared__ float s_M[G], s_invZ[G];
-  __shared__ __align__(16) int hist[2][kRadixBins];  // double-buffered: pass p builds hist[p & 1] while others may read the other
-  __shared__ int scan_scratch[64];
-  __shared__ RadixResult res;
-  __shared__ int cnt[2];               // this CTA's (equal to T, kept otherwise) counts, read by higher ranks
-  __shared__ int sums[NT];             // per-thread merged bin counts, then the counts above each thread
-
-  const int s = blockIdx.z, g = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = blockIdx.z, g = blockIdx.y;
   const int n_blk = a.n_blk[s];
   const int sl = (n_blk + C - 1) / C;
   const int lo = min(n_blk, crank * sl), hi = min(n_blk, lo + sl);
-  const int n_tiles = (n_blk + rows_per_tile - 1) / rows_per_tile;
+  const int len = hi - lo;
+  const int n_iter = (len + NT - 1) / NT;
   int32_t* kept_row = kept + ((int64_t)s * h_kv + g) * budget;
+  const bool select_all = n_blk <= budget;  // uniform across the cluster
+  const int cand_lo = n_sink, cand_hi = n_blk - n_recent;  // candidates [cand_lo, cand_hi)
+  auto is_cand = [&](int b) { return b >= cand_lo && b < cand_hi; };
+  float* gs_dst = group_scores ? group_scores + ((int64_t)s * h_kv + g) * max_blocks : nullptr;
 
+  // ---- 1. group scores of the slice as order keys, and the pass-0 histogram of the candidates
+  // (plain shared-memory atomics measured faster here than aggregating equal digits within the warp first)
+  auto put_key = [&](bool valid, int b, float gsv) {
+    const uint32_t k = order_key(gsv);
+    if (valid) {
+      key[b - lo] = k;
+      if (gs_dst && gs_dst != gs_in) gs_dst[b] = gsv;
+      if (!select_all && is_cand(b)) atomicAdd(&hist[0][k >> 20], 1);
+    }
+  };
   if (gs_in != nullptr) {
     // group scores given (step-level scoring): keys straight from them
     const float* src = gs_in + ((int64_t)s * h_kv + g) * max_blocks;
-    float* gs_dst = (group_scores && group_scores != gs_in) ? group_scores + ((int64_t)s * h_kv + g) * max_blocks
-                                                              : nullptr;
-    for (int b = lo + tid; b < hi; b += NT) {
-      const float gs = src[b];
-      key[b - lo] = order_key(gs);
-      if (gs_dst) gs_dst[b] = gs;
+    __syncthreads();  // hist[0] cleared
+    for (int j = 0; j < n_iter; ++j) {
+      const int b = lo + tid + j * NT;
+      put_key(b < hi, b, b < hi ? src[b] : 0.f);
     }
   } else {
-    // 1. softmax normalisers of the group's heads (every CTA computes them the same way)
+    const float* e_src = e_buf + ((int64_t)s * h_kv + g) * G * max_blocks;  // [G][max_blocks]
+    const int n_tiles = (n_blk + rows_per_tile - 1) / rows_per_tile;
+    const int t0 = lo / rows_per_tile;
+    const int nt = hi > lo ? (hi - 1) / rows_per_tile - t0 + 1 : 0;
+    // the first J keys' exponentials and the tile partials are requested together, before any of them is
+    // used (one round of L2 latency for both)
+    float ev[J][G];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int b = lo + tid + j * NT;
+#pragma unroll
+      for (int h = 0; h < G; ++h) ev[j][h] = b < hi ? ld_early(e_src + (int64_t)h * max_blocks + b) : 0.f;
+    }
+    // softmax normaliser of query head `warp` (< G): M = the largest tile maximum, Z = the tile sums rescaled
+    // to M; then the slice's per-tile coefficients exp(m_tile - M) / Z.  Each lane holds its tiles' partials.
     if (warp < G) {
       const float2* p = part + ((int64_t)s * h_q + g * G + warp) * max_tiles;
+      float2 pt[kSelTilesPerLane];
+#pragma unroll
+      for (int i = 0; i < kSelTilesPerLane; ++i) {
+        const int t = lane + 32 * i;
+        pt[i] = t < n_tiles ? ld_early2(p + t) : make_float2(-INFINITY, 0.f);
+      }
       float M = -INFINITY;
-      for (int t = lane; t < n_tiles; t += 32) M = fmaxf(M, p[t].x);
+#pragma unroll
+      for (int i = 0; i < kSelTilesPerLane; ++i) M = fmaxf(M, pt[i].x);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
       float Z = 0.f;
-      for (int t = lane; t < n_tiles; t += 32) Z += p[t].y * expf(p[t].x - M);
+#pragma unroll
+      for (int i = 0; i < kSelTilesPerLane; ++i)
+        if (lane + 32 * i < n_tiles) Z += pt[i].y * expf(pt[i].x - M);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) Z += __shfl_xor_sync(0xffffffffu, Z, o);
-      if (lane == 0) {
-        s_M[warp] = M;
-        s_invZ[warp] = 1.f / Z;
+      const float invZ = 1.f / Z;
+#pragma unroll
+      for (int i = 0; i < kSelTilesPerLane; ++i) {
+        const int t = lane + 32 * i;
+        if (t >= t0 && t < t0 + nt) coef[(t - t0) * G + warp] = expf(pt[i].x - M) * invZ;
       }
     }
-    __syncthreads();
-    // 2. per-tile coefficients exp(m_tile - M) / Z for the tiles overlapping this slice
-    const int t0 = lo / rows_per_tile;
-    const int nt = hi > lo ? (hi - 1) / rows_per_tile - t0 + 1 : 0;
-    for (int i = tid; i < nt * G; i += NT) {
-      const int t = t0 + i / G, h = i % G;
-      const float2 p = part[((int64_t)s * h_q + g * G + h) * max_tiles + t];
-      coef[i] = expf(p.x - s_M[h]) * s_invZ[h];
-    }
-    __syncthreads();
-    // 3. group scores of the slice
-    const float* e_src = e_buf + ((int64_t)s * h_kv + g) * max_blocks * G;
-    float* gs_dst = group_scores ? group_scores + ((int64_t)s * h_kv + g) * max_blocks : nullptr;
-#pragma unroll 4
-    for (int b = lo + tid; b < hi; b += NT) {
-      const float* cf = coef + (b / rows_per_tile - t0) * G;
-      float gs = 0.f;
+    __syncthreads();  // coefficients ready, hist[0] cleared
+    for (int j0 = 0; j0 < n_iter; j0 += J) {
+      if (j0 > 0) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) gs = fmaf(e_src[(int64_t)b * G + h], cf[h], gs);
-      key[b - lo] = order_key(gs);
-      if (gs_dst) gs_dst[b] = gs;
+        for (int j = 0; j < J; ++j) {
+          const int b = lo + tid + (j0 + j) * NT;
+#pragma unroll
+          for (int h = 0; h < G; ++h) ev[j][h] = b < hi ? __ldcg(e_src + (int64_t)h * max_blocks + b) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int b = lo + tid + (j0 + j) * NT;
+        if (j0 + j < n_iter) {  // uniform across the CTA
+          float gsv = 0.f;
+          if (b < hi) {
+            const float* cf = coef + (b / rows_per_tile - t0) * G;
+#pragma unroll
+            for (int h = 0; h < G; ++h) gsv = fmaf(ev[j][h], cf[h], gsv);
+          }
+          put_key(b < hi, b, gsv);
+        }
+      }
     }
   }
-  __syncthreads();
 
-  if (n_blk <= budget) {  // every block is kept (uniform across the cluster)
+  if (select_all) {  // every block is kept
     for (int b = lo + tid; b < hi; b += NT) kept_row[b] = b;
     if (crank == 0)
       for (int i = n_blk + tid; i < budget; i += NT) kept_row[i] = -1;
     return;  // no distributed shared memory access on this path
   }
-  const int cand_lo = n_sink, cand_hi = n_blk - n_recent;  // candidates [cand_lo, cand_hi)
-  const int len = hi - lo;
-  const int n_iter = (len + NT - 1) / NT;
 
-  // 4. exact radix select of the top_k-th largest candidate key (11 + 11 + 10 bits).  Each CTA builds the
-  //    histogram of its slice; after one cluster barrier every CTA pulls all C histograms (independent
-  //    loads) and scans the merged counts itself, so all CTAs reach the same digit without a second barrier.
-  uint32_t prefix = 0, pmask = 0;
-  int krem = top_k;
+  // ---- 2. radix select of the top_k-th largest candidate key.  After pass p the boundary is the bin `prefix`
+  //         of the key's bits above `sh`.  The passes stop early when the boundary bin holds exactly the keys
+  //         still to take (all of them are kept), or, after the second pass, when it holds at most kSelList
+  //         keys: those are then exchanged as a list and ranked exactly in the compaction.
+  uint32_t prefix = 0;
+  int sh = 32, krem = top_k, bcount = 0;
+  bool resolved = top_k == 0;  // no candidate is taken: the boundary lies above every key
+  bool list_mode = false;
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
-    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-    const int nb = pass == 2 ? 1024 : 2048;
+  for (int pass = 0; pass < 3 && !resolved; ++pass) {
+    const int shift = sel_shift(pass), nb = sel_bins(pass);
     int* h = hist[pass & 1];
-    for (int i = tid; i < kRadixBins; i += NT) h[i] = 0;
-    __syncthreads();
-#pragma unroll 4
-    for (int j = 0; j < n_iter; ++j) {
-      const int b = lo + tid + j * NT;
-      int d = -1;
-      if (b < hi && b >= cand_lo && b < cand_hi) {
-        const uint32_t k = key[b - lo];
-        if ((k & pmask) == prefix) d = (int)((k >> shift) & (uint32_t)(nb - 1));
-      }
-      if (d >= 0) atomicAdd(&h[d], 1);
-    }
-    cluster.sync();  // every slice's histogram is complete (and the previous pass's pulls are done)
-    // merged counts of this thread's 4 bins (one 16-byte remote load per rank), then keys in bins owned by
-    // higher threads (reversed scan)
-    int local[4] = {0, 0, 0, 0}, sum = 0;
-    if (4 * tid < nb) {
-      int4 parts[8];
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        if (r < C) parts[r] = *reinterpret_cast<const int4*>(cluster.map_shared_rank(h, r) + 4 * tid);
-#pragma unroll
-      for (int r = 0; r < 8; ++r)
-        if (r < C) {
-          local[0] += parts[r].x;
-          local[1] += parts[r].y;
-          local[2] += parts[r].z;
-          local[3] += parts[r].w;
+    int* sp = sup[pass & 1];
+    if (pass > 0) {
+      // histogram of this pass's digit over the candidates inside the boundary bin (h was cleared below)
+      for (int j = 0; j < n_iter; ++j) {
+        const int b = lo + tid + j * NT;
+        if (b < hi && is_cand(b)) {
+          const uint32_t k = key[b - lo];
+          if ((k >> sh) == prefix) atomicAdd(&h[(k >> shift) & (uint32_t)(nb - 1)], 1);
         }
-      sum = local[0] + local[1] + local[2] + local[3];
-    }
-    const int rev = NT - 1 - tid;
-    sums[tid] = sum;
-    __syncthreads();
-    int total;
-    const int excl_rev = block_exclusive_scan_n<NT>(sums[rev], scan_scratch, &total);
-    sums[rev] = excl_rev;  // keys in bins owned by threads above `rev`
-    __syncthreads();
-    int above = sums[tid];
-#pragma unroll
-    for (int jb = 3; jb >= 0; --jb) {
-      const int bin = 4 * tid + jb;
-      if (bin < nb && local[jb] > 0 && above < krem && krem <= above + local[jb]) {
-        res.digit = (uint32_t)bin;
-        res.krem = krem - above;
       }
-      above += local[jb];
+    }
+    __syncthreads();  // this CTA's histogram is complete
+    // per-CTA super-bin sums (nb / 64 bins each)
+    {
+      const int bw = nb / kSelSup;
+      for (int sbin = warp; sbin < kSelSup; sbin += NW) {
+        int v = 0;
+        for (int i = lane; i < bw; i += 32) v += h[sbin * bw + i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) sp[sbin] = v;
+      }
+    }
+    cluster.sync();
+    // the other buffer (read remotely in the previous pass, finished by every CTA before this barrier) is
+    // cleared for the next pass
+    if (pass < 2)
+      for (int i = tid; i < kSelBins; i += NT) hist[(pass + 1) & 1][i] = 0;
+    if (warp == 0) {
+      const SelResult r = sel_boundary(cluster, C, sp, h, nb, krem);
+      if (lane == 0) s_res = r;
     }
     __syncthreads();
-    prefix |= res.digit << shift;
-    pmask |= (uint32_t)(nb - 1) << shift;
-    krem = res.krem;
-    __syncthreads();  // res and sums are rewritten by the next pass
+    const SelResult r = s_res;
+    prefix = sh == 32 ? r.digit : ((prefix << (sh - shift)) | r.digit);
+    sh = shift;
+    krem = r.krem;
+    bcount = r.count;
+    list_mode = pass == 1 && bcount != krem && bcount <= kSelList;
+    resolved = bcount == krem || sh == 0 || list_mode;
+    __syncthreads();  // s_res is rewritten by the next pass
   }
-  const uint32_t T = prefix;
-  const int need_eq = krem;  // how many keys equal to T are taken (lowest ids first, over the whole cluster)
   griddep_launch_dependents();  // the view kernel may be scheduled while the compaction runs
 
-  // 5. stable compaction.  Warp w owns slice positions [w * 32 * n_iter, (w + 1) * 32 * n_iter), lane-interleaved
-  //    (conflict-free shared-memory reads); block order is kept within and across warps and CTAs.
-  auto is_cand = [&](int b) { return b >= cand_lo && b < cand_hi; };
+  // ---- 3. compaction.  A candidate is kept if its bits above sh exceed the boundary prefix, or equal it and
+  //         either the whole boundary bin is taken, or (list mode) it ranks among the first krem of the
+  //         exchanged boundary list by (key, lower block first), or (sh == 0, equal keys) it is among the first
+  //         krem of the cluster's equal keys in block order.  Warp w owns slice positions
+  //         [w * 32 * n_iter, (w+1) * 32 * n_iter), lane-interleaved, so block order is kept within and across
+  //         warps and CTAs.
+  const bool all_eq = top_k == 0 ? false : bcount == krem;
+  const bool tie_mode = !all_eq && !list_mode && top_k > 0;
+  // 0 = dropped, 1 = kept, 2 = equal to the boundary key (tie mode), 3 = in the boundary list (list mode)
+  auto classify = [&](int b) -> int {
+    if (b >= hi) return 0;
+    if (!is_cand(b)) return 1;
+    if (top_k == 0) return 0;
+    const uint32_t kp = key[b - lo] >> sh;
+    if (kp > prefix) return 1;
+    if (kp < prefix) return 0;
+    return all_eq ? 1 : (list_mode ? 3 : 2);
+  };
   const int wbase = lo + warp * 32 * n_iter;
-  int eq_w = 0, gt_w = 0, nc_w = 0;
+  int keep_w = 0, eq_w = 0;
   for (int j = 0; j < n_iter; ++j) {
     const int b = wbase + j * 32 + lane;
-    bool eq = false, gt = false, nc = false;
-    if (b < hi) {
-      if (!is_cand(b)) {
-        nc = true;
-      } else {
-        const uint32_t k = key[b - lo];
-        eq = k == T;
-        gt = k > T;
+    const int cl = classify(b);
+    keep_w += __popc(__ballot_sync(0xffffffffu, cl == 1));
+    eq_w += __popc(__ballot_sync(0xffffffffu, cl == 2));
+    if (cl == 3) {  // at most kSelList keys over the cluster
+      const int i = atomicAdd(&own_n, 1);
+      if (i < kSelList) {
+        own_taken[i] = b;  // scratch until the list is ranked
       }
     }
-    eq_w += __popc(__ballot_sync(0xffffffffu, eq));
-    gt_w += __popc(__ballot_sync(0xffffffffu, gt));
-    nc_w += __popc(__ballot_sync(0xffffffffu, nc));
   }
-  int eq_cta, other_cta;
-  const int eq_before = block_exclusive_scan_n<NT>(lane == 0 ? eq_w : 0, scan_scratch, &eq_cta);
-  block_exclusive_scan_n<NT>(lane == 0 ? gt_w + nc_w : 0, scan_scratch, &other_cta);
+  if (lane == 0) {
+    warp_cnt[warp][0] = keep_w;
+    warp_cnt[warp][1] = eq_w;
+  }
+  __syncthreads();
   if (tid == 0) {
-    cnt[0] = eq_cta;
-    cnt[1] = other_cta;
+    int kc = 0, ec = 0;
+    for (int w2 = 0; w2 < NW; ++w2) {
+      kc += warp_cnt[w2][0];
+      ec += warp_cnt[w2][1];
+    }
+    // pushed into every higher-ranked CTA: after the barrier each CTA reads only its own shared memory, so no
+    // CTA needs to wait for another before it exits
+    for (int r = crank + 1; r < C; ++r) {
+      int* dst = cluster.map_shared_rank(&cnts[0][0], r) + 2 * crank;
+      dst[0] = kc;
+      dst[1] = ec;
+    }
+  }
+  if (list_mode) {
+    // this CTA's boundary keys, pushed into every CTA of the cluster (itself included)
+    const int n_own = min(own_n, kSelList);
+    for (int i = tid; i < C * kSelList; i += NT) {
+      const int r = i / kSelList, k = i - r * kSelList;
+      if (k < n_own) {
+        const int b = own_taken[k];
+        cluster.map_shared_rank(&blist[0][0], r)[crank * kSelList + k] = make_uint2(key[b - lo], (uint32_t)b);
+      }
+      if (k == 0) cluster.map_shared_rank(blist_n, r)[crank] = n_own;
+    }
   }
   cluster.sync();
-  // counts of the lower ranks: ties before this CTA, and kept blocks before it
-  int eq_base = 0, keep_base = 0;
+  if (list_mode) {
+    // rank every listed key by (key descending, block ascending); the first krem are taken
+    if (warp == 0) {
+      uint2 e = make_uint2(0u, 0xFFFFFFFFu);
+      int src = -1, seen = 0;
+      for (int r = 0; r < C; ++r) {
+        const int n = blist_n[r];
+        if (lane >= seen && lane < seen + n) {
+          e = blist[r][lane - seen];
+          src = r;
+        }
+        seen += n;
+      }
+      int rank = 0;
+      for (int o = 0; o < seen; ++o) {
+        const uint32_t ok = __shfl_sync(0xffffffffu, e.x, o), ob = __shfl_sync(0xffffffffu, e.y, o);
+        rank += (ok > e.x || (ok == e.x && ob < e.y)) ? 1 : 0;
+      }
+      const bool take = src >= 0 && rank < krem;
+      if (take) {
+        atomicAdd(&taken_cnt[src], 1);
+        if (src == crank) {
+          own_taken[atomicAdd(&own_taken_n, 1)] = (int)e.y;
+          atomicAdd(&warp_taken[((int)e.y - lo) / (32 * n_iter)], 1);
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // blocks kept before this warp (cluster-wide, in block order), and ties taken before it
+  int keep_base = 0, eq_base = 0;
   for (int r = 0; r < crank; ++r) {
-    const int* rc = cluster.map_shared_rank(cnt, r);
-    const int e_r = rc[0], o_r = rc[1];
-    const int taken = max(0, min(e_r, need_eq - eq_base));
-    keep_base += o_r + taken;
-    eq_base += e_r;
+    const int taken = tie_mode ? max(0, min(cnts[r][1], krem - eq_base)) : (list_mode ? taken_cnt[r] : 0);
+    keep_base += cnts[r][0] + taken;
+    eq_base += cnts[r][1];
   }
-  // per warp: ties before the warp (within the cluster) and kept blocks before the warp
-  const int eq_warp0 = eq_base + __shfl_sync(0xffffffffu, eq_before, 0);
-  int keep_w = 0;
-  {
-    int eq_run = eq_warp0;
-    for (int j = 0; j < n_iter; ++j) {
-      const int b = wbase + j * 32 + lane;
-      bool keep = false, eq = false;
-      if (b < hi) {
-        if (!is_cand(b)) {
-          keep = true;
-        } else {
-          const uint32_t k = key[b - lo];
-          eq = k == T;
-          keep = k > T;
-        }
-      }
-      const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-      if (eq) keep = eq_run + __popc(eqm & ((1u << lane) - 1)) < need_eq;
-      eq_run += __popc(eqm);
-      keep_w += __popc(__ballot_sync(0xffffffffu, keep));
-    }
+  for (int w2 = 0; w2 < warp; ++w2) {
+    const int taken = tie_mode ? max(0, min(warp_cnt[w2][1], krem - eq_base)) : (list_mode ? warp_taken[w2] : 0);
+    keep_base += warp_cnt[w2][0] + taken;
+    eq_base += warp_cnt[w2][1];
   }
-  int keep_cta;
-  const int keep_before = block_exclusive_scan_n<NT>(lane == 0 ? keep_w : 0, scan_scratch, &keep_cta);
-  int pos = keep_base + __shfl_sync(0xffffffffu, keep_before, 0);
-  {
-    int eq_run = eq_warp0;
-    for (int j = 0; j < n_iter; ++j) {
-      const int b = wbase + j * 32 + lane;
-      bool keep = false, eq = false;
-      if (b < hi) {
-        if (!is_cand(b)) {
-          keep = true;
-        } else {
-          const uint32_t k = key[b - lo];
-          eq = k == T;
-          keep = k > T;
-        }
-      }
-      const unsigned eqm = __ballot_sync(0xffffffffu, eq);
-      if (eq) keep = eq_run + __popc(eqm & ((1u << lane) - 1)) < need_eq;
-      eq_run += __popc(eqm);
-      const unsigned km = __ballot_sync(0xffffffffu, keep);
-      if (keep) kept_row[pos + __popc(km & ((1u << lane) - 1))] = b;
-      pos += __popc(km);
-    }
+  int pos = keep_base, eq_run = eq_base;
+  for (int j = 0; j < n_iter; ++j) {
+    const int b = wbase + j * 32 + lane;
+    const int cl = classify(b);
+    bool kp = cl == 1;
+    const unsigned eqm = __ballot_sync(0xffffffffu, cl == 2);
+    if (cl == 2) kp = eq_run + __popc(eqm & ((1u << lane) - 1)) < krem;
+    eq_run += __popc(eqm);
+    if (cl == 3)
+      for (int i = 0; i < own_taken_n; ++i) kp |= own_taken[i] == b;
+    const unsigned km = __ballot_sync(0xffffffffu, kp);
+    const int slot = pos + __popc(km & ((1u << lane) - 1));
+    if (kp && slot < budget) kept_row[slot] = b;  // never past the row, whatever the keys hold
+    pos += __popc(km);
   }
-  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 template <int G>
@@ -489,11 +625,17 @@ cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, in
   if (part_heads < 0) part_heads = c.p.h_q;  // score rows per session in the tile partials
   int C = (max_blk + 4095) / 4096;
   C = C < 1 ? 1 : (C > 8 ? 8 : C);
+  if (gs_in == nullptr && (max_blk + rpt - 1) / rpt > 32 * kSelTilesPerLane) return cudaErrorInvalidValue;
   const int slice_cap = (max_blk + C - 1) / C;
   const int tiles_cap = slice_cap / rpt + 2;
   const size_t smem_b = (size_t)slice_cap * 4 + (size_t)tiles_cap * G * 4;
   auto kb = select_kernel<G>;
   cudaError_t e;
+  cudaFuncAttributes fa;
+  if ((e = cudaFuncGetAttributes(&fa, kb)) != cudaSuccess) return e;
+  int optin = 0;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device)) != cudaSuccess) return e;
+  if (smem_b + fa.sharedSizeBytes > (size_t)optin) return cudaErrorInvalidValue;
   if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
   return launch_pdl(kb, dim3(C, c.p.h_kv, n_sessions), dim3(kSelectThreads), smem_b, st, C, (const float*)c.e_buf,
                     (const float2*)c.part, c.max_tiles, c.p.max_blocks, c.p.h_kv, part_heads, a, rpt, c.p.n_sink,

@@ -209,7 +209,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // k = 8 cc + v (v < 8) with cc = lane % CPR.  Their offset cos/sin (r * theta_k, block-independent, from the
   // context's table) stay in registers for the whole kernel: of[pass][u] holds pairs 2u and 2u + 1.  They are
   // loaded before the wait on the preceding kernel, which wrote none of them.
-  float4 of[Q::PASSES][4];
+  // Each is held as two packed pairs (cos of pairs 2u and 2u + 1; sin of the same), the operands of the paired
+  // fp32 instructions below.
+  uint64_t ofc[Q::PASSES][4], ofs[Q::PASSES][4];
   if (kWrite && warp < kRot) {
     const int cc = lane % Q::CPR;
 #pragma unroll
@@ -218,7 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 4; ++u) {
         const float2* t = vp.rope_off + (lane / Q::CPR + Q::RPP * pass) * (D / 2) + 8 * cc + 2 * u;
         const float2 o0 = __ldg(t), o1 = __ldg(t + 1);
-        of[pass][u] = make_float4(o0.x, o0.y, o1.x, o1.y);
+        ofc[pass][u] = pk2(o0.x, o1.x);
+        ofs[pass][u] = pk2(o0.y, o1.y);
       }
   }
   griddep_wait();  // kept ids, queries, views and outputs belong to the stream order from here on
@@ -329,6 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ============================================================ rotation warps
     if (kWrite) {
       const int cc = lane % Q::CPR;
+      int prev_st = -1;  // stage of this warp's previous block, freed one block later
       for (int64_t jj = warp; jj < nb; jj += kRot) {
         const int st = (int)(jj % NS);
         const uint32_t phase = (uint32_t)((jj / NS) & 1);
@@ -350,81 +354,79 @@ __global__ void __launch_bounds__(kThreads, 1)
             unsigned char* kst = smem + st * 2 * Q::PAGE;
             uint4* kq = reinterpret_cast<uint4*>(kst);  // the stage's K page as 16-byte chunks
             const float4* __restrict__ tabh = reinterpret_cast<const float4*>(smem + Q::OFF_TAB + st * 2 * Q::TAB);
-            float2 bb[8];
+            // the block's base cos/sin for this lane's 8 pairs, as packed pairs (2u, 2u + 1)
+            uint64_t bc[4], bs[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const float4 t = tabh[4 * cc + u];
-              bb[2 * u] = make_float2(t.x, t.y);
-              bb[2 * u + 1] = make_float2(t.z, t.w);
+              const float4 t = tabh[4 * cc + u];  // (cos, sin) of pair 2u, then of pair 2u + 1
+              bc[u] = pk2(t.x, t.z);
+              bs[u] = pk2(t.y, t.w);
             }
-            // one pass = row r = lane / CPR + RPP * pass, chunks cc and cc + d/16 (8 pairs); the next pass's
-            // operands are loaded before this pass's results are stored.
+            // one pass = row r = lane / CPR + RPP * pass, chunks cc and cc + d/16 (8 pairs).  Each pair of pairs is
+            // rotated with
+            // the paired fp32 instructions, every element rounded exactly as by the scalar operations:
+            //   cs = fma(bc, oc, -bs * os), sn = fma(bs, oc, bc * os), f1 = fma(x1, cs, -x2 * sn),
+            //   f2 = fma(x2, cs, x1 * sn).
             // Accuracy: with the fp32 tables (each within 2^-24 relative of the fp64 value) the composed cos/sin
             // are within 4 * 2^-24 of exact and the rotated f within 2^-24 (5 (|x1| + |x2|) + |f|), less than one
-            // bf16 ulp of f (> 2^-8 |f|) whenever |f| >= 2^-13 (|x1| + |x2|).  Pairs below that (the rotation
-            // cancels) keep their original bits in the stage, are flagged, and are redone in float-float after
-            // the passes, so every stored key is within one ulp of the exact rotation.
+            // bf16 ulp of f (> 2^-8 |f|) whenever |f| >= 2^-13 (|x1| + |x2|).  A pass holding a pair below that
+            // (the rotation cancels) keeps the original bits of its row in the stage and is redone in
+            // float-float after the passes, so every stored key is within one ulp of the exact rotation.
             uint4 wa = kq[chunk_off(lane / Q::CPR, cc) >> 4], wb = kq[chunk_off(lane / Q::CPR, cc + D / 16) >> 4];
-            uint64_t redo_all = 0;  // bit 8 * pass + v
+            uint32_t redo_all = 0;  // bit pass
 #pragma unroll
             for (int pass = 0; pass < Q::PASSES; ++pass) {
               const int r = lane / Q::CPR + Q::RPP * pass;
-              uint4 wa_n = wa, wb_n = wb;
-              if (pass + 1 < Q::PASSES) {
-                const int rn = r + Q::RPP;
-                wa_n = kq[chunk_off(rn, cc) >> 4];
-                wb_n = kq[chunk_off(rn, cc + D / 16) >> 4];
+              if (pass > 0) {
+                wa = kq[chunk_off(r, cc) >> 4];
+                wb = kq[chunk_off(r, cc + D / 16) >> 4];
               }
               const uint32_t xa[4] = {wa.x, wa.y, wa.z, wa.w}, xb[4] = {wb.x, wb.y, wb.z, wb.w};
-              uint32_t oa[4], ob[4], redo = 0;
+              uint32_t oa[4], ob[4];
+              bool cancel = false;
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                float f1[2], f2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const int v = 2 * u + e;
-                  float cs, sn;
-                  rope_cs(bb[v], e ? of[pass][u].z : of[pass][u].x, e ? of[pass][u].w : of[pass][u].y, cs, sn);
-                  const float x1 = e ? bf16hi(xa[u]) : bf16lo(xa[u]);
-                  const float x2 = e ? bf16hi(xb[u]) : bf16lo(xb[u]);
-                  f1[e] = fmaf(x1, cs, -x2 * sn);
-                  f2[e] = fmaf(x2, cs, x1 * sn);
-                  redo |= (fminf(fabsf(f1[e]), fabsf(f2[e])) < 0x1p-13f * (fabsf(x1) + fabsf(x2))) ? (1u << v) : 0u;
-                }
-                oa[u] = pack_bf16x2(f1[0], f1[1]);
-                ob[u] = pack_bf16x2(f2[0], f2[1]);
+                const uint64_t cs = fma2(bc[u], ofc[pass][u], mul2(bs[u] ^ 0x8000000080000000ull, ofs[pass][u]));
+                const uint64_t sn = fma2(bs[u], ofc[pass][u], mul2(bc[u], ofs[pass][u]));
+                const float x1l = bf16lo(xa[u]), x1h = bf16hi(xa[u]), x2l = bf16lo(xb[u]), x2h = bf16hi(xb[u]);
+                const uint64_t x1 = pk2(x1l, x1h), x2 = pk2(x2l, x2h), nx2 = pk2(-x2l, -x2h);
+                float f1l, f1h, f2l, f2h;
+                up2(fma2(x1, cs, mul2(nx2, sn)), f1l, f1h);
+                up2(fma2(x2, cs, mul2(x1, sn)), f2l, f2h);
+                cancel |= fminf(fabsf(f1l), fabsf(f2l)) * 0x1p13f < fabsf(x1l) + fabsf(x2l);
+                cancel |= fminf(fabsf(f1h), fabsf(f2h)) * 0x1p13f < fabsf(x1h) + fabsf(x2h);
+                oa[u] = pack_bf16x2(f1l, f1h);
+                ob[u] = pack_bf16x2(f2l, f2h);
               }
-              if (redo) {  // flagged pairs keep their original bits until the fix-up below
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                  const uint32_t m = ((redo >> (2 * u)) & 1u ? 0x0000FFFFu : 0u) | ((redo >> (2 * u + 1)) & 1u ? 0xFFFF0000u : 0u);
-                  oa[u] = (oa[u] & ~m) | (xa[u] & m);
-                  ob[u] = (ob[u] & ~m) | (xb[u] & m);
-                }
-                redo_all |= (uint64_t)redo << (8 * pass);
+              if (cancel) {  // the row's chunks keep their original bits until the fix-up below
+                redo_all |= 1u << pass;
+              } else {
+                kq[chunk_off(r, cc) >> 4] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+                kq[chunk_off(r, cc + D / 16) >> 4] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
               }
-              kq[chunk_off(r, cc) >> 4] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-              kq[chunk_off(r, cc + D / 16) >> 4] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-              wa = wa_n;
-              wb = wb_n;
             }
-            if (redo_all) {  // rare: float-float rotation of the flagged pairs, read back from the stage
+            if (redo_all) {  // rare: float-float rotation of the flagged passes' pairs, read back from the stage
               const float2* tabl = reinterpret_cast<const float2*>(smem + Q::OFF_TAB + st * 2 * Q::TAB + Q::TAB);
               const float2* tabh2 = reinterpret_cast<const float2*>(tabh);
 #pragma unroll 1
-              for (uint64_t m = redo_all; m; m &= m - 1) {
-                const int bit = __ffsll((long long)m) - 1, pass = bit >> 3, v = bit & 7, k = 8 * cc + v;
+              for (uint32_t m = redo_all; m; m &= m - 1) {
+                const int pass = __ffs(m) - 1;
                 const int r = lane / Q::CPR + Q::RPP * pass;
-                uint16_t* e1 = reinterpret_cast<uint16_t*>(kst + chunk_off(r, cc)) + v;
-                uint16_t* e2 = reinterpret_cast<uint16_t*>(kst + chunk_off(r, cc + D / 16)) + v;
-                const float x1 = __uint_as_float((uint32_t)*e1 << 16), x2 = __uint_as_float((uint32_t)*e2 << 16);
-                const float2 bh = tabh2[k], bl = tabl[k];
-                const float2 oh = __ldg(vp.rope_off + r * (D / 2) + k), ol = __ldg(vp.rope_off_lo + r * (D / 2) + k);
-                float y1, y2;
-                rotate_exact(x1, x2, make_float4(bh.x, bl.x, bh.y, bl.y), make_float4(oh.x, ol.x, oh.y, ol.y), y1, y2);
-                const uint32_t y = pack_bf16x2(y1, y2);
-                *e1 = (uint16_t)(y & 0xFFFFu);
-                *e2 = (uint16_t)(y >> 16);
+#pragma unroll 1
+                for (int v = 0; v < 8; ++v) {
+                  const int k = 8 * cc + v;
+                  uint16_t* e1 = reinterpret_cast<uint16_t*>(kst + chunk_off(r, cc)) + v;
+                  uint16_t* e2 = reinterpret_cast<uint16_t*>(kst + chunk_off(r, cc + D / 16)) + v;
+                  const float x1 = __uint_as_float((uint32_t)*e1 << 16), x2 = __uint_as_float((uint32_t)*e2 << 16);
+                  const float2 bh = tabh2[k], bl = tabl[k];
+                  const float2 oh = __ldg(vp.rope_off + r * (D / 2) + k), ol = __ldg(vp.rope_off_lo + r * (D / 2) + k);
+                  float y1, y2;
+                  rotate_exact(x1, x2, make_float4(bh.x, bl.x, bh.y, bl.y), make_float4(oh.x, ol.x, oh.y, ol.y), y1,
+                               y2);
+                  const uint32_t y = pack_bf16x2(y1, y2);
+                  *e1 = (uint16_t)(y & 0xFFFFu);
+                  *e2 = (uint16_t)(y >> 16);
+                }
               }
             }
             if (valid < 32) {  // partial block: plain stores of the rows present, from the stage
@@ -450,16 +452,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_store_2d(&tm_kdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + b * Q::BOX);
                 tma_store_2d(&tm_vdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + Q::PAGE + b * Q::BOX);
               }
-              bulk_commit();
             }
         }
-        // the attention warp may read the rotated page now; the stage is free once the view stores read it
+        // The attention warp may read the rotated page now.  This block's view stores form one bulk group (empty
+        // when there are none); the stage is free once the group has read its source.  Fused: the stage's
+        // attention warp holds it for a while anyway, so this warp frees the stage of its previous block after
+        // issuing this block's stores and never waits for stores it has just issued.  Materialising only, the
+        // stage is freed at once (its load refill is then the one thing waiting on it).
         if (lane == 0) {
-          if (kAttend) mbar_arrive(&rotated[st]);
-          bulk_wait_read_all();
-          mbar_arrive(&empty[st]);
+          bulk_commit();
+          if constexpr (kAttend) {
+            mbar_arrive(&rotated[st]);
+            if (prev_st >= 0) {
+              bulk_wait_read<1>();
+              mbar_arrive(&empty[prev_st]);
+            }
+          } else {
+            bulk_wait_read<0>();
+            mbar_arrive(&empty[st]);
+          }
         }
+        prev_st = kAttend ? st : -1;
         __syncwarp();
+      }
+      if (kAttend && !aborted && prev_st >= 0 && lane == 0) {
+        bulk_wait_read<0>();
+        mbar_arrive(&empty[prev_st]);
       }
     }
   } else if (warp < kProducer) {
@@ -641,9 +659,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  griddep_launch_dependents();     // the next kernel may be scheduled while this one merges and drains
-  if (lane == 0) bulk_wait_all();  // this warp's view stores are complete
-  __threadfence();                 // this thread's records are visible GPU-wide before the CTA counts itself in
+  griddep_launch_dependents();  // the next kernel may be scheduled while this one merges and drains
+  // The view stores' shared-memory sources are read (the writes themselves complete with the grid; nothing in
+  // this kernel reads the view).  The attention warps' records are read below by this CTA only, after the
+  // barrier; the CTA record the other CTAs read is fenced before the CTA counts itself in.
+  if (lane == 0) bulk_wait_read_all();
   if (__syncthreads_or(aborted)) {
     if (warp == kProducer && lane == 0) {
       // copies still in flight into a stage must land before the CTA exits: wait (bounded) for the
