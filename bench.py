@@ -137,85 +137,144 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------------- CPU oracle timing
-def _oracle_child(name: str, reps: int, warmup: int):
-    """Child-process body: times the oracle on one KV head of layer 0 and prints JSON."""
+_UNIT = {}  # the sampled layer's inputs, shared with the forked workers (copy on write)
+
+
+def _oracle_unit(unit):
+    """One (session, KV head) unit of one layer's step, by the oracle; returns the kept block count."""
     from oracle import kvm_oracle as O
-    w = synth.WORKLOADS[name]
-    g = 0
-    bt = synth.block_table(w)
-    k, v = synth.kv_pool(w, 0, bt, sessions=[0], heads=(g, g + 1))
-    q = synth.queries(w, 0)[0, 0]
-    keys = O.paged_tokens(k, bt[0], g, w.n_tok)
-    vals = O.paged_tokens(v, bt[0], g, w.n_tok)
-    n_hist = w.n_tok - w.append_tok
-    hist_index = O.mean_k_index(keys[:n_hist]) if n_hist > 0 else np.zeros((0, w.d))
+    s, g = unit
+    w, k, v, bt, q = _UNIT["w"], _UNIT["k"], _UNIT["v"], _UNIT["bt"], _UNIT["q"]
     G = w.group
-    qg = q[G * g:G * (g + 1)]
-    times, n_keep = [], 0
-    static_idx = None if w.append_tok else O.mean_k_index(keys)  # no append: the index is state, as on the GPU
-    if w.n_q > 1:  # a step of n_q query tokens: step scores, select, materialise, step attention
-        qs = synth.queries(w, 0)[0][:, G * g:G * (g + 1)]
-        for i in range(warmup + reps):
-            t0 = time.perf_counter()
-            gs = O.step_group_scores(qs, static_idx[None])[0]
-            ids = O.select_blocks(gs, w.n_blk, w.n_sink, w.n_recent, w.top_k)
-            kv, vv = O.materialize(keys, vals, ids, w.n_tok, w.rope_theta)
-            O.step_view_attention(qs, kv, vv, w.rope_theta)
-            n_keep = len(ids)
-            if i >= warmup:
-                times.append(time.perf_counter() - t0)
-        print(json.dumps({"seconds": statistics.median(times), "n_keep": n_keep, "reps": len(times)}), flush=True)
-        return
-    for i in range(warmup + reps):
-        t0 = time.perf_counter()
-        idx = O.index_append(hist_index, keys, n_hist, w.append_tok) if w.append_tok else static_idx
+    keys = O.paged_tokens(k, bt[s], g, w.n_tok)
+    vals = O.paged_tokens(v, bt[s], g, w.n_tok)
+    if w.n_q > 1:  # a step of query tokens: step scores, select, materialise, step attention
+        qs = q[s][:, G * g:G * (g + 1)]
+        gs = O.step_group_scores(qs, _UNIT["hist_index"][unit][None])[0]
+        ids = O.select_blocks(gs, w.n_blk, w.n_sink, w.n_recent, w.top_k)
+        kv, vv = O.materialize(keys, vals, ids, w.n_tok, w.rope_theta)
+        O.step_view_attention(qs, kv, vv, w.rope_theta)
+    else:  # the decode step: append, score, select, materialise, attend
+        idx = _UNIT["hist_index"][unit]
+        if w.append_tok:
+            idx = O.index_append(idx, keys, w.n_tok - w.append_tok, w.append_tok)
+        qg = q[s, 0, G * g:G * (g + 1)]
         gs = O.gqa_softmax_sum(O.block_scores(qg, idx[None]), 1)[0]
         ids = O.select_blocks(gs, w.n_blk, w.n_sink, w.n_recent, w.top_k)
         kv, vv = O.materialize(keys, vals, ids, w.n_tok, w.rope_theta)
         O.decode_attention(qg, kv, vv, w.rope_theta)
-        n_keep = len(ids)
+    return len(ids)
+
+
+def _oracle_worker(conn, my_units):
+    """Worker process: builds the index state of its units (untimed), then runs them on every request."""
+    from oracle import kvm_oracle as O
+    w, k, bt = _UNIT["w"], _UNIT["k"], _UNIT["bt"]
+    n_hist = w.n_tok - w.append_tok
+    n_idx = n_hist if w.append_tok else w.n_tok
+    for s, g in my_units:  # the index before the step, built outside the timed region as on the GPU
+        parts = []  # block by block in pieces (the blocks are independent), so the temporaries stay small
+        for b0 in range(0, -(-n_idx // 32), 2048):
+            t0 = b0 * 32
+            t1 = min(n_idx, t0 + 2048 * 32)
+            parts.append(O.mean_k_index(O.paged_tokens(k, bt[s][b0:], g, t1 - t0)))
+        _UNIT["hist_index"][(s, g)] = np.concatenate(parts) if parts else np.zeros((0, w.d))
+    conn.send("ready")
+    n_keep = 0
+    while conn.recv() == "go":
+        for u in my_units:
+            n_keep = _oracle_unit(u)
+        conn.send(n_keep)
+
+
+def _oracle_child(name: str, reps: int, warmup: int, q_tokens: int):
+    """Child-process body (no GPU): times the oracle on every (session, KV head) unit of layer 0, the units
+    spread over one forked worker process per host core (each worker always runs the same units), and prints
+    JSON."""
+    import multiprocessing as mp
+    w = synth.WORKLOADS[name]
+    if q_tokens and w.n_q > q_tokens:
+        w = w.with_(n_q=q_tokens)
+    bt = synth.block_table(w)
+    k, v = synth.kv_pool(w, 0, bt)
+    q = synth.queries(w, 0)
+    units = [(s, g) for s in range(w.n_sessions) for g in range(w.h_kv)]
+    _UNIT.update(w=w, k=k, v=v, bt=bt, q=q, hist_index={})
+    n_workers = max(1, min(os.cpu_count() or 1, len(units)))
+    # forked once the inputs exist (this process never touches a GPU), so the workers share them
+    ctx = mp.get_context("fork")
+    pipes, procs = [], []
+    for i in range(n_workers):
+        a, b = ctx.Pipe()
+        p = ctx.Process(target=_oracle_worker, args=(b, units[i::n_workers]), daemon=True)
+        p.start()
+        pipes.append(a)
+        procs.append(p)
+    for a in pipes:
+        assert a.recv() == "ready"
+    walls, n_keep = [], 0
+    for i in range(warmup + reps):
+        t0 = time.perf_counter()
+        for a in pipes:
+            a.send("go")
+        n_keep = [a.recv() for a in pipes][0]
         if i >= warmup:
-            times.append(time.perf_counter() - t0)
-    print(json.dumps({"seconds": statistics.median(times), "n_keep": n_keep, "reps": len(times)}), flush=True)
+            walls.append(time.perf_counter() - t0)
+    for a in pipes:
+        a.send("stop")
+    for p in procs:
+        p.join(timeout=10)
+    print(json.dumps({"seconds": statistics.median(walls), "n_keep": n_keep, "reps": len(walls),
+                      "workers": n_workers, "units": len(units), "n_q": w.n_q}), flush=True)
 
 
 def oracle_sample(w: synth.Workload, reps: int, warmup: int):
-    """Times the oracle on one KV head of layer 0 (the step's work for that head), in a child
-    process with every BLAS / OpenMP pool pinned to one thread (so `cores` is exact).
+    """Times the oracle on one whole layer of the workload (every (session, KV head) unit, in parallel on the
+    host's cores), in a child process with every BLAS / OpenMP pool pinned to one thread per worker.  For a step
+    of many query tokens only the first 16 tokens are sampled (the rest of the step scales the score and the
+    attention work linearly).
 
-    Returns (seconds per sampled (layer, KV head) step, threads used, description).
+    Returns (seconds per layer, worker processes used, description).
     """
+    q_tokens = 16 if w.n_q > 16 else 0
     env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", w.name, str(reps), str(warmup)],
-                       capture_output=True, text=True, env=env, check=True)
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-child", w.name, str(reps), str(warmup),
+                        str(q_tokens)], capture_output=True, text=True, env=env, check=True)
     res = json.loads(r.stdout.strip().splitlines()[-1])
+    units = res["units"]
     if w.n_q > 1:
-        desc = (f"oracle (numpy fp64, 1 thread) on KV head 0 of layer 0 of {w.name}: step scores of {w.n_q} tokens x "
-                f"{w.group} query heads over {w.n_blk} blocks, select, materialise {res['n_keep']} blocks, causal "
-                f"attention of the {w.n_q} tokens over the view; per-layer value = {w.h_kv * w.n_sessions} "
-                f"(session, KV head) units x that time")
+        desc = (f"oracle (numpy fp64) on layer 0 of {w.name}: the first {res['n_q']} of the step's {w.n_q} query "
+                f"tokens (step scores over {w.n_blk} blocks, select, materialise {res['n_keep']} blocks, causal "
+                f"attention over the view) for all {units} (session, KV head) units, {res['workers']} worker "
+                f"processes of one thread each, wall time per layer (median of {res['reps']})")
     else:
-        desc = (f"oracle (numpy fp64, 1 thread) on KV head 0 of layer 0 of {w.name}: append {w.append_tok} tokens, "
-                f"score {w.n_blk} blocks for {w.group} query heads, select, materialise {res['n_keep']} blocks, "
-                f"attend; per-layer value = {w.h_kv * w.n_sessions} (session, KV head) units x that time")
-    return res["seconds"], 1, desc
+        desc = (f"oracle (numpy fp64) on layer 0 of {w.name}: append {w.append_tok} tokens, score {w.n_blk} blocks "
+                f"for {w.group} query heads, select, materialise {res['n_keep']} blocks, attend, for all {units} "
+                f"(session, KV head) units, {res['workers']} worker processes of one thread each, wall time per "
+                f"layer (median of {res['reps']})")
+    return res["seconds"], res["workers"], desc
 
 
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    per_head_s, threads, desc = oracle_sample(w, args.steps, args.warmup)
-    us_layer = per_head_s * w.h_kv * w.n_sessions * 1e6
+    layer_s, workers, desc = oracle_sample(w, args.steps, args.warmup)
+    scale = w.n_q / min(w.n_q, 16) if w.n_q > 1 else 1.0  # a step's sample covers its first 16 query tokens
+    if scale != 1.0:
+        desc += f"; scaled by {scale:g} to the step's {w.n_q} query tokens"
+    us_layer = layer_s * scale * 1e6
     gbs = must_touch_bytes(w) / (us_layer * 1e-6) / 1e9
     line = {"impl": "reference", "metric": METRIC if w.n_q == 1 else STEP_METRIC, "value": round(us_layer, 1),
             "unit": "us/layer",
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us_layer * w.n_layers / 1e3, 3),
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            # one timed step is one layer of the workload (all of its units), measured, not extrapolated
+            "ms_per_step": round(us_layer / 1e3, 3), "layers_per_step": 1,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "sample": "1 KV head of 1 layer per step"},
+            "config": {"workload": w.name, "sample": "layer 0 of the workload per step, every (session, KV head) unit"},
             "hbm_gbps_equivalent": round(gbs, 3),
-            "cpu_baseline": {"value": round(us_layer, 1), "unit": "us/layer", "cores": threads, "kind": "oracle",
+            "cpu_baseline": {"value": round(us_layer, 1), "unit": "us/layer", "cores": workers, "kind": "oracle",
                              "sample": desc},
             "e2e": {"value": round(us_layer, 1), "unit": "us/layer", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -313,6 +372,8 @@ def run_kvm(args, w):
         layers_after_appends(call_select, call_view)
 
     stage_fns = {"index_append": call_append, "score_select": call_select, "materialize_attn": call_view}
+    if not w.append_tok:
+        del stage_fns["index_append"]  # nothing is appended inside this workload's step
 
     for _ in range(args.warmup):
         step()
@@ -474,11 +535,22 @@ def run_kvm(args, w):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        per_head_s, threads, desc = oracle_sample(w, 1, 0)
-        cpu = {"value": round(per_head_s * w.h_kv * w.n_sessions * 1e6, 1), "unit": "us/layer", "cores": threads,
-               "kind": "oracle", "sample": desc}
+        layer_s, workers, desc = oracle_sample(w, 1, 0)
+        cpu = {"value": round(layer_s * 1e6, 1), "unit": "us/layer", "cores": workers, "kind": "oracle",
+               "sample": desc}
 
     traffic = recorded_traffic(w.name, "view_kernel", VIEW_KERNEL_SOURCES)
+
+    per_config = None
+    if (rank == 0 and world == 1 and not args.no_per_config and w.name == "ws1m_16layer" and args.layers is None
+            and args.selection == "kvmem"):
+        # the other workloads run in child processes; this one's pools are released first
+        kp.clear()
+        vp.clear()
+        index.clear()
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        per_config = per_config_entries(args)
 
     if rank == 0:
         line = {
@@ -488,7 +560,10 @@ def run_kvm(args, w):
             "config": {"workload": w.name, "h_q": w.h_q, "h_kv": w.h_kv, "d": w.d, "history_tokens": w.n_tok,
                        "layers": L, "sessions_per_gpu": S, "view_tokens": w.view_tokens, "append_tokens": w.append_tok,
                        "kv_dtype": "bf16", "cuda_graph": graph is not None, "selection": args.selection,
-                       "l2": "inputs larger than L2 (index 128 MiB + K/V pool 4 GiB per layer), no flush",
+                       "l2": (f"each layer's step touches {bytes_layer / 2**20:.0f} MiB (the index, kept K/V pages "
+                              f"and the views), more than the 126 MB L2: no flush" if bytes_layer > 126e6 else
+                              f"each layer's step touches {bytes_layer / 2**20:.2f} MiB, which stays in L2: a "
+                              f"launch-bound case, reported in microseconds only"),
                        "parallelism": f"replicas x{world}"},
             "hbm_gbps": round(gbs, 1), "must_touch_bytes_per_layer": bytes_layer,
             "hbm_frac_of_measured": round(bytes_layer / (us_layer * 1e-6) / 1e9 / peak, 4),
@@ -500,11 +575,49 @@ def run_kvm(args, w):
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": launches_per_layer * L * args.steps * (2 if stage_graphs else 1),
             "clocks": sampler.summary(),
+            "per_config": per_config,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+PER_CONFIG = ("tiny_8k_g4_d64", "gqa40x8_256k", "batch8x256k_8layer", "step256q_1m")
+
+
+def per_config_entries(args) -> dict:
+    """The other workloads, each measured by this script in a child process of its own (so each one's device
+    memory is freed before the next), summarised against the 60%-of-roofline bound on its must-touch bytes."""
+    peak, peak_kind = load_peaks()
+    out = {}
+    for name in PER_CONFIG:
+        w = synth.WORKLOADS[name]
+        cmd = [sys.executable, os.path.abspath(__file__), "--workload", name, "--steps", str(args.steps),
+               "--warmup", str(args.warmup), "--no-e2e", "--no-cpu-baseline", "--no-per-config"]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+        if r.returncode != 0 or not lines:
+            out[name] = {"error": (r.stderr.strip().splitlines() or ["no output"])[-1][:300]}
+            continue
+        d = json.loads(lines[-1])
+        e = {"us_per_layer": d["value"], "stages_us": d.get("stages_us_per_layer", d.get("stages_us")),
+             "roofline": d.get("roofline"), "clocks": d.get("clocks")}
+        if w.n_q == 1:
+            mt = must_touch_bytes(w)
+            gbs = mt / (d["value"] * 1e-6) / 1e9
+            e.update({"must_touch_bytes_per_layer": mt, "hbm_gbps": round(gbs, 1),
+                      "frac_of_measured_hbm": round(gbs / peak, 4),
+                      "bound_us_60pct_of_8TBs": round(mt / (0.6 * 8e12) * 1e6, 1),
+                      "bound_us_60pct_of_measured": round(mt / (0.6 * peak * 1e9) * 1e6, 1)})
+            e["meets_bound_60pct_of_8TBs"] = d["value"] <= e["bound_us_60pct_of_8TBs"]
+            if name.startswith("tiny"):
+                e["note"] = "launch-bound: 0.38 MB per layer; reported as microseconds only"
+        else:
+            e["step_scores"] = d.get("step_scores")
+            e["note"] = "tensor-bound; roofline of the step attention against the measured bf16 peak"
+        out[name] = e
+    return out
 
 
 def step_attn_flops(w: synth.Workload) -> int:
@@ -660,9 +773,11 @@ def run_kvm_step(args, w):
     achieved = attn_flops / (attn_us * 1e-6) / 1e12
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        per_head_s, threads, desc = oracle_sample(w, 1, 0)
-        cpu = {"value": round(per_head_s * w.h_kv * S * 1e6, 1), "unit": "us/layer", "cores": threads,
-               "kind": "oracle", "sample": desc}
+        layer_s, workers, desc = oracle_sample(w, 1, 0)
+        # the sample covers the first query tokens of the step; the oracle's work is linear in them
+        scale = w.n_q / min(w.n_q, 16)
+        cpu = {"value": round(layer_s * scale * 1e6, 1), "unit": "us/layer", "cores": workers, "kind": "oracle",
+               "sample": desc + f"; scaled by {scale:g} to the step's {w.n_q} query tokens"}
     if rank == 0:
         line = {
             "metric": STEP_METRIC, "value": round(step_ms * 1e3, 2), "unit": "us/layer", "n_gpus": world,
@@ -1041,10 +1156,12 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other workloads' entries (per_config) of the default run")
     ap.add_argument("--profile-step", action="store_true",
                     help="after warm-up, run one step between cudaProfilerStart/Stop and exit (for ncu)")
     if len(sys.argv) > 1 and sys.argv[1] == "--oracle-child":
-        _oracle_child(sys.argv[2], int(sys.argv[3]), int(sys.argv[4]))
+        _oracle_child(sys.argv[2], int(sys.argv[3]), int(sys.argv[4]), int(sys.argv[5]))
         return
     args = ap.parse_args()
     if args.warmup < 3:

@@ -89,7 +89,7 @@ typedef enum {
 
 /* Bits of the device status word. */
 #define KVM_DEV_BAD_PAGE 0x1u    /* block_table entry outside [0, n_pages)          */
-#define KVM_DEV_BAD_BLOCK 0x2u   /* kept id outside [0, n_blk) or not ascending     */
+#define KVM_DEV_BAD_BLOCK 0x2u   /* kept id outside [0, n_blk) or not above the entry before it (slot skipped) */
 #define KVM_DEV_TIMEOUT 0x4u     /* a pipeline wait exceeded its iteration limit    */
 #define KVM_DEV_BAD_VIEW 0x8u    /* kvm_step_attn: view_len outside [n_q, 32*budget] */
 
@@ -351,16 +351,31 @@ kvm_status kvm_device_status(kvm_ctx* ctx, uint32_t* out, int32_t clear, void* s
  * (h_q/h_kv) * 4) bytes plus 512; larger calls return KVM_ERR_SHAPE and launch
  * nothing (one session of 40/8 heads fits 32,768 blocks).  The first call on
  * each device looks up the array's device address with that device current;
- * make that first call before any stream capture.  Every call reuses the same
- * array and leaves its contents behind, so calls whose work overlaps on the
- * GPU (different streams, or other threads) race and must be serialised by
- * the caller.  No device memory is allocated or freed; errors are reported as
- * by the other calls (kvm_last_error()).
+ * make that first call before any stream capture (outside capture every call
+ * looks the address up again, so a reset device or another context is
+ * followed; during capture the address last seen on the device is used).
+ * Every call reuses the same array and leaves its contents behind, so calls
+ * whose work overlaps on the GPU (different streams, or other threads) race
+ * and must be serialised by the caller.  No device memory is allocated or
+ * freed.  Argument errors are returned at once (kvm_last_error()); errors only
+ * the device sees (a bounded wait that gave up: the kept ids of that call are
+ * then undefined) set bits in a status word inside the array, which stays set
+ * across calls until kvm_noalloc_status clears it.
  */
 #define KVM_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
 kvm_status kvm_score_select_noalloc(const kvm_params* p, const uint16_t* q, const float* index,
                                    const int64_t* n_tok, int32_t n_sessions, int32_t* kept_ids,
                                    float* group_scores, void* stream);
+
+/*
+ * Reads (and optionally clears) the status word of kvm_score_select_noalloc on
+ * the current device after synchronising `stream`: *out receives the KVM_DEV_*
+ * bits set by any allocation-free call since the word was last cleared.
+ * Returns KVM_OK when it is zero, KVM_ERR_TIMEOUT or KVM_ERR_DEVICE otherwise.
+ * Allocates nothing; like the calls it reports on, it has no counterpart in the
+ * method.
+ */
+kvm_status kvm_noalloc_status(uint32_t* out, int32_t clear, void* stream);
 
 #ifdef __cplusplus
 }

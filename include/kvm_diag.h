@@ -30,6 +30,24 @@ kvm_status kvm_attention_mass(kvm_ctx* ctx, const uint16_t* q, const uint16_t* k
                               const int32_t* block_table, const int64_t* n_tok, int32_t n_sessions, float* mass,
                               void* stream);
 
+/*
+ * Failure-path testing of the view calls (kvm_materialize, kvm_decode_attn,
+ * kvm_materialize_attn).  Their pipeline waits are bounded: a wait that gives
+ * up sets KVM_DEV_TIMEOUT, the kernel waits (with the full limit) for its
+ * copies in flight and returns without writing the outputs of the
+ * (session, KV head) units it had a share in; kvm_device_status with clear
+ * then also resets the per-call merge counters, so the context stays usable.
+ *   wait_ns           wall-clock limit of each pipeline wait, in [1000, 2e9]
+ *                     nanoseconds (2e9 by default; the waits for copies in
+ *                     flight always keep 2e9)
+ *   stall_first_wait  1: the first rotation wait of the first CTA is on a
+ *                     barrier that nothing completes, so that wait (and the
+ *                     waits on its stages) run out after wait_ns; 0: normal
+ * The pages define no such control; it exists so that tests can exercise the
+ * timeout path without faulting or hanging the GPU.
+ */
+kvm_status kvm_set_wait_limit(kvm_ctx* ctx, int64_t wait_ns, int32_t stall_first_wait);
+
 #ifdef __cplusplus
 }
 #endif

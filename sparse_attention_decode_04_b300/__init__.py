@@ -253,3 +253,28 @@ def kvm_score_select_noalloc(params: Params, q, index, n_tok, kept_ids, group_sc
     n = len(n_tok)
     _check(f(ctypes.byref(params), _ptr(q), _ptr(index), _i64(n_tok), n, _ptr(kept_ids), _ptr(group_scores),
              _stream(stream)))
+
+
+def kvm_noalloc_status(clear: bool = True, stream=None) -> int:
+    """Status word (KVM_DEV_* bits) of the allocation-free calls on the current device, after synchronising
+    the stream; optionally cleared.  Never raises on a non-zero word."""
+    L = lib()
+    f = L.kvm_noalloc_status
+    if f.argtypes is None:
+        f.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int32, ctypes.c_void_p]
+        f.restype = ctypes.c_int
+    out = ctypes.c_uint32(0)
+    st = f(ctypes.byref(out), int(bool(clear)), _stream(stream))
+    if st not in (0, 5, 6):
+        _check(st)
+    return int(out.value)
+
+
+def kvm_set_wait_limit(ctx: Context, wait_ns: int = 2_000_000_000, stall_first_wait: bool = False):
+    """Failure-path testing: the view calls' pipeline-wait limit, and a first wait nothing completes."""
+    L = lib()
+    f = L.kvm_set_wait_limit
+    if f.argtypes is None:
+        f.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32]
+        f.restype = ctypes.c_int
+    _check(f(ctx.handle, int(wait_ns), int(bool(stall_first_wait))))

@@ -267,6 +267,17 @@ kvm_status kvm_destroy(kvm_ctx* ctx) {
 
 size_t kvm_scratch_bytes(const kvm_ctx* ctx) { return ctx ? ctx->c.bytes : 0; }
 
+kvm_status kvm_set_wait_limit(kvm_ctx* ctx, int64_t wait_ns, int32_t stall_first_wait) {
+  if (!ctx) return fail(KVM_ERR_INVALID_ARG, "ctx is NULL");
+  if (wait_ns < 1000 || wait_ns > 2000000000ll)
+    return fail(KVM_ERR_INVALID_ARG, "wait_ns=%lld outside [1000, 2e9]", (long long)wait_ns);
+  if (stall_first_wait != 0 && stall_first_wait != 1)
+    return fail(KVM_ERR_INVALID_ARG, "stall_first_wait must be 0 or 1");
+  ctx->c.wait_ns = (uint64_t)wait_ns;
+  ctx->c.stall_first_wait = stall_first_wait;
+  return KVM_OK;
+}
+
 kvm_status kvm_index_append(kvm_ctx* ctx, const uint16_t* k_pool, int64_t n_pages, const int32_t* block_table,
                             int32_t n_sessions, const int64_t* tok_begin, const int64_t* n_tok, float* index,
                             void* stream) {
@@ -524,8 +535,18 @@ kvm_status kvm_attention_mass(kvm_ctx* ctx, const uint16_t* q, const uint16_t* k
     return fail(KVM_ERR_INVALID_ARG, "q and k_pool must be 16-byte aligned, mass and block_table 4-byte aligned");
   SessionArgs a;
   if ((s = history_args(c, n_tok, n_sessions, &a)) != KVM_OK) return s;
-  cudaError_t e = kvm::launch_attention_mass(c, q, k_pool, n_pages, block_table, n_sessions, a, mass,
-                                             (cudaStream_t)stream);
+  // the finalising kernel stages one fp32 factor per (32-block tile, query head of the group) in shared memory
+  int max_blk = 0, optin = 0;
+  for (int i = 0; i < n_sessions; ++i) max_blk = a.n_blk[i] > max_blk ? a.n_blk[i] : max_blk;
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
+  if (e != cudaSuccess) return cuda_fail(e, "kvm_attention_mass");
+  const size_t fac_bytes = (size_t)((max_blk + 31) / 32) * c.group * sizeof(float);
+  if (fac_bytes > (size_t)optin)
+    return fail(KVM_ERR_SHAPE,
+                "kvm_attention_mass: %d blocks x group %d need %zu bytes of per-tile factors in shared memory; "
+                "the device allows %d (at most %lld blocks for this group)",
+                max_blk, c.group, fac_bytes, optin, (long long)optin / (long long)(c.group * sizeof(float)) * 32);
+  e = kvm::launch_attention_mass(c, q, k_pool, n_pages, block_table, n_sessions, a, mass, (cudaStream_t)stream);
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_attention_mass launch");
 }
 

@@ -59,13 +59,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records KVM_DEV_TIMEOUT) if it has not completed within the limits.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status) {
+// records KVM_DEV_TIMEOUT) if it has not completed within the limits: the
+// iteration cap, and `limit_ns` of wall-clock time (2 s unless a context set a
+// shorter limit to exercise the failure path).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                          uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1; it < kWaitIters; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 1023u) == 0 && global_timer_ns() - t0 > kWaitNs) break;
+    if ((it & 63u) == 0 && global_timer_ns() - t0 > limit_ns) break;
   }
   atomicOr(status, KVM_DEV_TIMEOUT);
   return false;

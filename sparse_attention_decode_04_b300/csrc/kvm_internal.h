@@ -46,6 +46,8 @@ struct Ctx {
   float* rope_base_lo = nullptr;  // [budget + 1][d/2][2] what the fp32 rounding of rope_base dropped
   float* rope_off_lo = nullptr;   // [32][d/2][2] the same for rope_off (read on the cancellation fallback)
   uint32_t* status = nullptr;  // device status word
+  uint64_t wait_ns = 2000000000ull;  // wall-clock limit of the view kernel's pipeline waits
+  int stall_first_wait = 0;          // the view kernel's first rotation wait is on a barrier nothing completes
   int64_t max_tiles = 0;
   // step-level (multi-query) scoring scratch, allocated when max_queries > 1
   int64_t step_blk_cap_pad = 0;  // max_blocks rounded up to 256

@@ -225,6 +225,9 @@ cudaError_t launch_dg(const Ctx& c, const uint16_t* q, const uint16_t* k_pool, i
                              (float)(1.4426950408889634 / sqrt((double)D)), c.e_buf, c.part, c.max_tiles, c.status);
   if (e != cudaSuccess) return e;
   const size_t smem = (size_t)tiles * G * sizeof(float);
+  int optin = 0;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device)) != cudaSuccess) return e;
+  if (smem > (size_t)optin) return cudaErrorInvalidConfiguration;  // the caller checks this bound up front
   if ((e = ensure_smem(mass_finalize_kernel<G>, c.device, smem)) != cudaSuccess) return e;
   return launch_pdl(mass_finalize_kernel<G>, dim3(c.p.h_kv, n_sessions), dim3(1024), smem, st, 1,
                     (const float*)c.e_buf, (const float2*)c.part, c.max_tiles, c.p.max_blocks, c.p.h_kv, c.p.h_q, a,

@@ -40,20 +40,26 @@ kvm_status na_fail(kvm_status s, const char* fmt, ...) {
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Device address of the scratch array, looked up once per device with that
-// device current (the array's name is only a host-side stand-in).
+// Device address of the scratch array (its name is only a host-side stand-in).  Outside stream capture it is
+// looked up again on every call, with the call's device current, so a reloaded module (after a device reset,
+// or under another context) is always followed; during capture, when the runtime may not be asked, the
+// address last seen on that device is used.
 constexpr int kMaxDevices = 64;
 std::mutex g_addr_mu;
 void* g_addr[kMaxDevices] = {};
 
-cudaError_t scratch_address(int device, unsigned char** out) {
+cudaError_t scratch_address(int device, cudaStream_t st, unsigned char** out) {
   if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cap);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(g_addr_mu);
-  if (!g_addr[device]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
+    if ((e = cudaGetSymbolAddress(&p, g_noalloc_scratch)) != cudaSuccess) return e;
     g_addr[device] = p;
+  } else if (!g_addr[device]) {
+    return cudaErrorStreamCaptureUnsupported;  // the first call on a device must come before any capture
   }
   *out = static_cast<unsigned char*>(g_addr[device]);
   return cudaSuccess;
@@ -91,7 +97,7 @@ extern "C" kvm_status kvm_score_select_noalloc(const kvm_params* p, const uint16
   c.budget = (int)budget;
   c.max_tiles = (p->max_blocks + 31) / 32;
 
-  // scratch layout: status word | tile partials [S][h_q][max_tiles] | exponentials [S][h_kv][max_blocks][G]
+  // scratch layout: status word | tile partials [S][h_q][max_tiles] | exponentials [S][h_kv][G][max_blocks]
   const size_t off_part = 256;
   const size_t sz_part = (size_t)n_sessions * p->h_q * (size_t)c.max_tiles * sizeof(float2);
   const size_t off_e = align256(off_part + sz_part);
@@ -116,20 +122,37 @@ extern "C" kvm_status kvm_score_select_noalloc(const kvm_params* p, const uint16
   }
   a.seg_base[n_sessions] = base;
 
+  cudaStream_t st = (cudaStream_t)stream;
   cudaError_t e = cudaGetDevice(&c.device);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, c.device);
   unsigned char* scratch = nullptr;
-  if (e == cudaSuccess) e = scratch_address(c.device, &scratch);
+  if (e == cudaSuccess) e = scratch_address(c.device, st, &scratch);
   if (e != cudaSuccess)
     return na_fail(KVM_ERR_CUDA, "scratch address: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
+  // the status word (first bytes of the array) collects device-side errors until kvm_noalloc_status clears it
   c.status = reinterpret_cast<uint32_t*>(scratch);
   c.part = reinterpret_cast<float2*>(scratch + off_part);
   c.e_buf = reinterpret_cast<float*>(scratch + off_e);
 
-  cudaStream_t st = (cudaStream_t)stream;
-  e = cudaMemsetAsync(c.status, 0, sizeof(uint32_t), st);  // the status word starts each call at zero
-  if (e == cudaSuccess) e = kvm::launch_score_select(c, q, 1, index, n_sessions, a, kept_ids, group_scores, nullptr, st);
+  e = kvm::launch_score_select(c, q, 1, index, n_sessions, a, kept_ids, group_scores, nullptr, st);
   if (e != cudaSuccess)
     return na_fail(KVM_ERR_CUDA, "kvm_score_select_noalloc launch: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
   return KVM_OK;
+}
+
+extern "C" kvm_status kvm_noalloc_status(uint32_t* out, int32_t clear, void* stream) {
+  if (!out) return na_fail(KVM_ERR_INVALID_ARG, "out is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  int device = 0;
+  unsigned char* scratch = nullptr;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e == cudaSuccess) e = scratch_address(device, st, &scratch);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess) e = cudaMemcpy(out, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && clear) e = cudaMemset(scratch, 0, sizeof(uint32_t));
+  if (e != cudaSuccess)
+    return na_fail(KVM_ERR_CUDA, "kvm_noalloc_status: %s (%s)", cudaGetErrorName(e), cudaGetErrorString(e));
+  if (*out == 0) return KVM_OK;
+  if (*out & KVM_DEV_TIMEOUT) return na_fail(KVM_ERR_TIMEOUT, "a device-side wait timed out (status 0x%x)", *out);
+  return na_fail(KVM_ERR_DEVICE, "device status 0x%x", *out);
 }

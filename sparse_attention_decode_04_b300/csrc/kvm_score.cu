@@ -31,6 +31,8 @@
 //   resolve toward the lower id.
 #include <cooperative_groups.h>
 
+#include <algorithm>
+
 #include "kvm_device.cuh"
 #include "kvm_internal.h"
 
@@ -642,11 +644,15 @@ cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, in
                     c.p.n_recent, c.p.top_k, c.budget, slice_cap, kept, group_scores, gs_in);
 }
 
-// Rows per score tile: one wave of two CTAs per SM over the call (a multiple of 32 rows, 32..4096).
+// Rows per score tile (a multiple of 32, 32..4096): whole waves of two CTAs per SM, as many waves as keep tiles
+// near 900 rows (one wave for a 1M-token session's 8 heads, two for 8 sessions of 256K tokens), never more
+// tiles than fill the waves.
 int rows_per_tile(const Ctx& c, int n_sessions, int max_blk) {
   const int64_t units = (int64_t)c.p.h_kv * n_sessions;
-  const int64_t sms = c.num_sms > 0 ? c.num_sms : 1;
-  const int64_t tiles_per_head = (2 * sms + units - 1) / units;
+  const int64_t slots = 2 * (int64_t)(c.num_sms > 0 ? c.num_sms : 1);
+  const int64_t rows = units * max_blk;
+  const int64_t waves = std::min<int64_t>(4, std::max<int64_t>(1, (rows + slots * 448) / (slots * 896)));
+  const int64_t tiles_per_head = std::max<int64_t>(1, slots * waves / units);
   int64_t rpt64 = (max_blk + tiles_per_head - 1) / tiles_per_head;
   rpt64 = (rpt64 + kStageRows - 1) / kStageRows * kStageRows;
   return (int)(rpt64 < kStageRows ? kStageRows : (rpt64 > 4096 ? 4096 : rpt64));

@@ -97,6 +97,8 @@ struct ViewParams {
   int n_sessions;
   int P;  // CTAs
   float q_scale;  // log2(e) / sqrt(d)
+  uint64_t wait_ns;  // wall-clock limit of the pipeline waits (the drain of copies in flight keeps the full limit)
+  int stall;         // failure-path test: the rotation of flat block 0 first waits on a barrier nothing completes
 };
 
 // Attention record of one (CTA, segment, warp, query head): max, sum, 2 pad, output[D] (16-byte aligned).
@@ -194,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_addr(smem);
   int* meta = reinterpret_cast<int*>(smem + Q::OFF_META);
   __shared__ __align__(8) uint64_t full[NS], rotated[NS], empty[NS];
+  __shared__ __align__(8) uint64_t never;  // failure-path test only: initialised, never arrived on
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&rotated[st], 1);
       mbar_init(&empty[st], (kWrite ? 1 : 0) + (kAttend ? 1 : 0));  // the stage's rotation and attention warps
     }
+    mbar_init(&never, 1);
     mbar_fence_init();
   }
   // A rotation lane always rotates the same pairs of every block: rows r = lane / CPR + RPP * pass, pairs
@@ -297,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t round = (uint32_t)(jj / NS);
         int ok = 1;
         if (lane == 0) {
-          if (round > 0) ok = mbar_wait(&empty[st], (round - 1) & 1, vp.status);
+          if (round > 0) ok = mbar_wait(&empty[st], (round - 1) & 1, vp.status, vp.wait_ns);
           if (ok) {
             meta[st] = valid;
             unsigned char* kdst = smem + st * 2 * Q::PAGE;
@@ -340,7 +344,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = cu.s * vp.h_kv + cu.g;
         const int64_t ydst = (int64_t)q * Lcap + 32 * cu.i;
         const uint32_t vaddr = sbase + st * 2 * Q::PAGE + Q::PAGE;
-        if (__any_sync(0xffffffffu, !mbar_wait(&full[st], phase, vp.status))) {
+        if (__any_sync(0xffffffffu, !mbar_wait(&full[st], phase, vp.status, vp.wait_ns) ||
+                                        (vp.stall && fa + jj == 0 &&
+                                         !mbar_wait(&never, 0, vp.status, vp.wait_ns)))) {
           aborted = true;
           break;
         }
@@ -566,7 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t kaddr = sbase + st * 2 * Q::PAGE, vaddr = kaddr + Q::PAGE;
         // the rotated page (fused) or the view page as loaded (attention over a given view)
-        if (__any_sync(0xffffffffu, !mbar_wait(kWrite ? &rotated[st] : &full[st], phase, vp.status))) {
+        if (__any_sync(0xffffffffu, !mbar_wait(kWrite ? &rotated[st] : &full[st], phase, vp.status, vp.wait_ns))) {
           aborted = true;
           break;
         }
@@ -915,8 +921,12 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
   vp.h_kv = c.p.h_kv;
   vp.h_q = c.p.h_q;
   vp.n_sessions = n_sessions;
-  vp.P = c.view_ctas;
+  // one CTA per SM, but never more CTAs than kept blocks: every CTA then has a non-empty share (a small view
+  // would otherwise leave most CTAs idle and make the merge walk over empty shares)
+  vp.P = (int)(vp.total > 0 && vp.total < c.view_ctas ? vp.total : c.view_ctas);
   vp.q_scale = (float)(1.4426950408889634 / sqrt((double)c.p.d));
+  vp.wait_ns = c.wait_ns;
+  vp.stall = c.stall_first_wait;
   // tensor maps: sources (pool pages, or the view for mode 1) and destinations (the view)
   const uint64_t view_rows = (uint64_t)n_sessions * c.p.h_kv * 32 * c.budget;
   const uint64_t pool_rows = (uint64_t)n_pages * c.p.h_kv * 32;

@@ -37,11 +37,14 @@ def test_noalloc_matches_context_entry_point_on_two_calls(name):
     ref_ids = dev.kept.cpu().numpy()
     ref_gs = dev.gs.cpu().numpy()
     p = _params(w)
+    K.kvm_noalloc_status(clear=True)           # start from a clear word, whatever ran before in this process
     for call in range(2):                    # two calls in a row share the library's scratch array
         kept = torch.full_like(dev.kept, -7)
         gs = torch.full_like(dev.gs, float("nan"))
         K.kvm_score_select_noalloc(p, dev.q, dev.index, [w.n_tok], kept, gs)
         torch.cuda.synchronize()
+        # no device-side error was recorded by the call (the word is readable, and stays set until cleared)
+        assert K.kvm_noalloc_status(clear=False) == 0
         assert np.array_equal(kept.cpu().numpy(), ref_ids), f"call {call}: kept ids differ"
         got = gs.cpu().numpy()
         for g in range(w.h_kv):
