@@ -172,7 +172,8 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
   c.view_ctas = c.num_sms;
   c.max_tiles = (p->max_blocks + 31) / 32;
   const size_t S = (size_t)p->max_sessions;
-  const size_t sz_e = S * p->h_kv * (size_t)p->max_blocks * c.group * sizeof(float);
+  c.e_stride = (p->max_blocks + 3) & ~(int64_t)3;
+  const size_t sz_e = S * p->h_kv * (size_t)c.e_stride * c.group * sizeof(float);
   const size_t sz_part = S * p->h_q * (size_t)c.max_tiles * sizeof(float2);
   const size_t sz_rec =
       ((size_t)c.view_ctas + S * p->h_kv) * (kvm::kViewWarps + 1) * c.group * (4 + p->d) * sizeof(float);

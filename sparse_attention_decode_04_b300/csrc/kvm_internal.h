@@ -37,7 +37,8 @@ struct Ctx {
   int view_ctas = 0;    // persistent CTAs of the view kernels
   size_t bytes = 0;     // device bytes allocated
   // scratch (device)
-  float* e_buf = nullptr;      // [S][h_kv][group][max_blocks] exp(s - tile max) (score kernels)
+  float* e_buf = nullptr;      // [S][h_kv][group][e_stride] exp(s - tile max) (score kernels)
+  int64_t e_stride = 0;        // max_blocks rounded up to a multiple of 4 (16-byte rows for bulk copies)
   float2* part = nullptr;      // [S][h_q][max_tiles] (tile max, tile sum) in log2 domain
   float* rec = nullptr;        // [view_ctas + S*h_kv][kViewWarps + 1][group][4 + d] attention partials
   uint32_t* seg_count = nullptr;  // [S*h_kv] CTAs of a view call done with each segment (0 between calls)

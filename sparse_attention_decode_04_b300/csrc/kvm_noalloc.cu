@@ -97,11 +97,12 @@ extern "C" kvm_status kvm_score_select_noalloc(const kvm_params* p, const uint16
   c.budget = (int)budget;
   c.max_tiles = (p->max_blocks + 31) / 32;
 
-  // scratch layout: status word | tile partials [S][h_q][max_tiles] | exponentials [S][h_kv][G][max_blocks]
+  // scratch layout: status word | tile partials [S][h_q][max_tiles] | exponentials [S][h_kv][G][e_stride]
   const size_t off_part = 256;
   const size_t sz_part = (size_t)n_sessions * p->h_q * (size_t)c.max_tiles * sizeof(float2);
   const size_t off_e = align256(off_part + sz_part);
-  const size_t sz_e = (size_t)n_sessions * p->h_kv * (size_t)p->max_blocks * c.group * sizeof(float);
+  c.e_stride = (p->max_blocks + 3) & ~(int64_t)3;
+  const size_t sz_e = (size_t)n_sessions * p->h_kv * (size_t)c.e_stride * c.group * sizeof(float);
   if (off_e + sz_e > kNoAllocScratchBytes)
     return na_fail(KVM_ERR_SHAPE,
                    "scratch for %d session(s) x %lld blocks needs %zu bytes; this entry point holds at most %zu",

@@ -49,8 +49,8 @@ constexpr int kSelectThreads = 512;
 template <int D, int G>
 __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
     const uint16_t* __restrict__ q, const float* __restrict__ index, int64_t max_blocks, int h_kv, int h_q,
-    SessionArgs a, int rows_per_tile, float* __restrict__ e_buf, float2* __restrict__ part, int64_t max_tiles,
-    float* __restrict__ head_scores, uint32_t* __restrict__ status, int q_heads, int avg_group) {
+    SessionArgs a, int rows_per_tile, float* __restrict__ e_buf, int64_t e_stride, float2* __restrict__ part,
+    int64_t max_tiles, float* __restrict__ head_scores, uint32_t* __restrict__ status, int q_heads, int avg_group) {
   // q_heads: query heads per session in q.  avg_group > 0 (with G == 1): the withdrawn scoring, one score row
   // per KV head from the unweighted mean of its avg_group query heads (taken in fp32).
   constexpr int NV = D / 32;  // float4 chunks per lane per row
@@ -195,12 +195,12 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   __syncthreads();
   // e = exp(s - m_tile), written in place and to global head-major ([head][block]: the selection reads one
   // head of 32 consecutive blocks per warp-wide load).
-  float* e_dst = e_buf + ((int64_t)s * h_kv + g) * G * max_blocks + r0;
+  float* e_dst = e_buf + ((int64_t)s * h_kv + g) * G * e_stride + r0;
   for (int i = tid; i < nrows * G; i += kScoreThreads) {
     const int h = i / nrows, r = i - h * nrows;
     const float e = expf(s_tile[r * G + h] - tile_max[h]);
     s_tile[r * G + h] = e;
-    e_dst[(int64_t)h * max_blocks + r] = e;
+    e_dst[(int64_t)h * e_stride + r] = e;
   }
   __syncthreads();
   // Sum of e per head, fixed order: each warp owns heads h = warp, warp + 8, ...
@@ -292,31 +292,22 @@ __device__ __forceinline__ SelResult sel_boundary(cg::cluster_group& cluster, in
   return r;
 }
 
-// Loads that stay where they are written (volatile), so the exponentials are requested before the normalisers.
-__device__ __forceinline__ float ld_early(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-__device__ __forceinline__ float2 ld_early2(const float2* p) {
-  float2 v;
-  asm volatile("ld.global.cg.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "l"(p));
-  return v;
-}
-
 constexpr int kSelTilesPerLane = 10;  // tile partials a normaliser lane holds: up to 320 tiles per head
+constexpr int kSelChunk = 4096;       // blocks whose exponentials are staged in shared memory at a time (at most)
 constexpr int kSelList = 32;          // boundary keys resolved by an exchanged list instead of a third pass
 
 template <int G>
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(
-    const float* __restrict__ e_buf, const float2* __restrict__ part, int64_t max_tiles, int64_t max_blocks,
-    int h_kv, int h_q, SessionArgs a, int rows_per_tile, int n_sink, int n_recent, int top_k, int budget,
-    int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores, const float* __restrict__ gs_in) {
+    const float* __restrict__ e_buf, int64_t e_stride, const float2* __restrict__ part, int64_t max_tiles,
+    int64_t max_blocks, int h_kv, int h_q, SessionArgs a, int rows_per_tile, int n_sink, int n_recent, int top_k,
+    int budget, int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores,
+    const float* __restrict__ gs_in, uint32_t* __restrict__ status, int chunk) {
   constexpr int NT = kSelectThreads, NW = NT / 32;
-  constexpr int J = 8;  // keys per thread whose inputs are loaded together
   extern __shared__ __align__(128) unsigned char smem_raw[];
   uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw);        // [slice_cap]
-  float* coef = reinterpret_cast<float*>(key + slice_cap);       // [tiles in slice][G]
+  float* e_stage = reinterpret_cast<float*>(key + slice_cap);    // [G][chunk] exponentials of one chunk
+  float* coef = e_stage + (gs_in ? 0 : G * chunk);               // [tiles in slice][G]
+  __shared__ __align__(8) uint64_t e_bar;
   __shared__ __align__(16) int hist[2][kSelBins];  // pass p builds hist[p & 1]; the other may still be read remotely
   __shared__ __align__(16) int sup[2][kSelSup];
   __shared__ int warp_cnt[NW][2];     // per warp: blocks kept for sure, keys equal to the boundary key
@@ -331,6 +322,10 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int i = tid; i < kSelBins; i += NT) hist[0][i] = 0;
+  if (tid == 0) {
+    mbar_init(&e_bar, 1);
+    mbar_fence_init();
+  }
   if (tid < 8) taken_cnt[tid] = 0;
   if (tid < NW) warp_taken[tid] = 0;
   if (tid == 0) own_n = own_taken_n = 0;
@@ -340,7 +335,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
   const int C = (int)cluster.num_blocks();
   const int s = blockIdx.z, g = blockIdx.y;
   const int n_blk = a.n_blk[s];
-  const int sl = (n_blk + C - 1) / C;
+  const int sl = ((n_blk + C - 1) / C + 3) & ~3;  // slices start on 16-byte boundaries of the exponentials
   const int lo = min(n_blk, crank * sl), hi = min(n_blk, lo + sl);
   const int len = hi - lo;
   const int n_iter = (len + NT - 1) / NT;
@@ -369,19 +364,23 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
       put_key(b < hi, b, b < hi ? src[b] : 0.f);
     }
   } else {
-    const float* e_src = e_buf + ((int64_t)s * h_kv + g) * G * max_blocks;  // [G][max_blocks]
+    // The slice's exponentials (G rows of the head-major scratch) come in by 1-D bulk copies, `chunk` blocks
+    // at a time, while the normalisers are formed; the copies start and end on 16-byte boundaries (slices start
+    // at a multiple of 4 blocks, and the scratch rows are padded to a multiple of 4).
+    const float* e_src = e_buf + ((int64_t)s * h_kv + g) * G * e_stride + lo;
     const int n_tiles = (n_blk + rows_per_tile - 1) / rows_per_tile;
     const int t0 = lo / rows_per_tile;
     const int nt = hi > lo ? (hi - 1) / rows_per_tile - t0 + 1 : 0;
-    // the first J keys' exponentials and the tile partials are requested together, before any of them is
-    // used (one round of L2 latency for both)
-    float ev[J][G];
+    const int n_chunks = (len + chunk - 1) / chunk;
+    auto issue_chunk = [&](int k) {
+      const int c0 = k * chunk, cl = min(chunk, len - c0);
+      const uint32_t bytes = (uint32_t)(((cl + 3) & ~3) * 4);
+      mbar_arrive_expect_tx(&e_bar, bytes * G);
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int b = lo + tid + j * NT;
-#pragma unroll
-      for (int h = 0; h < G; ++h) ev[j][h] = b < hi ? ld_early(e_src + (int64_t)h * max_blocks + b) : 0.f;
-    }
+      for (int h = 0; h < G; ++h) bulk_g2s(e_stage + h * chunk, e_src + (int64_t)h * e_stride + c0, bytes, &e_bar);
+    };
+    __syncthreads();  // e_bar initialised
+    if (tid == 0 && n_chunks > 0) issue_chunk(0);
     // softmax normaliser of query head `warp` (< G): M = the largest tile maximum, Z = the tile sums rescaled
     // to M; then the slice's per-tile coefficients exp(m_tile - M) / Z.  Each lane holds its tiles' partials.
     if (warp < G) {
@@ -390,7 +389,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
 #pragma unroll
       for (int i = 0; i < kSelTilesPerLane; ++i) {
         const int t = lane + 32 * i;
-        pt[i] = t < n_tiles ? ld_early2(p + t) : make_float2(-INFINITY, 0.f);
+        pt[i] = t < n_tiles ? __ldcg(p + t) : make_float2(-INFINITY, 0.f);
       }
       float M = -INFINITY;
 #pragma unroll
@@ -411,27 +410,22 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
       }
     }
     __syncthreads();  // coefficients ready, hist[0] cleared
-    for (int j0 = 0; j0 < n_iter; j0 += J) {
-      if (j0 > 0) {
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const int b = lo + tid + (j0 + j) * NT;
-#pragma unroll
-          for (int h = 0; h < G; ++h) ev[j][h] = b < hi ? __ldcg(e_src + (int64_t)h * max_blocks + b) : 0.f;
-        }
+    for (int k = 0; k < n_chunks; ++k) {
+      if (k > 0) {
+        __syncthreads();  // every thread is done with the previous chunk
+        if (tid == 0) issue_chunk(k);
       }
+      if (!mbar_wait(&e_bar, (uint32_t)(k & 1), status)) {
+        // the copies never landed within the limit (the status word says so); no key of this chunk is valid
+      }
+      const int c0 = k * chunk, cl = min(chunk, len - c0);
+      for (int i = tid; i < cl; i += NT) {
+        const int b = lo + c0 + i;
+        const float* cf = coef + (b / rows_per_tile - t0) * G;
+        float gsv = 0.f;
 #pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int b = lo + tid + (j0 + j) * NT;
-        if (j0 + j < n_iter) {  // uniform across the CTA
-          float gsv = 0.f;
-          if (b < hi) {
-            const float* cf = coef + (b / rows_per_tile - t0) * G;
-#pragma unroll
-            for (int h = 0; h < G; ++h) gsv = fmaf(ev[j][h], cf[h], gsv);
-          }
-          put_key(b < hi, b, gsv);
-        }
+        for (int h = 0; h < G; ++h) gsv = fmaf(e_stage[h * chunk + i], cf[h], gsv);
+        put_key(true, b, gsv);
       }
     }
   }
@@ -628,20 +622,24 @@ cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, in
   int C = (max_blk + 4095) / 4096;
   C = C < 1 ? 1 : (C > 8 ? 8 : C);
   if (gs_in == nullptr && (max_blk + rpt - 1) / rpt > 32 * kSelTilesPerLane) return cudaErrorInvalidValue;
-  const int slice_cap = (max_blk + C - 1) / C;
+  const int slice_cap = ((max_blk + C - 1) / C + 3) & ~3;  // as the kernel's slices: multiples of 4 blocks
   const int tiles_cap = slice_cap / rpt + 2;
-  const size_t smem_b = (size_t)slice_cap * 4 + (size_t)tiles_cap * G * 4;
   auto kb = select_kernel<G>;
   cudaError_t e;
   cudaFuncAttributes fa;
   if ((e = cudaFuncGetAttributes(&fa, kb)) != cudaSuccess) return e;
   int optin = 0;
   if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device)) != cudaSuccess) return e;
-  if (smem_b + fa.sharedSizeBytes > (size_t)optin) return cudaErrorInvalidValue;
+  const size_t fixed = (size_t)slice_cap * 4 + (size_t)tiles_cap * G * 4 + fa.sharedSizeBytes;
+  if (fixed + (gs_in ? 0 : (size_t)256 * G * 4) > (size_t)optin) return cudaErrorInvalidValue;
+  // the exponentials' staging chunk: as many blocks as the remaining shared memory holds, up to kSelChunk
+  const int chunk = gs_in ? 0 : (int)std::min<size_t>(kSelChunk, ((size_t)optin - fixed) / (G * 4)) & ~3;
+  const size_t smem_b = fixed - fa.sharedSizeBytes + (size_t)chunk * G * 4;
   if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
   return launch_pdl(kb, dim3(C, c.p.h_kv, n_sessions), dim3(kSelectThreads), smem_b, st, C, (const float*)c.e_buf,
-                    (const float2*)c.part, c.max_tiles, c.p.max_blocks, c.p.h_kv, part_heads, a, rpt, c.p.n_sink,
-                    c.p.n_recent, c.p.top_k, c.budget, slice_cap, kept, group_scores, gs_in);
+                    c.e_stride, (const float2*)c.part, c.max_tiles, c.p.max_blocks, c.p.h_kv, part_heads, a, rpt,
+                    c.p.n_sink, c.p.n_recent, c.p.top_k, c.budget, slice_cap, kept, group_scores, gs_in, c.status,
+                    chunk);
 }
 
 // Rows per score tile (a multiple of 32, 32..4096): whole waves of two CTAs per SM, as many waves as keep tiles
@@ -673,7 +671,8 @@ cudaError_t launch_withdrawn(const Ctx& c, const uint16_t* q, const float* index
   if (e != cudaSuccess) return e;
   // partial rows are indexed per KV head here (h_kv score rows per session)
   if ((e = launch_pdl(ka, dim3(tiles, c.p.h_kv, n_sessions), dim3(kScoreThreads), smem_a, st, 1, q, index,
-                      c.p.max_blocks, c.p.h_kv, c.p.h_kv, a, rpt, c.e_buf, c.part, c.max_tiles, (float*)nullptr,
+                      c.p.max_blocks, c.p.h_kv, c.p.h_kv, a, rpt, c.e_buf, c.e_stride, c.part, c.max_tiles,
+                      (float*)nullptr,
                       c.status, c.p.h_q, c.group)) != cudaSuccess)
     return e;
   return launch_select<1>(c, n_sessions, a, rpt, max_blk, kept, group_scores, nullptr, st, c.p.h_kv);
@@ -709,7 +708,7 @@ cudaError_t launch_g(const Ctx& c, const uint16_t* q, const float* index, int n_
   cudaError_t e = ensure_smem(ka, c.device, smem_a);
   if (e != cudaSuccess) return e;
   if ((e = launch_pdl(ka, dim3(tiles, c.p.h_kv, n_sessions), dim3(kScoreThreads), smem_a, st, 1, q, index,
-                      c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.e_buf, c.part, c.max_tiles, head_scores,
+                      c.p.max_blocks, c.p.h_kv, c.p.h_q, a, rpt, c.e_buf, c.e_stride, c.part, c.max_tiles, head_scores,
                       c.status, c.p.h_q, 0)) != cudaSuccess)
     return e;
 
