@@ -20,9 +20,11 @@
  *   kvm_step_attn         attention of a whole step's query tokens over the
  *                         view (tensor cores), after a multi-query selection.
  * Page tiers beyond the bf16 HBM pool:
- *   kvm_quantize_pages, kvm_index_append_fp8, kvm_materialize_fp8
+ *   kvm_quantize_pages, kvm_index_append_fp8, kvm_materialize_fp8,
+ *   kvm_materialize_attn_fp8
  *                         FP8 E4M3 pages (one fp32 scale per page and KV head),
- *                         dequantised inside the index and the gather.
+ *                         dequantised inside the index and the gather (the
+ *                         last fused with attention).
  *   kvm_materialize_host  the gather from a pool in mapped pinned host memory.
  *
  * Conventions shared by every call
@@ -284,6 +286,18 @@ kvm_status kvm_materialize_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const float
                                const float* v_scales, int64_t n_pages, const int32_t* block_table,
                                const int64_t* n_tok, int32_t n_sessions, const int32_t* kept_ids, uint16_t* k_view,
                                uint16_t* v_view, int32_t* view_len, void* stream);
+
+/*
+ * kvm_materialize_attn from quantised pages: the same outputs as
+ * kvm_materialize_fp8 followed by kvm_decode_attn, in one pass that reads
+ * each kept code page once (the bf16 view is written and never read back).
+ * Arguments as kvm_materialize_fp8, plus q and out as in kvm_decode_attn.
+ */
+kvm_status kvm_materialize_attn_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const float* k_scales,
+                                    const uint8_t* v_pool8, const float* v_scales, int64_t n_pages,
+                                    const int32_t* block_table, const int64_t* n_tok, int32_t n_sessions,
+                                    const int32_t* kept_ids, const uint16_t* q, uint16_t* k_view,
+                                    uint16_t* v_view, int32_t* view_len, float* out, void* stream);
 
 /*
  * Host tier.  KVMEM reproduction README, "Background and main changes" and

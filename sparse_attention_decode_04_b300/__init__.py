@@ -210,6 +210,21 @@ def kvm_materialize_fp8(ctx: Context, k_pool8, k_scales, v_pool8, v_scales, n_pa
                                      _ptr(v_view), _ptr(view_len), _stream(stream)))
 
 
+def kvm_materialize_attn_fp8(ctx: Context, k_pool8, k_scales, v_pool8, v_scales, n_pages: int, block_table, n_tok,
+                             kept_ids, q, k_view, v_view, view_len, out, stream=None):
+    """View from FP8 pages and decode attention over it in one pass (kvm_materialize_fp8 + kvm_decode_attn)."""
+    L = lib()
+    f = L.kvm_materialize_attn_fp8
+    if f.argtypes is None:
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        f.argtypes = [P, P, P, P, P, i64, P, P, i32, P, P, P, P, P, P, P]
+        f.restype = ctypes.c_int
+    n = len(n_tok)
+    _check(f(ctx.handle, _ptr(k_pool8), _ptr(k_scales), _ptr(v_pool8), _ptr(v_scales), int(n_pages), _ptr(block_table),
+             _i64(n_tok), n, _ptr(kept_ids), _ptr(q), _ptr(k_view), _ptr(v_view), _ptr(view_len), _ptr(out),
+             _stream(stream)))
+
+
 def kvm_materialize_host(ctx: Context, k_pool_host, v_pool_host, n_pages: int, block_table, n_tok, kept_ids,
                          k_view, v_view, view_len, stream=None):
     """The view from K/V pools in pinned, mapped host memory (e.g. torch.empty(..., pin_memory=True))."""

@@ -444,7 +444,8 @@ kvm_status kvm_select_control(kvm_ctx* ctx, int32_t control, const uint16_t* q, 
 static kvm_status view_call(kvm_ctx* ctx, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,
                             const int32_t* block_table, const int64_t* n_tok, int32_t n_sessions,
                             const int32_t* kept_ids, const uint16_t* q, uint16_t* k_view, uint16_t* v_view,
-                            int32_t* view_len, float* out, void* stream) {
+                            int32_t* view_len, float* out, void* stream, const float* k_scales = nullptr,
+                            const float* v_scales = nullptr) {
   kvm_status s = check_ctx(ctx);
   if (s != KVM_OK) return s;
   const Ctx& c = ctx->c;
@@ -458,6 +459,8 @@ static kvm_status view_call(kvm_ctx* ctx, int mode, const uint16_t* k_src, const
   if (!aligned(k_src, 16) || !aligned(v_src, 16) || !aligned(k_view, 16) || !aligned(v_view, 16) ||
       !aligned(q, 16) || !aligned(out, 16) || !aligned(view_len, 4) || !aligned(kept_ids, 4))
     return fail(KVM_ERR_INVALID_ARG, "K/V/q/out buffers must be 16-byte aligned");
+  if (mode == 3 && (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4)))
+    return fail(KVM_ERR_INVALID_ARG, "FP8 pages need 4-byte aligned K and V scale arrays");
   SessionArgs a;
   if (mode == 1) {
     // the view lengths live on the device: walk every slot of each view, skip the empty ones
@@ -475,8 +478,18 @@ static kvm_status view_call(kvm_ctx* ctx, int mode, const uint16_t* k_src, const
     return s;
   }
   cudaError_t e = kvm::launch_view(c, mode, k_src, v_src, n_pages, block_table, n_sessions, a, kept_ids, q, k_view,
-                                   v_view, view_len, out, (cudaStream_t)stream);
+                                   v_view, view_len, out, (cudaStream_t)stream, k_scales, v_scales);
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "view kernel launch");
+}
+
+kvm_status kvm_materialize_attn_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const float* k_scales, const uint8_t* v_pool8,
+                                    const float* v_scales, int64_t n_pages, const int32_t* block_table,
+                                    const int64_t* n_tok, int32_t n_sessions, const int32_t* kept_ids,
+                                    const uint16_t* q, uint16_t* k_view, uint16_t* v_view, int32_t* view_len,
+                                    float* out, void* stream) {
+  return view_call(ctx, 3, reinterpret_cast<const uint16_t*>(k_pool8), reinterpret_cast<const uint16_t*>(v_pool8),
+                   n_pages, block_table, n_tok, n_sessions, kept_ids, q, k_view, v_view, view_len, out, stream,
+                   k_scales, v_scales);
 }
 
 kvm_status kvm_materialize(kvm_ctx* ctx, const uint16_t* k_pool, const uint16_t* v_pool, int64_t n_pages,

@@ -9,6 +9,8 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "kvm.h"
@@ -102,6 +104,14 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Two E4M3 codes (low byte first) -> their exact values (E4M3 is a subset of fp16) times `scale`, one fp32
+// rounding each: the value of a quantised element.
+__device__ __forceinline__ float2 dequant_e4m3x2(uint32_t codes16, float scale) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(codes16 & 0xFFFFu), __NV_E4M3);
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h));
+  return make_float2(f.x * scale, f.y * scale);
 }
 
 // Monotone map fp32 -> uint32: a > b  <=>  key(a) > key(b) (for non-NaN values).

@@ -106,11 +106,12 @@ cudaError_t launch_gather_view(const Ctx& c, bool fp8, const void* k_src, const 
                                const SessionArgs& a, const int32_t* kept, uint16_t* k_view, uint16_t* v_view,
                                int32_t* view_len, cudaStream_t st);
 
-// kvm_view.cu — mode: 0 materialise, 1 attend over a view, 2 fused
+// kvm_view.cu — mode: 0 materialise, 1 attend over a view, 2 fused, 3 fused from FP8 pages (k_src / v_src are
+// then the code pools, with their per-(page, KV head) scales)
 cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,
                         const int32_t* bt, int n_sessions, const SessionArgs& a, const int32_t* kept,
                         const uint16_t* q, uint16_t* k_view, uint16_t* v_view, int32_t* view_len, float* out,
-                        cudaStream_t st);
+                        cudaStream_t st, const float* k_scale = nullptr, const float* v_scale = nullptr);
 
 cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st);
 

@@ -88,6 +88,10 @@ struct ViewParams {
   const float2* rope_off;      // [32][d/2]
   const float2* rope_off_lo;   // [32][d/2]
   float* out;
+  const float* k_scale;  // FP8 pages: [n_pages][h_kv] scale of each K page
+  const float* v_scale;
+  const uint8_t* k8;     // FP8 pages: [n_pages][h_kv][32][d] codes
+  const uint8_t* v8;
   uint32_t* status;
   int64_t total;  // kept blocks over all (session, KV head)
   int any_empty;  // some session keeps no block
@@ -105,22 +109,27 @@ struct ViewParams {
 template <int D>
 constexpr int kRecFloats = 4 + D;
 
-template <int D>
+template <int D, bool F8 = false>
 struct Geo {
   static constexpr int BOXES = D / 64;          // 64-column (128-byte) boxes per page row
   static constexpr uint32_t BOX = 32 * 128;     // bytes of one box (32 rows)
-  static constexpr uint32_t PAGE = 32 * D * 2;  // bytes of one K (or V) page
+  static constexpr uint32_t PAGE = 32 * D * 2;  // bytes of one K (or V) page in bf16
+  static constexpr uint32_t CPAGE = 32 * D;     // bytes of one page of FP8 codes
+  // a stage: the bf16 K and V pages (as loaded, or decoded from FP8), then, FP8 only, the K and V code pages
+  static constexpr uint32_t STAGE = 2 * PAGE + (F8 ? 2 * CPAGE : 0);
   static constexpr int CPR = D / 16;            // rotation items (chunk pairs) per row
   static constexpr int RPP = 32 / CPR;          // rows per rotation pass
   static constexpr int PASSES = CPR;            // rotation passes per page
   static constexpr int KS = D / 16;             // MMA k-steps over the head dimension
   static constexpr int NO = D / 8;              // output n-tiles
-  static constexpr int NS = D == 128 ? 12 : 24;  // pipeline stages: a multiple of kRot and of kAttn
+  static constexpr int NS = F8 ? (D == 128 ? 8 : 16) : (D == 128 ? 12 : 24);  // a multiple of kRot and kAttn
   static constexpr uint32_t TAB = D / 2 * 8;     // bytes of one table row ((cos, sin) per pair)
   // shared memory, from the 1024-byte-aligned base
-  static constexpr uint32_t OFF_TAB = NS * 2 * PAGE;             // [NS][hi row | lo row] base table rows
-  static constexpr uint32_t OFF_META = OFF_TAB + NS * 2 * TAB;  // [NS] int: tokens of the staged block
-  static constexpr uint32_t BYTES = OFF_META + NS * 4 + 1024;    // + alignment slack
+  static constexpr uint32_t OFF_TAB = NS * STAGE;                 // [NS][hi row | lo row] base table rows
+  static constexpr uint32_t OFF_META = OFF_TAB + NS * 2 * TAB;    // [NS] int: tokens of the staged block
+  static constexpr uint32_t OFF_SCALE = OFF_META + NS * 4;        // [NS] float2: FP8 K and V page scales
+  static constexpr uint32_t BYTES = OFF_SCALE + NS * 8 + 1024;    // + alignment slack
+  static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
 };
 
 __device__ __forceinline__ int64_t cta_begin(int c, int64_t total, int P) { return (int64_t)c * total / P; }
@@ -182,12 +191,13 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = pack_bf16x2(x0 - bf16lo(hi), x1 - bf16hi(hi));
 }
 
-template <int D, int G, int MODE>
+template <int D, int G, int MODE, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     view_kernel(const __grid_constant__ CUtensorMap tm_ksrc, const __grid_constant__ CUtensorMap tm_vsrc,
                 const __grid_constant__ CUtensorMap tm_kdst, const __grid_constant__ CUtensorMap tm_vdst,
                 const ViewParams vp, const SessionArgs a) {
-  using Q = Geo<D>;
+  using Q = Geo<D, F8>;
+  static_assert(!F8 || MODE == 2, "FP8 pages are a source of the fused mode");
   constexpr bool kWrite = MODE != 1;
   constexpr bool kAttend = MODE != 0;
   constexpr int NS = Q::NS;
@@ -195,6 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_addr(smem);
   int* meta = reinterpret_cast<int*>(smem + Q::OFF_META);
+  float2* meta_scale = reinterpret_cast<float2*>(smem + Q::OFF_SCALE);
   __shared__ __align__(8) uint64_t full[NS], rotated[NS], empty[NS];
   __shared__ __align__(8) uint64_t never;  // failure-path test only: initialised, never arrived on
 
@@ -256,10 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kProducer) {
     // ============================================================ producer
     // lane l resolves block jb + l: tokens present (0 = skip), source tile row, view slot
-    auto resolve = [&](int64_t jb, int& valid, int& ysrc, int& slot) {
+    auto resolve = [&](int64_t jb, int& valid, int& ysrc, int& slot, float& sk, float& sv) {
       valid = 0;
       ysrc = 0;
       slot = 0;
+      sk = sv = 0.f;
       const int64_t j = jb + lane;
       if (j >= nb) return;
       const Cursor cu = locate(fa + j, a, vp.n_sessions);
@@ -278,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (page >= 0 && page < vp.n_pages) {
             valid = block_tokens(id, a, cu.s);
             ysrc = (int)(((int64_t)page * vp.h_kv + cu.g) * 32);
+            if (F8) {
+              sk = vp.k_scale[(int64_t)page * vp.h_kv + cu.g];
+              sv = vp.v_scale[(int64_t)page * vp.h_kv + cu.g];
+            }
           } else {
             atomicOr(vp.status, KVM_DEV_BAD_PAGE);
           }
@@ -287,15 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
     int v_cur, y_cur, i_cur;
-    resolve(0, v_cur, y_cur, i_cur);
+    float sk_cur, sv_cur;
+    resolve(0, v_cur, y_cur, i_cur, sk_cur, sv_cur);
     for (int64_t jb = 0; jb < nb && !aborted; jb += 32) {
       int v_nxt = 0, y_nxt = 0, i_nxt = 0;
-      if (jb + 32 < nb) resolve(jb + 32, v_nxt, y_nxt, i_nxt);  // in flight while this batch is issued
+      float sk_nxt = 0.f, sv_nxt = 0.f;
+      if (jb + 32 < nb) resolve(jb + 32, v_nxt, y_nxt, i_nxt, sk_nxt, sv_nxt);  // in flight while this batch is issued
       const int cnt = (int)(nb - jb < 32 ? nb - jb : 32);
       for (int l = 0; l < cnt; ++l) {
         const int valid = __shfl_sync(0xffffffffu, v_cur, l);
         const int ysrc = __shfl_sync(0xffffffffu, y_cur, l);
         const int slot = __shfl_sync(0xffffffffu, i_cur, l);
+        const float sk = F8 ? __shfl_sync(0xffffffffu, sk_cur, l) : 0.f;
+        const float sv = F8 ? __shfl_sync(0xffffffffu, sv_cur, l) : 0.f;
         const int64_t jj = jb + l;
         const int st = (int)(jj % NS);
         const uint32_t round = (uint32_t)(jj / NS);
@@ -304,13 +324,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (round > 0) ok = mbar_wait(&empty[st], (round - 1) & 1, vp.status, vp.wait_ns);
           if (ok) {
             meta[st] = valid;
-            unsigned char* kdst = smem + st * 2 * Q::PAGE;
+            unsigned char* kdst = smem + st * Q::STAGE;
             if (valid > 0) {
-              mbar_arrive_expect_tx(&full[st], 2 * Q::PAGE + (kWrite ? 2 * Q::TAB : 0));
+              if constexpr (F8) {
+                // the two code pages (contiguous 32 x d bytes each) by 1-D bulk copies, after the bf16 pages
+                meta_scale[st] = make_float2(sk, sv);
+                mbar_arrive_expect_tx(&full[st], 2 * Q::CPAGE + 2 * Q::TAB);
+                bulk_g2s(kdst + 2 * Q::PAGE, vp.k8 + (int64_t)ysrc * D, Q::CPAGE, &full[st]);
+                bulk_g2s(kdst + 2 * Q::PAGE + Q::CPAGE, vp.v8 + (int64_t)ysrc * D, Q::CPAGE, &full[st]);
+              } else {
+                mbar_arrive_expect_tx(&full[st], 2 * Q::PAGE + (kWrite ? 2 * Q::TAB : 0));
 #pragma unroll
-              for (int b = 0; b < Q::BOXES; ++b) {
-                tma_load_2d(kdst + b * Q::BOX, &tm_ksrc, 64 * b, ysrc, &full[st]);
-                tma_load_2d(kdst + Q::PAGE + b * Q::BOX, &tm_vsrc, 64 * b, ysrc, &full[st]);
+                for (int b = 0; b < Q::BOXES; ++b) {
+                  tma_load_2d(kdst + b * Q::BOX, &tm_ksrc, 64 * b, ysrc, &full[st]);
+                  tma_load_2d(kdst + Q::PAGE + b * Q::BOX, &tm_vsrc, 64 * b, ysrc, &full[st]);
+                }
               }
               if (kWrite) {
                 unsigned char* tdst = smem + Q::OFF_TAB + st * 2 * Q::TAB;
@@ -331,6 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       v_cur = v_nxt;
       y_cur = y_nxt;
       i_cur = i_nxt;
+      sk_cur = sk_nxt;
+      sv_cur = sv_nxt;
     }
   } else if (warp < kRot) {
     // ============================================================ rotation warps
@@ -343,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Cursor cu = locate(fa + jj, a, vp.n_sessions);
         const int q = cu.s * vp.h_kv + cu.g;
         const int64_t ydst = (int64_t)q * Lcap + 32 * cu.i;
-        const uint32_t vaddr = sbase + st * 2 * Q::PAGE + Q::PAGE;
+        const uint32_t vaddr = sbase + st * Q::STAGE + Q::PAGE;
         if (__any_sync(0xffffffffu, !mbar_wait(&full[st], phase, vp.status, vp.wait_ns) ||
                                         (vp.stall && fa + jj == 0 &&
                                          !mbar_wait(&never, 0, vp.status, vp.wait_ns)))) {
@@ -357,7 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           vp.view_len[q] = 32 * (nk - 1) + ((last >= 0 && last < a.n_blk[cu.s]) ? block_tokens(last, a, cu.s) : 32);
         }
         if (valid > 0) {
-            unsigned char* kst = smem + st * 2 * Q::PAGE;
+            unsigned char* kst = smem + st * Q::STAGE;
             uint4* kq = reinterpret_cast<uint4*>(kst);  // the stage's K page as 16-byte chunks
             const float4* __restrict__ tabh = reinterpret_cast<const float4*>(smem + Q::OFF_TAB + st * 2 * Q::TAB);
             // the block's base cos/sin for this lane's 8 pairs, as packed pairs (2u, 2u + 1)
@@ -378,6 +408,95 @@ __global__ void __launch_bounds__(kThreads, 1)
             // bf16 ulp of f (> 2^-8 |f|) whenever |f| >= 2^-13 (|x1| + |x2|).  A pass holding a pair below that
             // (the rotation cancels) keeps the original bits of its row in the stage and is redone in
             // float-float after the passes, so every stored key is within one ulp of the exact rotation.
+            if constexpr (F8) {
+            // FP8 pages: K is decoded (code * scale, fp32) as it is rotated, with the same paired-fp32 rotation
+            // as bf16 pages; each rotated value is stored, and a pair that cancels is redone in float-float after
+            // the passes from its codes.  V is decoded and rounded to bf16 into the stage's V page, which the
+            // view store and the attention then read.
+            const unsigned char* codes = kst + 2 * Q::PAGE;
+            const float2 scl = meta_scale[st];
+            uint32_t redo_all = 0;  // bit pass: the pass holds a pair whose rotation cancels
+#pragma unroll
+            for (int pass = 0; pass < Q::PASSES; ++pass) {
+              const int r = lane / Q::CPR + Q::RPP * pass;
+              const uint2 ca = *reinterpret_cast<const uint2*>(codes + r * D + 8 * cc);
+              const uint2 cb = *reinterpret_cast<const uint2*>(codes + r * D + D / 2 + 8 * cc);
+              const uint32_t cw[4] = {ca.x, ca.y, cb.x, cb.y};
+              float xa_f[8], xb_f[8];  // elements 8cc + v and their rotation partners d/2 further
+#pragma unroll
+              for (int k2 = 0; k2 < 4; ++k2) {
+                const float2 lo = dequant_e4m3x2(cw[k2], scl.x), hi = dequant_e4m3x2(cw[k2] >> 16, scl.x);
+                float* dst = k2 < 2 ? xa_f + 4 * k2 : xb_f + 4 * (k2 - 2);
+                dst[0] = lo.x;
+                dst[1] = lo.y;
+                dst[2] = hi.x;
+                dst[3] = hi.y;
+              }
+              uint32_t oa[4], ob[4];
+              bool cancel = false;
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const uint64_t cs = fma2(bc[u], ofc[pass][u], mul2(bs[u] ^ 0x8000000080000000ull, ofs[pass][u]));
+                const uint64_t sn = fma2(bs[u], ofc[pass][u], mul2(bc[u], ofs[pass][u]));
+                const float x1l = xa_f[2 * u], x1h = xa_f[2 * u + 1], x2l = xb_f[2 * u], x2h = xb_f[2 * u + 1];
+                const uint64_t x1 = pk2(x1l, x1h), x2 = pk2(x2l, x2h), nx2 = pk2(-x2l, -x2h);
+                float f1l, f1h, f2l, f2h;
+                up2(fma2(x1, cs, mul2(nx2, sn)), f1l, f1h);
+                up2(fma2(x2, cs, mul2(x1, sn)), f2l, f2h);
+                cancel |= fminf(fabsf(f1l), fabsf(f2l)) * 0x1p13f < fabsf(x1l) + fabsf(x2l);
+                cancel |= fminf(fabsf(f1h), fabsf(f2h)) * 0x1p13f < fabsf(x1h) + fabsf(x2h);
+                oa[u] = pack_bf16x2(f1l, f1h);
+                ob[u] = pack_bf16x2(f2l, f2h);
+              }
+              kq[chunk_off(r, cc) >> 4] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
+              kq[chunk_off(r, cc + D / 16) >> 4] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+              redo_all |= cancel ? 1u << pass : 0u;
+            }
+#pragma unroll 2
+            for (int pass = 0; pass < Q::PASSES; ++pass) {
+              const int r = lane / Q::CPR + Q::RPP * pass;
+              const uint2 va = *reinterpret_cast<const uint2*>(codes + Q::CPAGE + r * D + 8 * cc);
+              const uint2 vb = *reinterpret_cast<const uint2*>(codes + Q::CPAGE + r * D + D / 2 + 8 * cc);
+              const uint32_t vw[4] = {va.x, va.y, vb.x, vb.y};
+              uint32_t vo[8];
+#pragma unroll
+              for (int k2 = 0; k2 < 4; ++k2) {
+                const float2 wl = dequant_e4m3x2(vw[k2], scl.y), wh = dequant_e4m3x2(vw[k2] >> 16, scl.y);
+                vo[2 * k2] = pack_bf16x2(wl.x, wl.y);
+                vo[2 * k2 + 1] = pack_bf16x2(wh.x, wh.y);
+              }
+              sts128(vaddr + chunk_off(r, cc), make_uint4(vo[0], vo[1], vo[2], vo[3]));
+              sts128(vaddr + chunk_off(r, cc + D / 16), make_uint4(vo[4], vo[5], vo[6], vo[7]));
+            }
+            if (redo_all) {  // rare: each pair of a flagged pass rotated again from its codes, in float-float if it cancels
+              const float2* tabl = reinterpret_cast<const float2*>(smem + Q::OFF_TAB + st * 2 * Q::TAB + Q::TAB);
+              const float2* tabh2 = reinterpret_cast<const float2*>(tabh);
+#pragma unroll 1
+              for (uint32_t m = redo_all; m; m &= m - 1) {
+                const int pass = __ffs(m) - 1;
+                const int r = lane / Q::CPR + Q::RPP * pass;
+#pragma unroll 1
+                for (int v = 0; v < 8; ++v) {
+                  const int k = 8 * cc + v;
+                  const float x1 = dequant_e4m3x2(codes[r * D + k], scl.x).x;
+                  const float x2 = dequant_e4m3x2(codes[r * D + D / 2 + k], scl.x).x;
+                  const float2 bh = tabh2[k], oh = __ldg(vp.rope_off + r * (D / 2) + k);
+                  float cs, sn;
+                  rope_cs(bh, oh.x, oh.y, cs, sn);
+                  if (!(fminf(fabsf(fmaf(x1, cs, -x2 * sn)), fabsf(fmaf(x2, cs, x1 * sn))) * 0x1p13f <
+                        fabsf(x1) + fabsf(x2)))
+                    continue;  // this pair was stored correctly by the pass
+                  const float2 bl = tabl[k], ol = __ldg(vp.rope_off_lo + r * (D / 2) + k);
+                  float y1, y2;
+                  rotate_exact(x1, x2, make_float4(bh.x, bl.x, bh.y, bl.y), make_float4(oh.x, ol.x, oh.y, ol.y), y1,
+                               y2);
+                  const uint32_t y = pack_bf16x2(y1, y2);
+                  *(reinterpret_cast<uint16_t*>(kst + chunk_off(r, cc)) + v) = (uint16_t)(y & 0xFFFFu);
+                  *(reinterpret_cast<uint16_t*>(kst + chunk_off(r, cc + D / 16)) + v) = (uint16_t)(y >> 16);
+                }
+              }
+            }
+            } else {
             uint4 wa = kq[chunk_off(lane / Q::CPR, cc) >> 4], wb = kq[chunk_off(lane / Q::CPR, cc + D / 16) >> 4];
             uint32_t redo_all = 0;  // bit pass
 #pragma unroll
@@ -435,6 +554,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
               }
             }
+            }
             if (valid < 32) {  // partial block: plain stores of the rows present, from the stage
               __syncwarp();
 #pragma unroll 1
@@ -455,8 +575,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid == 32 && lane == 0) {
 #pragma unroll
               for (int b = 0; b < Q::BOXES; ++b) {
-                tma_store_2d(&tm_kdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + b * Q::BOX);
-                tma_store_2d(&tm_vdst, 64 * b, (int)ydst, smem + st * 2 * Q::PAGE + Q::PAGE + b * Q::BOX);
+                tma_store_2d(&tm_kdst, 64 * b, (int)ydst, smem + st * Q::STAGE + b * Q::BOX);
+                tma_store_2d(&tm_vdst, 64 * b, (int)ydst, smem + st * Q::STAGE + Q::PAGE + b * Q::BOX);
               }
             }
         }
@@ -570,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           seg = q;
           begin_segment(cu, q);
         }
-        const uint32_t kaddr = sbase + st * 2 * Q::PAGE, vaddr = kaddr + Q::PAGE;
+        const uint32_t kaddr = sbase + st * Q::STAGE, vaddr = kaddr + Q::PAGE;
         // the rotated page (fused) or the view page as loaded (attention over a given view)
         if (__any_sync(0xffffffffu, !mbar_wait(kWrite ? &rotated[st] : &full[st], phase, vp.status, vp.wait_ns))) {
           aborted = true;
@@ -864,15 +984,16 @@ cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, int d) {
 template <int D, int G>
 cudaError_t launch_dg(const Ctx& c, int mode, const CUtensorMap* maps, const ViewParams& vp, const SessionArgs& a,
                       cudaStream_t st) {
-  using Q = Geo<D>;
-  static_assert(Q::BYTES <= 227 * 1024, "view kernel shared memory");
+  static_assert(Geo<D>::BYTES <= 227 * 1024 && Geo<D, true>::BYTES <= 227 * 1024, "view kernel shared memory");
   if (vp.total == 0 && !vp.any_empty) return cudaSuccess;
   void (*kern)(const CUtensorMap, const CUtensorMap, const CUtensorMap, const CUtensorMap, const ViewParams,
                const SessionArgs) =
-      mode == 0 ? view_kernel<D, G, 0> : (mode == 1 ? view_kernel<D, G, 1> : view_kernel<D, G, 2>);
-  cudaError_t e = ensure_smem(kern, c.device, Q::BYTES);
+      mode == 0 ? view_kernel<D, G, 0>
+                : (mode == 1 ? view_kernel<D, G, 1> : (mode == 2 ? view_kernel<D, G, 2> : view_kernel<D, G, 2, true>));
+  const uint32_t bytes = mode == 3 ? Geo<D, true>::BYTES : Geo<D>::BYTES;
+  cudaError_t e = ensure_smem(kern, c.device, bytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(vp.P), dim3(kThreads), Q::BYTES, st, 1, maps[0], maps[1], maps[2], maps[3], vp, a);
+  return launch_pdl(kern, dim3(vp.P), dim3(kThreads), bytes, st, 1, maps[0], maps[1], maps[2], maps[3], vp, a);
 }
 
 template <int D>
@@ -896,7 +1017,7 @@ cudaError_t launch_d(const Ctx& c, int mode, const CUtensorMap* maps, const View
 cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uint16_t* v_src, int64_t n_pages,
                         const int32_t* bt, int n_sessions, const SessionArgs& a, const int32_t* kept,
                         const uint16_t* q, uint16_t* k_view, uint16_t* v_view, int32_t* view_len, float* out,
-                        cudaStream_t st) {
+                        cudaStream_t st, const float* k_scale, const float* v_scale) {
   ViewParams vp;
   vp.bt = bt;
   vp.max_blocks = c.p.max_blocks;
@@ -913,6 +1034,10 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
   vp.rope_base_lo = reinterpret_cast<const float2*>(c.rope_base_lo);
   vp.rope_off_lo = reinterpret_cast<const float2*>(c.rope_off_lo);
   vp.out = out;
+  vp.k_scale = k_scale;
+  vp.v_scale = v_scale;
+  vp.k8 = reinterpret_cast<const uint8_t*>(k_src);
+  vp.v8 = reinterpret_cast<const uint8_t*>(v_src);
   vp.status = c.status;
   vp.total = a.seg_base[n_sessions];
   vp.any_empty = 0;
@@ -938,6 +1063,11 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
     if ((e = make_map(&maps[1], v_src, view_rows, c.p.d)) != cudaSuccess) return e;
     maps[2] = maps[0];
     maps[3] = maps[1];
+  } else if (mode == 3) {  // FP8 code pages come in by 1-D bulk copies: only the view maps are used
+    if ((e = make_map(&maps[2], k_view, view_rows, c.p.d)) != cudaSuccess) return e;
+    if ((e = make_map(&maps[3], v_view, view_rows, c.p.d)) != cudaSuccess) return e;
+    maps[0] = maps[2];
+    maps[1] = maps[3];
   } else {
     if ((e = make_map(&maps[0], k_src, pool_rows, c.p.d)) != cudaSuccess) return e;
     if ((e = make_map(&maps[1], v_src, pool_rows, c.p.d)) != cudaSuccess) return e;

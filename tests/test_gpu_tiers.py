@@ -100,13 +100,24 @@ def test_fp8_index_view_and_attention_match_oracle(name, n_tok):
     K.kvm_decode_attn(ctx, q, k_view, v_view, view_len, S, out)
     torch.cuda.synchronize()
     assert K.kvm_device_status(ctx) == 0
+    # the same view and attention in one pass (kvm_materialize_attn_fp8), into fresh buffers
+    k_view2 = torch.zeros_like(k_view)
+    v_view2 = torch.zeros_like(v_view)
+    view_len2 = torch.full_like(view_len, -7)
+    out2 = torch.full_like(out, float("nan"))
+    K.kvm_materialize_attn_fp8(ctx, k8, ks, v8, vs, w.n_pages, bt, [n_tok], kept, q, k_view2, v_view2, view_len2, out2)
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
     for g in range(w.h_kv):
         check_index_values(index[0, g].cpu().numpy(), keys[g], O.mean_k_index_of(keys[g]))
         kv, vv = O.materialize_values(keys[g], vals[g], ids[g], n_tok, w.rope_theta)
-        assert int(view_len[0, g]) == kv.shape[0]
-        check_view(host_u16(k_view[0, g]), host_u16(v_view[0, g]), kv, vv)
         ref = O.decode_attention(li.q[0, 0, G * g:G * (g + 1)], kv, vv, w.rope_theta)
-        check_out(out[0, G * g:G * (g + 1)].cpu().numpy(), ref)
+        for kvd, vvd, vld, od in ((k_view, v_view, view_len, out), (k_view2, v_view2, view_len2, out2)):
+            assert int(vld[0, g]) == kv.shape[0]
+            check_view(host_u16(kvd[0, g]), host_u16(vvd[0, g]), kv, vv)
+            check_out(od[0, G * g:G * (g + 1)].cpu().numpy(), ref)
+    # V from either path is the same bf16 rounding of the same fp32 values: bit-identical
+    assert torch.equal(v_view.view(torch.int16), v_view2.view(torch.int16))
     ctx.close()
 
 
@@ -189,8 +200,16 @@ def test_fp8_full_size_1m_token_layer_sampled_heads():
     K.kvm_materialize_fp8(ctx, k8, ks, v8, vs, w.n_pages, bt, [w.n_tok], kept, k_view, v_view, view_len)
     out = torch.full((1, w.h_q, w.d), float("nan"), dtype=torch.float32, device="cuda")
     K.kvm_decode_attn(ctx, q, k_view, v_view, view_len, 1, out)
+    # the fused FP8 call (the bench's launch configuration for FP8 pages), into its own buffers
+    k_view2 = torch.empty_like(k_view)
+    v_view2 = torch.empty_like(v_view)
+    view_len2 = torch.full_like(view_len, -7)
+    out2 = torch.full_like(out, float("nan"))
+    K.kvm_materialize_attn_fp8(ctx, k8, ks, v8, vs, w.n_pages, bt, [w.n_tok], kept, q, k_view2, v_view2, view_len2,
+                               out2)
     torch.cuda.synchronize()
     assert K.kvm_device_status(ctx) == 0
+    assert torch.equal(view_len, view_len2) and torch.equal(v_view.view(torch.int16), v_view2.view(torch.int16))
     G = w.group
     same = 0
     for g in (1, 6):
@@ -217,7 +236,9 @@ def test_fp8_full_size_1m_token_layer_sampled_heads():
             continue
         same += 1
         kv, vv = O.materialize_values(keys, vals, ids, w.n_tok, w.rope_theta)
-        check_view(host_u16(k_view[0, g]), host_u16(v_view[0, g]), kv, vv)
-        check_out(out[0, G * g:G * (g + 1)].cpu().numpy(), O.decode_attention(qg, kv, vv, w.rope_theta))
+        ref = O.decode_attention(qg, kv, vv, w.rope_theta)
+        for kvd, vvd, od in ((k_view, v_view, out), (k_view2, v_view2, out2)):
+            check_view(host_u16(kvd[0, g]), host_u16(vvd[0, g]), kv, vv)
+            check_out(od[0, G * g:G * (g + 1)].cpu().numpy(), ref)
     assert same >= 1
     ctx.close()
