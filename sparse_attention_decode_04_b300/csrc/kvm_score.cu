@@ -46,6 +46,46 @@ constexpr int kStageRows = 32;
 constexpr int kStages = 5;
 constexpr int kSelectThreads = 512;
 
+// The query slice a lane holds for its row's dot products (LPR lanes per row), scaled by 1/sqrt(d): dims
+// 4*sub + 4*LPR*i + {0..3} of each of the G query heads of KV head g.  avg_group > 0 (with G == 1): the withdrawn scoring's single row, the
+// unweighted mean of the group's avg_group query heads (taken in fp32).
+template <int D, int G, int LPR>
+__device__ __forceinline__ void load_query(float (&qv)[G][D / LPR], const uint16_t* __restrict__ q, int s, int g,
+                                           int q_heads, int avg_group, int sub) {
+  constexpr int NV = D / (4 * LPR);  // float4 chunks per lane per row
+  const float inv_sqrt_d = __frsqrt_rn((float)D);
+  if (G == 1 && avg_group > 0) {
+#pragma unroll
+    for (int j = 0; j < NV * 4; ++j) qv[0][j] = 0.f;
+    for (int h = 0; h < avg_group; ++h) {
+      const uint16_t* qh = q + ((int64_t)s * q_heads + g * avg_group + h) * D;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh + 4 * sub + 4 * LPR * i));
+        qv[0][4 * i + 0] += bf16lo(w.x);
+        qv[0][4 * i + 1] += bf16hi(w.x);
+        qv[0][4 * i + 2] += bf16lo(w.y);
+        qv[0][4 * i + 3] += bf16hi(w.y);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < NV * 4; ++j) qv[0][j] = qv[0][j] / (float)avg_group * inv_sqrt_d;
+  } else {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const uint16_t* qh = q + ((int64_t)s * q_heads + g * G + h) * D;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh + 4 * sub + 4 * LPR * i));
+        qv[h][4 * i + 0] = bf16lo(w.x) * inv_sqrt_d;
+        qv[h][4 * i + 1] = bf16hi(w.x) * inv_sqrt_d;
+        qv[h][4 * i + 2] = bf16lo(w.y) * inv_sqrt_d;
+        qv[h][4 * i + 3] = bf16hi(w.y) * inv_sqrt_d;
+      }
+    }
+  }
+}
+
 template <int D, int G>
 __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
     const uint16_t* __restrict__ q, const float* __restrict__ index, int64_t max_blocks, int h_kv, int h_q,
@@ -88,39 +128,8 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   if (tid == 0)
     for (int k = 0; k < min(kStages, nstage); ++k) issue(k);
 
-  // Query slice of this lane, scaled by 1/sqrt(d): dims 4*sub + 32*i + {0..3}.
   float qv[G][NV * 4];
-  const float inv_sqrt_d = __frsqrt_rn((float)D);
-  if (G == 1 && avg_group > 0) {
-#pragma unroll
-    for (int j = 0; j < NV * 4; ++j) qv[0][j] = 0.f;
-    for (int h = 0; h < avg_group; ++h) {
-      const uint16_t* qh = q + ((int64_t)s * q_heads + g * avg_group + h) * D;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh + 4 * sub + 32 * i));
-        qv[0][4 * i + 0] += bf16lo(w.x);
-        qv[0][4 * i + 1] += bf16hi(w.x);
-        qv[0][4 * i + 2] += bf16lo(w.y);
-        qv[0][4 * i + 3] += bf16hi(w.y);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < NV * 4; ++j) qv[0][j] = qv[0][j] / (float)avg_group * inv_sqrt_d;
-  } else {
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const uint16_t* qh = q + ((int64_t)s * q_heads + g * G + h) * D;
-#pragma unroll
-      for (int i = 0; i < NV; ++i) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2*>(qh + 4 * sub + 32 * i));
-        qv[h][4 * i + 0] = bf16lo(w.x) * inv_sqrt_d;
-        qv[h][4 * i + 1] = bf16hi(w.x) * inv_sqrt_d;
-        qv[h][4 * i + 2] = bf16lo(w.y) * inv_sqrt_d;
-        qv[h][4 * i + 3] = bf16hi(w.y) * inv_sqrt_d;
-      }
-    }
-  }
+  load_query<D, G, 8>(qv, q, s, g, q_heads, avg_group, sub);
   float run_max = -INFINITY;  // lane (sub == h) tracks head h over its rows
 
   int k = 0;
@@ -218,6 +227,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
 // super-bins (each nb/64 bins) are pulled first, then the bins of the one super-bin that holds the boundary.
 constexpr int kSelBins = 4096;
 constexpr int kSelSup = 64;
+constexpr int kMaxCluster = 8;  // CTAs per cluster at most
 
 __device__ __forceinline__ int sel_shift(int pass) { return pass == 0 ? 20 : (pass == 1 ? 8 : 0); }
 __device__ __forceinline__ int sel_bins(int pass) { return pass == 2 ? 256 : kSelBins; }
@@ -228,25 +238,28 @@ struct SelResult {
   int count;       // keys in the boundary bin (cluster-wide)
 };
 
+// Split cluster barrier: every CTA arrives when it starts and waits before its first store into another CTA's
+// shared memory, so that no CTA is written before it runs.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 // Warp 0: finds, over the cluster's merged counts, the bin holding the krem-th largest key of this pass.
-// sup / hist are this CTA's buffers; the same offsets are read in every CTA of the cluster.
-__device__ __forceinline__ SelResult sel_boundary(cg::cluster_group& cluster, int C, const int* sup,
+// sup_all[r] holds CTA r's super-bin sums (pushed into every CTA before the pass's cluster barrier); hist is this
+// CTA's histogram buffer, and the same offsets are read in every CTA of the cluster.
+__device__ __forceinline__ SelResult sel_boundary(cg::cluster_group& cluster, int C, const int (*sup_all)[kSelSup],
                                                   const int* hist, int nb, int krem) {
   const int lane = threadIdx.x & 31;
-  // 1. super-bins 2*lane and 2*lane + 1, summed over the cluster (independent remote loads)
+  // 1. super-bins 2*lane and 2*lane + 1, summed over the cluster (local loads)
   int c0 = 0, c1 = 0;
-  {
-    int2 v[8];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (r < C) v[r] = *reinterpret_cast<const int2*>(cluster.map_shared_rank(sup, r) + 2 * lane);
-#pragma unroll
-    for (int r = 0; r < 8; ++r)
-      if (r < C) {
-        c0 += v[r].x;
-        c1 += v[r].y;
-      }
-  }
+  for (int r = 0; r < kMaxCluster; ++r)
+    if (r < C) {
+      const int2 v = *reinterpret_cast<const int2*>(sup_all[r] + 2 * lane);
+      c0 += v.x;
+      c1 += v.y;
+    }
   // keys above each of this lane's super-bins: inclusive suffix sum over the higher lanes
   int suf = c0 + c1;
 #pragma unroll
@@ -264,12 +277,12 @@ __device__ __forceinline__ SelResult sel_boundary(cg::cluster_group& cluster, in
   const int bw = nb / kSelSup;
   int b0 = 0, b1 = 0;
   if (2 * lane < bw) {
-    int2 v[8];
+    int2 v[kMaxCluster];
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < kMaxCluster; ++r)
       if (r < C) v[r] = *reinterpret_cast<const int2*>(cluster.map_shared_rank(hist, r) + sb * bw + 2 * lane);
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < kMaxCluster; ++r)
       if (r < C) {
         b0 += v[r].x;
         b1 += v[r].y;
@@ -295,6 +308,283 @@ __device__ __forceinline__ SelResult sel_boundary(cg::cluster_group& cluster, in
 constexpr int kSelTilesPerLane = 10;  // tile partials a normaliser lane holds: up to 320 tiles per head
 constexpr int kSelChunk = 4096;       // blocks whose exponentials are staged in shared memory at a time (at most)
 constexpr int kSelList = 32;          // boundary keys resolved by an exchanged list instead of a third pass
+constexpr int kSelSlice = 2048;       // blocks per CTA of the selection cluster (up to kMaxCluster CTAs)
+
+// Shared-memory state of the radix select and the compaction (one per CTA).
+struct SelShared {
+  static constexpr int NW = kSelectThreads / 32;
+  int hist[2][kSelBins];  // pass p builds hist[p & 1]; the other may still be read remotely
+  int sup_all[2][kMaxCluster][kSelSup];  // pass p: every CTA's super-bin sums, pushed by their owners
+  int warp_cnt[NW][2];               // per warp: blocks kept for sure, keys equal to the boundary key
+  int warp_taken[NW];                // per warp: boundary-list keys taken (list mode)
+  int cnts[kMaxCluster][2];          // pushed by the lower-ranked CTAs of the cluster: the same, per CTA
+  uint2 blist[kMaxCluster][kSelList];  // list mode: each CTA's boundary-bin keys (key, block), pushed to all
+  int blist_n[kMaxCluster];
+  int taken_cnt[kMaxCluster];        // list mode: keys of each CTA's list that are taken
+  int own_taken[kSelList];           // list mode: this CTA's taken blocks
+  uint2 flat[kSelList];              // list mode: the cluster's boundary keys in one row
+  uint32_t tmask[kSelectThreads];    // list mode: per thread, which of its slice positions are taken
+  int own_n, own_taken_n;
+  SelResult res;
+};
+
+// Clears what the selection accumulates into; the caller synchronises the CTA before the keys' histogram.
+__device__ __forceinline__ void sel_init(SelShared& S) {
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kSelBins; i += kSelectThreads) S.hist[0][i] = 0;
+  if (tid < kMaxCluster) S.taken_cnt[tid] = 0;
+  if (tid < SelShared::NW) S.warp_taken[tid] = 0;
+  if (tid == 0) S.own_n = S.own_taken_n = 0;
+  S.tmask[tid] = 0;
+}
+
+// The order keys of the slice's blocks [lo, hi) are in key[0 .. hi - lo), and S.hist[0] holds the pass-0
+// histogram of this CTA's candidates.  Finds the top_k-th largest candidate key over the cluster and writes the
+// kept blocks (candidates above it, the forced sink / recent blocks, ties resolved toward the lower block) to
+// kept_row in ascending block order.
+__device__ void sel_radix_compact(cg::cluster_group& cluster, SelShared& S, const uint32_t* key, int lo, int hi,
+                                  int cand_lo, int cand_hi, int top_k, int budget, int32_t* kept_row) {
+  constexpr int NT = kSelectThreads, NW = SelShared::NW;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int crank = (int)cluster.block_rank();
+  const int C = (int)cluster.num_blocks();
+  const int n_iter = (hi - lo + NT - 1) / NT;
+  auto is_cand = [&](int b) { return b >= cand_lo && b < cand_hi; };
+
+  // ---- radix select of the top_k-th largest candidate key.  After pass p the boundary is the bin `prefix`
+  //      of the key's bits above `sh`.  The passes stop early when the boundary bin holds exactly the keys
+  //      still to take (all of them are kept), or, after the second pass, when it holds at most kSelList
+  //      keys: those are then exchanged as a list and ranked exactly in the compaction.
+  cluster_wait();  // paired with the arrival at the kernel's start: every CTA of the cluster is running
+  uint32_t prefix = 0;
+  int sh = 32, krem = top_k, bcount = 0;
+  bool resolved = top_k == 0;  // no candidate is taken: the boundary lies above every key
+  bool list_mode = false;
+#pragma unroll 1
+  for (int pass = 0; pass < 3 && !resolved; ++pass) {
+    const int shift = sel_shift(pass), nb = sel_bins(pass);
+    int* h = S.hist[pass & 1];
+    if (pass > 0) {
+      // histogram of this pass's digit over the candidates inside the boundary bin (h was cleared below)
+      for (int j = 0; j < n_iter; ++j) {
+        const int b = lo + tid + j * NT;
+        if (b < hi && is_cand(b)) {
+          const uint32_t k = key[b - lo];
+          if ((k >> sh) == prefix) atomicAdd(&h[(k >> shift) & (uint32_t)(nb - 1)], 1);
+        }
+      }
+    }
+    __syncthreads();  // this CTA's histogram is complete
+    // per-CTA super-bin sums (nb / 64 bins each): 4096 bins, 8 per thread, then over 8 consecutive lanes; or
+    // 256 bins, 4 per thread in the first 64 threads
+    static_assert(kSelBins == 8 * NT && kSelSup * 8 == NT, "super-bin sums assume 512 threads and 4096 bins");
+    // each sum is pushed into every CTA of the cluster (itself included): thread 8 * sbin + j stores super-bin
+    // sbin into CTAs j, j + 8, so the boundary search reads all of them locally after the barrier
+    if (nb == kSelBins) {
+      const int4 u = reinterpret_cast<const int4*>(h)[2 * tid], w = reinterpret_cast<const int4*>(h)[2 * tid + 1];
+      int v = u.x + u.y + u.z + u.w + w.x + w.y + w.z + w.w;
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      v += __shfl_xor_sync(0xffffffffu, v, 4);
+      for (int r = lane & 7; r < C; r += 8)
+        cluster.map_shared_rank(&S.sup_all[pass & 1][0][0], r)[crank * kSelSup + (tid >> 3)] = v;
+    } else if (tid < kSelSup) {
+      const int4 u = reinterpret_cast<const int4*>(h)[tid];
+      const int v = u.x + u.y + u.z + u.w;
+      for (int r = 0; r < C; ++r) cluster.map_shared_rank(&S.sup_all[pass & 1][0][0], r)[crank * kSelSup + tid] = v;
+    }
+    cluster.sync();
+    // the other buffer (read remotely in the previous pass, finished by every CTA before this barrier) is
+    // cleared for the next pass
+    if (pass < 2) {
+      int4* nh = reinterpret_cast<int4*>(S.hist[(pass + 1) & 1]);
+      nh[2 * tid] = make_int4(0, 0, 0, 0);
+      nh[2 * tid + 1] = make_int4(0, 0, 0, 0);
+    }
+    if (warp == 0) {
+      const SelResult r = sel_boundary(cluster, C, S.sup_all[pass & 1], h, nb, krem);
+      if (lane == 0) S.res = r;
+    }
+    __syncthreads();
+    const SelResult r = S.res;
+    prefix = sh == 32 ? r.digit : ((prefix << (sh - shift)) | r.digit);
+    sh = shift;
+    krem = r.krem;
+    bcount = r.count;
+    list_mode = pass == 1 && bcount != krem && bcount <= kSelList;
+    resolved = bcount == krem || sh == 0 || list_mode;
+    __syncthreads();  // S.res is rewritten by the next pass
+  }
+  griddep_launch_dependents();  // the view kernel may be scheduled while the compaction runs
+
+  // ---- compaction.  A candidate is kept if its bits above sh exceed the boundary prefix, or equal it and
+  //      either the whole boundary bin is taken, or (list mode) it ranks among the first krem of the
+  //      exchanged boundary list by (key, lower block first), or (sh == 0, equal keys) it is among the first
+  //      krem of the cluster's equal keys in block order.  Thread t owns the consecutive slice positions
+  //      [t * per, (t + 1) * per), so block order runs across threads, warps and CTAs; the positions of its
+  //      kept blocks come from scans of the per-thread counts.
+  const bool all_eq = top_k == 0 ? false : bcount == krem;
+  const bool tie_mode = !all_eq && !list_mode && top_k > 0;
+  // 0 = dropped, 1 = kept, 2 = equal to the boundary key (tie mode), 3 = in the boundary list (list mode)
+  auto classify = [&](int b) -> int {
+    if (!is_cand(b)) return 1;
+    if (top_k == 0) return 0;
+    const uint32_t kp = key[b - lo] >> sh;
+    if (kp > prefix) return 1;
+    if (kp < prefix) return 0;
+    return all_eq ? 1 : (list_mode ? 3 : 2);
+  };
+  const int per = (hi - lo + NT - 1) / NT;
+  const int p0 = min(hi, lo + tid * per), p1 = min(hi, p0 + per);
+  const bool cache = per <= 16;  // the classes of the thread's positions kept in one register, 2 bits each
+  uint32_t cls = 0;
+  int keep_t = 0, eq_t = 0;
+  for (int b = p0; b < p1; ++b) {
+    const int cl = classify(b);
+    if (cache) cls |= (uint32_t)cl << (2 * (b - p0));
+    keep_t += cl == 1;
+    eq_t += cl == 2;
+    if (cl == 3) {  // at most kSelList keys over the cluster
+      const int i = atomicAdd(&S.own_n, 1);
+      if (i < kSelList) S.own_taken[i] = b;  // scratch until the list is ranked
+    }
+  }
+  // inclusive scans over the warp's threads
+  int keep_inc = keep_t, eq_inc = eq_t;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, keep_inc, o), z = __shfl_up_sync(0xffffffffu, eq_inc, o);
+    if (lane >= o) {
+      keep_inc += y;
+      eq_inc += z;
+    }
+  }
+  if (lane == 31) {
+    S.warp_cnt[warp][0] = keep_inc;
+    S.warp_cnt[warp][1] = eq_inc;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int kc = 0, ec = 0;
+    for (int w2 = 0; w2 < NW; ++w2) {
+      kc += S.warp_cnt[w2][0];
+      ec += S.warp_cnt[w2][1];
+    }
+    // pushed into every higher-ranked CTA: after the barrier each CTA reads only its own shared memory, so no
+    // CTA needs to wait for another before it exits
+    for (int r = crank + 1; r < C; ++r) {
+      int* dst = cluster.map_shared_rank(&S.cnts[0][0], r) + 2 * crank;
+      dst[0] = kc;
+      dst[1] = ec;
+    }
+  }
+  if (list_mode) {
+    // this CTA's boundary keys, pushed into every CTA of the cluster (itself included)
+    const int n_own = min(S.own_n, kSelList);
+    for (int i = tid; i < C * kSelList; i += NT) {
+      const int r = i / kSelList, k = i - r * kSelList;
+      if (k < n_own) {
+        const int b = S.own_taken[k];
+        cluster.map_shared_rank(&S.blist[0][0], r)[crank * kSelList + k] = make_uint2(key[b - lo], (uint32_t)b);
+      }
+      if (k == 0) cluster.map_shared_rank(S.blist_n, r)[crank] = n_own;
+    }
+  }
+  cluster.sync();
+  if (list_mode) {
+    // rank every listed key by (key descending, block ascending); the first krem are taken
+    if (warp == 0) {
+      uint2 e = make_uint2(0u, 0xFFFFFFFFu);
+      int src = -1, seen = 0;
+      for (int r = 0; r < C; ++r) {
+        const int n = S.blist_n[r];
+        if (lane >= seen && lane < seen + n) {
+          e = S.blist[r][lane - seen];
+          src = r;
+        }
+        seen += n;
+      }
+      S.flat[lane] = e;  // the listed keys in one row, read back as broadcasts
+      __syncwarp();
+      int rank = 0;
+#pragma unroll
+      for (int o = 0; o < kSelList; ++o) {
+        const uint2 f = S.flat[o];
+        rank += (o < seen && (f.x > e.x || (f.x == e.x && f.y < e.y))) ? 1 : 0;
+      }
+      const bool take = src >= 0 && rank < krem;
+      if (take) {
+        atomicAdd(&S.taken_cnt[src], 1);
+        if (src == crank) {
+          const int off = (int)e.y - lo;
+          S.own_taken[atomicAdd(&S.own_taken_n, 1)] = (int)e.y;
+          atomicAdd(&S.warp_taken[off / per / 32], 1);
+          if (per <= 32) atomicOr(&S.tmask[off / per], 1u << (off % per));
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // listed blocks of this thread that are taken (a bit per position where a thread holds at most 32), and the
+  // same over the warp's threads before it
+  int list_t = 0, list_excl = 0;
+  const uint32_t tmask = list_mode && per <= 32 ? S.tmask[tid] : 0u;
+  if (list_mode) {
+    if (per <= 32) {
+      list_t = __popc(tmask);
+    } else {
+      const int nt = S.own_taken_n;
+      for (int i = 0; i < nt; ++i) {
+        const int b = S.own_taken[i];
+        list_t += (b >= p0 && b < p1) ? 1 : 0;
+      }
+    }
+    int inc = list_t;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o);
+      if (lane >= o) inc += y;
+    }
+    list_excl = inc - list_t;
+  }
+  // blocks kept before this thread (cluster-wide, in block order), and equal keys before it
+  int keep_base = 0, eq_base = 0;
+  for (int r = 0; r < crank; ++r) {
+    const int taken = tie_mode ? max(0, min(S.cnts[r][1], krem - eq_base)) : (list_mode ? S.taken_cnt[r] : 0);
+    keep_base += S.cnts[r][0] + taken;
+    eq_base += S.cnts[r][1];
+  }
+  for (int w2 = 0; w2 < warp; ++w2) {
+    const int taken =
+        tie_mode ? max(0, min(S.warp_cnt[w2][1], krem - eq_base)) : (list_mode ? S.warp_taken[w2] : 0);
+    keep_base += S.warp_cnt[w2][0] + taken;
+    eq_base += S.warp_cnt[w2][1];
+  }
+  {
+    const int eq_excl = eq_inc - eq_t;
+    const int taken = tie_mode ? max(0, min(eq_excl, krem - eq_base)) : list_excl;
+    keep_base += keep_inc - keep_t + taken;
+    eq_base += eq_excl;
+  }
+  int pos = keep_base, eq_run = eq_base;
+  for (int b = p0; b < p1; ++b) {
+    const int cl = cache ? (int)((cls >> (2 * (b - p0))) & 3u) : classify(b);
+    bool kp = cl == 1;
+    if (cl == 2) kp = eq_run++ < krem;
+    if (cl == 3) {
+      if (per <= 32) {
+        kp = (tmask >> (b - p0)) & 1u;
+      } else {
+        const int nt = S.own_taken_n;
+        for (int i = 0; i < nt; ++i) kp |= S.own_taken[i] == b;
+      }
+    }
+    if (kp) {
+      if (pos < budget) kept_row[pos] = b;  // never past the row, whatever the keys hold
+      ++pos;
+    }
+  }
+}
 
 template <int G>
 __global__ void __launch_bounds__(kSelectThreads) select_kernel(
@@ -302,33 +592,21 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     int64_t max_blocks, int h_kv, int h_q, SessionArgs a, int rows_per_tile, int n_sink, int n_recent, int top_k,
     int budget, int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores,
     const float* __restrict__ gs_in, uint32_t* __restrict__ status, int chunk) {
-  constexpr int NT = kSelectThreads, NW = NT / 32;
+  constexpr int NT = kSelectThreads;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw);        // [slice_cap]
   float* e_stage = reinterpret_cast<float*>(key + slice_cap);    // [G][chunk] exponentials of one chunk
   float* coef = e_stage + (gs_in ? 0 : G * chunk);               // [tiles in slice][G]
   __shared__ __align__(8) uint64_t e_bar;
-  __shared__ __align__(16) int hist[2][kSelBins];  // pass p builds hist[p & 1]; the other may still be read remotely
-  __shared__ __align__(16) int sup[2][kSelSup];
-  __shared__ int warp_cnt[NW][2];     // per warp: blocks kept for sure, keys equal to the boundary key
-  __shared__ int warp_taken[NW];      // per warp: boundary-list keys taken (list mode)
-  __shared__ int cnts[8][2];          // pushed by the lower-ranked CTAs of the cluster: the same, per CTA
-  __shared__ uint2 blist[8][kSelList];  // list mode: each CTA's boundary-bin keys (key, block), pushed to all
-  __shared__ int blist_n[8];
-  __shared__ int taken_cnt[8];        // list mode: keys of each CTA's list that are taken
-  __shared__ int own_taken[kSelList];  // list mode: this CTA's taken blocks
-  __shared__ int own_n, own_taken_n;
-  __shared__ SelResult s_res;
+  __shared__ __align__(16) SelShared S;
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < kSelBins; i += NT) hist[0][i] = 0;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  sel_init(S);
   if (tid == 0) {
     mbar_init(&e_bar, 1);
     mbar_fence_init();
   }
-  if (tid < 8) taken_cnt[tid] = 0;
-  if (tid < NW) warp_taken[tid] = 0;
-  if (tid == 0) own_n = own_taken_n = 0;
+  cluster_arrive_relaxed();  // paired with the wait before the first store into another CTA's shared memory
   griddep_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const int crank = (int)cluster.block_rank();
@@ -352,7 +630,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     if (valid) {
       key[b - lo] = k;
       if (gs_dst && gs_dst != gs_in) gs_dst[b] = gsv;
-      if (!select_all && is_cand(b)) atomicAdd(&hist[0][k >> 20], 1);
+      if (!select_all && is_cand(b)) atomicAdd(&S.hist[0][k >> 20], 1);
     }
   };
   if (gs_in != nullptr) {
@@ -434,193 +712,21 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     for (int b = lo + tid; b < hi; b += NT) kept_row[b] = b;
     if (crank == 0)
       for (int i = n_blk + tid; i < budget; i += NT) kept_row[i] = -1;
-    return;  // no distributed shared memory access on this path
+    cluster_wait();  // completes the start barrier; no distributed shared memory access on this path
+    return;
   }
-
-  // ---- 2. radix select of the top_k-th largest candidate key.  After pass p the boundary is the bin `prefix`
-  //         of the key's bits above `sh`.  The passes stop early when the boundary bin holds exactly the keys
-  //         still to take (all of them are kept), or, after the second pass, when it holds at most kSelList
-  //         keys: those are then exchanged as a list and ranked exactly in the compaction.
-  uint32_t prefix = 0;
-  int sh = 32, krem = top_k, bcount = 0;
-  bool resolved = top_k == 0;  // no candidate is taken: the boundary lies above every key
-  bool list_mode = false;
-#pragma unroll 1
-  for (int pass = 0; pass < 3 && !resolved; ++pass) {
-    const int shift = sel_shift(pass), nb = sel_bins(pass);
-    int* h = hist[pass & 1];
-    int* sp = sup[pass & 1];
-    if (pass > 0) {
-      // histogram of this pass's digit over the candidates inside the boundary bin (h was cleared below)
-      for (int j = 0; j < n_iter; ++j) {
-        const int b = lo + tid + j * NT;
-        if (b < hi && is_cand(b)) {
-          const uint32_t k = key[b - lo];
-          if ((k >> sh) == prefix) atomicAdd(&h[(k >> shift) & (uint32_t)(nb - 1)], 1);
-        }
-      }
-    }
-    __syncthreads();  // this CTA's histogram is complete
-    // per-CTA super-bin sums (nb / 64 bins each)
-    {
-      const int bw = nb / kSelSup;
-      for (int sbin = warp; sbin < kSelSup; sbin += NW) {
-        int v = 0;
-        for (int i = lane; i < bw; i += 32) v += h[sbin * bw + i];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) sp[sbin] = v;
-      }
-    }
-    cluster.sync();
-    // the other buffer (read remotely in the previous pass, finished by every CTA before this barrier) is
-    // cleared for the next pass
-    if (pass < 2)
-      for (int i = tid; i < kSelBins; i += NT) hist[(pass + 1) & 1][i] = 0;
-    if (warp == 0) {
-      const SelResult r = sel_boundary(cluster, C, sp, h, nb, krem);
-      if (lane == 0) s_res = r;
-    }
-    __syncthreads();
-    const SelResult r = s_res;
-    prefix = sh == 32 ? r.digit : ((prefix << (sh - shift)) | r.digit);
-    sh = shift;
-    krem = r.krem;
-    bcount = r.count;
-    list_mode = pass == 1 && bcount != krem && bcount <= kSelList;
-    resolved = bcount == krem || sh == 0 || list_mode;
-    __syncthreads();  // s_res is rewritten by the next pass
-  }
-  griddep_launch_dependents();  // the view kernel may be scheduled while the compaction runs
-
-  // ---- 3. compaction.  A candidate is kept if its bits above sh exceed the boundary prefix, or equal it and
-  //         either the whole boundary bin is taken, or (list mode) it ranks among the first krem of the
-  //         exchanged boundary list by (key, lower block first), or (sh == 0, equal keys) it is among the first
-  //         krem of the cluster's equal keys in block order.  Warp w owns slice positions
-  //         [w * 32 * n_iter, (w+1) * 32 * n_iter), lane-interleaved, so block order is kept within and across
-  //         warps and CTAs.
-  const bool all_eq = top_k == 0 ? false : bcount == krem;
-  const bool tie_mode = !all_eq && !list_mode && top_k > 0;
-  // 0 = dropped, 1 = kept, 2 = equal to the boundary key (tie mode), 3 = in the boundary list (list mode)
-  auto classify = [&](int b) -> int {
-    if (b >= hi) return 0;
-    if (!is_cand(b)) return 1;
-    if (top_k == 0) return 0;
-    const uint32_t kp = key[b - lo] >> sh;
-    if (kp > prefix) return 1;
-    if (kp < prefix) return 0;
-    return all_eq ? 1 : (list_mode ? 3 : 2);
-  };
-  const int wbase = lo + warp * 32 * n_iter;
-  int keep_w = 0, eq_w = 0;
-  for (int j = 0; j < n_iter; ++j) {
-    const int b = wbase + j * 32 + lane;
-    const int cl = classify(b);
-    keep_w += __popc(__ballot_sync(0xffffffffu, cl == 1));
-    eq_w += __popc(__ballot_sync(0xffffffffu, cl == 2));
-    if (cl == 3) {  // at most kSelList keys over the cluster
-      const int i = atomicAdd(&own_n, 1);
-      if (i < kSelList) {
-        own_taken[i] = b;  // scratch until the list is ranked
-      }
-    }
-  }
-  if (lane == 0) {
-    warp_cnt[warp][0] = keep_w;
-    warp_cnt[warp][1] = eq_w;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    int kc = 0, ec = 0;
-    for (int w2 = 0; w2 < NW; ++w2) {
-      kc += warp_cnt[w2][0];
-      ec += warp_cnt[w2][1];
-    }
-    // pushed into every higher-ranked CTA: after the barrier each CTA reads only its own shared memory, so no
-    // CTA needs to wait for another before it exits
-    for (int r = crank + 1; r < C; ++r) {
-      int* dst = cluster.map_shared_rank(&cnts[0][0], r) + 2 * crank;
-      dst[0] = kc;
-      dst[1] = ec;
-    }
-  }
-  if (list_mode) {
-    // this CTA's boundary keys, pushed into every CTA of the cluster (itself included)
-    const int n_own = min(own_n, kSelList);
-    for (int i = tid; i < C * kSelList; i += NT) {
-      const int r = i / kSelList, k = i - r * kSelList;
-      if (k < n_own) {
-        const int b = own_taken[k];
-        cluster.map_shared_rank(&blist[0][0], r)[crank * kSelList + k] = make_uint2(key[b - lo], (uint32_t)b);
-      }
-      if (k == 0) cluster.map_shared_rank(blist_n, r)[crank] = n_own;
-    }
-  }
-  cluster.sync();
-  if (list_mode) {
-    // rank every listed key by (key descending, block ascending); the first krem are taken
-    if (warp == 0) {
-      uint2 e = make_uint2(0u, 0xFFFFFFFFu);
-      int src = -1, seen = 0;
-      for (int r = 0; r < C; ++r) {
-        const int n = blist_n[r];
-        if (lane >= seen && lane < seen + n) {
-          e = blist[r][lane - seen];
-          src = r;
-        }
-        seen += n;
-      }
-      int rank = 0;
-      for (int o = 0; o < seen; ++o) {
-        const uint32_t ok = __shfl_sync(0xffffffffu, e.x, o), ob = __shfl_sync(0xffffffffu, e.y, o);
-        rank += (ok > e.x || (ok == e.x && ob < e.y)) ? 1 : 0;
-      }
-      const bool take = src >= 0 && rank < krem;
-      if (take) {
-        atomicAdd(&taken_cnt[src], 1);
-        if (src == crank) {
-          own_taken[atomicAdd(&own_taken_n, 1)] = (int)e.y;
-          atomicAdd(&warp_taken[((int)e.y - lo) / (32 * n_iter)], 1);
-        }
-      }
-    }
-    __syncthreads();
-  }
-  // blocks kept before this warp (cluster-wide, in block order), and ties taken before it
-  int keep_base = 0, eq_base = 0;
-  for (int r = 0; r < crank; ++r) {
-    const int taken = tie_mode ? max(0, min(cnts[r][1], krem - eq_base)) : (list_mode ? taken_cnt[r] : 0);
-    keep_base += cnts[r][0] + taken;
-    eq_base += cnts[r][1];
-  }
-  for (int w2 = 0; w2 < warp; ++w2) {
-    const int taken = tie_mode ? max(0, min(warp_cnt[w2][1], krem - eq_base)) : (list_mode ? warp_taken[w2] : 0);
-    keep_base += warp_cnt[w2][0] + taken;
-    eq_base += warp_cnt[w2][1];
-  }
-  int pos = keep_base, eq_run = eq_base;
-  for (int j = 0; j < n_iter; ++j) {
-    const int b = wbase + j * 32 + lane;
-    const int cl = classify(b);
-    bool kp = cl == 1;
-    const unsigned eqm = __ballot_sync(0xffffffffu, cl == 2);
-    if (cl == 2) kp = eq_run + __popc(eqm & ((1u << lane) - 1)) < krem;
-    eq_run += __popc(eqm);
-    if (cl == 3)
-      for (int i = 0; i < own_taken_n; ++i) kp |= own_taken[i] == b;
-    const unsigned km = __ballot_sync(0xffffffffu, kp);
-    const int slot = pos + __popc(km & ((1u << lane) - 1));
-    if (kp && slot < budget) kept_row[slot] = b;  // never past the row, whatever the keys hold
-    pos += __popc(km);
-  }
+  sel_radix_compact(cluster, S, key, lo, hi, cand_lo, cand_hi, top_k, budget, kept_row);
 }
 
 template <int G>
 cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, int rpt, int max_blk, int32_t* kept,
                           float* group_scores, const float* gs_in, cudaStream_t st, int part_heads = -1) {
   if (part_heads < 0) part_heads = c.p.h_q;  // score rows per session in the tile partials
-  int C = (max_blk + 4095) / 4096;
-  C = C < 1 ? 1 : (C > 8 ? 8 : C);
+  // slices of about kSelSlice blocks, as many CTAs as one per SM allows across the call's (session, KV head)
+  // units, at most kMaxCluster per unit
+  const int units = n_sessions * c.p.h_kv;
+  int C = std::min((max_blk + kSelSlice - 1) / kSelSlice, std::max(1, (c.num_sms > 0 ? c.num_sms : 1) / units));
+  C = C < 1 ? 1 : (C > kMaxCluster ? kMaxCluster : C);
   if (gs_in == nullptr && (max_blk + rpt - 1) / rpt > 32 * kSelTilesPerLane) return cudaErrorInvalidValue;
   const int slice_cap = ((max_blk + C - 1) / C + 3) & ~3;  // as the kernel's slices: multiples of 4 blocks
   const int tiles_cap = slice_cap / rpt + 2;
@@ -633,7 +739,8 @@ cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, in
   const size_t fixed = (size_t)slice_cap * 4 + (size_t)tiles_cap * G * 4 + fa.sharedSizeBytes;
   if (fixed + (gs_in ? 0 : (size_t)256 * G * 4) > (size_t)optin) return cudaErrorInvalidValue;
   // the exponentials' staging chunk: as many blocks as the remaining shared memory holds, up to kSelChunk
-  const int chunk = gs_in ? 0 : (int)std::min<size_t>(kSelChunk, ((size_t)optin - fixed) / (G * 4)) & ~3;
+  const int chunk =
+      gs_in ? 0 : (int)std::min<size_t>(std::min(kSelChunk, slice_cap), ((size_t)optin - fixed) / (G * 4)) & ~3;
   const size_t smem_b = fixed - fa.sharedSizeBytes + (size_t)chunk * G * 4;
   if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
   return launch_pdl(kb, dim3(C, c.p.h_kv, n_sessions), dim3(kSelectThreads), smem_b, st, C, (const float*)c.e_buf,
