@@ -322,6 +322,19 @@ def run_kvm(args, w):
     view_len = torch.empty((S, w.h_kv), dtype=torch.int32, device=dev)
     torch.cuda.synchronize()
     assert K.kvm_device_status(ctx) == 0
+    # the full history index build of one layer (setup work, timed on its own): the same call again, which
+    # rewrites layer 0's index with the same values
+    build_ms = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        K.kvm_index_append(ctx, kp[0], n_pages, bt, [0] * S, [n_hist] * S, index[0], stream=stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        build_ms.append(e0.elapsed_time(e1))
+    assert K.kvm_device_status(ctx) == 0
+    build_us = float(np.median(build_ms)) * 1e3
+    build_bytes = S * n_hist * w.h_kv * w.d * 2 + S * w.h_kv * (-(-n_hist // BLOCK)) * w.d * 4
     n_tok = [w.n_tok] * S
     # [append,] score + select (recent-only: one kernel), the fused view kernel
     launches_per_layer = (1 if w.append_tok else 0) + (1 if args.selection == "recent" else 2) + 1
@@ -576,6 +589,11 @@ def run_kvm(args, w):
             "gpu_launches": launches_per_layer * L * args.steps * (2 if stage_graphs else 1),
             "clocks": sampler.summary(),
             "per_config": per_config,
+            "index_build": {"us_per_layer": round(build_us, 1), "tokens": S * n_hist, "bytes": build_bytes,
+                            "gbps": round(build_bytes / (build_us * 1e-6) / 1e9, 1),
+                            "frac_of_measured": round(build_bytes / (build_us * 1e-6) / 1e9 / peak, 4),
+                            "note": "kvm_index_append over the whole history of one layer (keys read once, "
+                                    "index written once), timed apart from the step"},
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -615,17 +615,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY, l_run = 0.f;      // head gq, log2 domain; l is this thread's partial sum
     int seg = -1, last_written = seg_first - 1;
 
+    // At the end of each of the CTA's segments (every one in [seg_first, seg_last], in order, neutral where a
+    // warp had no block of it) the two attention warps meet: warp 1 leaves its state in shared memory, warp 0
+    // combines it with its own (log-sum-exp, warp 0 first) and writes the CTA record of the segment.  Both warps
+    // make the same sequence of calls on every path, aborted ones included, so the named barriers pair up.
+    static_assert(kAttn == 2, "the segment records combine exactly two attention warps");
+    __shared__ float2 xs_ml[32];
+    __shared__ float2 xs_o[Q::NO][32];
     auto write_record = [&](int sq, bool neutral) {
       float l = neutral ? 0.f : l_run;
       l += __shfl_xor_sync(0xffffffffu, l, 1);
       l += __shfl_xor_sync(0xffffffffu, l, 2);
-      if (gq >= G) return;
-      float* rec = vp.rec + (((int64_t)(c + sq) * (kAttn + 1) + aw) * G + gq) * kRecFloats<D>;
-      if (tq == 0) *reinterpret_cast<float2*>(rec) = make_float2(neutral ? -INFINITY : m_run, l);
+      const float m = neutral ? -INFINITY : m_run;
+      if (aw == 1) {
+        xs_ml[lane] = make_float2(m, l);
 #pragma unroll
-      for (int n = 0; n < Q::NO; ++n)
-        *reinterpret_cast<float2*>(rec + 4 + 8 * n + 2 * tq) =
-            neutral ? make_float2(0.f, 0.f) : make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+        for (int n = 0; n < Q::NO; ++n)
+          xs_o[n][lane] = neutral ? make_float2(0.f, 0.f) : make_float2(o[n][0] + o[n][2], o[n][1] + o[n][3]);
+      }
+      named_sync(1, 2 * 32);  // warp 1's state is in shared memory
+      if (aw == 0 && gq < G) {
+        const float2 ml1 = xs_ml[lane];
+        const float M = fmaxf(m, ml1.x);
+        float lv = 0.f, sc0 = 0.f, sc1 = 0.f;
+        if (M != -INFINITY) {
+          sc0 = m == -INFINITY ? 0.f : exp2f(m - M);
+          sc1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - M);
+          lv = fmaf(l, sc0, lv);
+          lv = fmaf(ml1.y, sc1, lv);
+        }
+        float* rec = vp.rec + (((int64_t)(c + sq) * (kAttn + 1) + kAttn) * G + gq) * kRecFloats<D>;
+        if (tq == 0) *reinterpret_cast<float2*>(rec) = make_float2(M, lv);
+#pragma unroll
+        for (int n = 0; n < Q::NO; ++n) {
+          const float2 b = xs_o[n][lane];
+          float2 r = make_float2(0.f, 0.f);
+          if (M != -INFINITY) {
+            const float ax = neutral ? 0.f : o[n][0] + o[n][2], ay = neutral ? 0.f : o[n][1] + o[n][3];
+            r.x = fmaf(ax, sc0, r.x);
+            r.x = fmaf(b.x, sc1, r.x);
+            r.y = fmaf(ay, sc0, r.y);
+            r.y = fmaf(b.y, sc1, r.y);
+          }
+          *reinterpret_cast<float2*>(rec + 4 + 8 * n + 2 * tq) = r;
+        }
+      }
+      named_sync(1, 2 * 32);  // warp 0 has read the buffer
     };
     auto neutral_upto = [&](int sq_end) {  // neutral records for segments (last_written, sq_end)
       for (int sq = last_written + 1; sq < sq_end; ++sq) write_record(sq, true);
@@ -775,13 +810,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
       }
-      if (!aborted) {
-        if (seg >= 0) {
-          write_record(seg, false);
-          last_written = seg;
-        }
-        neutral_upto(seg_last + 1);
+      // every path closes the remaining segments, so that both warps meet at the same barriers (after an
+      // abort the records are not used: the CTA leaves before counting itself in)
+      if (seg >= 0) {
+        write_record(seg, false);
+        last_written = seg;
       }
+      neutral_upto(seg_last + 1);
     }
   }
 
@@ -802,10 +837,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!kAttend) return;
 
   // ------------------------------------------------------------ merge
-  // Records: per (CTA c, segment sq) a group of kAttn + 1 slots at ((c + sq) * (kAttn + 1)) * G;
-  // slot w < kAttn holds attention warp w's partial state, slot kAttn the CTA's merged state.
-  // 1. the CTA folds its attention warps' records of each of its segments into its CTA record (one round of
-  //    independent loads per thread: thread i owns head i / (D/4), dims 4 * (i % (D/4)) .. + 3)
+  // Records: per (CTA c, segment sq) a group of kAttn + 1 slots at ((c + sq) * (kAttn + 1)) * G; slot kAttn
+  // holds the CTA's state of the segment, written by attention warp 0 at the segment's end (thread i of a merge
+  // owns head i / (D/4), dims 4 * (i % (D/4)) .. + 3).
   constexpr int kSlots = kAttn + 1;
   constexpr int Q4 = D / 4;
   const bool all_live = vp.total >= vp.P;  // then no CTA share is empty
@@ -813,40 +847,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto rec_at = [&](int cc, int sq, int slot, int h) {
     return vp.rec + ((((int64_t)(cc + sq) * kSlots + slot) * G) + h) * kRecFloats<D>;
   };
-  for (int item = tid; item < (seg_last - seg_first + 1) * G * Q4; item += kThreads) {
-    const int sq = seg_first + item / (G * Q4), h = (item / Q4) % G, d4 = item % Q4;
-    float2 ml[kAttn];
-    float4 ov[kAttn];
-#pragma unroll
-    for (int w = 0; w < kAttn; ++w) {
-      const float* r = rec_at(c, sq, w, h);
-      ml[w] = __ldcg(reinterpret_cast<const float2*>(r));
-      ov[w] = __ldcg(reinterpret_cast<const float4*>(r + 4) + d4);
-    }
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kAttn; ++w) M = fmaxf(M, ml[w].x);
-    float lv = 0.f;
-    float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < kAttn; ++w) {
-        const float sc = ml[w].x == -INFINITY ? 0.f : exp2f(ml[w].x - M);
-        lv = fmaf(ml[w].y, sc, lv);
-        av.x = fmaf(ov[w].x, sc, av.x);
-        av.y = fmaf(ov[w].y, sc, av.y);
-        av.z = fmaf(ov[w].z, sc, av.z);
-        av.w = fmaf(ov[w].w, sc, av.w);
-      }
-    }
-    float* r = rec_at(c, sq, kAttn, h);
-    if (d4 == 0) *reinterpret_cast<float2*>(r) = make_float2(M, lv);
-    reinterpret_cast<float4*>(r + 4)[d4] = av;
-  }
-  __threadfence();
-  __syncthreads();
-  // 2. count this CTA in on each of its segments (one atomic per segment, in parallel); the CTA that
-  //    completes a segment merges it
+  // count this CTA in on each of its segments (one atomic per segment, in parallel; acquire-release, so the
+  // records written before the barrier above are published with it, and the CTA that completes a segment
+  // sees every other CTA's record); that CTA merges the segment
   __shared__ int s_last[64];
   for (int sq0 = seg_first; sq0 <= seg_last; sq0 += 64) {
     const int n_here = min(64, seg_last - sq0 + 1);
@@ -861,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         n_cov = c1 - c0 + 1;
       else
         for (int cc = c0; cc <= c1; ++cc) n_cov += live_cta(cc);
-      const uint32_t prev = atomicAdd(&vp.seg_count[sq], 1u);
+      const uint32_t prev = atom_add_acq_rel_gpu(&vp.seg_count[sq], 1u);
       s_last[tid] = prev + 1 == n_cov;
       if (prev + 1 == n_cov) vp.seg_count[sq] = 0;  // every CTA of the segment has counted: ready for the next call
     }
@@ -869,7 +872,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 3. merge of the CTA records of each completed segment, up to 24 CTAs per round of independent loads
     for (int k = 0; k < n_here; ++k) {
       if (!s_last[k]) continue;
-      __threadfence();
       const int sq = sq0 + k;
       const int s = sq / vp.h_kv, g = sq % vp.h_kv;
       const int nk = a.n_keep[s];
