@@ -236,12 +236,15 @@ kvm_status kvm_materialize_attn(kvm_ctx* ctx, const uint16_t* k_pool, const uint
  * -- the rotated query and the probabilities -- is split into a bf16 part
  * and its bf16 residual); accumulation is fp32.
  *   q          [n_sessions][n_q][h_q][d] bf16, post-q-norm, pre-RoPE
- *   k_view, v_view, view_len as written by kvm_materialize
+ *   k_view, v_view, view_len as written by kvm_materialize ([n_sessions][h_kv]
+ *              [32*budget][d] bf16, read in place in 64-token tiles; slots
+ *              at or past view_len may hold anything: they never contribute)
  *   out        [n_sessions][n_q][h_q][d] fp32 (16-byte aligned)
- * Needs a context created with max_queries > 1 (it owns the packed operand
- * scratch) and 1 <= n_q <= max_queries, n_q <= 32*budget (KVM_ERR_SHAPE
- * otherwise).  A view_len outside [n_q, 32*budget] sets KVM_DEV_BAD_VIEW;
- * that head's outputs are then undefined.
+ * Needs a context created with max_queries > 1 (it owns the packed query
+ * rows and the partial-state scratch) and 1 <= n_q <= max_queries,
+ * n_q <= 32*budget (KVM_ERR_SHAPE otherwise).  A view_len outside
+ * [n_q, 32*budget] sets KVM_DEV_BAD_VIEW; that head's outputs are then
+ * undefined.
  */
 kvm_status kvm_step_attn(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const uint16_t* k_view,
                          const uint16_t* v_view, const int32_t* view_len, int32_t n_sessions, float* out,

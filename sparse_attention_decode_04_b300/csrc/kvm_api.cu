@@ -205,31 +205,26 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
     c.step_blk_cap_pad = (p->max_blocks + 255) / 256 * 256;
     c.step_rows_cap_pad = (int)(((int64_t)p->max_queries * c.group + 255) / 256 * 256);
     const size_t SG = S * p->h_kv;
-    c.attn_l_pad = ((int64_t)kvm::kBlock * c.budget + 63) / 64 * 64;
     c.attn_units_cap = 8 * c.num_sms;
-    const size_t sz[10] = {SG * c.step_blk_cap_pad * p->d * 2,
+    const size_t sz[8] = {SG * c.step_blk_cap_pad * p->d * 2,
                           SG * c.step_rows_cap_pad * p->d * 2,
                           SG * kvm::kStepMaxRanges * c.step_rows_cap_pad * sizeof(float2),
                           SG * c.step_rows_cap_pad * sizeof(float2),
                           SG * p->max_blocks * sizeof(float),
                           2 * SG * c.step_rows_cap_pad * p->d * 2,
-                          SG * c.attn_l_pad * p->d * 2,
-                          SG * c.attn_l_pad * p->d * 2,
                           (size_t)c.attn_units_cap * 128 * (p->d + 2) * sizeof(float),
                           (size_t)c.attn_units_cap * sizeof(uint32_t)};
-    void* q5[10] = {};
-    for (int i = 0; i < 10 && e == cudaSuccess; ++i) e = cudaMalloc(&q5[i], sz[i]);
+    void* q5[8] = {};
+    for (int i = 0; i < 8 && e == cudaSuccess; ++i) e = cudaMalloc(&q5[i], sz[i]);
     c.step_kpk = (uint16_t*)q5[0];
     c.step_qpk = (uint16_t*)q5[1];
     c.step_part = (float2*)q5[2];
     c.step_stats = (float2*)q5[3];
     c.step_gs = (float*)q5[4];
     c.attn_q = (uint16_t*)q5[5];
-    c.attn_kpk = (uint16_t*)q5[6];
-    c.attn_vtpk = (uint16_t*)q5[7];
-    c.attn_part = (float*)q5[8];
-    c.attn_cnt = (uint32_t*)q5[9];
-    if (e == cudaSuccess) e = cudaMemset(c.attn_cnt, 0, sz[9]);
+    c.attn_part = (float*)q5[6];
+    c.attn_cnt = (uint32_t*)q5[7];
+    if (e == cudaSuccess) e = cudaMemset(c.attn_cnt, 0, sz[7]);
     for (size_t b : sz) c.bytes += b;
     if (e != cudaSuccess) {
       kvm_destroy(ctx);
@@ -256,9 +251,9 @@ kvm_status kvm_destroy(kvm_ctx* ctx) {
   cudaGetDevice(&prev);
   if (prev != c.device) cudaSetDevice(c.device);
   cudaError_t e = cudaDeviceSynchronize();
-  void* ptrs[19] = {c.e_buf,      c.part,       c.rec,      c.rope_base, c.rope_off,   c.status,  c.rope_base_lo,
-                    c.rope_off_lo, c.step_kpk,   c.step_qpk, c.step_part, c.step_stats, c.step_gs, c.seg_count,
-                    c.attn_q,      c.attn_kpk,   c.attn_vtpk, c.attn_part, c.attn_cnt};
+  void* ptrs[17] = {c.e_buf,       c.part,     c.rec,       c.rope_base,  c.rope_off, c.status,
+                    c.rope_base_lo, c.rope_off_lo, c.step_kpk, c.step_qpk, c.step_part, c.step_stats,
+                    c.step_gs,      c.seg_count, c.attn_q,   c.attn_part, c.attn_cnt};
   for (void* q : ptrs)
     if (q) cudaFree(q);
   if (prev >= 0 && prev != c.device) cudaSetDevice(prev);
@@ -526,7 +521,7 @@ kvm_status kvm_step_attn(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const uin
     return fail(KVM_ERR_INVALID_ARG, "kvm_step_attn: NULL pointer argument");
   if (n_q < 1 || n_q > c.p.max_queries)
     return fail(KVM_ERR_SHAPE, "n_q=%d outside [1, max_queries=%d]", n_q, c.p.max_queries);
-  if (!c.attn_kpk) return fail(KVM_ERR_SHAPE, "kvm_step_attn needs a context created with max_queries > 1");
+  if (!c.attn_q) return fail(KVM_ERR_SHAPE, "kvm_step_attn needs a context created with max_queries > 1");
   if ((int64_t)n_q > (int64_t)kvm::kBlock * c.budget)
     return fail(KVM_ERR_SHAPE, "n_q=%d exceeds the view capacity %d", n_q, kvm::kBlock * c.budget);
   if (!aligned(q, 16) || !aligned(k_view, 16) || !aligned(v_view, 16) || !aligned(out, 16) || !aligned(view_len, 4))

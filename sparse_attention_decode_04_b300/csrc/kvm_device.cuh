@@ -233,6 +233,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int x, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
 }
+// 4-D tile load global -> shared, completing on `bar` (x0 innermost).
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* map, int x0, int x1, int x2, int x3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x0), "r"(x1), "r"(x2), "r"(x3), "r"(smem_addr(bar))
+      : "memory");
+}
 // 2-D tile store shared -> global (bulk group of the issuing thread).
 __device__ __forceinline__ void tma_store_2d(const void* map, int x, int y, const void* src) {
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(

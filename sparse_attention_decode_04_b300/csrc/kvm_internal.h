@@ -2,6 +2,7 @@
 // files: the context object and the per-step launch functions.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,10 +60,7 @@ struct Ctx {
   float2* step_stats = nullptr;  // row (max + log2 sum, 1/sum) [S*h_kv][rows]
   float* step_gs = nullptr;      // group scores when the caller does not ask for them [S][h_kv][max_blocks]
   // step attention over the view (multi-query), allocated when max_queries > 1
-  int64_t attn_l_pad = 0;         // 32 * budget rounded up to 64 (view tokens per packed head)
   uint16_t* attn_q = nullptr;     // rotated, scaled query rows, bf16 part then residual: [2][S*h_kv][rows][d]
-  uint16_t* attn_kpk = nullptr;   // view keys, core-matrix order [S*h_kv][attn_l_pad][d]
-  uint16_t* attn_vtpk = nullptr;  // view values transposed per 64-token tile [S*h_kv][attn_l_pad / 64][d][64]
   int attn_units_cap = 0;         // (row tile, view chunk) units a split step-attention call may use
   float* attn_part = nullptr;     // per unit: unnormalised O [128][d], then (max, sum) [128][2]
   uint32_t* attn_cnt = nullptr;   // per (KV head, row tile): chunks done (0 between calls)
@@ -114,6 +112,8 @@ cudaError_t launch_view(const Ctx& c, int mode, const uint16_t* k_src, const uin
                         cudaStream_t st, const float* k_scale = nullptr, const float* v_scale = nullptr);
 
 cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st);
+// kvm_view.cu: a 4-D tensor map whose 64-row boxes are the tensor cores' no-swizzle core-matrix layout
+cudaError_t make_core_matrix_map(CUtensorMap* m, const void* base, uint64_t rows, int d);
 
 // Sets the message kvm_last_error() returns on this thread (kvm_api.cu).
 void set_last_error(const char* msg);

@@ -9,15 +9,19 @@
 // head g the R = T*G query rows (row r = t*G + hh) form a dense
 // R x L x d contraction twice (scores, then P.V):
 //   pack    queries rotated at p_t and scaled by log2(e)/sqrt(d), split into a
-//           bf16 part and its bf16 residual; K and V^T of the view re-laid out
-//           in the no-swizzle K-major core-matrix layout (8 rows x 16 bytes per
-//           core matrix), so every operand tile is one contiguous bulk copy;
+//           bf16 part and its bf16 residual, in the no-swizzle K-major
+//           core-matrix layout (8 rows x 16 bytes per core matrix);
+//   K, V    64-token tiles come straight from the view through 4-D tensor-map
+//           boxes that land in the same core-matrix layout: a K tile is the
+//           K-major B operand of the scores, a V tile the MN-major B operand
+//           of P.V (no transposed copy); in the last tile the rows past the
+//           view length are zeroed in shared memory before P.V reads them;
 //   attend  per 128 query rows, over 64-token tiles of the view:
 //             S  = Q_hi K^T + Q_lo K^T          (one fp32 TMEM accumulator)
 //             P  = exp2(S - m) per row          (online softmax in registers)
 //             O += P_hi V + P_lo V              (fp32 TMEM accumulator)
 //           with the split operands giving fp32-accurate products on bf16 MMAs.
-// Warp roles: warp 0 issues the bulk copies, warp 1 owns TMEM and issues the
+// Warp roles: warp 0 issues the copies, warp 1 owns TMEM and issues the
 // MMAs (S of the next tile is issued before P.V of this one, into a second S
 // buffer), warps 2..9 run the softmax in two streams (even and odd tiles), each
 // thread owning one query row of its stream (a warp can only read its quarter
@@ -84,53 +88,12 @@ __global__ void step_pack_q_kernel(const uint16_t* __restrict__ q, const int32_t
   dl[cm_index(row, i + D / 2, D)] = (uint16_t)(l >> 16);
 }
 
-// One 64-token tile of the view of KV head (s, g): K packed [tokens][D], V^T packed [D][tokens]; tokens past
-// the view length are zero (their probabilities are zero, and zero values keep P.V finite).
-template <int D>
-__global__ void __launch_bounds__(256) step_pack_kv_kernel(const uint16_t* __restrict__ k_view,
-                                                           const uint16_t* __restrict__ v_view,
-                                                           const int32_t* __restrict__ view_len, int n_q, int Lcap,
-                                                           int64_t l_pad, uint16_t* __restrict__ k_pk,
-                                                           uint16_t* __restrict__ vt_pk) {
-  griddep_wait();
-  __shared__ __align__(16) uint16_t vs[kTile][D];
-  const int sg = blockIdx.y, tile = blockIdx.x;
-  const int L = clamp_view_len(view_len[sg], n_q, Lcap);
-  const int tok0 = tile * kTile;
-  if (tok0 >= L) return;  // never read by the attention kernel
-  const uint16_t* ksrc = k_view + (int64_t)sg * Lcap * D;
-  const uint16_t* vsrc = v_view + (int64_t)sg * Lcap * D;
-  uint16_t* kdst = k_pk + ((int64_t)sg * l_pad + tok0) * D;
-  uint16_t* vdst = vt_pk + ((int64_t)sg * (l_pad / kTile) + tile) * kTile * D;
-  // 16-byte chunks in packed order (8 token rows of one core matrix are consecutive), so the writes are contiguous
-  for (int c = threadIdx.x; c < kTile * (D / 8); c += blockDim.x) {
-    const int rr = c & 7, c8 = (c >> 3) % (D / 8), r = (c / D) * 8 + rr;
-    const int tok = tok0 + r;
-    uint4 kw = make_uint4(0, 0, 0, 0), vw = make_uint4(0, 0, 0, 0);
-    if (tok < L) {
-      kw = __ldg(reinterpret_cast<const uint4*>(ksrc + (int64_t)tok * D + 8 * c8));
-      vw = __ldg(reinterpret_cast<const uint4*>(vsrc + (int64_t)tok * D + 8 * c8));
-    }
-    *reinterpret_cast<uint4*>(kdst + (int64_t)c * 8) = kw;
-    *reinterpret_cast<uint4*>(&vs[r][8 * c8]) = vw;
-  }
-  __syncthreads();
-  for (int c = threadIdx.x; c < D * (kTile / 8); c += blockDim.x) {  // 16-byte chunks (dim, 8 tokens), dim fastest
-    const int dd = c % D, t8 = c / D;
-    uint32_t w[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-      w[u] = (uint32_t)vs[8 * t8 + 2 * u][dd] | ((uint32_t)vs[8 * t8 + 2 * u + 1][dd] << 16);
-    *reinterpret_cast<uint4*>(vdst + cm_index(dd, 8 * t8, kTile)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 constexpr int kStages = 4;  // K tile stages and V tile stages in shared memory
 constexpr int kSP = 4;      // S/P buffers in TMEM: two per stream
 
 struct AttnBars {
   uint64_t q_full, k_full[kStages], k_empty[kStages], v_full[kStages], v_empty[kStages];
-  uint64_t s_full[kSP], p_full[kSP], pv_done[kSP], drain;
+  uint64_t s_full[kSP], p_full[kSP], pv_done[kSP], drain, v_tail;
   uint64_t xch[4];  // per lane quarter: both softmax warps have published their row state
 };
 
@@ -174,18 +137,21 @@ static_assert(attn_smem_bytes<128>() + 3 * 1024 <= 227 * 1024, "step attention: 
 // needs a step the waiter has not taken).
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
-    const uint16_t* __restrict__ q_hi, const uint16_t* __restrict__ q_lo, const uint16_t* __restrict__ k_pk,
-    const uint16_t* __restrict__ vt_pk, const int32_t* __restrict__ view_len, int n_q, int rows_pad, int Lcap,
-    int64_t l_pad, int h_kv, int h_q, int kv_chunk, float* __restrict__ part, uint32_t* __restrict__ cnt,
-    float* __restrict__ out, uint32_t* __restrict__ status) {
+    const uint16_t* __restrict__ q_hi, const uint16_t* __restrict__ q_lo, const __grid_constant__ CUtensorMap tm_k,
+    const __grid_constant__ CUtensorMap tm_v, const int32_t* __restrict__ view_len, int n_q, int rows_pad, int Lcap,
+    int h_kv, int h_q, int kv_chunk, float* __restrict__ part, uint32_t* __restrict__ cnt, float* __restrict__ out,
+    uint32_t* __restrict__ status) {
   constexpr uint32_t Q_BYTES = kRows * D * 2, KV_BYTES = kTile * D * 2;
-  constexpr uint32_t SBO_Q = D / 8 * 128, SBO_V = kTile / 8 * 128, LBO = 128;
-  constexpr uint32_t IDESC_S = idesc_bf16_f32(kRows, kTile), IDESC_O = idesc_bf16_f32(kRows, D);
+  // core matrices: K-major operands (Q, K) step 128 bytes along K and D * 16 bytes across 8-row groups; the
+  // MN-major V tile steps 128 bytes along MN (dims) and D * 16 bytes along K (8-token groups)
+  constexpr uint32_t SBO_Q = D / 8 * 128, LBO = 128, LBO_V = D * 16, SBO_V = 128;
+  constexpr uint32_t IDESC_S = idesc_bf16_f32(kRows, kTile);
+  constexpr uint32_t IDESC_O = idesc_bf16_f32(kRows, D) | (1u << 16);  // B (V) is MN-major
   extern __shared__ __align__(128) unsigned char smem[];  // no-swizzle operands need 16-byte alignment
   unsigned char* qh_s = smem;
   unsigned char* ql_s = qh_s + Q_BYTES;
-  unsigned char* k_s = ql_s + Q_BYTES;            // [kStages] tiles
-  unsigned char* v_s = k_s + kStages * KV_BYTES;  // [kStages] tiles (V^T)
+  unsigned char* v_s = ql_s + Q_BYTES;            // [kStages] V tiles
+  unsigned char* k_s = v_s + kStages * KV_BYTES;  // [kStages] K tiles
   __shared__ AttnBars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
@@ -225,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
     }
     for (int i = 0; i < 4; ++i) mbar_init(&bars.xch[i], 2);
     mbar_init(&bars.drain, 1);
+    mbar_init(&bars.v_tail, 1);
     mbar_fence_init();
   }
   tc_fence_before();
@@ -248,8 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
           break;
         }
         mbar_arrive_expect_tx(&bars.k_full[sk], KV_BYTES);
-        bulk_g2s(k_s + sk * KV_BYTES, k_pk + ((int64_t)sg * l_pad + (int64_t)(kv0 + i) * kTile) * D, KV_BYTES,
-                 &bars.k_full[sk]);
+        tma_load_4d(k_s + sk * KV_BYTES, &tm_k, 0, 0, 0, (sg * Lcap + (kv0 + i) * kTile) / 8, &bars.k_full[sk]);
         nk = i + 1;
       }
       const int jv = i - 2;
@@ -259,9 +225,27 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
           abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(&bars.v_full[sv], KV_BYTES);
-        bulk_g2s(v_s + sv * KV_BYTES, vt_pk + ((int64_t)sg * (l_pad / kTile) + kv0 + jv) * kTile * D, KV_BYTES,
-                 &bars.v_full[sv]);
+        const int tok0 = (kv0 + jv) * kTile, y = (sg * Lcap + tok0) / 8;
+        unsigned char* vt = v_s + sv * KV_BYTES;
+        if (tok0 + kTile <= L) {
+          mbar_arrive_expect_tx(&bars.v_full[sv], KV_BYTES);
+          tma_load_4d(vt, &tm_v, 0, 0, 0, y, &bars.v_full[sv]);
+        } else {
+          // the view's last tile: its rows past the view length (unwritten view slots, possibly not finite) are
+          // zeroed before P.V, whose probabilities there are zero, reads them
+          mbar_arrive_expect_tx(&bars.v_tail, KV_BYTES);
+          tma_load_4d(vt, &tm_v, 0, 0, 0, y, &bars.v_tail);
+          if (!mbar_wait(&bars.v_tail, 0, status)) {
+            abort_flag = 1;
+            break;
+          }
+          for (int r = L - tok0; r < kTile; ++r)
+#pragma unroll 4
+            for (int c8 = 0; c8 < D / 8; ++c8)
+              *reinterpret_cast<uint4*>(vt + ((r >> 3) * (D / 8) + c8) * 128 + (r & 7) * 16) = make_uint4(0, 0, 0, 0);
+          fence_proxy_async_smem();  // visible to the tensor cores
+          mbar_arrive(&bars.v_full[sv]);
+        }
         nv = jv + 1;
       }
     }
@@ -309,8 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
       const uint32_t o = tm_o + (j & 1) * D;   // this tile's stream accumulator
 #pragma unroll
       for (int kk = 0; kk < kTile / 16; ++kk) {
-        mma_bf16_tmem_a(o, p_t + kk * 8, smem_desc(v_a + kk * 256, LBO, SBO_V), IDESC_O, (j >= 2 || kk > 0));
-        mma_bf16_tmem_a(o, p_t + kTile / 2 + kk * 8, smem_desc(v_a + kk * 256, LBO, SBO_V), IDESC_O, 1);
+        // 16 tokens per MMA: two 8-token core-matrix groups along K
+        mma_bf16_tmem_a(o, p_t + kk * 8, smem_desc(v_a + kk * 2 * LBO_V, LBO_V, SBO_V), IDESC_O, (j >= 2 || kk > 0));
+        mma_bf16_tmem_a(o, p_t + kTile / 2 + kk * 8, smem_desc(v_a + kk * 2 * LBO_V, LBO_V, SBO_V), IDESC_O, 1);
       }
       mma_commit(&bars.pv_done[pb]);
       mma_commit(&bars.v_empty[sv]);
@@ -506,7 +491,6 @@ cudaError_t launch_dg(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* 
   const int SG = n_sessions * c.p.h_kv;
   const int rows_pad = (n_q * G + kRows - 1) / kRows * kRows;  // query rows per KV head, padded to the CTA tile
   const int Lcap = 32 * c.budget;
-  const int64_t l_pad = c.attn_l_pad;
   cudaError_t e;
   const int nqp = rows_pad * (D / 2);
   if ((e = launch_pdl(step_pack_q_kernel<D>, dim3((nqp + 255) / 256, SG), dim3(256), 0, st, 1, q, view_len, n_q,
@@ -514,8 +498,10 @@ cudaError_t launch_dg(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* 
                       reinterpret_cast<const float2*>(c.rope_off), (float)(1.4426950408889634 / sqrt((double)D)),
                       c.attn_q, c.attn_q + (int64_t)SG * rows_pad * D, c.status)) != cudaSuccess)
     return e;
-  if ((e = launch_pdl(step_pack_kv_kernel<D>, dim3((unsigned)(l_pad / kTile), SG), dim3(256), 0, st, 1, k_view, v_view,
-                      view_len, n_q, Lcap, l_pad, c.attn_kpk, c.attn_vtpk)) != cudaSuccess)
+  // K and V tiles of every KV head's view, read in place (rows past the last head read as zeros)
+  CUtensorMap tm_k, tm_v;
+  if ((e = make_core_matrix_map(&tm_k, k_view, (uint64_t)SG * Lcap, D)) != cudaSuccess ||
+      (e = make_core_matrix_map(&tm_v, v_view, (uint64_t)SG * Lcap, D)) != cudaSuccess)
     return e;
   const size_t smem = attn_smem_bytes<D>();
   auto ka = step_attn_kernel<D, G>;
@@ -538,9 +524,8 @@ cudaError_t launch_dg(const Ctx& c, const uint16_t* q, int n_q, const uint16_t* 
   }
   const int kv_chunk = (tiles_max + splits - 1) / splits;
   return launch_pdl(ka, dim3(rows_pad / kRows, splits, SG), dim3(kThreads), smem, st, 1, (const uint16_t*)c.attn_q,
-                    (const uint16_t*)(c.attn_q + (int64_t)SG * rows_pad * D), (const uint16_t*)c.attn_kpk,
-                    (const uint16_t*)c.attn_vtpk, view_len, n_q, rows_pad, Lcap, l_pad, c.p.h_kv, c.p.h_q, kv_chunk,
-                    c.attn_part, c.attn_cnt, out, c.status);
+                    (const uint16_t*)(c.attn_q + (int64_t)SG * rows_pad * D), tm_k, tm_v, view_len, n_q, rows_pad,
+                    Lcap, c.p.h_kv, c.p.h_q, kv_chunk, c.attn_part, c.attn_cnt, out, c.status);
 }
 
 template <int D>

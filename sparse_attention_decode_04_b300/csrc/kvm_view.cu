@@ -1087,4 +1087,24 @@ cudaError_t launch_rope_tables(const Ctx& c, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// 4-D map over `rows` rows of d bf16 values whose boxes land in shared memory in the tensor cores' no-swizzle
+// core-matrix order: dims (8 columns, 8 rows, d/8 column groups, rows/8 row groups), strides (2 B, 2d B, 16 B,
+// 16d B), one box = 64 rows = 8 row groups.  Element (r, c) of a box is then at
+// ((r / 8) * (d / 8) + c / 8) * 64 + (r % 8) * 8 + c % 8: 8 x 16-byte core matrices, adjacent along the columns
+// 128 bytes apart and along the rows d * 16 bytes apart.  Rows past `rows` read as zeros.
+cudaError_t make_core_matrix_map(CUtensorMap* m, const void* base, uint64_t rows, int d) {
+  memset(m, 0, sizeof(*m));
+  auto enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  if (rows % 8 != 0 || d % 8 != 0) return cudaErrorInvalidValue;
+  const cuuint64_t dims[4] = {8, 8, (cuuint64_t)d / 8, (cuuint64_t)rows / 8};
+  const cuuint64_t strides[3] = {(cuuint64_t)d * 2, 16, (cuuint64_t)d * 16};
+  const cuuint32_t box[4] = {8, 8, (cuuint32_t)d / 8, 8};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace kvm
