@@ -145,6 +145,9 @@ size_t kvm_scratch_bytes(const kvm_ctx* ctx);
  *   tok_begin    host int64[n_sessions]
  *   n_tok        host int64[n_sessions] (0 = nothing to do for that session)
  *   index        [n_sessions][h_kv][max_blocks][d] fp32, updated in place
+ * With max_queries > 1 the context also keeps a bf16 copy (nearest even) of
+ * the rows it writes, for the multi-query scoring; the copy follows the index
+ * pointer of the latest append (an append to another index starts it over).
  */
 kvm_status kvm_index_append(kvm_ctx* ctx, const uint16_t* k_pool, int64_t n_pages,
                             const int32_t* block_table, int32_t n_sessions,
@@ -171,6 +174,13 @@ kvm_status kvm_index_append(kvm_ctx* ctx, const uint16_t* k_pool, int64_t n_page
  *   kept_ids     [n_sessions][h_kv][budget] int32 out: ascending ids, -1 after n_keep
  *   group_scores [n_sessions][h_kv][max_blocks] fp32 out, or NULL
  *   head_scores  [n_sessions][h_q][max_blocks] fp32 out (raw s, n_q == 1 only), or NULL
+ * n_q > 1 multiplies bf16 operands on the tensor cores: the index rows rounded
+ * to bf16 come from the context's copy when `index` is the one last appended
+ * to through this context and every scored block was written by those
+ * appends; otherwise the call converts `index` itself (and the copy is then
+ * dropped until the next append).  An index changed by other means since its
+ * last kvm_index_append must be appended again (or converted) before an
+ * n_q > 1 call, as the copy would not see the change.
  */
 kvm_status kvm_score_select(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const float* index,
                             const int64_t* n_tok, int32_t n_sessions, int32_t* kept_ids,

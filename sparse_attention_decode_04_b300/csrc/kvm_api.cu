@@ -225,6 +225,7 @@ kvm_status kvm_create(const kvm_params* p, kvm_ctx** out) {
     c.attn_part = (float*)q5[6];
     c.attn_cnt = (uint32_t*)q5[7];
     if (e == cudaSuccess) e = cudaMemset(c.attn_cnt, 0, sz[7]);
+    if (e == cudaSuccess) e = cudaMemset(c.step_kpk, 0, sz[0]);  // rows no append wrote read as zeros
     for (size_t b : sz) c.bytes += b;
     if (e != cudaSuccess) {
       kvm_destroy(ctx);
@@ -290,7 +291,21 @@ kvm_status kvm_index_append(kvm_ctx* ctx, const uint16_t* k_pool, int64_t n_page
   SessionArgs a;
   int max_count = 0;
   if ((s = append_args(c, n_sessions, tok_begin, n_tok, &a, &max_count)) != KVM_OK) return s;
-  cudaError_t e = kvm::launch_index_append(c, k_pool, n_pages, block_table, n_sessions, a, max_count, index,
+  // the bf16 copy (contexts that score many queries at once): it follows one index; an append to another index
+  // restarts it, and a session's copy counts as complete up to the last block of a run of appends from block 0
+  Ctx& cm = ctx->c;
+  uint16_t* shadow = cm.step_kpk;
+  if (shadow) {
+    if (cm.shadow_of != index) {
+      cm.shadow_of = index;
+      for (int64_t& nb : cm.shadow_blocks) nb = 0;
+    }
+    for (int i = 0; i < n_sessions; ++i) {
+      const int64_t b0 = tok_begin[i] / kvm::kBlock, b1 = (tok_begin[i] + n_tok[i] + kvm::kBlock - 1) / kvm::kBlock;
+      if (n_tok[i] > 0 && b0 <= cm.shadow_blocks[i] && b1 > cm.shadow_blocks[i]) cm.shadow_blocks[i] = b1;
+    }
+  }
+  cudaError_t e = kvm::launch_index_append(c, k_pool, n_pages, block_table, n_sessions, a, max_count, index, shadow,
                                            (cudaStream_t)stream);
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_index_append launch");
 }
@@ -311,6 +326,7 @@ kvm_status kvm_index_append_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const floa
   SessionArgs a;
   int max_count = 0;
   if ((s = append_args(c, n_sessions, tok_begin, n_tok, &a, &max_count)) != KVM_OK) return s;
+  if (ctx->c.shadow_of == index) ctx->c.shadow_of = nullptr;  // the bf16 copy does not follow this append
   cudaError_t e = kvm::launch_index_append_q(c, k_pool8, k_scales, n_pages, block_table, n_sessions, a, max_count,
                                              index, (cudaStream_t)stream);
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_index_append_fp8 launch");
@@ -406,8 +422,10 @@ kvm_status kvm_score_select(kvm_ctx* ctx, const uint16_t* q, int32_t n_q, const 
     return fail(KVM_ERR_INVALID_ARG, "q and index must be 16-byte aligned, outputs 4-byte aligned");
   SessionArgs a;
   if ((s = history_args(c, n_tok, n_sessions, &a)) != KVM_OK) return s;
+  const bool converts = n_q > 1 && !kvm::shadow_ready(c, index, n_sessions, a);
   cudaError_t e = kvm::launch_score_select(c, q, n_q, index, n_sessions, a, kept_ids, group_scores, head_scores,
                                            (cudaStream_t)stream);
+  if (converts) ctx->c.shadow_of = nullptr;  // the conversion overwrote the appends' bf16 copy
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_score_select launch");
 }
 

@@ -3,7 +3,10 @@
 // KVMEM reproduction README, "Core equation" (index vector kbar_b per block);
 // Evolve review of KVMem, "Summary" (a position-independent Mean-K index over
 // 32-token blocks).  kbar_b is the mean of the block's pre-RoPE keys,
-// accumulated in fp32.
+// accumulated in fp32.  A context that scores many query tokens at once
+// (max_queries > 1) also gets each written row rounded to bf16 (nearest
+// even) in the tensor cores' core-matrix order, the operand layout of the
+// step scoring, so that scoring need not convert the whole index each call.
 //
 // One warp per (session, KV head, block touched by the append).  Lane l owns
 // d/32 consecutive dimensions; every load instruction reads one contiguous
@@ -26,7 +29,8 @@ __global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_
                                                                    const int32_t* __restrict__ bt,
                                                                    int64_t max_blocks, int h_kv, SessionArgs a,
                                                                    float* __restrict__ index,
-                                                                   uint32_t* __restrict__ status) {
+                                                                   uint16_t* __restrict__ shadow,
+                                                                   int64_t shadow_rows, uint32_t* __restrict__ status) {
   constexpr int PER = D / 32;  // dims per lane
   griddep_wait();
   const int s = blockIdx.z, g = blockIdx.y;
@@ -73,24 +77,38 @@ __global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_
   }
   float* dst = index + (((int64_t)s * h_kv + g) * max_blocks + b) * D + lane * PER;
   const float n = (float)nv;  // 32 for full blocks: the division is then exact
+  float m[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) m[i] = acc[i] / n;
   if constexpr (PER == 4) {
-    *reinterpret_cast<float4*>(dst) = make_float4(acc[0] / n, acc[1] / n, acc[2] / n, acc[3] / n);
+    *reinterpret_cast<float4*>(dst) = make_float4(m[0], m[1], m[2], m[3]);
   } else {
-    *reinterpret_cast<float2*>(dst) = make_float2(acc[0] / n, acc[1] / n);
+    *reinterpret_cast<float2*>(dst) = make_float2(m[0], m[1]);
+  }
+  if (shadow) {
+    // element (b, c) at ((b / 8) * (D / 8) + c / 8) * 64 + (b % 8) * 8 + c % 8 of this head's rows
+    const int c = lane * PER;
+    uint16_t* sdst = shadow + ((int64_t)s * h_kv + g) * shadow_rows * D + ((b >> 3) * (D / 8) + (c >> 3)) * 64 +
+                     (b & 7) * 8 + (c & 7);
+    if constexpr (PER == 4) {
+      *reinterpret_cast<uint2*>(sdst) = make_uint2(pack_bf16x2(m[0], m[1]), pack_bf16x2(m[2], m[3]));
+    } else {
+      *reinterpret_cast<uint32_t*>(sdst) = pack_bf16x2(m[0], m[1]);
+    }
   }
 }
 
 }  // namespace
 
 cudaError_t launch_index_append(const Ctx& c, const uint16_t* k_pool, int64_t n_pages, const int32_t* bt,
-                                int n_sessions, const SessionArgs& a, int max_count, float* index,
+                                int n_sessions, const SessionArgs& a, int max_count, float* index, uint16_t* shadow,
                                 cudaStream_t st) {
   if (max_count <= 0) return cudaSuccess;
   dim3 grid((max_count + kWarps - 1) / kWarps, c.p.h_kv, n_sessions);
   return c.p.d == 128 ? launch_pdl(index_append_kernel<128>, grid, dim3(kWarps * 32), 0, st, 1, k_pool, n_pages, bt,
-                                    c.p.max_blocks, c.p.h_kv, a, index, c.status)
+                                    c.p.max_blocks, c.p.h_kv, a, index, shadow, c.step_blk_cap_pad, c.status)
                        : launch_pdl(index_append_kernel<64>, grid, dim3(kWarps * 32), 0, st, 1, k_pool, n_pages, bt,
-                                    c.p.max_blocks, c.p.h_kv, a, index, c.status);
+                                    c.p.max_blocks, c.p.h_kv, a, index, shadow, c.step_blk_cap_pad, c.status);
 }
 
 }  // namespace kvm

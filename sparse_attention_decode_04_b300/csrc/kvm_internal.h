@@ -54,7 +54,10 @@ struct Ctx {
   // step-level (multi-query) scoring scratch, allocated when max_queries > 1
   int64_t step_blk_cap_pad = 0;  // max_blocks rounded up to 256
   int step_rows_cap_pad = 0;     // max_queries * group rounded up to 256
-  uint16_t* step_kpk = nullptr;  // packed bf16 index [S*h_kv][step_blk_cap_pad][d] (core-matrix order)
+  uint16_t* step_kpk = nullptr;  // packed bf16 index [S*h_kv][step_blk_cap_pad][d] (core-matrix order): the
+                                 // bf16 copy that kvm_index_append keeps of the index it writes
+  const float* shadow_of = nullptr;            // the index the bf16 copy mirrors
+  int64_t shadow_blocks[kMaxSessionsHost] = {};  // per session: leading blocks the copy holds (written by appends)
   uint16_t* step_qpk = nullptr;  // packed bf16 query rows [S*h_kv][step_rows_cap_pad][d]
   float2* step_part = nullptr;   // row (max, sum) per column range [S*h_kv][kStepMaxRanges][rows]
   float2* step_stats = nullptr;  // row (max + log2 sum, 1/sum) [S*h_kv][rows]
@@ -69,8 +72,9 @@ struct Ctx {
 constexpr int kStepMaxRanges = 64;
 
 // kvm_index.cu
+// (shadow: the context's bf16 copy of the index in the step scoring's core-matrix order, or null)
 cudaError_t launch_index_append(const Ctx& c, const uint16_t* k_pool, int64_t n_pages, const int32_t* bt,
-                                int n_sessions, const SessionArgs& a, int max_count, float* index,
+                                int n_sessions, const SessionArgs& a, int max_count, float* index, uint16_t* shadow,
                                 cudaStream_t st);
 
 // kvm_score.cu
@@ -81,6 +85,14 @@ cudaError_t launch_score_select(const Ctx& c, const uint16_t* q, int n_q, const 
 // kvm_score.cu: the selection controls (recent-only; withdrawn head-averaged scoring)
 cudaError_t launch_select_control(const Ctx& c, int control, const uint16_t* q, const float* index, int n_sessions,
                                   const SessionArgs& a, int32_t* kept, float* group_scores, cudaStream_t st);
+
+// The context's bf16 copy of the index holds every block the call scores (appended to this very index).
+inline bool shadow_ready(const Ctx& c, const float* index, int n_sessions, const SessionArgs& a) {
+  if (!c.step_kpk || index != c.shadow_of) return false;
+  for (int s = 0; s < n_sessions; ++s)
+    if (a.n_blk[s] > c.shadow_blocks[s]) return false;
+  return true;
+}
 
 // kvm_step_score.cu: step-level scores of n_q > 1 query tokens (tcgen05) into gs_out [S][h_kv][max_blocks]
 cudaError_t launch_step_scores(const Ctx& c, const uint16_t* q, int n_q, const float* index, int n_sessions,

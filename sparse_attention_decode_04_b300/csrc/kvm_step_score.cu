@@ -394,8 +394,12 @@ cudaError_t launch_step_d(const Ctx& c, const uint16_t* q, int n_q, const float*
   {
     const int64_t groups = (int64_t)(max_blk + 255) / 256 * 32;
     const int64_t n = groups * (D / 8) * 8;
-    pack_index_kernel<D><<<dim3((unsigned)((n + 255) / 256), 1, SG), 256, 0, st>>>(index, c.p.max_blocks, a,
-                                                                                    c.p.h_kv, blk_cap_pad, c.step_kpk);
+    // the bf16 operand: the copy kept by the appends when it holds every scored block, else converted here
+    // (which overwrites the copy: the caller then marks it stale)
+    if (!shadow_ready(c, index, n_sessions, a))
+      pack_index_kernel<D><<<dim3((unsigned)((n + 255) / 256), 1, SG), 256, 0, st>>>(index, c.p.max_blocks, a,
+                                                                                      c.p.h_kv, blk_cap_pad,
+                                                                                      c.step_kpk);
     const int nq = rows_pad / 8 * (D / 8) * 8;
     pack_query_kernel<D><<<dim3((nq + 255) / 256, 1, SG), 256, 0, st>>>(q, n_q, c.p.h_q, c.p.h_kv, G, rows_pad,
                                                                         c.step_qpk);

@@ -103,3 +103,48 @@ def test_step_scores_full_size_256_queries_1m_tokens():
         check_group_scores(gs[0, g], gs64, extra64)
         ids64 = O.select_blocks(gs64, w.n_blk, w.n_sink, w.n_recent, w.top_k)
         check_ids(kept[0, g], ids64, gs64, w, extra64)
+
+
+def test_bf16_copy_of_the_index_and_the_conversion_give_identical_scores():
+    """The appends' bf16 copy of the index (kept for the multi-query scoring) holds exactly the rounding the
+    conversion of the fp32 index gives: scores and ids are bit-identical whichever the call uses.  The copy is
+    used only when it holds every scored block of the index it was appended to."""
+    w = synth.Workload("step_copy", h_q=8, h_kv=2, d=128, n_tok=300 * 32 + 7, n_sink=3, n_recent=5, top_k=40,
+                       rope_theta=1e6, n_planted=4, seed=37, n_q=40, attend=False)
+    li = synth.layer_inputs(w, 0)
+    ctx = K.Context.for_workload(w)
+    kp = dev_u16(li.k_pool)
+    bt = torch.from_numpy(li.block_table).cuda()
+    q = dev_u16(li.q)
+    n = w.n_tok
+
+    def score(index):
+        kept = torch.full((1, w.h_kv, ctx.budget), -7, dtype=torch.int32, device="cuda")
+        gs = torch.zeros((1, w.h_kv, w.n_blk), dtype=torch.float32, device="cuda")
+        K.kvm_score_select(ctx, q, w.n_q, index, [n], kept, gs)
+        torch.cuda.synchronize()
+        assert K.kvm_device_status(ctx) == 0
+        return gs, kept
+
+    index = torch.zeros((1, w.h_kv, w.n_blk, w.d), dtype=torch.float32, device="cuda")
+    K.kvm_index_append(ctx, kp, w.n_pages, bt, [0], [5000], index)          # two ragged appends
+    K.kvm_index_append(ctx, kp, w.n_pages, bt, [5000], [n - 5000], index)
+    gs1, kept1 = score(index)                                                 # from the appends' copy
+    other = torch.zeros_like(index)
+    K.kvm_index_append(ctx, kp, w.n_pages, bt, [0], [0], other)              # the copy now follows `other`
+    gs2, kept2 = score(index)                                                 # converted by the call
+    assert torch.equal(gs1, gs2) and torch.equal(kept1, kept2)
+    # an index whose later rows were written by other means: the copy lacks them, so the call converts
+    index3 = torch.zeros_like(index)
+    K.kvm_index_append(ctx, kp, w.n_pages, bt, [0], [4000], index3)          # blocks 0..124
+    index3[:, :, 125:] = index[:, :, 125:]
+    gs3, kept3 = score(index3)
+    assert torch.equal(gs1, gs3) and torch.equal(kept1, kept3)
+    # and the result matches the oracle
+    ora = oracle_step(w, li, 0, range(w.h_kv))
+    for g in range(w.h_kv):
+        gs_o, tol = ora[g]
+        check_group_scores(gs1[0, g].cpu().numpy(), gs_o, tol)
+        ids = O.select_blocks(gs_o, w.n_blk, w.n_sink, w.n_recent, w.top_k)
+        check_ids(kept1[0, g].cpu().numpy(), ids, gs_o, w, tol)
+    ctx.close()
