@@ -808,8 +808,8 @@ def run_kvm_step(args, w):
                        "l2": "inputs larger than L2 (K/V pool 4 GiB, index 128 MiB, view 256 MiB), no flush",
                        "parallelism": f"replicas x{world}"},
             "stages_us": {k: round(v * 1e3, 2) for k, v in stage_ms.items()},
-            "roofline": {"bound": "tensor", "kernel": "kvm_step_attn (query packing + view packing + tcgen05 "
-                                                      "attention, timed together)",
+            "roofline": {"bound": "tensor", "kernel": "kvm_step_attn (query packing + tcgen05 attention reading "
+                                                      "K and V from the view, timed together)",
                          "achieved": round(achieved, 1), "peak": peak_tf, "peak_kind": peak_kind, "unit": "TFLOP/s",
                          "frac": round(achieved / peak_tf, 4),
                          "traffic": recorded_traffic(w.name, "step_attn_kernel", STEP_ATTN_SOURCES),
