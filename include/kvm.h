@@ -94,6 +94,7 @@ typedef enum {
 #define KVM_DEV_BAD_BLOCK 0x2u   /* kept id outside [0, n_blk) or not above the entry before it (slot skipped) */
 #define KVM_DEV_TIMEOUT 0x4u     /* a pipeline wait exceeded its iteration limit    */
 #define KVM_DEV_BAD_VIEW 0x8u    /* kvm_step_attn: view_len outside [n_q, 32*budget] */
+#define KVM_DEV_DEBUG_CHECK 0x10u /* debug build only: an index check inside a kernel failed */
 
 typedef struct kvm_ctx kvm_ctx; /* opaque */
 
@@ -115,6 +116,11 @@ const char* kvm_status_string(kvm_status s);
 
 /* Message describing the last error returned on this thread (static, thread-local). */
 const char* kvm_last_error(void);
+
+/* 1 in the debug build of the library (libkvm_debug.so: kernels check the indices they compute, before the
+ * accesses that use them, and set KVM_DEV_DEBUG_CHECK in the status word when one is out of range; nothing
+ * traps), 0 in the release build.  Results are identical in both builds. */
+int32_t kvm_debug_checks(void);
 
 /*
  * Creates a context on the current CUDA device: validates `p`, allocates the

@@ -15,13 +15,14 @@ import ctypes
 import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG, "libkvm.so")
+# KVM_LIBRARY=debug selects the debug build (device-side index checks reported through the status word)
+LIB_PATH = os.path.join(PKG, "libkvm_debug.so" if os.environ.get("KVM_LIBRARY") == "debug" else "libkvm.so")
 BLOCK = 32
 
 KVM_OK = 0
 STATUS_NAMES = {0: "KVM_OK", 1: "KVM_ERR_INVALID_ARG", 2: "KVM_ERR_SHAPE", 3: "KVM_ERR_BUDGET", 4: "KVM_ERR_CUDA",
                 5: "KVM_ERR_TIMEOUT", 6: "KVM_ERR_DEVICE"}
-DEV_BAD_PAGE, DEV_BAD_BLOCK, DEV_TIMEOUT, DEV_BAD_VIEW = 0x1, 0x2, 0x4, 0x8
+DEV_BAD_PAGE, DEV_BAD_BLOCK, DEV_TIMEOUT, DEV_BAD_VIEW, DEV_DEBUG_CHECK = 0x1, 0x2, 0x4, 0x8, 0x10
 CONTROL_RECENT_ONLY, CONTROL_WITHDRAWN_AVERAGE = 1, 2
 
 
@@ -283,6 +284,15 @@ def kvm_noalloc_status(clear: bool = True, stream=None) -> int:
     if st not in (0, 5, 6):
         _check(st)
     return int(out.value)
+
+
+def kvm_debug_checks() -> bool:
+    """True for the debug build of the library (device-side index checks)."""
+    L = lib()
+    f = L.kvm_debug_checks
+    f.argtypes = []
+    f.restype = ctypes.c_int32
+    return bool(f())
 
 
 def kvm_set_wait_limit(ctx: Context, wait_ns: int = 2_000_000_000, stall_first_wait: bool = False):

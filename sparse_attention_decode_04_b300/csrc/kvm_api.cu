@@ -120,6 +120,14 @@ cudaError_t kvm::ensure_smem_impl(const void* kernel, int device, size_t bytes) 
 
 extern "C" {
 
+int32_t kvm_debug_checks(void) {
+#ifdef KVM_DEBUG_CHECKS
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 const char* kvm_status_string(kvm_status s) {
   switch (s) {
     case KVM_OK: return "KVM_OK";

@@ -20,6 +20,19 @@ namespace kvm {
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s wall-clock limit for one wait
 constexpr uint32_t kWaitIters = 1u << 26;    // and an iteration cap, whichever comes first
 
+// Index checks of the debug build (compiled with KVM_DEBUG_CHECKS): a computed index outside its buffer sets
+// KVM_DEV_DEBUG_CHECK in the status word (the access itself is guarded where it is made).  No-ops otherwise.
+#ifdef KVM_DEBUG_CHECKS
+#define KVM_DEBUG_CHECK(cond, status)                          \
+  do {                                                         \
+    if (!(cond)) atomicOr((status), (unsigned)KVM_DEV_DEBUG_CHECK); \
+  } while (0)
+#else
+#define KVM_DEBUG_CHECK(cond, status) \
+  do {                                \
+  } while (0)
+#endif
+
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

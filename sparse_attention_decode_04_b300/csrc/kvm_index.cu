@@ -38,6 +38,7 @@ __global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_
   const int64_t bi = (int64_t)blockIdx.x * kWarps + warp;
   if (bi >= a.count[s]) return;
   const int64_t b = a.aux[s] + bi;                         // block id
+  KVM_DEBUG_CHECK(b < max_blocks, status);
   const int64_t present = a.n_tok[s] - b * kBlock;          // tokens of this block present so far
   const int nv = present >= kBlock ? kBlock : (int)present;
   const int32_t page = bt[(int64_t)s * max_blocks + b];

@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   if (r0 >= n_blk) return;
   const int nrows = (int)(rows_per_tile < n_blk - r0 ? (int64_t)rows_per_tile : n_blk - r0);
   const int nstage = (nrows + kStageRows - 1) / kStageRows;
+  KVM_DEBUG_CHECK(r0 + nrows <= max_blocks && r0 + nrows <= e_stride && tile < max_tiles, status);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sub = lane & 7;                 // 8 lanes per row
   const int rsel = warp * 4 + (lane >> 3);  // row within a stage
@@ -343,7 +344,8 @@ __device__ __forceinline__ void sel_init(SelShared& S) {
 // kept blocks (candidates above it, the forced sink / recent blocks, ties resolved toward the lower block) to
 // kept_row in ascending block order.
 __device__ void sel_radix_compact(cg::cluster_group& cluster, SelShared& S, const uint32_t* key, int lo, int hi,
-                                  int cand_lo, int cand_hi, int top_k, int budget, int32_t* kept_row) {
+                                  int cand_lo, int cand_hi, int top_k, int budget, int32_t* kept_row,
+                                  uint32_t* status) {
   constexpr int NT = kSelectThreads, NW = SelShared::NW;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int crank = (int)cluster.block_rank();
@@ -580,6 +582,7 @@ __device__ void sel_radix_compact(cg::cluster_group& cluster, SelShared& S, cons
       }
     }
     if (kp) {
+      KVM_DEBUG_CHECK(pos < budget, status);
       if (pos < budget) kept_row[pos] = b;  // never past the row, whatever the keys hold
       ++pos;
     }
@@ -617,6 +620,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
   const int lo = min(n_blk, crank * sl), hi = min(n_blk, lo + sl);
   const int len = hi - lo;
   const int n_iter = (len + NT - 1) / NT;
+  KVM_DEBUG_CHECK(len <= slice_cap && hi <= max_blocks && (gs_in != nullptr || chunk > 0), status);
   int32_t* kept_row = kept + ((int64_t)s * h_kv + g) * budget;
   const bool select_all = n_blk <= budget;  // uniform across the cluster
   const int cand_lo = n_sink, cand_hi = n_blk - n_recent;  // candidates [cand_lo, cand_hi)
@@ -715,7 +719,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
     cluster_wait();  // completes the start barrier; no distributed shared memory access on this path
     return;
   }
-  sel_radix_compact(cluster, S, key, lo, hi, cand_lo, cand_hi, top_k, budget, kept_row);
+  sel_radix_compact(cluster, S, key, lo, hi, cand_lo, cand_hi, top_k, budget, kept_row, status);
 }
 
 template <int G>

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_attn_kernel(
   const int splits = gridDim.y, kv0 = blockIdx.y * kv_chunk;
   const int nt = min(nt_full - kv0, kv_chunk);
   if (nt <= 0) return;  // past the view: the chunk count of this row tile does not include it
+  KVM_DEBUG_CHECK(row0 < rows_pad && (int64_t)(kv0 + nt) * kTile <= (int64_t)Lcap + kTile, status);
   __shared__ int s_last;
 
   if (warp == 1) {

@@ -260,6 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const Cursor firstc = locate(fa, a, vp.n_sessions), lastc = locate(fb - 1, a, vp.n_sessions);
   const int seg_first = firstc.s * vp.h_kv + firstc.g;
   const int seg_last = lastc.s * vp.h_kv + lastc.g;
+  KVM_DEBUG_CHECK(seg_first <= seg_last && c + seg_last < vp.P + vp.n_sessions * vp.h_kv, vp.status);
   bool aborted = false;
   int64_t issued = 0;  // producer: blocks whose copies were issued
 
@@ -373,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const Cursor cu = locate(fa + jj, a, vp.n_sessions);
         const int q = cu.s * vp.h_kv + cu.g;
         const int64_t ydst = (int64_t)q * Lcap + 32 * cu.i;
+        KVM_DEBUG_CHECK(cu.i < vp.budget && ydst + 32 <= (int64_t)vp.n_sessions * vp.h_kv * Lcap, vp.status);
         const uint32_t vaddr = sbase + st * Q::STAGE + Q::PAGE;
         if (__any_sync(0xffffffffu, !mbar_wait(&full[st], phase, vp.status, vp.wait_ns) ||
                                         (vp.stall && fa + jj == 0 &&

@@ -93,3 +93,14 @@ def test_product_and_oracle_share_no_code():
         if f.endswith(".py"):
             text = open(os.path.join(ROOT, "oracle", f)).read()
             assert "sparse_attention_decode_04_b300" not in text and "libkvm" not in text, f
+
+
+def test_debug_build_exports_the_same_symbols_and_says_so(lib):
+    """libkvm_debug.so (device-side index checks) is the same interface; kvm_debug_checks tells them apart."""
+    path = B.build(debug=True)
+    dbg = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(dbg, n), f"{n} is declared in kvm.h but not exported by the debug build"
+    dbg.kvm_debug_checks.restype = ctypes.c_int32
+    lib.kvm_debug_checks.restype = ctypes.c_int32
+    assert dbg.kvm_debug_checks() == 1 and lib.kvm_debug_checks() == 0
