@@ -579,18 +579,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stage is freed at once (its load refill is then the one thing waiting on it).
         if (lane == 0) {
           bulk_commit();
-          if constexpr (kAttend) {
+          if constexpr (kAttend && !F8) {
             mbar_arrive(&rotated[st]);
             if (prev_st >= 0) {
               bulk_wait_read<1>();
               mbar_arrive(&empty[prev_st]);
             }
           } else {
+            // materialising only, or FP8 pages (8 larger stages, 2 per rotation warp: holding a second one
+            // would leave the loads no stage to run ahead in): the stage is released as soon as its stores
+            // have read it
+            if constexpr (kAttend) mbar_arrive(&rotated[st]);
             bulk_wait_read<0>();
             mbar_arrive(&empty[st]);
           }
         }
-        prev_st = kAttend ? st : -1;
+        prev_st = (kAttend && !F8) ? st : -1;
         __syncwarp();
       }
       if (kAttend && !aborted && prev_st >= 0 && lane == 0) {
