@@ -27,7 +27,9 @@
 namespace kvm {
 namespace {
 
-constexpr int kEpiWarps = 8;    // epilogue: two warps per TMEM lane quarter, each taking half of a tile's columns
+constexpr int kEpiWarps = 16;   // epilogue: four warps per TMEM lane quarter, each taking a quarter of a tile's
+                                // columns (pass 1) or rows (pass 2)
+constexpr int kParts = kEpiWarps / 4;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // producer, MMA issuer, epilogue
 constexpr int kRowsM = 128;     // MMA M
 constexpr int kColsN = 256;     // MMA N
@@ -108,7 +110,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
-  __shared__ float2 half_state[2][kRowsM];  // each column half's (max, sum) per row
+  __shared__ float2 half_state[kParts][kRowsM];  // each column part's (max, sum) per row
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sg = blockIdx.z, s = sg / h_kv;
@@ -173,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
     }
     if (j > 0) mbar_wait(&bars.d_full[(j - 1) & 1], ((j - 1) >> 1) & 1, status);  // last MMAs done
   } else if (warp >= 2) {
-    // epilogue: one query row per thread, half of each tile's columns per warp
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    // epilogue: one query row per thread, a part of each tile's columns per warp
+    const int quarter = warp & 3, half = (warp - 2) >> 2;  // half: the column part
     float m = -INFINITY, z = 0.f;
     for (int j = 0; j < nt; ++j) {
       const int st = j & 1;
@@ -186,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
       const int col0 = (j0 + j) * kColsN;
       const bool full = col0 + kColsN <= n_blk;  // no column past the history in this tile
 #pragma unroll 1
-      for (int cc = half * (kColsN / 64); cc < (half + 1) * (kColsN / 64); ++cc) {
+      for (int cc = half * (kColsN / 32 / kParts); cc < (half + 1) * (kColsN / 32 / kParts); ++cc) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + st * kColsN + cc * 32, v);
         tmem_wait_ld();
@@ -223,13 +225,19 @@ __global__ void __launch_bounds__(kThreads, 1) step_rowstats_kernel(
   }
   tc_fence_before();
   __syncthreads();
-  if (warp >= 2 && warp < 6) {  // the two column halves of each row: (max, sum) combined
+  if (warp >= 2 && warp < 6) {  // the column parts of each row: (max, sum) combined in part order
     const int r = (warp & 3) * 32 + lane, row = row0 + r;
-    const float2 p0 = half_state[0][r], p1 = half_state[1][r];
-    const float M = fmaxf(p0.x, p1.x);
-    const float z = M == -INFINITY ? 0.f
-                                   : (p0.x == -INFINITY ? 0.f : p0.y * fast_exp2(p0.x - M)) +
-                                         (p1.x == -INFINITY ? 0.f : p1.y * fast_exp2(p1.x - M));
+    float M = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kParts; ++k) M = fmaxf(M, half_state[k][r].x);
+    float z = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int k = 0; k < kParts; ++k) {
+        const float2 pk = half_state[k][r];
+        z += pk.x == -INFINITY ? 0.f : pk.y * fast_exp2(pk.x - M);
+      }
+    }
     if (row < rows_pad) part[((int64_t)sg * n_ranges + blockIdx.y) * rows_pad + row] = make_float2(M, z);
   }
   if (warp == 1) {
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
   __shared__ Bars bars;
   __shared__ uint32_t tmem_slot;
   __shared__ volatile int abort_flag;
-  __shared__ float half_acc[2][kRowsM];  // each half's partial group score per block
+  __shared__ float half_acc[kParts][kRowsM];  // each part's partial group score per block
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int sg = blockIdx.z, s = sg / h_kv;
@@ -339,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
     }
     if (j > 0) mbar_wait(&bars.d_full[(j - 1) & 1], ((j - 1) >> 1) & 1, status);
   } else if (warp >= 2) {
-    // one block per thread, half of each tile's query rows per warp
-    const int quarter = warp & 3, half = (warp - 2) >> 2;
+    // one block per thread, a part of each tile's query rows per warp
+    const int quarter = warp & 3, half = (warp - 2) >> 2;  // half: the row part
     float acc = 0.f;
     for (int j = 0; j < nchunk; ++j) {
       const int st = j & 1;
@@ -350,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
       }
       tc_fence_after();
 #pragma unroll 1
-      for (int cc = half * (kColsN / 64); cc < (half + 1) * (kColsN / 64); ++cc) {
+      for (int cc = half * (kColsN / 32 / kParts); cc < (half + 1) * (kColsN / 32 / kParts); ++cc) {
         uint32_t v[32];
         tmem_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + st * kColsN + cc * 32, v);
         tmem_wait_ld();
@@ -369,9 +377,12 @@ __global__ void __launch_bounds__(kThreads, 1) step_colsum_kernel(
   }
   tc_fence_before();
   __syncthreads();
-  if (warp >= 2 && warp < 6) {  // the two halves of the query rows summed
+  if (warp >= 2 && warp < 6) {  // the parts of the query rows summed in part order
     const int r = (warp & 3) * 32 + lane, blk = blk0 + r;
-    if (blk < n_blk) gs_out[(int64_t)sg * max_blocks + blk] = half_acc[0][r] + half_acc[1][r];
+    float g = 0.f;
+#pragma unroll
+    for (int k = 0; k < kParts; ++k) g += half_acc[k][r];
+    if (blk < n_blk) gs_out[(int64_t)sg * max_blocks + blk] = g;
   }
   if (warp == 1) {
     tc_fence_after();
