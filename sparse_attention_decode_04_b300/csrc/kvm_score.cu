@@ -15,8 +15,9 @@
 // Kernel B (select_kernel), grid (C, h_kv, sessions), clusters of C CTAs:
 //   each CTA owns 1/C of the blocks.  From the tiles' partials it forms the
 //   softmax normalisers, Gs[b] = sum_h e[b][h] * exp(m_tile - M_h) / Z_h (the
-//   exponentials are requested before the normalisers are formed, so the two
-//   L2 round trips overlap), and builds the first radix histogram as it goes.
+//   exponentials are loaded into registers before the normalisers are formed,
+//   so the two L2 round trips overlap), and builds the first radix histogram as
+//   it goes.
 //   Exact radix select over the candidates' order keys, 12 + 12 + 8 bits: per
 //   pass one cluster barrier, then a single warp locates the boundary bin over
 //   the merged counts with two rounds of distributed-shared-memory loads (64
@@ -307,7 +308,7 @@ __device__ __forceinline__ SelResult sel_boundary(cg::cluster_group& cluster, in
 }
 
 constexpr int kSelTilesPerLane = 10;  // tile partials a normaliser lane holds: up to 320 tiles per head
-constexpr int kSelChunk = 4096;       // blocks whose exponentials are staged in shared memory at a time (at most)
+constexpr int kSelPre = 2;            // 4-block groups of exponentials a thread loads before the normalisers
 constexpr int kSelList = 32;          // boundary keys resolved by an exchanged list instead of a third pass
 constexpr int kSelSlice = 2048;       // blocks per CTA of the selection cluster (up to kMaxCluster CTAs)
 
@@ -590,25 +591,19 @@ __device__ void sel_radix_compact(cg::cluster_group& cluster, SelShared& S, cons
 }
 
 template <int G>
-__global__ void __launch_bounds__(kSelectThreads) select_kernel(
+__global__ void __launch_bounds__(kSelectThreads, 1) select_kernel(
     const float* __restrict__ e_buf, int64_t e_stride, const float2* __restrict__ part, int64_t max_tiles,
     int64_t max_blocks, int h_kv, int h_q, SessionArgs a, int rows_per_tile, int n_sink, int n_recent, int top_k,
     int budget, int slice_cap, int32_t* __restrict__ kept, float* __restrict__ group_scores,
-    const float* __restrict__ gs_in, uint32_t* __restrict__ status, int chunk) {
+    const float* __restrict__ gs_in, uint32_t* __restrict__ status) {
   constexpr int NT = kSelectThreads;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   uint32_t* key = reinterpret_cast<uint32_t*>(smem_raw);        // [slice_cap]
-  float* e_stage = reinterpret_cast<float*>(key + slice_cap);    // [G][chunk] exponentials of one chunk
-  float* coef = e_stage + (gs_in ? 0 : G * chunk);               // [tiles in slice][G]
-  __shared__ __align__(8) uint64_t e_bar;
+  float* coef = reinterpret_cast<float*>(key + slice_cap);       // [tiles in slice][G]
   __shared__ __align__(16) SelShared S;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   sel_init(S);
-  if (tid == 0) {
-    mbar_init(&e_bar, 1);
-    mbar_fence_init();
-  }
   cluster_arrive_relaxed();  // paired with the wait before the first store into another CTA's shared memory
   griddep_wait();
   cg::cluster_group cluster = cg::this_cluster();
@@ -620,7 +615,7 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
   const int lo = min(n_blk, crank * sl), hi = min(n_blk, lo + sl);
   const int len = hi - lo;
   const int n_iter = (len + NT - 1) / NT;
-  KVM_DEBUG_CHECK(len <= slice_cap && hi <= max_blocks && (gs_in != nullptr || chunk > 0), status);
+  KVM_DEBUG_CHECK(len <= slice_cap && hi <= max_blocks, status);
   int32_t* kept_row = kept + ((int64_t)s * h_kv + g) * budget;
   const bool select_all = n_blk <= budget;  // uniform across the cluster
   const int cand_lo = n_sink, cand_hi = n_blk - n_recent;  // candidates [cand_lo, cand_hi)
@@ -646,23 +641,25 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
       put_key(b < hi, b, b < hi ? src[b] : 0.f);
     }
   } else {
-    // The slice's exponentials (G rows of the head-major scratch) come in by 1-D bulk copies, `chunk` blocks
-    // at a time, while the normalisers are formed; the copies start and end on 16-byte boundaries (slices start
-    // at a multiple of 4 blocks, and the scratch rows are padded to a multiple of 4).
+    // The slice's exponentials (G rows of the head-major scratch, just written by the score kernel and still in
+    // L2) go straight into registers, four blocks per 16-byte load; the first kSelPre groups of each thread are
+    // requested before the normalisers are formed, so their latency hides behind that step.  Slices start at a
+    // multiple of 4 blocks and the scratch rows are padded to a multiple of 4, so every load is aligned and
+    // stays inside its row; lanes past the slice's end are masked when the keys are formed.
     const float* e_src = e_buf + ((int64_t)s * h_kv + g) * G * e_stride + lo;
     const int n_tiles = (n_blk + rows_per_tile - 1) / rows_per_tile;
     const int t0 = lo / rows_per_tile;
     const int nt = hi > lo ? (hi - 1) / rows_per_tile - t0 + 1 : 0;
-    const int n_chunks = (len + chunk - 1) / chunk;
-    auto issue_chunk = [&](int k) {
-      const int c0 = k * chunk, cl = min(chunk, len - c0);
-      const uint32_t bytes = (uint32_t)(((cl + 3) & ~3) * 4);
-      mbar_arrive_expect_tx(&e_bar, bytes * G);
+    const int n_grp = (len + 3) >> 2;
+    KVM_DEBUG_CHECK(lo + 4 * (int64_t)n_grp <= e_stride, status);
+    auto load_group = [&](int q4, float4 (&e4)[G]) {
 #pragma unroll
-      for (int h = 0; h < G; ++h) bulk_g2s(e_stage + h * chunk, e_src + (int64_t)h * e_stride + c0, bytes, &e_bar);
+      for (int h = 0; h < G; ++h) e4[h] = __ldcg(reinterpret_cast<const float4*>(e_src + (int64_t)h * e_stride) + q4);
     };
-    __syncthreads();  // e_bar initialised
-    if (tid == 0 && n_chunks > 0) issue_chunk(0);
+    float4 ev[kSelPre][G];
+#pragma unroll
+    for (int j = 0; j < kSelPre; ++j)
+      if (tid + j * NT < n_grp) load_group(tid + j * NT, ev[j]);
     // softmax normaliser of query head `warp` (< G): M = the largest tile maximum, Z = the tile sums rescaled
     // to M; then the slice's per-tile coefficients exp(m_tile - M) / Z.  Each lane holds its tiles' partials.
     if (warp < G) {
@@ -692,23 +689,31 @@ __global__ void __launch_bounds__(kSelectThreads) select_kernel(
       }
     }
     __syncthreads();  // coefficients ready, hist[0] cleared
-    for (int k = 0; k < n_chunks; ++k) {
-      if (k > 0) {
-        __syncthreads();  // every thread is done with the previous chunk
-        if (tid == 0) issue_chunk(k);
-      }
-      if (!mbar_wait(&e_bar, (uint32_t)(k & 1), status)) {
-        // the copies never landed within the limit (the status word says so); no key of this chunk is valid
-      }
-      const int c0 = k * chunk, cl = min(chunk, len - c0);
-      for (int i = tid; i < cl; i += NT) {
-        const int b = lo + c0 + i;
-        const float* cf = coef + (b / rows_per_tile - t0) * G;
-        float gsv = 0.f;
+    // the four blocks of a group lie in one tile (tiles are multiples of 32 rows, groups start at multiples of 4)
+    auto put_group = [&](int q4, const float4 (&e4)[G]) {
+      const int b0 = lo + 4 * q4;
+      const float* cf = coef + (b0 / rows_per_tile - t0) * G;
+      float g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f;
 #pragma unroll
-        for (int h = 0; h < G; ++h) gsv = fmaf(e_stage[h * chunk + i], cf[h], gsv);
-        put_key(true, b, gsv);
+      for (int h = 0; h < G; ++h) {
+        const float c = cf[h];
+        g0 = fmaf(e4[h].x, c, g0);
+        g1 = fmaf(e4[h].y, c, g1);
+        g2 = fmaf(e4[h].z, c, g2);
+        g3 = fmaf(e4[h].w, c, g3);
       }
+      put_key(b0 < hi, b0, g0);
+      put_key(b0 + 1 < hi, b0 + 1, g1);
+      put_key(b0 + 2 < hi, b0 + 2, g2);
+      put_key(b0 + 3 < hi, b0 + 3, g3);
+    };
+#pragma unroll
+    for (int j = 0; j < kSelPre; ++j)
+      if (tid + j * NT < n_grp) put_group(tid + j * NT, ev[j]);
+    for (int q4 = tid + kSelPre * NT; q4 < n_grp; q4 += NT) {
+      float4 e4[G];
+      load_group(q4, e4);
+      put_group(q4, e4);
     }
   }
 
@@ -740,17 +745,12 @@ cudaError_t launch_select(const Ctx& c, int n_sessions, const SessionArgs& a, in
   if ((e = cudaFuncGetAttributes(&fa, kb)) != cudaSuccess) return e;
   int optin = 0;
   if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device)) != cudaSuccess) return e;
-  const size_t fixed = (size_t)slice_cap * 4 + (size_t)tiles_cap * G * 4 + fa.sharedSizeBytes;
-  if (fixed + (gs_in ? 0 : (size_t)256 * G * 4) > (size_t)optin) return cudaErrorInvalidValue;
-  // the exponentials' staging chunk: as many blocks as the remaining shared memory holds, up to kSelChunk
-  const int chunk =
-      gs_in ? 0 : (int)std::min<size_t>(std::min(kSelChunk, slice_cap), ((size_t)optin - fixed) / (G * 4)) & ~3;
-  const size_t smem_b = fixed - fa.sharedSizeBytes + (size_t)chunk * G * 4;
+  const size_t smem_b = (size_t)slice_cap * 4 + (gs_in ? 0 : (size_t)tiles_cap * G * 4);
+  if (smem_b + fa.sharedSizeBytes > (size_t)optin) return cudaErrorInvalidValue;
   if ((e = ensure_smem(kb, c.device, smem_b)) != cudaSuccess) return e;
   return launch_pdl(kb, dim3(C, c.p.h_kv, n_sessions), dim3(kSelectThreads), smem_b, st, C, (const float*)c.e_buf,
                     c.e_stride, (const float2*)c.part, c.max_tiles, c.p.max_blocks, c.p.h_kv, part_heads, a, rpt,
-                    c.p.n_sink, c.p.n_recent, c.p.top_k, c.budget, slice_cap, kept, group_scores, gs_in, c.status,
-                    chunk);
+                    c.p.n_sink, c.p.n_recent, c.p.top_k, c.budget, slice_cap, kept, group_scores, gs_in, c.status);
 }
 
 // Rows per score tile (a multiple of 32, 32..4096): whole waves of two CTAs per SM, as many waves as keep tiles
