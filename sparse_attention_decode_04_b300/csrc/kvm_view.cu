@@ -36,12 +36,19 @@
 //     online softmax per head in the log2 domain (the running maximum is raised
 //     only when it grows by more than 8) and accumulates P.V with mma.sync, P
 //     split the same way, then frees its share of the stage.
+// FP8 pages (fused mode): eight rotation warps, and the producer fills a ring
+// of code slots instead of the stages (the K and V code pages and the block's
+// base table row, by 1-D bulk copies); the rotation warp that owns the block
+// decodes it into its stage (K rotated, V scaled and rounded to bf16), frees
+// the code slot at once, and the stage goes on as for bf16 pages.  The
+// per-offset cos/sin then come from a shared-memory copy of the table.
 // NS is a multiple of both warp counts, so every rotation and every attention
 // warp owns whole stages and meets their rounds strictly in order: a wait on a
 // stage barrier is never more than one phase ahead, which the parity waits
-// need.  The 7 warps fit two per SM sub-partition, so every warp may hold up
-// to 255 registers; the rotation (about four times the attention's work per
-// block) gets four warps.
+// need.  The 7 warps of the bf16 modes fit two per SM sub-partition, so every
+// warp may hold up to 255 registers; the rotation (about four times the
+// attention's work per block) gets four warps.  FP8 pages: 11 warps, at most
+// three per sub-partition, 168 registers each.
 // No warp reads global memory on the per-block path.  Each attention warp
 // writes one partial record (max, sum, output) per segment (session, KV head)
 // of its CTA's share — a neutral record for a segment it had no block of — in
@@ -67,10 +74,17 @@
 namespace kvm {
 namespace {
 
-constexpr int kRot = 4;                      // rotation warps per CTA (warps 0 .. kRot-1)
-constexpr int kAttn = kViewWarps;            // attention warps per CTA (attention-record slots)
-constexpr int kProducer = kRot + kAttn;      // warp index of the producer
-constexpr int kThreads = (kRot + kAttn + 1) * 32;
+constexpr int kAttn = kViewWarps;  // attention warps per CTA (attention-record slots)
+// Rotation warps per CTA (warps 0 .. rot_warps - 1): four for bf16 pages; eight for FP8 pages, whose decoding
+// doubles the rotation warps' work per block.  The producer is the warp after the attention warps.
+template <bool F8>
+constexpr int rot_warps() {
+  return F8 ? 8 : 4;
+}
+template <bool F8>
+constexpr int view_threads() {
+  return (rot_warps<F8>() + kAttn + 1) * 32;
+}
 
 struct ViewParams {
   const int32_t* bt;
@@ -115,20 +129,31 @@ struct Geo {
   static constexpr uint32_t BOX = 32 * 128;     // bytes of one box (32 rows)
   static constexpr uint32_t PAGE = 32 * D * 2;  // bytes of one K (or V) page in bf16
   static constexpr uint32_t CPAGE = 32 * D;     // bytes of one page of FP8 codes
-  // a stage: the bf16 K and V pages (as loaded, or decoded from FP8), then, FP8 only, the K and V code pages
-  static constexpr uint32_t STAGE = 2 * PAGE + (F8 ? 2 * CPAGE : 0);
+  // a stage: the bf16 K and V pages (as loaded, or decoded from FP8 pages)
+  static constexpr uint32_t STAGE = 2 * PAGE;
   static constexpr int CPR = D / 16;            // rotation items (chunk pairs) per row
   static constexpr int RPP = 32 / CPR;          // rows per rotation pass
   static constexpr int PASSES = CPR;            // rotation passes per page
   static constexpr int KS = D / 16;             // MMA k-steps over the head dimension
   static constexpr int NO = D / 8;              // output n-tiles
-  static constexpr int NS = F8 ? (D == 128 ? 8 : 16) : (D == 128 ? 12 : 24);  // a multiple of kRot and kAttn
+  static constexpr int NS = F8 ? (D == 128 ? 8 : 16) : (D == 128 ? 12 : 24);  // a multiple of both warp counts
   static constexpr uint32_t TAB = D / 2 * 8;     // bytes of one table row ((cos, sin) per pair)
+  // FP8 pages: the loads fill a ring of their own, NC code slots (the K and V code pages, then the block's base
+  // table row), which a rotation warp frees as soon as it has decoded the block into a stage; the stage then
+  // only waits for the view stores and the attention.  bf16 pages: the loads fill the stages (NC = NS).  NC is
+  // a multiple of the rotation warps, so each code slot, like each stage, belongs to one rotation warp.
+  static constexpr int NC = NS;
+  static constexpr uint32_t CSLOT = 2 * CPAGE + TAB;  // bytes of one code slot
+  static constexpr uint32_t OFS = 32 * TAB;           // FP8: the per-offset (cos, sin) table, [32 rows][d/2]
   // shared memory, from the 1024-byte-aligned base
-  static constexpr uint32_t OFF_TAB = NS * STAGE;                 // [NS][hi row | lo row] base table rows
-  static constexpr uint32_t OFF_META = OFF_TAB + NS * 2 * TAB;    // [NS] int: tokens of the staged block
-  static constexpr uint32_t OFF_SCALE = OFF_META + NS * 4;        // [NS] float2: FP8 K and V page scales
-  static constexpr uint32_t BYTES = OFF_SCALE + NS * 8 + 1024;    // + alignment slack
+  static constexpr uint32_t OFF_CODE = NS * STAGE;                        // FP8: [NC] code slots
+  static constexpr uint32_t OFF_OFS = OFF_CODE + (F8 ? NC * CSLOT : 0);   // FP8: offset table (swizzled)
+  static constexpr uint32_t OFF_TAB = OFF_OFS + (F8 ? OFS : 0);           // bf16: [NS][hi | lo] table rows
+  static constexpr uint32_t OFF_META = OFF_TAB + (F8 ? 0 : NS * 2 * TAB); // [NS] int: tokens of the block
+  static constexpr uint32_t OFF_CMETA = OFF_META + NS * 4;                // FP8: [NC] int, per code slot
+  static constexpr uint32_t OFF_SCALE = OFF_CMETA + (F8 ? NC * 4 : 0);    // FP8: [NC] float2 page scales
+  static constexpr uint32_t BYTES = OFF_SCALE + (F8 ? NC * 8 : 0) + 1024; // + alignment slack
+  static_assert(CSLOT % 16 == 0 && OFF_OFS % 16 == 0 && OFF_SCALE % 8 == 0, "bulk-copy and vector alignment");
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
 };
 
@@ -182,7 +207,7 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
 }
 
 template <int D, int G, int MODE, bool F8 = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(view_threads<F8>(), 1)
     view_kernel(const __grid_constant__ CUtensorMap tm_ksrc, const __grid_constant__ CUtensorMap tm_vsrc,
                 const __grid_constant__ CUtensorMap tm_kdst, const __grid_constant__ CUtensorMap tm_vdst,
                 const ViewParams vp, const SessionArgs a) {
@@ -191,19 +216,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kWrite = MODE != 1;
   constexpr bool kAttend = MODE != 0;
   constexpr int NS = Q::NS;
+  constexpr int NC = Q::NC;  // slots the loads fill: code slots (FP8 pages), else the stages themselves
+  constexpr int kRot = rot_warps<F8>();
+  constexpr int kProducer = kRot + kAttn;
+  constexpr int kThreads = view_threads<F8>();
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024 - (smem_addr(smem_raw) & 1023)) & 1023);
   const uint32_t sbase = smem_addr(smem);
   int* meta = reinterpret_cast<int*>(smem + Q::OFF_META);
+  int* cmeta = F8 ? reinterpret_cast<int*>(smem + Q::OFF_CMETA) : meta;  // tokens per loaded slot
   float2* meta_scale = reinterpret_cast<float2*>(smem + Q::OFF_SCALE);
-  __shared__ __align__(8) uint64_t full[NS], rotated[NS], empty[NS];
+  // full: per loaded slot; rotated, empty: per stage; cempty (FP8): per code slot, freed by its rotation warp
+  __shared__ __align__(8) uint64_t full[NC], rotated[NS], empty[NS], cempty[F8 ? NC : 1];
   __shared__ __align__(8) uint64_t never;  // failure-path test only: initialised, never arrived on
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x;
   if (tid == 0) {
+    for (int cs = 0; cs < NC; ++cs) {
+      mbar_init(&full[cs], 1);
+      if (F8) mbar_init(&cempty[cs], 1);
+    }
     for (int st = 0; st < NS; ++st) {
-      mbar_init(&full[st], 1);
       mbar_init(&rotated[st], 1);
       mbar_init(&empty[st], (kWrite ? 1 : 0) + (kAttend ? 1 : 0));  // the stage's rotation and attention warps
     }
@@ -216,8 +250,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // loaded before the wait on the preceding kernel, which wrote none of them.
   // Each is held as two packed pairs (cos of pairs 2u and 2u + 1; sin of the same), the operands of the paired
   // fp32 instructions below.
+  // FP8 pages: the table sits in shared memory instead (the eight rotation warps have no room for it in
+  // registers); a lane reads its pass's four float4 (cos, sin of pairs 2u and 2u + 1) from a layout whose float4
+  // index u is XOR-swizzled with the lane's chunk pair (and, for d = 64, its row parity), so the eight lanes of a
+  // quarter warp hit eight different bank groups.
   uint64_t ofc[Q::PASSES][4], ofs[Q::PASSES][4];
-  if (kWrite && warp < kRot) {
+  auto ofs_swz = [](int r, int cc) { return ((cc >> 1) & 3) ^ (D == 64 ? (r & 1) << 1 : 0); };
+  if constexpr (F8) {
+    float4* o4 = reinterpret_cast<float4*>(smem + Q::OFF_OFS);
+    const float4* src = reinterpret_cast<const float4*>(vp.rope_off);
+    for (int i = tid; i < 32 * (D / 4); i += kThreads) {
+      const int r = i / (D / 4), j = i % (D / 4), cc = j >> 2, u = j & 3;
+      o4[r * (D / 4) + 4 * cc + (u ^ ofs_swz(r, cc))] = __ldg(src + i);
+    }
+  } else if (kWrite && warp < kRot) {
     const int cc = lane % Q::CPR;
 #pragma unroll
     for (int pass = 0; pass < Q::PASSES; ++pass)
@@ -254,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   bool aborted = false;
   int64_t issued = 0;  // producer: blocks whose copies were issued
 
-  static_assert(NS % kRot == 0 && NS % kAttn == 0, "each rotation and each attention warp owns whole stages");
+  static_assert(NS % kRot == 0 && NS % kAttn == 0 && NC % kRot == 0,
+                "each rotation and each attention warp owns whole stages, each rotation warp whole code slots");
   if (warp == kProducer) {
     // ============================================================ producer
     // lane l resolves block jb + l: tokens present (0 = skip), source tile row, view slot
@@ -308,21 +355,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sk = F8 ? __shfl_sync(0xffffffffu, sk_cur, l) : 0.f;
         const float sv = F8 ? __shfl_sync(0xffffffffu, sv_cur, l) : 0.f;
         const int64_t jj = jb + l;
-        const int st = (int)(jj % NS);
-        const uint32_t round = (uint32_t)(jj / NS);
+        const int st = (int)(jj % NC);  // the slot this block's loads fill
+        const uint32_t round = (uint32_t)(jj / NC);
         int ok = 1;
         if (lane == 0) {
-          if (round > 0) ok = mbar_wait(&empty[st], (round - 1) & 1, vp.status, vp.wait_ns);
+          if (round > 0) ok = mbar_wait(F8 ? &cempty[st] : &empty[st], (round - 1) & 1, vp.status, vp.wait_ns);
           if (ok) {
-            meta[st] = valid;
-            unsigned char* kdst = smem + st * Q::STAGE;
+            cmeta[st] = valid;
+            unsigned char* kdst = F8 ? smem + Q::OFF_CODE + st * Q::CSLOT : smem + st * Q::STAGE;
             if (valid > 0) {
               if constexpr (F8) {
-                // the two code pages (contiguous 32 x d bytes each) by 1-D bulk copies, after the bf16 pages
+                // the two code pages (contiguous 32 x d bytes each) and the base table's hi row by 1-D bulk
+                // copies into the code slot
                 meta_scale[st] = make_float2(sk, sv);
-                mbar_arrive_expect_tx(&full[st], 2 * Q::CPAGE + 2 * Q::TAB);
-                bulk_g2s(kdst + 2 * Q::PAGE, vp.k8 + (int64_t)ysrc * D, Q::CPAGE, &full[st]);
-                bulk_g2s(kdst + 2 * Q::PAGE + Q::CPAGE, vp.v8 + (int64_t)ysrc * D, Q::CPAGE, &full[st]);
+                mbar_arrive_expect_tx(&full[st], 2 * Q::CPAGE + Q::TAB);
+                bulk_g2s(kdst, vp.k8 + (int64_t)ysrc * D, Q::CPAGE, &full[st]);
+                bulk_g2s(kdst + Q::CPAGE, vp.v8 + (int64_t)ysrc * D, Q::CPAGE, &full[st]);
+                bulk_g2s(kdst + 2 * Q::CPAGE, vp.rope_base + (int64_t)slot * (D / 2), Q::TAB, &full[st]);
               } else {
                 mbar_arrive_expect_tx(&full[st], 2 * Q::PAGE + (kWrite ? 2 * Q::TAB : 0));
 #pragma unroll
@@ -331,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tma_load_2d(kdst + Q::PAGE + b * Q::BOX, &tm_vsrc, 64 * b, ysrc, &full[st]);
                 }
               }
-              if (kWrite) {
+              if (kWrite && !F8) {
                 unsigned char* tdst = smem + Q::OFF_TAB + st * 2 * Q::TAB;
                 bulk_g2s(tdst, vp.rope_base + (int64_t)slot * (D / 2), Q::TAB, &full[st]);
                 bulk_g2s(tdst + Q::TAB, vp.rope_base_lo + (int64_t)slot * (D / 2), Q::TAB, &full[st]);
@@ -361,18 +410,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int64_t jj = warp; jj < nb; jj += kRot) {
         const int st = (int)(jj % NS);
         const uint32_t phase = (uint32_t)((jj / NS) & 1);
+        const int cslot = (int)(jj % NC);  // the slot the block was loaded into (the stage itself for bf16 pages)
+        const uint32_t cphase = (uint32_t)((jj / NC) & 1);
         const Cursor cu = locate(fa + jj, a, vp.n_sessions);
         const int q = cu.s * vp.h_kv + cu.g;
         const int64_t ydst = (int64_t)q * Lcap + 32 * cu.i;
         KVM_DEBUG_CHECK(cu.i < vp.budget && ydst + 32 <= (int64_t)vp.n_sessions * vp.h_kv * Lcap, vp.status);
         const uint32_t vaddr = sbase + st * Q::STAGE + Q::PAGE;
-        if (__any_sync(0xffffffffu, !mbar_wait(&full[st], phase, vp.status, vp.wait_ns) ||
-                                        (vp.stall && fa + jj == 0 &&
-                                         !mbar_wait(&never, 0, vp.status, vp.wait_ns)))) {
+        bool bad = !mbar_wait(&full[cslot], cphase, vp.status, vp.wait_ns);
+        if (F8 && jj >= NS) {
+          // FP8 pages: the stage is written here, so block jj - NS must be done with it: this warp's own view
+          // stores of that block have read it (its share, given now), and its attention warp has arrived
+          if (lane == 0) {
+            bulk_wait_read<NS / kRot - 1>();  // this warp's later blocks' stores may still be reading
+            mbar_arrive(&empty[st]);
+          }
+          __syncwarp();
+          bad = bad || !mbar_wait(&empty[st], phase ^ 1u, vp.status, vp.wait_ns);
+        }
+        bad = bad || (vp.stall && fa + jj == 0 && !mbar_wait(&never, 0, vp.status, vp.wait_ns));
+        if (__any_sync(0xffffffffu, bad)) {
           aborted = true;
           break;
         }
-        const int valid = meta[st];
+        const int valid = cmeta[cslot];
         if (cu.i == 0 && lane == 0) {  // the segment's view length, written by the rotation warp of its block 0
           const int nk = a.n_keep[cu.s];
           const int last = vp.kept[(int64_t)q * vp.budget + nk - 1];
@@ -381,7 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (valid > 0) {
             unsigned char* kst = smem + st * Q::STAGE;
             uint4* kq = reinterpret_cast<uint4*>(kst);  // the stage's K page as 16-byte chunks
-            const float4* __restrict__ tabh = reinterpret_cast<const float4*>(smem + Q::OFF_TAB + st * 2 * Q::TAB);
+            // the block's base table row: in its code slot (FP8 pages) or beside its stage
+            const unsigned char* tab_hi =
+                F8 ? smem + Q::OFF_CODE + cslot * Q::CSLOT + 2 * Q::CPAGE : smem + Q::OFF_TAB + st * 2 * Q::TAB;
+            const float4* __restrict__ tabh = reinterpret_cast<const float4*>(tab_hi);
             // the block's base cos/sin for this lane's 8 pairs, as packed pairs (2u, 2u + 1)
             uint64_t bc[4], bs[4];
 #pragma unroll
@@ -405,10 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             // as bf16 pages; each rotated value is stored, and a pair that cancels is redone in float-float after
             // the passes from its codes.  V is decoded and rounded to bf16 into the stage's V page, which the
             // view store and the attention then read.
-            const unsigned char* codes = kst + 2 * Q::PAGE;
-            const float2 scl = meta_scale[st];
+            const unsigned char* codes = smem + Q::OFF_CODE + cslot * Q::CSLOT;
+            const float2 scl = meta_scale[cslot];
+            const float4* o4 = reinterpret_cast<const float4*>(smem + Q::OFF_OFS);
             uint32_t redo_all = 0;  // bit pass: the pass holds a pair whose rotation cancels
-#pragma unroll
+            // (two passes per iteration: the whole kernel's code then stays within the instruction cache, which
+            // the fully unrolled FP8 decode and rotation of eight warps did not)
+#pragma unroll 2
             for (int pass = 0; pass < Q::PASSES; ++pass) {
               const int r = lane / Q::CPR + Q::RPP * pass;
               const uint2 ca = *reinterpret_cast<const uint2*>(codes + r * D + 8 * cc);
@@ -428,8 +495,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               bool cancel = false;
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
-                const uint64_t cs = fma2(bc[u], ofc[pass][u], mul2(bs[u] ^ 0x8000000080000000ull, ofs[pass][u]));
-                const uint64_t sn = fma2(bs[u], ofc[pass][u], mul2(bc[u], ofs[pass][u]));
+                const float4 t = o4[r * (D / 4) + 4 * cc + (u ^ ofs_swz(r, cc))];
+                const uint64_t oc2 = pk2(t.x, t.z), os2 = pk2(t.y, t.w);
+                const uint64_t cs = fma2(bc[u], oc2, mul2(bs[u] ^ 0x8000000080000000ull, os2));
+                const uint64_t sn = fma2(bs[u], oc2, mul2(bc[u], os2));
                 const float x1l = xa_f[2 * u], x1h = xa_f[2 * u + 1], x2l = xb_f[2 * u], x2h = xb_f[2 * u + 1];
                 const uint64_t x1 = pk2(x1l, x1h), x2 = pk2(x2l, x2h), nx2 = pk2(-x2l, -x2h);
                 float f1l, f1h, f2l, f2h;
@@ -461,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               sts128(vaddr + chunk_off(r, cc + D / 16), make_uint4(vo[4], vo[5], vo[6], vo[7]));
             }
             if (redo_all) {  // rare: each pair of a flagged pass rotated again from its codes, in float-float if it cancels
-              const float2* tabl = reinterpret_cast<const float2*>(smem + Q::OFF_TAB + st * 2 * Q::TAB + Q::TAB);
+              const float2* tabl = vp.rope_base_lo + (int64_t)cu.i * (D / 2);  // not staged: rare path
               const float2* tabh2 = reinterpret_cast<const float2*>(tabh);
 #pragma unroll 1
               for (uint32_t m = redo_all; m; m &= m - 1) {
@@ -478,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (!(fminf(fabsf(fmaf(x1, cs, -x2 * sn)), fabsf(fmaf(x2, cs, x1 * sn))) * 0x1p13f <
                         fabsf(x1) + fabsf(x2)))
                     continue;  // this pair was stored correctly by the pass
-                  const float2 bl = tabl[k], ol = __ldg(vp.rope_off_lo + r * (D / 2) + k);
+                  const float2 bl = __ldg(tabl + k), ol = __ldg(vp.rope_off_lo + r * (D / 2) + k);
                   float y1, y2;
                   rotate_exact(x1, x2, make_float4(bh.x, bl.x, bh.y, bl.y), make_float4(oh.x, ol.x, oh.y, ol.y), y1,
                                y2);
@@ -572,24 +641,30 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
         }
+        if constexpr (F8) {
+          // the block's codes and table row are consumed: its code slot may be refilled.  The stage's token count
+          // goes with the rotated arrival below.
+          __syncwarp();
+          if (lane == 0) {
+            meta[st] = valid;
+            mbar_arrive(&cempty[cslot]);
+          }
+        }
         // The attention warp may read the rotated page now.  This block's view stores form one bulk group (empty
         // when there are none); the stage is free once the group has read its source.  Fused: the stage's
         // attention warp holds it for a while anyway, so this warp frees the stage of its previous block after
-        // issuing this block's stores and never waits for stores it has just issued.  Materialising only, the
-        // stage is freed at once (its load refill is then the one thing waiting on it).
+        // issuing this block's stores and never waits for stores it has just issued (FP8 pages: one stage per
+        // warp, freed just before the warp's next block is decoded into it).  Materialising only, the stage is
+        // freed at once (its load refill is then the one thing waiting on it).
         if (lane == 0) {
           bulk_commit();
-          if constexpr (kAttend && !F8) {
+          if constexpr (kAttend) {
             mbar_arrive(&rotated[st]);
-            if (prev_st >= 0) {
+            if (!F8 && prev_st >= 0) {
               bulk_wait_read<1>();
               mbar_arrive(&empty[prev_st]);
             }
           } else {
-            // materialising only, or FP8 pages (8 larger stages, 2 per rotation warp: holding a second one
-            // would leave the loads no stage to run ahead in): the stage is released as soon as its stores
-            // have read it
-            if constexpr (kAttend) mbar_arrive(&rotated[st]);
             bulk_wait_read<0>();
             mbar_arrive(&empty[st]);
           }
@@ -825,8 +900,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kProducer && lane == 0) {
       // copies still in flight into a stage must land before the CTA exits: wait (bounded) for the
       // last round issued on each stage
-      for (int st = 0; st < NS; ++st)
-        if (issued > st) mbar_wait(&full[st], (uint32_t)(((issued - 1 - st) / NS) & 1), vp.status);
+      for (int st = 0; st < NC; ++st)
+        if (issued > st) mbar_wait(&full[st], (uint32_t)(((issued - 1 - st) / NC) & 1), vp.status);
     }
     return;
   }
@@ -991,7 +1066,8 @@ cudaError_t launch_dg(const Ctx& c, int mode, const CUtensorMap* maps, const Vie
   const uint32_t bytes = mode == 3 ? Geo<D, true>::BYTES : Geo<D>::BYTES;
   cudaError_t e = ensure_smem(kern, c.device, bytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(kern, dim3(vp.P), dim3(kThreads), bytes, st, 1, maps[0], maps[1], maps[2], maps[3], vp, a);
+  const int threads = mode == 3 ? view_threads<true>() : view_threads<false>();
+  return launch_pdl(kern, dim3(vp.P), dim3(threads), bytes, st, 1, maps[0], maps[1], maps[2], maps[3], vp, a);
 }
 
 template <int D>

@@ -54,6 +54,49 @@ def test_view_wait_timeout_is_reported_and_the_context_recovers():
     ctx.close()
 
 
+
+def test_fp8_view_wait_timeout_is_reported_and_the_context_recovers():
+    """The same on the FP8 view path, whose loads fill a ring of code slots and whose rotation warps wait for their
+    stages: the timed-out call reports KVM_DEV_TIMEOUT, and the next calls give the first call's view and output
+    bit for bit."""
+    w = synth.WORKLOADS["gqa40x8_256k"].with_(n_tok=40000)
+    li = synth.layer_inputs(w, 0)
+    ctx = K.Context.for_workload(w)
+    dev = LayerOnDevice(w, li, ctx)
+    dev.index_build()
+    dev.score_select()
+    n = dev.n_pages
+    pages = torch.arange(n, dtype=torch.int32, device="cuda")
+    k8 = torch.empty((n, w.h_kv, 32, w.d), dtype=torch.uint8, device="cuda")
+    v8 = torch.empty_like(k8)
+    ks = torch.empty((n, w.h_kv), dtype=torch.float32, device="cuda")
+    vs = torch.empty_like(ks)
+    K.kvm_quantize_pages(ctx, dev.k_pool, n, pages, k8, ks)
+    K.kvm_quantize_pages(ctx, dev.v_pool, n, pages, v8, vs)
+
+    def fused8():
+        K.kvm_materialize_attn_fp8(ctx, k8, ks, v8, vs, n, dev.bt, dev.n_tok, dev.kept, dev.q, dev.k_view,
+                                   dev.v_view, dev.view_len, dev.out)
+
+    fused8()
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    out0, kview0, vview0 = dev.out.clone(), dev.k_view.clone(), dev.v_view.clone()
+    K.kvm_set_wait_limit(ctx, 100_000, True)       # 0.1 ms; the first rotation wait can never complete
+    dev.out.fill_(float("nan"))
+    fused8()
+    assert K.kvm_device_status(ctx, clear=True) & K.DEV_TIMEOUT
+    assert K.kvm_device_status(ctx) == 0
+    K.kvm_set_wait_limit(ctx)
+    for _ in range(2):
+        dev.out.fill_(float("nan"))
+        fused8()
+        torch.cuda.synchronize()
+        assert K.kvm_device_status(ctx) == 0
+        assert torch.equal(dev.out, out0)
+        assert torch.equal(dev.k_view, kview0) and torch.equal(dev.v_view, vview0)
+    ctx.close()
+
 def _expected_view_and_out(w, li, slots, q_group, L):
     """View rows and attention output for {slot: block id} (the valid slots), query at position L."""
     keys = oracle_keys(w, li, 0, 0)
