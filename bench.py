@@ -4,10 +4,10 @@ Default workload (ws1m_16layer): 40 query heads / 8 KV heads, d = 128, a
 1,048,576-token history per layer with 16 layers resident in HBM (64 GiB of
 bf16 K/V pages + 2 GiB fp32 Mean-K index), a 65,536-token view per layer
 (4 sink + 32 recent + 2012 top-k blocks), one decode query per layer.  One
-step = the step's 512 new tokens appended to every layer's index (kvm_index_append, on a side
-stream: no layer's append depends on an earlier layer), then for each of the 16 layers, in order:
-    kvm_score_select (after that layer's append) -> kvm_materialize_attn (gather + re-RoPE view,
-    decode attention).
+step = the step's 512 new tokens appended to every layer's index (kvm_index_append_layers: one
+launch for all layers, as no layer's append depends on an earlier layer), then for each of the 16
+layers, in order:
+    kvm_score_select -> kvm_materialize_attn (gather + re-RoPE view, decode attention).
 Metric: step latency per layer (us) and the HBM GB/s of the bytes each layer
 must touch (index read + appended keys + kept K/V read + view write).
 
@@ -336,8 +336,9 @@ def run_kvm(args, w):
     build_us = float(np.median(build_ms)) * 1e3
     build_bytes = S * n_hist * w.h_kv * w.d * 2 + S * w.h_kv * (-(-n_hist // BLOCK)) * w.d * 4
     n_tok = [w.n_tok] * S
-    # [append,] score + select (recent-only: one kernel), the fused view kernel
-    launches_per_layer = (1 if w.append_tok else 0) + (1 if args.selection == "recent" else 2) + 1
+    # [one append launch for every layer,] then per layer score + select (recent-only: one kernel) and the fused
+    # view kernel
+    launches_per_step = (1 if w.append_tok else 0) + L * ((1 if args.selection == "recent" else 2) + 1)
 
     def call_append(layer):
         if w.append_tok:
@@ -355,36 +356,22 @@ def run_kvm(args, w):
                                v_view, view_len, outs[layer])
 
     # The step's new tokens have their keys for every layer when the step starts, so no layer's index append
-    # waits on an earlier layer's output: all appends go to a side stream at the start of the step, and each
-    # layer's scoring waits only for its own append.
-    app_stream = torch.cuda.Stream()
-    app_done = [torch.cuda.Event() for _ in range(L)]
-
-    def appends_ahead(before_append=None):
-        app_stream.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(app_stream):
-            for layer in range(L):
-                if before_append is not None:
-                    before_append(layer)
-                call_append(layer)
-                app_done[layer].record(app_stream)
-
-    def layers_after_appends(select_fn, view_fn):
-        main = torch.cuda.current_stream()
-        for layer in range(L):
-            if w.append_tok:
-                main.wait_event(app_done[layer])
-            select_fn(layer)
-            view_fn(layer)
+    # waits on an earlier layer's output: every layer's append runs in one launch at the start of the step
+    # (kvm_index_append_layers), and from there on each kernel follows the previous one on one stream, so under
+    # programmatic dependent launch each may start early and prefetch while the previous one finishes.
+    def append_all():
         if w.append_tok:
-            main.wait_stream(app_stream)
+            K.kvm_index_append_layers(ctx, kp, n_pages, bt, [n_hist] * S, [w.append_tok] * S, index)
 
     def step():
-        if w.append_tok:
-            appends_ahead()
-        layers_after_appends(call_select, call_view)
+        append_all()
+        for layer in range(L):
+            call_select(layer)
+            call_view(layer)
 
-    stage_fns = {"index_append": call_append, "score_select": call_select, "materialize_attn": call_view}
+    # (the append stage is the one launch for every layer, divided over the layers like the others)
+    stage_fns = {"index_append": lambda layer: append_all() if layer == 0 else None, "score_select": call_select,
+                 "materialize_attn": call_view}
     if not w.append_tok:
         del stage_fns["index_append"]  # nothing is appended inside this workload's step
 
@@ -400,7 +387,7 @@ def run_kvm(args, w):
         torch.cuda.synchronize()
         torch.cuda.profiler.stop()
         if rank == 0:
-            print(json.dumps({"profile_step": w.name, "launches": launches_per_layer * L}), flush=True)
+            print(json.dumps({"profile_step": w.name, "launches": launches_per_step}), flush=True)
         return
 
     # CUDA graphs: one whole step (all layers), and each stage alone over all layers (per-call durations)
@@ -586,7 +573,7 @@ def run_kvm(args, w):
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "algorithmic_bytes_per_launch": vb},
             "cpu_baseline": cpu, "e2e": e2e,
-            "gpu_launches": launches_per_layer * L * args.steps * (2 if stage_graphs else 1),
+            "gpu_launches": launches_per_step * args.steps * (2 if stage_graphs else 1),
             "clocks": sampler.summary(),
             "per_config": per_config,
             "index_build": {"us_per_layer": round(build_us, 1), "tokens": S * n_hist, "bytes": build_bytes,
@@ -921,15 +908,34 @@ def run_kvm_tier(args, w):
         K.kvm_materialize_attn_fp8(ctx, k8, ks, v8, vs, n_pages, bt, n_tok, kept, qs[layer], k_view, v_view,
                                    view_len, outs[layer])
 
+    # As in the bf16 leg: every layer's append on a side stream at the start of the step; layer 0's scoring
+    # waits for its own, layer 1's for all of them, and later kernels follow each other with no cross-stream edge.
+    appends = bool(w.append_tok) and not host
+    app_stream = torch.cuda.Stream()
+    app_first = torch.cuda.Event()
+
     def step():
+        main = torch.cuda.current_stream()
+        if appends:
+            app_stream.wait_stream(main)
+            with torch.cuda.stream(app_stream):
+                for layer in range(L):
+                    call_append(layer)
+                    if layer == 0:
+                        app_first.record(app_stream)
         for layer in range(L):
-            call_append(layer)
+            if appends and layer == 0:
+                main.wait_event(app_first)
+            if appends and layer == 1:
+                main.wait_stream(app_stream)
             call_select(layer)
             if host:
                 call_gather(layer)
                 call_attend(layer)
             else:
                 call_fused(layer)
+        if appends and L == 1:
+            main.wait_stream(app_stream)
 
     for _ in range(args.warmup):
         step()

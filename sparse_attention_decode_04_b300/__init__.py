@@ -71,10 +71,11 @@ def lib() -> ctypes.CDLL:
         L.kvm_materialize_fp8.argtypes = [P, P, P, P, P, i64, P, P, i32, P, P, P, P, P]
         L.kvm_materialize_host.argtypes = [P, P, P, i64, P, P, i32, P, P, P, P, P]
         L.kvm_attention_mass.argtypes = [P, P, P, i64, P, P, i32, P, P]
+        L.kvm_index_append_layers.argtypes = [P, i32, P, i64, P, i32, P, P, P, P]
         for name in ("kvm_create", "kvm_destroy", "kvm_index_append", "kvm_score_select", "kvm_materialize",
                      "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status", "kvm_select_control",
                      "kvm_step_attn", "kvm_quantize_pages", "kvm_index_append_fp8", "kvm_materialize_fp8",
-                     "kvm_materialize_host", "kvm_attention_mass"):
+                     "kvm_materialize_host", "kvm_attention_mass", "kvm_index_append_layers"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -147,6 +148,18 @@ def kvm_index_append(ctx: Context, k_pool, n_pages: int, block_table, tok_begin,
     n = len(n_tok)
     _check(lib().kvm_index_append(ctx.handle, _ptr(k_pool), int(n_pages), _ptr(block_table), n, _i64(tok_begin),
                                   _i64(n_tok), _ptr(index), _stream(stream)))
+
+
+def kvm_index_append_layers(ctx: Context, k_pools, n_pages: int, block_table, tok_begin, n_tok, indexes,
+                            stream=None):
+    """kvm_index_append for several layers (lists of key pools and indexes, one per layer) in one launch."""
+    if len(k_pools) != len(indexes):
+        raise ValueError("one index per key pool")
+    n, nl = len(n_tok), len(k_pools)
+    pools = (ctypes.c_void_p * max(1, nl))(*[_ptr(t) for t in k_pools])
+    idx = (ctypes.c_void_p * max(1, nl))(*[_ptr(t) for t in indexes])
+    _check(lib().kvm_index_append_layers(ctx.handle, nl, pools, int(n_pages), _ptr(block_table), n, _i64(tok_begin),
+                                         _i64(n_tok), idx, _stream(stream)))
 
 
 def kvm_score_select(ctx: Context, q, n_q: int, index, n_tok, kept_ids, group_scores=None, head_scores=None,

@@ -12,8 +12,10 @@
 #include <utility>
 
 #include "kvm.h"
+#include "kvm_batch.h"
 #include "kvm_diag.h"
 #include "kvm_internal.h"
+#include "kvm_layers.h"
 #include "kvm_mass.h"
 
 using kvm::Ctx;
@@ -316,6 +318,45 @@ kvm_status kvm_index_append(kvm_ctx* ctx, const uint16_t* k_pool, int64_t n_page
   cudaError_t e = kvm::launch_index_append(c, k_pool, n_pages, block_table, n_sessions, a, max_count, index, shadow,
                                            (cudaStream_t)stream);
   return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_index_append launch");
+}
+
+kvm_status kvm_index_append_layers(kvm_ctx* ctx, int32_t n_layers, const uint16_t* const* k_pools,
+                                   int64_t n_pages, const int32_t* block_table, int32_t n_sessions,
+                                   const int64_t* tok_begin, const int64_t* n_tok, float* const* indexes,
+                                   void* stream) {
+  kvm_status s = check_ctx(ctx);
+  if (s != KVM_OK) return s;
+  const Ctx& c = ctx->c;
+  if ((s = check_sessions(c, n_sessions)) != KVM_OK) return s;
+  if (n_layers < 1 || n_layers > kvm::kMaxAppendLayers)
+    return fail(KVM_ERR_INVALID_ARG, "n_layers=%d must be in [1, %d]", n_layers, kvm::kMaxAppendLayers);
+  if (!k_pools || !indexes || !block_table || !tok_begin || !n_tok)
+    return fail(KVM_ERR_INVALID_ARG, "kvm_index_append_layers: NULL pointer argument");
+  if (n_pages < 1) return fail(KVM_ERR_INVALID_ARG, "n_pages=%lld must be >= 1", (long long)n_pages);
+  kvm::AppendLayers layers;
+  memset(&layers, 0, sizeof(layers));
+  for (int i = 0; i < n_layers; ++i) {
+    if (!k_pools[i] || !indexes[i])
+      return fail(KVM_ERR_INVALID_ARG, "kvm_index_append_layers: layer %d has a NULL pointer", i);
+    if (!aligned(k_pools[i], 16) || !aligned(indexes[i], 16))
+      return fail(KVM_ERR_INVALID_ARG, "layer %d: k_pool and index must be 16-byte aligned", i);
+    layers.k_pool[i] = k_pools[i];
+    layers.index[i] = indexes[i];
+  }
+  if (n_sessions == 0) return KVM_OK;
+  SessionArgs a;
+  int max_count = 0;
+  if ((s = append_args(c, n_sessions, tok_begin, n_tok, &a, &max_count)) != KVM_OK) return s;
+  // the bf16 copy follows single-layer appends only: an index it mirrors is about to change without it
+  Ctx& cm = ctx->c;
+  for (int i = 0; i < n_layers; ++i)
+    if (cm.step_kpk && indexes[i] == cm.shadow_of) {
+      cm.shadow_of = nullptr;
+      for (int64_t& nb : cm.shadow_blocks) nb = 0;
+    }
+  cudaError_t e = kvm::launch_index_append_layers(c, layers, n_layers, n_pages, block_table, n_sessions, a,
+                                                  max_count, (cudaStream_t)stream);
+  return e == cudaSuccess ? KVM_OK : cuda_fail(e, "kvm_index_append_layers launch");
 }
 
 kvm_status kvm_index_append_fp8(kvm_ctx* ctx, const uint8_t* k_pool8, const float* k_scales, int64_t n_pages,

@@ -17,25 +17,22 @@
 
 #include "kvm_device.cuh"
 #include "kvm_internal.h"
+#include "kvm_layers.h"
 
 namespace kvm {
 namespace {
 
 constexpr int kWarps = 4;
 
+// One warp: the index row of block a.aux[s] + bi of session s, KV head g (and its bf16 copy when shadow is set).
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_t* __restrict__ k_pool,
-                                                                   int64_t n_pages,
-                                                                   const int32_t* __restrict__ bt,
-                                                                   int64_t max_blocks, int h_kv, SessionArgs a,
-                                                                   float* __restrict__ index,
-                                                                   uint16_t* __restrict__ shadow,
-                                                                   int64_t shadow_rows, uint32_t* __restrict__ status) {
+__device__ __forceinline__ void append_block(const uint16_t* __restrict__ k_pool, int64_t n_pages,
+                                             const int32_t* __restrict__ bt, int64_t max_blocks, int h_kv,
+                                             const SessionArgs& a, float* __restrict__ index,
+                                             uint16_t* __restrict__ shadow, int64_t shadow_rows,
+                                             uint32_t* __restrict__ status, int s, int g, int64_t bi) {
   constexpr int PER = D / 32;  // dims per lane
-  griddep_wait();
-  const int s = blockIdx.z, g = blockIdx.y;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t bi = (int64_t)blockIdx.x * kWarps + warp;
+  const int lane = threadIdx.x & 31;
   if (bi >= a.count[s]) return;
   const int64_t b = a.aux[s] + bi;                         // block id
   KVM_DEBUG_CHECK(b < max_blocks, status);
@@ -99,7 +96,44 @@ __global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_
   }
 }
 
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) index_append_kernel(const uint16_t* __restrict__ k_pool,
+                                                                   int64_t n_pages,
+                                                                   const int32_t* __restrict__ bt,
+                                                                   int64_t max_blocks, int h_kv, SessionArgs a,
+                                                                   float* __restrict__ index,
+                                                                   uint16_t* __restrict__ shadow,
+                                                                   int64_t shadow_rows, uint32_t* __restrict__ status) {
+  griddep_wait();
+  append_block<D>(k_pool, n_pages, bt, max_blocks, h_kv, a, index, shadow, shadow_rows, status, blockIdx.z,
+                  blockIdx.y, (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5));
+}
+
+// The same appends for several layers in one launch: grid z runs over (layer, session), layer-major.
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) index_append_layers_kernel(const AppendLayers layers, int n_sessions,
+                                                                          int64_t n_pages,
+                                                                          const int32_t* __restrict__ bt,
+                                                                          int64_t max_blocks, int h_kv, SessionArgs a,
+                                                                          uint32_t* __restrict__ status) {
+  griddep_wait();
+  const int layer = blockIdx.z / n_sessions, s = blockIdx.z % n_sessions;
+  append_block<D>(layers.k_pool[layer], n_pages, bt, max_blocks, h_kv, a, layers.index[layer], nullptr, 0, status,
+                  s, blockIdx.y, (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5));
+}
+
 }  // namespace
+
+cudaError_t launch_index_append_layers(const Ctx& c, const AppendLayers& layers, int n_layers, int64_t n_pages,
+                                       const int32_t* bt, int n_sessions, const SessionArgs& a, int max_count,
+                                       cudaStream_t st) {
+  if (max_count <= 0) return cudaSuccess;
+  dim3 grid((max_count + kWarps - 1) / kWarps, c.p.h_kv, n_layers * n_sessions);
+  return c.p.d == 128 ? launch_pdl(index_append_layers_kernel<128>, grid, dim3(kWarps * 32), 0, st, 1, layers,
+                                    n_sessions, n_pages, bt, c.p.max_blocks, c.p.h_kv, a, c.status)
+                       : launch_pdl(index_append_layers_kernel<64>, grid, dim3(kWarps * 32), 0, st, 1, layers,
+                                    n_sessions, n_pages, bt, c.p.max_blocks, c.p.h_kv, a, c.status);
+}
 
 cudaError_t launch_index_append(const Ctx& c, const uint16_t* k_pool, int64_t n_pages, const int32_t* bt,
                                 int n_sessions, const SessionArgs& a, int max_count, float* index, uint16_t* shadow,

@@ -12,6 +12,8 @@
 //   barrier per stage), computes the G scores of
 //   each row with 8 lanes per row and shuffle reductions, then writes
 //   e[b][h] = exp(s[b][h] - m_tile[h]) and the tile's (m_tile, sum e) per head.
+//   Before waiting for the preceding kernel it prefetches the rows of its first
+//   stages into L2.
 // Kernel B (select_kernel), grid (C, h_kv, sessions), clusters of C CTAs:
 //   each CTA owns 1/C of the blocks.  From the tiles' partials it forms the
 //   softmax normalisers, Gs[b] = sum_h e[b][h] * exp(m_tile - M_h) / Z_h (the
@@ -41,6 +43,11 @@ namespace cg = cooperative_groups;
 
 namespace kvm {
 namespace {
+
+// Moves [src, src + bytes) into L2 (no completion to wait for); src and bytes multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
 
 constexpr int kScoreThreads = 256;  // 8 warps, 4 rows each per stage
 constexpr int kStageRows = 32;
@@ -102,6 +109,18 @@ __global__ void __launch_bounds__(kScoreThreads) score_tile_kernel(
   __shared__ float red[kScoreThreads / 32][G];
   __shared__ float tile_max[G];
 
+  // While the preceding kernel finishes, warm L2 with the rows of this tile's first stages.  A prefetch only
+  // moves lines into L2, the point of coherence, so rows written before the wait below completes (an index
+  // append earlier in the stream) are still what the stage loads read.
+  if (threadIdx.x == 0) {
+    const int64_t nb = a.n_blk[blockIdx.z], rr0 = (int64_t)blockIdx.x * rows_per_tile;
+    if (rr0 < nb) {
+      const int64_t cap = kStages * kStageRows < rows_per_tile ? kStages * kStageRows : rows_per_tile;
+      const int64_t pr = cap < nb - rr0 ? cap : nb - rr0;
+      prefetch_l2(index + (((int64_t)blockIdx.z * h_kv + blockIdx.y) * max_blocks + rr0) * D,
+                  (uint32_t)(pr * D * 4));
+    }
+  }
   griddep_wait();
   const int s = blockIdx.z, g = blockIdx.y, tile = blockIdx.x;
   const int64_t n_blk = a.n_blk[s];

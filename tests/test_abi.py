@@ -31,7 +31,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert {"kvm_create", "kvm_destroy", "kvm_index_append", "kvm_score_select", "kvm_materialize",
             "kvm_decode_attn", "kvm_materialize_attn", "kvm_device_status", "kvm_step_attn",
             "kvm_select_control", "kvm_quantize_pages", "kvm_index_append_fp8", "kvm_materialize_fp8",
-            "kvm_materialize_host", "kvm_attention_mass"} <= set(names)
+            "kvm_materialize_host", "kvm_attention_mass", "kvm_index_append_layers"} <= set(names)
     for n in names:
         assert hasattr(lib, n), f"{n} is declared in kvm.h but not exported"
 
@@ -75,6 +75,7 @@ def test_calls_reject_null_context(lib):
     assert lib.kvm_materialize_fp8(None, None, None, None, None, 1, None, n, 1, None, None, None, None, None) == 1
     assert lib.kvm_materialize_host(None, None, None, 1, None, n, 1, None, None, None, None, None) == 1
     assert lib.kvm_attention_mass(None, None, None, 1, None, n, 1, None, None) == 1
+    assert lib.kvm_index_append_layers(None, 2, None, 1, None, 1, n, n, None, None) == 1
     out = ctypes.c_uint32(0)
     assert lib.kvm_device_status(None, ctypes.byref(out), 0, None) == 1
     assert lib.kvm_destroy(None) == 0

@@ -264,6 +264,36 @@ def test_index_append_in_ragged_pieces_equals_full_build():
     ctx.close()
 
 
+@pytest.mark.parametrize("name", ["gqa40x8_256k", "tiny_8k_g4_d64"])
+def test_index_append_layers_equals_one_append_per_layer(name):
+    """kvm_index_append_layers over three layers, on a ragged token range after a ragged history, leaves every
+    layer's index bit for bit as kvm_index_append does; the rows match the oracle's block means."""
+    w = synth.WORKLOADS[name]
+    w = w.with_(n_tok=min(w.n_tok, 12000))
+    ctx = K.Context.for_workload(w)
+    lis = [synth.layer_inputs(w, layer) for layer in range(3)]
+    assert all(np.array_equal(li.block_table, lis[0].block_table) for li in lis)  # the layers share it
+    devs = [LayerOnDevice(w, li, ctx) for li in lis]
+    S = w.n_sessions
+    b0 = w.n_tok // 3 + 7                        # mid-block on both ends
+    hist, new = [b0] * S, [w.n_tok - b0] * S
+    for d in devs:
+        K.kvm_index_append(ctx, d.k_pool, d.n_pages, d.bt, [0] * S, hist, d.index)
+    refs = [d.index.clone() for d in devs]
+    for d, r in zip(devs, refs):
+        K.kvm_index_append(ctx, d.k_pool, d.n_pages, d.bt, hist, new, r)
+    K.kvm_index_append_layers(ctx, [d.k_pool for d in devs], devs[0].n_pages, devs[0].bt, hist, new,
+                              [d.index for d in devs])
+    torch.cuda.synchronize()
+    assert K.kvm_device_status(ctx) == 0
+    for d, r in zip(devs, refs):
+        assert torch.equal(d.index, r)
+    g = w.h_kv - 1
+    keys = oracle_keys(w, lis[2], 0, g)
+    check_index(devs[2].index[0, g, :w.n_blk].cpu().numpy(), keys, O.mean_k_index(keys))
+    ctx.close()
+
+
 def test_bad_page_is_reported_not_faulted():
     w = synth.WORKLOADS["tiny_8k_g4_d64"]
     li = synth.layer_inputs(w, 0)
