@@ -21,7 +21,7 @@
 //     and V pages by TMA tiled loads (64-column boxes, 128-byte swizzle) and,
 //     when writing a view, the block's rows of the RoPE base tables by 1-D bulk
 //     copies, all completing on the stage's `full` mbarrier;
-//   - four rotation warps take every fourth block of the share: each rotates
+//   - four rotation warps (eight for FP8 pages, below) take every fourth block of the share: each rotates
 //     K in place at view positions 32*i + r (cos/sin composed in fp32 from the
 //     staged per-slot row and the per-offset values, which a lane keeps in
 //     registers because it always rotates the same (row, pair) slots; both
