@@ -157,6 +157,11 @@ struct Geo {
   static_assert(STAGE % 1024 == 0, "stages stay 1024-byte aligned for the 128-byte swizzle");
 };
 
+// Moves [src, src + bytes) into L2 (no completion to wait for); src and bytes multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ int64_t cta_begin(int c, int64_t total, int P) { return (int64_t)c * total / P; }
 // CTA whose share contains flat block f (shares are [floor(cT/P), floor((c+1)T/P))).
 __device__ __forceinline__ int cta_of(int64_t f, int64_t total, int P) {
@@ -274,6 +279,20 @@ __global__ void __launch_bounds__(view_threads<F8>(), 1)
         ofc[pass][u] = pk2(o0.x, o1.x);
         ofs[pass][u] = pk2(o0.y, o1.y);
       }
+  }
+  // While the preceding kernel finishes, warm L2 with the block-table rows of this CTA's sessions (the producer's
+  // first page lookups then hit L2).  A prefetch only moves lines into L2, the point of coherence, so it cannot
+  // make a lookup see an older table; only whole 16-byte pieces inside each row are prefetched.
+  if (MODE != 1 && warp == kProducer && lane == 0 && vp.total > 0) {
+    const int64_t f0 = cta_begin(c, vp.total, vp.P), f1 = cta_begin(c + 1, vp.total, vp.P);
+    if (f0 < f1) {
+      const int s0 = locate(f0, a, vp.n_sessions).s, s1 = locate(f1 - 1, a, vp.n_sessions).s;
+      for (int s = s0; s <= s1; ++s) {
+        const int32_t* row = vp.bt + (int64_t)s * vp.max_blocks;
+        const uint32_t bytes = (uint32_t)(((int64_t)a.n_blk[s] * 4) & ~(int64_t)15);
+        if ((reinterpret_cast<uintptr_t>(row) & 15) == 0 && bytes > 0) prefetch_l2(row, bytes);
+      }
+    }
   }
   griddep_wait();  // kept ids, queries, views and outputs belong to the stream order from here on
   if (vp.any_empty) {
