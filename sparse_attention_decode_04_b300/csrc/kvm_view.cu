@@ -281,16 +281,22 @@ __global__ void __launch_bounds__(view_threads<F8>(), 1)
       }
   }
   // While the preceding kernel finishes, warm L2 with the block-table rows of this CTA's sessions (the producer's
-  // first page lookups then hit L2).  A prefetch only moves lines into L2, the point of coherence, so it cannot
-  // make a lookup see an older table; only whole 16-byte pieces inside each row are prefetched.
+  // first page lookups then hit L2): the CTAs sharing a session each take one slice of its row, so the row is
+  // requested once.  A prefetch only moves lines into L2, the point of coherence, so it cannot make a lookup see
+  // an older table; only whole 16-byte pieces inside each row are prefetched.
   if (MODE != 1 && warp == kProducer && lane == 0 && vp.total > 0) {
     const int64_t f0 = cta_begin(c, vp.total, vp.P), f1 = cta_begin(c + 1, vp.total, vp.P);
     if (f0 < f1) {
       const int s0 = locate(f0, a, vp.n_sessions).s, s1 = locate(f1 - 1, a, vp.n_sessions).s;
       for (int s = s0; s <= s1; ++s) {
-        const int32_t* row = vp.bt + (int64_t)s * vp.max_blocks;
-        const uint32_t bytes = (uint32_t)(((int64_t)a.n_blk[s] * 4) & ~(int64_t)15);
-        if ((reinterpret_cast<uintptr_t>(row) & 15) == 0 && bytes > 0) prefetch_l2(row, bytes);
+        if (a.seg_base[s + 1] <= a.seg_base[s]) continue;
+        const int cA = cta_of(a.seg_base[s], vp.total, vp.P), cB = cta_of(a.seg_base[s + 1] - 1, vp.total, vp.P);
+        const char* row = reinterpret_cast<const char*>(vp.bt + (int64_t)s * vp.max_blocks);
+        const int64_t row_bytes = ((int64_t)a.n_blk[s] * 4) & ~(int64_t)15;
+        const int64_t n = cB - cA + 1, chunk = ((row_bytes + n - 1) / n + 15) & ~(int64_t)15;
+        const int64_t off = (int64_t)(c - cA) * chunk;
+        if ((reinterpret_cast<uintptr_t>(row) & 15) == 0 && off < row_bytes)
+          prefetch_l2(row + off, (uint32_t)(chunk < row_bytes - off ? chunk : row_bytes - off));
       }
     }
   }
